@@ -1,0 +1,422 @@
+"""Pins for the CPU oracle: values printed on the pages, closed forms, brute force.
+
+Each test checks the oracle against something other than itself, so that a
+plausible slip in it (a dropped term, a wrong index or sign, a swapped operand,
+a wrong tie-break) fails at least one of them.
+"""
+
+import itertools
+import math
+
+import numpy as np
+import pytest
+
+import oracle as orc
+from synth import host_fill, normal_K, NORMAL
+
+
+# --------------------------------------------------------------------------
+# helpers: an independent dense formulation, written the way the adv12 page's
+# step table orders the forward (softmax over all experts, top-k on the
+# probabilities, divide by their sum, mask-weighted sum over every expert).
+# --------------------------------------------------------------------------
+
+def bf16_bits_to_f64(a):
+    return (np.asarray(a, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16_value(v):
+    """float64 -> float32 (RNE) -> bf16 (RNE via the carry trick), returned as float64."""
+    f = np.asarray(v, np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return bf16_bits_to_f64(u.astype(np.uint16))
+
+
+def as_f64(a):
+    return bf16_bits_to_f64(a) if a.dtype == np.uint16 else a.astype(np.float64)
+
+
+def dense_expert(kind, X, w1, b1, w2, b2, F):
+    """All tokens through one expert (float64), textbook formulas."""
+    W1 = as_f64(w1)
+    A = X @ W1.T + (0 if b1 is None else b1.astype(np.float64))
+    if kind == orc.LINEAR:
+        return A
+    if kind == orc.GELU:
+        from scipy.special import erf
+        H = 0.5 * A * (1 + erf(A / math.sqrt(2)))
+    else:
+        g, u = A[:, :F], A[:, F:]
+        H = g / (1 + np.exp(-g)) * u
+    if w1.dtype == np.uint16:
+        H = f64_to_bf16_value(H)
+    Y = H @ as_f64(w2).T + (0 if b2 is None else b2.astype(np.float64))
+    return Y
+
+
+def dense_forward(kind, x, Wg, gb, W, k, F, add_residual=False):
+    X = as_f64(x)
+    T, d = X.shape
+    E = Wg.shape[1]
+    L = X @ Wg.astype(np.float64) + (0 if gb is None else gb.astype(np.float64))
+    L = L.astype(np.float32).astype(np.float64)     # the layer's logits are fp32
+    P = np.exp(L - L.max(axis=1, keepdims=True))
+    P /= P.sum(axis=1, keepdims=True)
+    M = np.zeros((T, E))
+    for t in range(T):
+        order = sorted(range(E), key=lambda e: (-P[t, e], e))[:k]
+        s = sum(P[t, e] for e in order)
+        for e in order:
+            M[t, e] = P[t, e] / s
+    out = X.copy() if add_residual else np.zeros((T, d))
+    for e in range(E):
+        Ye = dense_expert(kind, X, W["w1"][e], None if W["b1"] is None else W["b1"][e],
+                          None if W["w2"] is None else W["w2"][e],
+                          None if W["b2"] is None else W["b2"][e], F)
+        out += M[:, [e]] * Ye
+    if W.get("shared") is not None:
+        sw1, sb1, sw2, sb2 = W["shared"]
+        out += dense_expert(kind, X, sw1, sb1, sw2, sb2, F)
+    return out, M
+
+
+def rand(shape, seed, tid, std=1.0, bf16=False):
+    n = int(np.prod(shape))
+    return host_fill(seed, tid, 0, n, NORMAL, normal_K(std), bf16).reshape(shape)
+
+
+def small_problem(kind, T, d, E, k, F, seed, bf16, biases=False, shared=False):
+    x = rand((T, d), seed, 1, 1.0, bf16)
+    Wg = rand((d, E), seed, 2, 1 / math.sqrt(d))
+    N1 = d if kind == orc.LINEAR else (F if kind == orc.GELU else 2 * F)
+    W = dict(w1=rand((E, N1, d), seed, 4, 1 / math.sqrt(d), bf16),
+             b1=rand((E, N1), seed, 5, 1 / math.sqrt(d)) if biases else None,
+             w2=None if kind == orc.LINEAR else rand((E, d, F), seed, 6, 1 / math.sqrt(F), bf16),
+             b2=rand((E, d), seed, 7, 0.1) if (biases and kind != orc.LINEAR) else None)
+    W["shared"] = None
+    if shared:
+        W["shared"] = (rand((N1, d), seed, 8, 1 / math.sqrt(d), bf16), None,
+                       rand((d, F), seed, 10, 1 / math.sqrt(F), bf16), None)
+    return x, Wg, W
+
+
+def run_oracle(kind, x, Wg, gb, W, k, F, cf=0.0, add_residual=False):
+    return orc.forward(kind, x, Wg, gb, W["w1"], W["b1"], W["w2"], W["b2"], k, F, cf=cf,
+                       add_residual=add_residual, shared=W.get("shared"))
+
+
+# --------------------------------------------------------------------------
+# values printed on the pages
+# --------------------------------------------------------------------------
+
+def test_renorm_printed_example(golden):
+    g = golden("renorm_adv12_q1.json")
+    logits = np.log(np.array([g["probs"]], np.float64)).astype(np.float32)
+    idx, w = orc.topk_renorm(logits, g["k"])
+    assert idx[0].tolist() == g["expected_idx"]
+    assert np.round(w[0].astype(np.float64), g["printed_decimals"]).tolist() == g["expected_w"]
+    # the exact values are 4/7 and 3/7
+    assert abs(w[0, 0] - 4 / 7) < 2e-7 and abs(w[0, 1] - 3 / 7) < 2e-7
+    assert abs(sum(g["probs"][:2]) - g["unnormalised_sum"]) < 1e-12
+
+
+def test_aggregation_printed_example(golden):
+    g = golden("aggregation_moe_notes.json")
+    ys = np.array(g["expert_outputs"], np.float64)
+    x_row = np.zeros(2, np.float32)
+    out = orc.combine_row(x_row, False, g["weights"], [1, 1], ys, None, orc.F32)
+    assert np.allclose(out, g["expected"], atol=1e-7)
+
+
+def test_aggregation_through_whole_forward(golden):
+    """Same example driven through the full oracle forward: two LINEAR experts with
+    zero weight matrices and biases equal to the printed outputs; the gate bias
+    makes the renormalised routing weights 0.7 and 0.3."""
+    g = golden("aggregation_moe_notes.json")
+    T, d, E, k = 1, 2, 2, 2
+    x = np.zeros((T, d), np.float32)
+    Wg = np.zeros((d, E), np.float32)
+    gb = np.log(np.array(g["weights"], np.float64)).astype(np.float32)
+    w1 = np.zeros((E, d, d), np.float32)
+    b1 = np.array(g["expert_outputs"], np.float32)
+    r = orc.forward(orc.LINEAR, x, Wg, gb, w1, b1, None, None, k, d)
+    assert r["idx"][0].tolist() == [0, 1]
+    assert np.allclose(r["w"][0], g["weights"], atol=1e-7)
+    assert np.allclose(r["out"][0], g["expected"], atol=1e-6)
+
+
+def test_capacity_printed_example(golden):
+    g = golden("capacity_adv12_q2.json")
+    T, k, E = g["T"], g["k"], g["E"]
+    # a routing table with the page's loads: each token picks two different experts
+    idx = np.zeros((T, k), np.int32)
+    remaining = list(g["loads"])
+    for t in range(T):
+        order = sorted(range(E), key=lambda e: (-remaining[e], e))[:k]
+        idx[t] = order
+        for e in order:
+            remaining[e] -= 1
+    assert remaining == [0] * E
+    ld = orc.load(idx, E)
+    assert ld.tolist() == g["loads"] and int(ld.sum()) == g["total_routings"] == T * k
+    counts, offsets, pt, ps, sd = orc.dispatch(idx, E, g["capacity"])
+    assert counts[0] == g["expert0_kept"]
+    assert int((sd[idx == 0] < 0).sum()) == g["expert0_overflow"]
+    assert counts.tolist() == [min(l, g["capacity"]) for l in g["loads"]]
+    # the kept ones are the earliest tokens of each expert
+    for e in range(E):
+        toks = [t for t in range(T) if e in idx[t]]
+        assert pt[offsets[e]:offsets[e + 1]].tolist() == toks[:g["capacity"]]
+
+
+def test_capacity_factor_definition():
+    # capacity = ceil(cf * T * k / E), clipped to [1, T]; cf <= 0 means no limit
+    assert orc.capacity(1.25, 8192, 1, 64) == 160           # Switch-shaped workload
+    assert orc.capacity(1.0, 8192, 8, 256) == 256            # DeepSeek-shaped, cf 1.0
+    assert orc.capacity(1.25, 8192, 8, 256) == 320           # DeepSeek-shaped, cf 1.25
+    assert orc.capacity(0.625, 64, 2, 4) == 20               # the adv12 Q2 capacity
+    assert orc.capacity(0.0, 100, 2, 4) == 100
+    assert orc.capacity(-1.0, 100, 2, 4) == 100
+    assert orc.capacity(1.0, 10, 1, 3) == 4                  # ceil(3.33)
+    assert orc.capacity(1e-9, 10, 1, 3) == 1                 # clipped below
+    assert orc.capacity(100.0, 10, 2, 4) == 10               # clipped above
+
+
+def test_load_report_printed_example(golden):
+    g = golden("eplb_adv12.json")
+    r = orc.load_report(np.array(g["loads"], np.int32), g["devices"])
+    assert r["assign"].tolist() == g["lpt_assignment"]
+    assert r["dev_load"].tolist() == g["lpt_device_load"]
+    assert r["naive_load"].tolist() == g["naive_device_load"]
+    assert r["var_naive"] == g["naive_variance"]
+    assert r["var_lpt"] == g["lpt_variance"]
+    assert round(r["imbalance"], 3) == g["imbalance_3dp"]
+    assert max(r["dev_load"]) == g["optimum_makespan"]
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_lpt_four_thirds_bound(seed):
+    """LPT makespan <= (4/3 - 1/(3D)) * optimum (Graham), optimum by brute force."""
+    rng = np.random.default_rng(seed)
+    E = int(rng.integers(2, 9))
+    D = int(rng.integers(2, 4))
+    loads = rng.integers(0, 50, E).astype(np.int32)
+    r = orc.load_report(loads, D)
+    opt = min(max(sum(int(loads[e]) for e in range(E) if a[e] == dv) for dv in range(D))
+              for a in itertools.product(range(D), repeat=E))
+    assert max(r["dev_load"]) <= (4 / 3 - 1 / (3 * D)) * opt + 1e-9
+    assert int(r["dev_load"].sum()) == int(loads.sum())
+    # greedy rule: each expert went to a least-loaded device at its turn
+    order = sorted(range(E), key=lambda e: (-loads[e], e))
+    dl = [0] * D
+    for e in order:
+        dv = dl.index(min(dl))
+        assert r["assign"][e] == dv
+        dl[dv] += int(loads[e])
+
+
+# --------------------------------------------------------------------------
+# closed forms and special cases
+# --------------------------------------------------------------------------
+
+def test_gelu_and_silu_closed_forms(golden):
+    g = golden("normal_cdf_table.json")
+    for xs, phi in g["phi"].items():
+        x = float(xs)
+        assert abs(orc.gelu(x) - x * phi) < 1e-15 * max(1, abs(x)) + 1e-16
+    lg = g["logistic"]
+    for xs, s in lg.items():
+        if xs == "source":
+            continue
+        x = float(xs)
+        assert abs(orc.silu(x) - x * s) < 1e-15
+    assert orc.silu(40.0) == pytest.approx(40.0, rel=1e-15)
+    assert abs(orc.silu(-40.0)) < 1e-15
+
+
+def test_bf16_rounding_cases():
+    assert orc.bf16_round(1.0) == 0x3F80
+    assert orc.bf16_round(-2.0) == 0xC000
+    assert orc.bf16_round(1 + 2 ** -8) == 0x3F80            # tie -> even (down)
+    assert orc.bf16_round(1 + 3 * 2 ** -8) == 0x3F82        # tie -> even (up)
+    assert orc.bf16_round(1 + 2 ** -8 + 2 ** -30) == 0x3F81  # just above the tie
+    assert orc.bf16_round(0.0) == 0x0000
+    assert orc.bf16_round(-0.0) == 0x8000
+    assert orc.bf16_round(3.0e38) == 0x7F62                   # 3.0e38 -> 0x7F62 (2.997e38..)
+    assert orc.bf16_round(1e39) == 0x7F80                     # overflow -> inf
+    assert orc.bf16_round(2.0 ** -133) == 0x0001              # smallest subnormal
+
+
+def test_k1_weight_is_exactly_one():
+    """Switch routing (k = 1): the renormalised weight is exactly 1."""
+    rng = np.random.default_rng(3)
+    logits = rng.normal(size=(50, 16)).astype(np.float32)
+    idx, w = orc.topk_renorm(logits, 1)
+    assert (w == 1.0).all()
+    assert (idx[:, 0] == logits.argmax(axis=1)).all()
+
+
+def test_zero_gate_ties_to_lower_ids():
+    logits = np.zeros((5, 8), np.float32)
+    idx, w = orc.topk_renorm(logits, 3)
+    assert (idx == np.array([0, 1, 2])).all()
+    assert np.allclose(w, 1 / 3, atol=1e-7)
+    # -0.0 and +0.0 compare equal: still ties toward the lower id
+    logits[:, 0] = -0.0
+    idx, _ = orc.topk_renorm(logits, 2)
+    assert (idx == np.array([0, 1])).all()
+
+
+def test_ties_mixed_with_larger_values():
+    logits = np.array([[1.0, 3.0, 3.0, 2.0, 3.0]], np.float32)
+    idx, w = orc.topk_renorm(logits, 4)
+    assert idx[0].tolist() == [1, 2, 4, 3]
+    assert w[0, 0] == w[0, 1] == w[0, 2]
+
+
+def test_weights_sum_to_one_and_order():
+    rng = np.random.default_rng(4)
+    logits = (rng.normal(size=(200, 32)) * 3).astype(np.float32)
+    idx, w = orc.topk_renorm(logits, 8)
+    assert np.allclose(w.astype(np.float64).sum(axis=1), 1.0, atol=2e-6)
+    assert (np.diff(w, axis=1) <= 0).all()            # slot order = descending logit
+    for t in range(200):
+        ref = sorted(range(32), key=lambda e: (-logits[t, e], e))[:8]
+        assert idx[t].tolist() == ref
+
+
+def test_textbook_ffn_single_token():
+    """1 token, 1 expert, no capacity: the layer is that expert's FFN."""
+    for kind in (orc.GELU, orc.SWIGLU):
+        x, Wg, W = small_problem(kind, 1, 16, 1, 1, 8, seed=5, bf16=True)
+        r = run_oracle(kind, x, Wg, None, W, 1, 8)
+        ref = dense_expert(kind, as_f64(x), W["w1"][0], None, W["w2"][0], None, 8)
+        assert np.allclose(bf16_bits_to_f64(r["out"]), f64_to_bf16_value(ref), rtol=0, atol=0)
+
+
+def test_swiglu_gate_rows_come_first():
+    """W1 rows [0,F) are the gate (inside silu), rows [F,2F) the up projection."""
+    d, F = 1, 1
+    x = np.array([1.0], np.float32)
+    w1 = np.array([[1.0], [2.0]], np.float32)     # gate -> 1, up -> 2
+    w2 = np.array([[1.0]], np.float32)
+    y = orc.expert_row(orc.SWIGLU, x, w1, None, w2, None, d, F)
+    s1 = 1 / (1 + math.exp(-1.0))
+    assert abs(y[0] - 1.0 * s1 * 2.0) < 1e-15     # silu(1)*2, not silu(2)*1
+
+
+def test_expert_biases_enter_where_stated():
+    d, F = 2, 2
+    x = np.array([0.0, 0.0], np.float32)
+    w1 = np.zeros((F, d), np.float32)
+    b1 = np.array([1.0, -1.0], np.float32)
+    w2 = np.eye(2, dtype=np.float32)
+    b2 = np.array([0.5, 0.25], np.float32)
+    y = orc.expert_row(orc.GELU, x, w1, b1, w2, b2, d, F)
+    assert np.allclose(y, [orc.gelu(1.0) + 0.5, orc.gelu(-1.0) + 0.25], atol=1e-15)
+    y = orc.expert_row(orc.LINEAR, x, np.eye(2, dtype=np.float32), b1, None, None, d, F)
+    assert np.allclose(y, b1, atol=0)
+
+
+def test_gate_logits_bruteforce():
+    x = rand((7, 24), 9, 1, 1.0, True)
+    Wg = rand((24, 5), 9, 2, 0.2)
+    gb = rand((5,), 9, 3, 1.0)
+    L = orc.gate_logits(x, Wg, gb)
+    ref = bf16_bits_to_f64(x) @ Wg.astype(np.float64) + gb
+    assert np.array_equal(L, ref.astype(np.float32))
+    Lr = orc.gate_logits(x, Wg, gb, rows=[6, 2])
+    assert np.array_equal(Lr, L[[6, 2]])
+
+
+# --------------------------------------------------------------------------
+# brute force on tiny inputs
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", range(6))
+def test_dispatch_bruteforce(seed):
+    rng = np.random.default_rng(100 + seed)
+    T, E = int(rng.integers(1, 40)), int(rng.integers(1, 9))
+    k = int(rng.integers(1, E + 1))
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    cap = int(rng.integers(1, T + 1))
+    counts, offsets, pt, ps, sd = orc.dispatch(idx, E, cap)
+    pos = 0
+    for e in range(E):
+        assert offsets[e] == pos
+        hits = [(t, j) for t in range(T) for j in range(k) if idx[t, j] == e]
+        kept, dropped = hits[:cap], hits[cap:]
+        assert counts[e] == len(kept)
+        for r, (t, j) in enumerate(kept):
+            assert pt[pos + r] == t and ps[pos + r] == j and sd[t, j] == pos + r
+        for (t, j) in dropped:
+            assert sd[t, j] == -1
+        pos += len(kept)
+    assert offsets[E] == pos == counts.sum()
+    assert counts.sum() == np.minimum(orc.load(idx, E), cap).sum()
+
+
+@pytest.mark.parametrize("kind", [orc.LINEAR, orc.GELU, orc.SWIGLU])
+@pytest.mark.parametrize("k", [1, 2, 3])
+def test_dense_bruteforce_equals_sparse(kind, k):
+    """Dense sum over all experts masked by the renormalised routing weights
+    equals the oracle's sparse top-k path (no capacity limit)."""
+    T, d, E, F = 9, 16, 4, 8
+    bf16 = kind != orc.LINEAR
+    x, Wg, W = small_problem(kind, T, d, E, k, F, seed=20 + k + 3 * kind, bf16=bf16,
+                             biases=True)
+    gb = rand((E,), 21, 3, 0.5)
+    r = run_oracle(kind, x, Wg, gb, W, k, F)
+    ref, M = dense_forward(kind, x, Wg, gb, W, k, F)
+    w_dense = np.take_along_axis(M, r["idx"].astype(np.int64), axis=1)
+    assert np.allclose(r["w"], w_dense, atol=2e-7)
+    got = as_f64(r["out"])
+    if bf16:
+        assert np.abs(got - ref).max() <= 2 ** -7 * np.abs(ref).max()
+    else:
+        assert np.allclose(got, ref, rtol=1e-6, atol=1e-6)
+
+
+def test_k_equals_E_is_dense_softmax_mixture():
+    T, d, E, F = 6, 8, 4, 8
+    x, Wg, W = small_problem(orc.LINEAR, T, d, E, E, F, seed=31, bf16=False, biases=True)
+    r = run_oracle(orc.LINEAR, x, Wg, None, W, E, F)
+    X = x.astype(np.float64)
+    L = (X @ Wg.astype(np.float64)).astype(np.float32).astype(np.float64)
+    P = np.exp(L - L.max(1, keepdims=True))
+    P /= P.sum(1, keepdims=True)
+    ref = sum(P[:, [e]] * (X @ W["w1"][e].astype(np.float64).T + W["b1"][e]) for e in range(E))
+    assert np.allclose(r["out"], ref, rtol=1e-6, atol=1e-6)
+    assert all(sorted(row) == list(range(E)) for row in r["idx"].tolist())
+
+
+def test_shared_expert_weight_one_and_residual():
+    T, d, E, k, F = 5, 16, 3, 2, 8
+    x, Wg, W = small_problem(orc.SWIGLU, T, d, E, k, F, seed=41, bf16=True, shared=True)
+    r = run_oracle(orc.SWIGLU, x, Wg, None, W, k, F, add_residual=True)
+    ref, _ = dense_forward(orc.SWIGLU, x, Wg, None, W, k, F, add_residual=True)
+    assert np.abs(as_f64(r["out"]) - ref).max() <= 2 ** -7 * np.abs(ref).max()
+
+
+def test_dropped_tokens_pass_through_unchanged():
+    """With the residual on, a token whose every slot overflowed outputs x bit-exactly."""
+    T, d, E, k, F = 40, 64, 2, 1, 64
+    x, Wg, W = small_problem(orc.GELU, T, d, E, k, F, seed=51, bf16=True)
+    gb = np.array([5.0, -5.0], np.float32)                # everyone wants expert 0
+    r = run_oracle(orc.GELU, x, Wg, gb, W, k, F, cf=0.25, add_residual=True)
+    cap = orc.capacity(0.25, T, k, E)
+    assert cap == 5
+    dropped = (r["slot_dest"] < 0).all(axis=1)
+    assert dropped.sum() >= T - 2 * cap
+    assert np.array_equal(r["out"][dropped], x[dropped])
+    assert not np.array_equal(r["out"][~dropped], x[~dropped])
+
+
+def test_load_sums_to_T_times_k():
+    rng = np.random.default_rng(8)
+    for _ in range(5):
+        T, E = int(rng.integers(1, 300)), int(rng.integers(1, 40))
+        k = int(rng.integers(1, E + 1))
+        idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+        assert orc.load(idx, E).sum() == T * k
