@@ -1,0 +1,447 @@
+#!/usr/bin/env python3
+"""MoE-layer forward throughput on B300: tokens/s per layer and roofline fraction.
+
+One step = one whole forward of the layer (route -> dispatch -> expert FFNs ->
+combine) over one batch of T synthetic tokens, through the C ABI. Inputs are
+seeded synthetic tensors with the workload's shapes and distributions (no
+dataset or trained weights are involved). Default workload: the Switch-style
+top-1 layer (T=8192, d=1024, E=64, GELU d->4096->d, capacity factor 1.25).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, timed as the reference arm
+
+Prints exactly one JSON line on stdout (rank 0). With N > 1 (torchrun) every rank
+runs an independent replica (weak scaling: no collective on the data path); the
+reported time is the max over ranks.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+METRIC = "MoE-layer fwd tokens/s on 1 B300; % of bf16 tensor / HBM roofline"
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="switch")
+    ap.add_argument("--flush-mib", type=int, default=256,
+                    help="L2 flush buffer written between timed steps (L2 is 126 MB)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return FALLBACK_PEAKS, "fallback"
+
+
+# ---------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception as e:   # no nvidia-smi: clocks unknown
+            log(f"clock sampling unavailable: {e}")
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                n += 1
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() in ("active", "1"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# ---------------------------------------------------------------------------------
+# algorithmic cost per kernel (for the roofline object)
+# ---------------------------------------------------------------------------------
+def kernel_algorithmic_cost(wl, name, P, touched):
+    """(flops, bytes) per STEP for all launches of kernel `name`, from the
+    algorithm's sizes (not from measured traffic)."""
+    es = 2 if wl.bf16 else 4
+    T, d, F, E = wl.T, wl.d, wl.F, wl.E
+    N1 = wl.N1
+    up = {"grouped_gemm_gelu", "grouped_gemm_swiglu"}
+    if name in up:
+        fl = 2.0 * P * d * N1
+        by = touched * N1 * d * 2 + P * d * 2 + P * F * 2
+        if wl.has_shared:
+            fl += 2.0 * T * d * N1
+            by += N1 * d * 2 + T * d * 2 + T * F * 2
+        return fl, by
+    if name == "grouped_gemm_scale":
+        return 2.0 * P * F * d, touched * d * F * 2 + P * F * 2 + P * d * 4
+    if name == "grouped_gemm_f32":        # shared expert down projection
+        return 2.0 * T * F * d, d * F * 2 + T * F * 2 + T * d * 4
+    if name.startswith("router_logits"):
+        return 2.0 * T * d * E, T * d * es + d * E * 4 + T * E * 4
+    if name.startswith("combine"):
+        rows = P + (T if wl.has_shared else 0)
+        return 0.0, rows * d * 4 + T * d * es * (2 if wl.add_residual else 1) + T * wl.k * 4
+    if name == "gather_rows":
+        return 0.0, 2.0 * P * d * es + P * 4
+    if name == "linear_expert":
+        return 2.0 * P * d * d, E * d * d * 4 + P * d * 8
+    return 0.0, 0.0
+
+
+def kernel_sources_hash():
+    import glob
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "top_routing_expert_renorm_b300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """Per-launch DRAM bytes from a committed ncu summary, when it was taken on the
+    current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_sources_sha") != kernel_sources_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_step"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------------
+# CPU baseline (the oracle, as it stands, single-threaded)
+# ---------------------------------------------------------------------------------
+def cpu_oracle_sample(wl, sample_tokens, seed=0):
+    """Time the oracle on a bounded sample: full routing + dispatch over all T tokens,
+    expert FFNs + combine for `sample_tokens` seeded tokens. Returns
+    (tokens_per_s, seconds_total, description)."""
+    import numpy as np
+    import oracle as orc
+    rng = np.random.default_rng(seed)
+    S = min(sample_tokens, wl.T)
+    rows = np.sort(rng.choice(wl.T, size=S, replace=False))
+    x = wl.x_host()
+    Wg, gb = wl.wg_host(), wl.gate_bias_host()
+    t0 = time.perf_counter()
+    L = orc.gate_logits(x, Wg, gb)
+    idx, w = orc.topk_renorm(L, wl.k)
+    cap = orc.capacity(np.float32(wl.cf), wl.T, wl.k, wl.E)
+    counts, offsets, pt, ps, sd = orc.dispatch(idx, wl.E, cap)
+    t_route = time.perf_counter() - t0
+    need = sorted({int(idx[t, j]) for t in rows for j in range(wl.k) if sd[t, j] >= 0})
+    Wc = {e: (wl.w1_host(e), wl.b1_host(e), wl.w2_host(e), wl.b2_host(e)) for e in need}
+    shared = ((wl.w1_host(0, True), wl.b1_host(0, True), wl.w2_host(0, True),
+               wl.b2_host(0, True)) if wl.has_shared else None)
+    t0 = time.perf_counter()
+    for t in rows:
+        xr = np.ascontiguousarray(x[t])
+        ys = np.zeros((wl.k, wl.d))
+        kept = (sd[t] >= 0).astype(np.int32)
+        for j in range(wl.k):
+            if kept[j]:
+                w1, b1, w2, b2 = Wc[int(idx[t, j])]
+                ys[j] = orc.expert_row(wl.kind_code, xr, w1, b1, w2, b2, wl.d, wl.F)
+        ysh = orc.expert_row(wl.kind_code, xr, *shared, wl.d, wl.F) if shared else None
+        orc.combine_row(xr, wl.add_residual, w[t], kept, ys, ysh,
+                        orc.BF16 if wl.bf16 else orc.F32)
+    t_ffn = time.perf_counter() - t0
+    per_token = t_route / wl.T + t_ffn / S
+    desc = (f"routing+dispatch of all {wl.T} tokens ({t_route:.2f} s) + expert FFN and "
+            f"combine of {S} seeded tokens ({t_ffn:.2f} s); tokens/s = 1/(t_route/T + t_ffn/S)")
+    return 1.0 / per_token, t_route + t_ffn, desc
+
+
+def default_sample(wl):
+    """Sample size giving roughly 2-5 s of single-core oracle work per run."""
+    m = {"linear": 1, "gelu": 2, "swiglu": 3}[wl.kind]
+    per_row = 2.0 * m * wl.d * (wl.F if wl.kind != "linear" else wl.d) * (
+        wl.k + (1 if wl.has_shared else 0))
+    return int(max(1, min(wl.T, 3e9 / per_row)))
+
+
+# ---------------------------------------------------------------------------------
+# reference arm: the oracle timed as the reference implementation
+# ---------------------------------------------------------------------------------
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    S = max(1, default_sample(wl) // 2)
+    vals = []
+    descs = None
+    for i in range(args.warmup + args.steps):
+        v, secs, desc = cpu_oracle_sample(wl, S, seed=i)
+        if i >= args.warmup:
+            vals.append((v, secs))
+            descs = desc
+    total_tokens = sum(v * s for v, s in vals)   # token-equivalents processed
+    total_s = sum(s for _, s in vals)
+    value = total_tokens / total_s
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * total_s / max(1, len(vals)), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "top_k": wl.k,
+                   "F": wl.F, "kind": wl.kind, "capacity_factor": wl.cf},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": descs},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+    import numpy as np
+    import __graft_entry__
+    __graft_entry__.build()
+    import top_routing_expert_renorm_b300 as moe
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+
+    inp = wl.device_inputs(dev)
+    cfg = moe.config_for(wl)
+    layer = moe.MoELayer(cfg, inp["wg"], inp["gate_bias"], inp["w1"], inp["b1"], inp["w2"],
+                         inp["b2"], inp["shared"])
+    x = inp["x"]
+    out = torch.empty_like(x)
+    load = torch.empty(wl.E, dtype=torch.int32, device=dev)
+    flush = torch.empty(args.flush_mib * 2 ** 20 // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        layer(x, out=out, load=load)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    st = moe.last_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {moe.status_string(st)}")
+    ld = load.cpu().numpy()
+    cap = moe.capacity(cfg)
+    P = int(np.minimum(ld, cap).sum())
+    touched = int((np.minimum(ld, cap) > 0).sum())
+
+    # ---- timed region ----
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    n_launch0 = moe.kernel_launch_count()
+    moe.profile_begin()
+    for i in range(K):
+        flush.zero_()                      # L2 flush between timed steps (not timed)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    kstats = moe.profile_end()
+    n_launch = moe.kernel_launch_count() - n_launch0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    st = moe.last_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after timing: {moe.status_string(st)}")
+    value = wl.T * K * world / (total_ms / 1000.0)
+
+    # ---- roofline of the dominant kernel ----
+    peaks, peak_src = load_peaks()
+    dom = max(kstats.items(), key=lambda kv: kv[1][1])
+    dname, (dlaunch, dms) = dom
+    fl, by = kernel_algorithmic_cost(wl, dname, P, touched)
+    t_step_s = dms / K / 1000.0
+    hbm = float(peaks["hbm_gbs"])
+    tflops = float(peaks["bf16_tflops"])
+    if fl / (tflops * 1e12) > by / (hbm * 1e9):
+        roof = {"bound": "tensor", "achieved": fl / t_step_s / 1e12, "peak": tflops,
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": by / t_step_s / 1e9, "peak": hbm, "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    tr = recorded_traffic(dname, wl.name)
+    roof["traffic"] = None if tr is None else tr / (dlaunch / K)
+    roof["kernel"] = dname
+    roof["launches_per_step"] = dlaunch / K
+    roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
+    roof["algorithmic_bytes_per_step"] = by
+    roof["algorithmic_flops_per_step"] = fl
+    # whole-layer roofline (slower of FLOPs at tensor peak and bytes at HBM peak)
+    lay_fl = wl.flops(P)
+    lay_by = wl.bytes(touched)
+    layer_roof_s = max(lay_fl / (tflops * 1e12), lay_by / (hbm * 1e9))
+    layer_frac = layer_roof_s / (total_ms / K / 1000.0)
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        xh.copy_(x)
+        oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        xd = torch.empty_like(x)
+        def e2e_step():
+            xd.copy_(xh, non_blocking=True)
+            layer(xd, out=out)
+            oh.copy_(out, non_blocking=True)
+        for _ in range(max(args.warmup, 3)):
+            e2e_step()
+        torch.cuda.synchronize()
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        for i in range(K):
+            flush.zero_()
+            ev2[i][0].record(stream)
+            e2e_step()
+            ev2[i][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = sum(a.elapsed_time(b) for a, b in ev2)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        nb = x.numel() * x.element_size()
+        e2e = {"value": wl.T * K * world / (e2e_ms / 1000.0), "unit": "tokens/s",
+               "h2d_bytes_per_step": nb, "d2h_bytes_per_step": out.numel() * out.element_size()}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, secs, desc = cpu_oracle_sample(wl, default_sample(wl))
+        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": desc, "seconds": secs}
+
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.bf16 else "f32",
+        "data": "synthetic (seeded counter-based generator; random-init weights)",
+        "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "top_k": wl.k,
+                   "F": wl.F, "kind": wl.kind, "capacity_factor": wl.cf,
+                   "shared_expert": wl.has_shared, "residual": wl.add_residual,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"flushed between steps ({args.flush_mib} MiB write)",
+                   "kept_rows_P": P, "touched_experts": touched},
+        "roofline": roof,
+        "layer_roofline_frac": layer_frac,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": n_launch,
+        "clocks": clk,
+        "kernels_ms_per_step": {k: v[1] / K for k, v in sorted(kstats.items(),
+                                                                key=lambda kv: -kv[1][1])},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    from synth import get
+    wl = get(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -37,7 +37,7 @@ class Workload:
     add_residual: bool = False
     has_shared: bool = False
     gate_dist: str = "normal"   # "normal" | "uniform"
-    gate_bias: str = "none"     # "none" | "zipf"
+    gate_bias: str = "none"     # "none" | "zipf" | "hot" (+20 on expert 0: one expert takes all)
     expert_bias: bool = False
     seed: int = 0
     note: str = ""
@@ -92,6 +92,10 @@ class Workload:
     def gate_bias_host(self):
         if self.gate_bias == "none":
             return None
+        if self.gate_bias == "hot":
+            b = np.zeros(self.E, np.float32)
+            b[0] = 20.0
+            return b
         p = np.array([(e + 1) ** -1.1 for e in range(self.E)], np.float64)
         p /= p.sum()
         return np.log(p).astype(np.float32)

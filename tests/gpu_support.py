@@ -1,0 +1,200 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the C ABI, run the
+oracle on the same seeded inputs, and compare under the stated criteria.
+
+Criteria (the layer's parity contract):
+  * logits: |gpu - oracle| <= 1e-5 * (sum_i |x_i * Wg_ie| + |b_e|)
+  * top-k ids, load, counts, offsets, permutation and drop masks: bit-exact, with
+    the oracle fed the GPU's own fp32 logits
+  * kept weights: |gpu - oracle| <= 2e-6
+  * bf16 expert outputs: max|gpu - oracle| <= 2e-2 * max|oracle| and
+    mean(|gpu - oracle| / (|oracle| + 1e-3 * max|oracle|)) <= 5e-3
+  * fp32 (Linear experts) outputs: max|gpu - oracle| <= 1e-5 * max|oracle|
+"""
+
+import numpy as np
+import torch
+
+import oracle as orc
+import top_routing_expert_renorm_b300 as moe
+
+
+def bf16_to_f64(a):
+    a = np.asarray(a)
+    return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def to_np(t):
+    """torch tensor (any device) -> numpy; bf16 becomes uint16 bit patterns."""
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def as_f64(a):
+    return bf16_to_f64(a) if a.dtype == np.uint16 else a.astype(np.float64)
+
+
+class GpuRun:
+    """Inputs of a workload on the device and on the host, and the CUDA path's
+    stage outputs (route, dispatch, expert FFN, combine) plus moe_forward."""
+
+    def __init__(self, wl, device="cuda"):
+        self.wl = wl
+        self.dev = device
+        self.inp = wl.device_inputs(device)
+        self.cfg = moe.config_for(wl)
+
+    def run(self):
+        wl, inp, cfg = self.wl, self.inp, self.cfg
+        T, E, k, d = wl.T, wl.E, wl.k, wl.d
+        i32 = dict(dtype=torch.int32, device=self.dev)
+        f32 = dict(dtype=torch.float32, device=self.dev)
+        ws = torch.empty(moe.workspace_size(cfg), dtype=torch.uint8, device=self.dev)
+        Pmax = T * k
+        self.logits = torch.empty(T, E, **f32)
+        self.idx = torch.empty(T, k, **i32)
+        self.w = torch.empty(T, k, **f32)
+        moe.route(cfg, inp["x"], inp["wg"], inp["gate_bias"], self.logits, self.idx, self.w, ws)
+        self.load = torch.empty(E, **i32)
+        self.counts = torch.empty(E, **i32)
+        self.offsets = torch.empty(E + 1, **i32)
+        self.perm_token = torch.full((Pmax,), -7, **i32)
+        self.perm_slot = torch.full((Pmax,), -7, **i32)
+        self.slot_dest = torch.empty(T, k, **i32)
+        self.x_perm = torch.empty(Pmax, d, dtype=inp["x"].dtype, device=self.dev)
+        moe.dispatch(cfg, self.idx, inp["x"], self.load, self.counts, self.offsets,
+                     self.perm_token, self.perm_slot, self.slot_dest, self.x_perm, ws)
+        routed = moe.weights(inp["w1"], inp["b1"], inp["w2"], inp["b2"])
+        shared = moe.weights(*inp["shared"]) if inp["shared"] is not None else None
+        self.y = torch.empty(Pmax + (T if wl.has_shared else 0), d, **f32)
+        moe.expert_ffn(cfg, self.x_perm, self.offsets, routed, shared, inp["x"], self.w,
+                       self.perm_token, self.perm_slot, self.y, ws)
+        self.out_stages = torch.empty_like(inp["x"])
+        moe.combine(cfg, inp["x"], self.y, self.slot_dest, self.out_stages)
+        # the fused entry point on a fresh workspace
+        ws2 = torch.empty_like(ws)
+        self.out = torch.empty_like(inp["x"])
+        self.idx_f = torch.empty(T, k, **i32)
+        self.w_f = torch.empty(T, k, **f32)
+        self.load_f = torch.empty(E, **i32)
+        moe.forward(cfg, inp["x"], inp["wg"], inp["gate_bias"], routed, shared, self.out, ws2,
+                    topk_idx=self.idx_f, topk_w=self.w_f, load=self.load_f)
+        st = moe.last_device_status()
+        assert st == 0, f"device status {moe.status_string(st)}"
+        torch.cuda.synchronize()
+        return self
+
+
+# ---- comparisons --------------------------------------------------------------------
+
+def check_logits(wl, x_host, rows, L_gpu_rows):
+    Wg = wl.wg_host()
+    gb = wl.gate_bias_host()
+    L_ref = orc.gate_logits(x_host, Wg, gb, rows=rows)
+    X = as_f64(x_host[rows])
+    scale = np.abs(X) @ np.abs(Wg.astype(np.float64))
+    if gb is not None:
+        scale += np.abs(gb.astype(np.float64))
+    err = np.abs(L_gpu_rows.astype(np.float64) - L_ref.astype(np.float64))
+    worst = float((err / (scale + 1e-30)).max())
+    assert (err <= 1e-5 * scale + 1e-30).all(), f"logit error {worst:.3e} of scale"
+    return worst
+
+
+def check_routing(r):
+    """idx bit-exact and w within 2e-6 against the oracle fed the GPU logits."""
+    L = to_np(r.logits)
+    idx_ref, w_ref = orc.topk_renorm(L, r.wl.k)
+    idx = to_np(r.idx)
+    assert np.array_equal(idx, idx_ref), f"{(idx != idx_ref).sum()} top-k ids differ"
+    w = to_np(r.w)
+    assert np.abs(w - w_ref).max() <= 2e-6
+    assert np.array_equal(to_np(r.idx_f), idx_ref)
+    assert np.abs(to_np(r.w_f) - w_ref).max() <= 2e-6
+    return idx_ref, w_ref
+
+
+def check_dispatch(r, idx_ref):
+    wl = r.wl
+    cap = orc.capacity(np.float32(wl.cf), wl.T, wl.k, wl.E)
+    assert moe.capacity(r.cfg) == cap
+    counts, offsets, pt, ps, sd = orc.dispatch(idx_ref, wl.E, cap)
+    ld = orc.load(idx_ref, wl.E)
+    assert np.array_equal(to_np(r.load), ld)
+    assert np.array_equal(to_np(r.load_f), ld)
+    assert np.array_equal(to_np(r.counts), counts)
+    assert np.array_equal(to_np(r.offsets), offsets)
+    P = int(offsets[-1])
+    assert np.array_equal(to_np(r.perm_token)[:P], pt)
+    assert np.array_equal(to_np(r.perm_slot)[:P], ps)
+    assert np.array_equal(to_np(r.slot_dest), sd)
+    return cap, sd, P
+
+
+def oracle_rows(wl, x_host_rows, rows, idx_ref, w_ref, sd, cache):
+    """Oracle outputs for the given tokens, with routing fed from the GPU logits."""
+    out = []
+    for t_i, t in enumerate(rows):
+        xr = np.ascontiguousarray(x_host_rows[t_i])
+        ys = np.zeros((wl.k, wl.d))
+        kept = (sd[t] >= 0).astype(np.int32)
+        for j in range(wl.k):
+            if kept[j]:
+                e = int(idx_ref[t, j])
+                if e not in cache:
+                    cache[e] = (wl.w1_host(e), wl.b1_host(e), wl.w2_host(e), wl.b2_host(e))
+                w1, b1, w2, b2 = cache[e]
+                ys[j] = orc.expert_row(wl.kind_code, xr, w1, b1, w2, b2, wl.d, wl.F)
+        ysh = None
+        if wl.has_shared:
+            if "shared" not in cache:
+                cache["shared"] = (wl.w1_host(0, True), wl.b1_host(0, True),
+                                   wl.w2_host(0, True), wl.b2_host(0, True))
+            sw1, sb1, sw2, sb2 = cache["shared"]
+            ysh = orc.expert_row(wl.kind_code, xr, sw1, sb1, sw2, sb2, wl.d, wl.F)
+        out.append(orc.combine_row(xr, wl.add_residual, w_ref[t], kept, ys, ysh,
+                                   orc.BF16 if wl.bf16 else orc.F32))
+    return np.stack(out)
+
+
+def check_outputs(wl, got, ref):
+    g, o = as_f64(got), as_f64(ref)
+    mx = np.abs(o).max()
+    err = np.abs(g - o)
+    if wl.bf16:
+        eps = 1e-3 * mx
+        mean_rel = float((err / (np.abs(o) + eps)).mean())
+        assert err.max() <= 2e-2 * mx, f"max err {err.max():.3e} vs {2e-2 * mx:.3e}"
+        assert mean_rel <= 5e-3, f"mean relative error {mean_rel:.3e}"
+        return float(err.max() / mx), mean_rel
+    assert err.max() <= 1e-5 * mx, f"max err {err.max():.3e} vs {1e-5 * mx:.3e}"
+    return float(err.max() / mx), 0.0
+
+
+def full_check(wl, sample=None, seed=0):
+    """Run the CUDA path on `wl` and check it against the oracle.
+    sample=None: every token; otherwise that many seeded tokens (routing and
+    dispatch are still checked in full)."""
+    r = GpuRun(wl).run()
+    if sample is None or sample >= wl.T:
+        rows = np.arange(wl.T)
+        x_rows = wl.x_host()
+        x_all = x_rows
+    else:
+        rng = np.random.default_rng(seed)
+        rows = np.sort(rng.choice(wl.T, size=sample, replace=False))
+        x_all = wl.x_host()
+        x_rows = x_all[rows]
+    check_logits(wl, x_all, rows, to_np(r.logits)[rows])
+    idx_ref, w_ref = check_routing(r)
+    cap, sd, P = check_dispatch(r, idx_ref)
+    # gathered rows are exact copies
+    xp = to_np(r.x_perm)[:P]
+    pt = to_np(r.perm_token)[:P]
+    chk = np.arange(0, P, max(1, P // 512))
+    assert np.array_equal(xp[chk], x_all[pt[chk]])
+    ref = oracle_rows(wl, x_rows, rows, idx_ref, w_ref, sd, {})
+    stats = check_outputs(wl, to_np(r.out)[rows], ref)
+    check_outputs(wl, to_np(r.out_stages)[rows], ref)
+    return r, stats

@@ -1,0 +1,166 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the oracle on the
+same seeded inputs (criteria in gpu_support.py)."""
+
+import numpy as np
+import pytest
+import torch
+
+import top_routing_expert_renorm_b300 as moe
+from synth import Workload, get, host_fill, dev_fill, normal_K, uniform_K, NORMAL, UNIFORM
+from gpu_support import GpuRun, full_check, to_np, as_f64
+
+pytestmark = pytest.mark.gpu
+
+W = Workload
+SMALL = {
+    # the tiny tutorial layer itself (fp32, Linear(8->8)+bias experts)
+    "tiny": get("tiny"),
+    # Linear experts with capacity drops, residual and a shared expert
+    "linear_cap_res_shared": W("lcrs", T=96, d=16, E=5, k=2, F=16, kind="linear", act="f32",
+                               cf=0.75, add_residual=True, has_shared=True, expert_bias=True),
+    # top-1 GELU with capacity and residual; 3 M tiles per expert, ragged N tile (320)
+    "gelu_cap_res": W("gcr", T=1000, d=128, E=4, k=1, F=320, kind="gelu", act="bf16", cf=1.25,
+                      add_residual=True),
+    "gelu_bias_k2": W("gb2", T=333, d=192, E=6, k=2, F=256, kind="gelu", act="bf16",
+                      expert_bias=True),
+    # Zipf-skewed SwiGLU with a shared expert; ragged N tiles (F=192, d=192)
+    "swiglu_zipf_shared": W("szs", T=700, d=192, E=6, k=2, F=192, kind="swiglu", act="bf16",
+                            gate_bias="zipf", has_shared=True),
+    "swiglu_k8_cap_shared": W("sk8", T=260, d=256, E=32, k=8, F=128, kind="swiglu", act="bf16",
+                              cf=1.0, has_shared=True),
+    "swiglu_bias": W("sb", T=150, d=128, E=3, k=2, F=64, kind="swiglu", act="bf16",
+                     expert_bias=True),
+    "k_equals_E": W("kE", T=100, d=64, E=4, k=4, F=64, kind="gelu", act="bf16"),
+    "one_expert": W("e1", T=200, d=64, E=1, k=1, F=64, kind="swiglu", act="bf16"),
+    "single_token": W("t1", T=1, d=128, E=16, k=4, F=128, kind="swiglu", act="bf16"),
+    "hot_expert_cap": W("hot", T=400, d=64, E=8, k=2, F=128, kind="gelu", act="bf16", cf=0.5,
+                        gate_bias="hot", add_residual=True),
+    "max_E_max_k": W("mx", T=64, d=64, E=1024, k=32, F=64, kind="gelu", act="bf16"),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    moe._capi.load()
+    yield
+    torch.cuda.synchronize()
+
+
+def test_device_generator_matches_host():
+    for dist, K in ((NORMAL, normal_K(0.7)), (UNIFORM, uniform_K(0.3))):
+        for dt in (torch.float32, torch.bfloat16):
+            t = torch.empty(100003, dtype=dt, device="cuda")
+            dev_fill(t, 5, 9, 777, dist, K)
+            h = host_fill(5, 9, 777, 100003, dist, K, dt == torch.bfloat16)
+            assert np.array_equal(to_np(t), h)
+
+
+@pytest.mark.parametrize("M,row_splits,N,K", [
+    (300, [0, 100, 100, 300], 256, 128),      # an empty group
+    (1000, [0, 129, 400, 401, 1000, 1000], 320, 192),   # ragged N tile
+    (129, [0, 129], 64, 64),
+    (64, [0, 1, 64], 512, 1024),
+])
+def test_grouped_gemm_building_block(M, row_splits, N, K):
+    G = len(row_splits) - 1
+    g = torch.Generator(device="cpu").manual_seed(M + N + K)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    B = (torch.randn(G, N, K, generator=g) / K ** 0.5).to(torch.bfloat16)
+    ro = torch.tensor(row_splits, dtype=torch.int32)
+    D = torch.full((M, N), float("nan"), device="cuda")
+    ws = torch.empty(moe.grouped_gemm_ws_size(G), dtype=torch.uint8, device="cuda")
+    moe.grouped_gemm(A.cuda(), B.cuda(), ro.cuda(), D, ws)
+    assert moe.last_device_status() == 0
+    Ad, Bd = A.double().numpy(), B.double().numpy()
+    got = D.cpu().numpy()
+    for gi in range(G):
+        r0, r1 = row_splits[gi], row_splits[gi + 1]
+        if r1 == r0:
+            continue
+        ref = Ad[r0:r1] @ Bd[gi].T
+        scale = np.abs(Ad[r0:r1]) @ np.abs(Bd[gi]).T
+        assert (np.abs(got[r0:r1] - ref) <= 1e-5 * scale + 1e-6).all()
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_parity(name):
+    full_check(SMALL[name])
+
+
+def test_dropped_tokens_leave_as_x_bit_exact():
+    wl = SMALL["hot_expert_cap"]
+    r = GpuRun(wl).run()
+    sd = to_np(r.slot_dest)
+    dropped = (sd < 0).all(axis=1)
+    assert dropped.sum() > 0
+    x = to_np(r.inp["x"])
+    assert np.array_equal(to_np(r.out)[dropped], x[dropped])
+
+
+def test_forward_is_deterministic():
+    wl = SMALL["swiglu_k8_cap_shared"]
+    a = GpuRun(wl).run()
+    b = GpuRun(wl).run()
+    assert np.array_equal(to_np(a.out), to_np(b.out))
+    assert np.array_equal(to_np(a.out), to_np(a.out_stages))
+
+
+@pytest.mark.parametrize("name,sample", [
+    ("switch", 32), ("mixtral", 8), ("deepseek", 4), ("deepseek_cf125", 4),
+    ("decode1", None), ("decode8", 4), ("decode64", 4),
+])
+def test_full_size_sampled(name, sample):
+    r, stats = full_check(get(name), sample=sample, seed=1)
+    del r
+    torch.cuda.empty_cache()
+
+
+def test_layer_object_matches_forward():
+    wl = SMALL["gelu_bias_k2"]
+    r = GpuRun(wl).run()
+    inp = r.inp
+    layer = moe.MoELayer(r.cfg, inp["wg"], inp["gate_bias"], inp["w1"], inp["b1"], inp["w2"],
+                         inp["b2"])
+    out = layer(inp["x"])
+    assert torch.equal(out, r.out)
+    # fewer tokens than the layer was built for
+    out2 = layer(inp["x"][:50].contiguous())
+    assert out2.shape == (50, wl.d)
+
+
+def test_bounded_wait_timeout_is_reported():
+    assert moe.last_device_status() == 0
+    moe.selftest_wait_timeout(200000)
+    assert moe.last_device_status() == moe._capi.MOE_ERR_TIMEOUT
+    assert moe.last_device_status() == 0          # the word is cleared after reading
+
+
+def test_out_of_range_expert_id_is_skipped_and_reported():
+    wl = SMALL["gelu_cap_res"]
+    cfg = moe.config_for(wl)
+    T, k, E = wl.T, wl.k, wl.E
+    idx = torch.randint(0, E, (T, k), dtype=torch.int32, device="cuda")
+    idx[5, 0] = E
+    idx[17, 0] = -3
+    i32 = dict(dtype=torch.int32, device="cuda")
+    outs = [torch.empty(E, **i32), torch.empty(E, **i32), torch.empty(E + 1, **i32),
+            torch.empty(T * k, **i32), torch.empty(T * k, **i32), torch.empty(T, k, **i32)]
+    ws = torch.empty(moe.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    moe.dispatch(cfg, idx, None, *outs, None, ws)
+    assert moe.last_device_status() == moe._capi.MOE_ERR_DEVICE_INDEX
+    sd = to_np(outs[5])
+    assert sd[5, 0] == -1 and sd[17, 0] == -1
+    assert to_np(outs[0]).sum() == T * k - 2
+
+
+def test_profile_and_launch_count():
+    wl = SMALL["swiglu_bias"]
+    n0 = moe.kernel_launch_count()
+    moe.profile_begin()
+    GpuRun(wl).run()
+    stats = moe.profile_end()
+    assert moe.kernel_launch_count() > n0
+    assert "grouped_gemm_swiglu" in stats and "grouped_gemm_scale" in stats
+    assert all(v[0] >= 1 and v[1] >= 0 for v in stats.values())

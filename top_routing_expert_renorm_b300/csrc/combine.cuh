@@ -1,0 +1,108 @@
+// Linear (fp32) experts and the weighted combine.
+// ["adv12 — MoE + EPLB" 4.1: experts are nn.Linear(d_model, d_model) and
+//  out[mask] += weight * expert_e(x[mask]); "MOE 学习笔记" 输出聚合示例 (weighted sum of
+//  the selected experts' outputs); "MoE 并行" Capacity Factor (overflow -> residual).]
+#pragma once
+#include "common.cuh"
+
+namespace moe {
+
+// ---- LINEAR experts in fp32: y[r] = scale_r * (W_g x[r] + b_g) -------------------------
+// One thread per output element; row r belongs to the group g with
+// row_offsets[g] <= r < row_offsets[g+1] (binary search); P = row_offsets[G].
+// scale_r = topk_w[perm_token[r]*k + perm_slot[r]] when topk_w is given, else 1.
+__global__ void __launch_bounds__(256) linear_expert_kernel(
+    const float* __restrict__ xin, const int* __restrict__ row_offsets, int G,
+    const float* __restrict__ W, const float* __restrict__ b, const float* __restrict__ topk_w,
+    const int* __restrict__ perm_token, const int* __restrict__ perm_slot, int k,
+    float* __restrict__ y, int d, long long max_rows) {
+    const int P = row_offsets[G];
+    const long long n = (long long)P * d;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n && i < max_rows * d;
+         i += stride) {
+        const long long r = i / d;
+        const int o = (int)(i % d);
+        int lo = 0, hi = G;   // row_offsets[lo] <= r < row_offsets[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (row_offsets[mid] <= r) lo = mid;
+            else hi = mid;
+        }
+        const float* wrow = W + ((long long)lo * d + o) * d;
+        const float* xr = xin + r * d;
+        float acc = 0.0f;
+        for (int c = 0; c < d; ++c) acc = fmaf(wrow[c], xr[c], acc);
+        if (b) acc += b[(long long)lo * d + o];
+        if (topk_w) acc *= topk_w[(long long)perm_token[r] * k + perm_slot[r]];
+        y[i] = acc;
+    }
+}
+
+// ---- combine: out[t] = (res ? x[t] : 0) + sum_j kept y[slot_dest[t,j]] (+ y_shared[t]) ----
+// One CTA per token, 4 columns per thread (16-byte loads of y). The k slot rows are
+// summed in slot order, so the result does not depend on scheduling.
+template <typename OT>
+__device__ __forceinline__ void load4(const OT* p, float4& v);
+template <>
+__device__ __forceinline__ void load4<float>(const float* p, float4& v) {
+    v = *reinterpret_cast<const float4*>(p);
+}
+template <>
+__device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, float4& v) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+    const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+    v = make_float4(fa.x, fa.y, fb.x, fb.y);
+}
+template <typename OT>
+__device__ __forceinline__ void store4(OT* p, const float4& v);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, const float4& v) {
+    *reinterpret_cast<float4*>(p) = v;
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, const float4& v) {
+    uint2 u;
+    u.x = pack_bf16x2(v.x, v.y);
+    u.y = pack_bf16x2(v.z, v.w);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+
+template <typename OT>
+__global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ x,
+                                                      const float* __restrict__ y,
+                                                      const int* __restrict__ slot_dest,
+                                                      const float* __restrict__ y_shared,
+                                                      OT* __restrict__ out, int d, int k,
+                                                      int add_residual) {
+    __shared__ int s_dest[32];
+    const long long t = blockIdx.x;
+    if (threadIdx.x < k) s_dest[threadIdx.x] = slot_dest[t * k + threadIdx.x];
+    __syncthreads();
+    for (int c = threadIdx.x * 4; c < d; c += blockDim.x * 4) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (add_residual) load4<OT>(x + t * d + c, acc);
+        for (int j = 0; j < k; ++j) {
+            const int r = s_dest[j];
+            if (r >= 0) {
+                const float4 v = *reinterpret_cast<const float4*>(y + (long long)r * d + c);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+        }
+        if (y_shared) {
+            const float4 v = *reinterpret_cast<const float4*>(y_shared + t * d + c);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        store4<OT>(out + t * d + c, acc);
+    }
+}
+
+}  // namespace moe

@@ -1,0 +1,206 @@
+// Dispatch: per-expert histogram -> prefix sums with capacity -> stable ranks ->
+// permutation into expert-contiguous rows -> row gather.
+// ["MoE 并行" 流程说明 (Token Dispatch groups tokens by expert) and Capacity Factor
+//  (overflow tokens take the residual path); adv12 3.2 (bincount of the routing)
+//  and Q2 (capacity 20: load 38 keeps 20, overflows 18).]
+//
+// The flattened assignment list s = t*k + j is cut into chunks of kDispTok tokens,
+// one CTA each. Ranks are stable in token order: inside a CTA every warp owns a
+// contiguous run of assignments, ranks inside a warp come from __match_any_sync
+// groups, and per-(warp, expert) running counters are prefix-summed across warps
+// and across CTAs. Nothing depends on the order in which atomics land, so every
+// output is deterministic.
+#pragma once
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kDispTok = 256;    // tokens per dispatch chunk (one CTA)
+constexpr int kDispWarps = 8;
+constexpr int kMTile = 128;      // rows per tensor-core M tile
+
+// ---- histogram: blockcnt[b][e] = assignments of chunk b routed to e ------------------
+__global__ void __launch_bounds__(256) dispatch_hist_kernel(const int* __restrict__ idx, int T,
+                                                            int k, int E,
+                                                            int* __restrict__ blockcnt) {
+    extern __shared__ int cnt[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    const long long beg = (long long)blockIdx.x * kDispTok * k;
+    const long long end = min((long long)(blockIdx.x + 1) * kDispTok, (long long)T) * k;
+    for (long long i = beg + threadIdx.x; i < end; i += blockDim.x) {
+        const int e = idx[i];
+        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);   // shared-memory count, order-free
+        else raise_error(DEVERR_INDEX);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) blockcnt[(long long)blockIdx.x * E + e] = cnt[e];
+}
+
+// ---- block-wide exclusive scan of one int per thread (blockDim.x == 1024) -------------
+__device__ __forceinline__ int block_excl_scan_1024(int v, int* s_warp /*[32]*/, int& total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) s_warp[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int s = s_warp[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, s, off);
+            if (lane >= off) s += y;
+        }
+        s_warp[lane] = s;   // inclusive over warps
+    }
+    __syncthreads();
+    total = s_warp[31];
+    const int warp_base = wid ? s_warp[wid - 1] : 0;
+    const int r = warp_base + x - v;
+    __syncthreads();
+    return r;
+}
+
+// ---- one CTA: load, capacity, offsets, per-chunk rank bases, M-tile table ----------
+// blockoff[b][e] = assignments of e in chunks before b (rank base of chunk b).
+// mtile_offsets[e] = exclusive prefix sum over experts of ceil(counts/128).
+__global__ void __launch_bounds__(1024) dispatch_scan_kernel(
+    const int* __restrict__ blockcnt, int nb, int E, int cap, int* __restrict__ blockoff,
+    int* __restrict__ load, int* __restrict__ counts, int* __restrict__ offsets,
+    int* __restrict__ mtile_offsets) {
+    __shared__ int s_warp[32];
+    const int e = threadIdx.x;
+    int kept = 0;
+    if (e < E) {
+        int run = 0;
+        for (int b = 0; b < nb; ++b) {
+            const long long i = (long long)b * E + e;
+            const int c = blockcnt[i];
+            blockoff[i] = run;
+            run += c;
+        }
+        load[e] = run;
+        kept = min(run, cap);
+        counts[e] = kept;
+    }
+    int total;
+    const int off = block_excl_scan_1024(kept, s_warp, total);
+    if (e < E) offsets[e] = off;
+    if (e == 0) offsets[E] = total;
+    const int tiles = (kept + kMTile - 1) / kMTile;
+    int ttot;
+    const int toff = block_excl_scan_1024(tiles, s_warp, ttot);
+    if (mtile_offsets) {
+        if (e < E) mtile_offsets[e] = toff;
+        if (e == 0) mtile_offsets[E] = ttot;
+    }
+}
+
+// ---- stable rank + scatter of the kept assignments ------------------------------------
+__global__ void __launch_bounds__(256) dispatch_rank_kernel(
+    const int* __restrict__ idx, int T, int k, int E, int cap, const int* __restrict__ blockoff,
+    const int* __restrict__ offsets, int* __restrict__ perm_token, int* __restrict__ perm_slot,
+    int* __restrict__ slot_dest) {
+    extern __shared__ int wcnt[];   // [kDispWarps][E] running counters
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < kDispWarps * E; i += blockDim.x) wcnt[i] = 0;
+    __syncthreads();
+    const long long beg = (long long)blockIdx.x * kDispTok * k;
+    const long long end = min((long long)(blockIdx.x + 1) * kDispTok, (long long)T) * k;
+    const long long n = end - beg;
+    const long long seg = ((n + kDispWarps - 1) / kDispWarps + 31) / 32 * 32;
+    const long long wbeg = beg + wid * seg;
+    const long long wend = min(wbeg + seg, end);
+    int* my = wcnt + wid * E;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    // pass 1: per-warp totals
+    for (long long base = wbeg; base < wend; base += 32) {
+        const long long i = base + lane;
+        int e = (i < wend) ? idx[i] : -1;
+        if (e >= E) e = -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && (peers & lt_mask) == 0) my[e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    // pass 2: exclusive scan over warps, seeded with the chunk's rank base
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = blockoff[(long long)blockIdx.x * E + e];
+        for (int w = 0; w < kDispWarps; ++w) {
+            const int c = wcnt[w * E + e];
+            wcnt[w * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    // pass 3: ranks and scatter
+    for (long long base = wbeg; base < wend; base += 32) {
+        const long long i = base + lane;
+        int e = (i < wend) ? idx[i] : -1;
+        if (e >= E) e = -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        int rank = 0;
+        if (e >= 0) rank = my[e] + __popc(peers & lt_mask);
+        __syncwarp();
+        if (e >= 0 && (peers & lt_mask) == 0) my[e] += __popc(peers);
+        __syncwarp();
+        if (i < wend) {
+            if (e >= 0 && rank < cap) {
+                const int pos = offsets[e] + rank;
+                perm_token[pos] = (int)(i / k);
+                perm_slot[pos] = (int)(i % k);
+                slot_dest[i] = pos;
+            } else {
+                slot_dest[i] = -1;
+            }
+        }
+    }
+}
+
+// ---- x_perm[p] = x[perm_token[p]] for p < P = offsets[E]; one warp per row -----------
+// 16-byte vector copies; row_bytes is a multiple of 16.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restrict__ x,
+                                                          const int* __restrict__ perm_token,
+                                                          const int* __restrict__ total_rows,
+                                                          uint8_t* __restrict__ x_perm,
+                                                          int row_bytes) {
+    const int P = *total_rows;
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < P;
+         r += warps) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + (long long)perm_token[r] * row_bytes);
+        uint4* dst = reinterpret_cast<uint4*>(x_perm + r * row_bytes);
+        for (int c = lane; c < row_bytes / 16; c += 32) dst[c] = __ldg(src + c);
+    }
+}
+
+// ---- M-tile table from offsets (expert stage entry): single CTA of 1024 threads ----
+__global__ void __launch_bounds__(1024) mtile_table_kernel(const int* __restrict__ offsets, int G,
+                                                           int* __restrict__ mtile_offsets) {
+    __shared__ int s_warp[32];
+    const int g = threadIdx.x;
+    int tiles = 0;
+    if (g < G) tiles = (offsets[g + 1] - offsets[g] + kMTile - 1) / kMTile;
+    int tot;
+    const int off = block_excl_scan_1024(tiles, s_warp, tot);
+    if (g < G) mtile_offsets[g] = off;
+    if (g == 0) mtile_offsets[G] = tot;
+}
+
+// Row and M-tile tables of a single group of `rows` rows (the shared expert).
+__global__ void single_group_table_kernel(int rows, int* __restrict__ row_offsets,
+                                          int* __restrict__ mtile_offsets) {
+    if (threadIdx.x == 0) {
+        row_offsets[0] = 0;
+        row_offsets[1] = rows;
+        mtile_offsets[0] = 0;
+        mtile_offsets[1] = (rows + kMTile - 1) / kMTile;
+    }
+}
+
+}  // namespace moe

@@ -1,0 +1,661 @@
+// Host side of the MoE layer library: argument validation, workspace carving,
+// TMA descriptor encoding, kernel launches and the exported C ABI (include/moe.h).
+// Everything is stream-ordered; nothing here synchronises the host except
+// moe_last_device_status() and moe_profile_end().
+#include "moe.h"
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <numeric>
+#include <vector>
+
+#include "common.cuh"
+#include "router.cuh"
+#include "dispatch.cuh"
+#include "grouped_gemm.cuh"
+#include "combine.cuh"
+
+using namespace moe;
+
+namespace {
+
+// ---------------------------------------------------------------------------------
+// launch accounting and optional per-kernel event timing
+// ---------------------------------------------------------------------------------
+std::atomic<uint64_t> g_launches{0};
+
+struct ProfRec {
+    const char* name;
+    cudaEvent_t a, b;
+};
+struct Prof {
+    std::mutex mu;
+    bool on = false;
+    std::vector<ProfRec> recs;
+    std::vector<cudaEvent_t> pool;
+    size_t used = 0;
+} g_prof;
+
+cudaEvent_t prof_event_locked() {
+    if (g_prof.used == g_prof.pool.size()) {
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+        g_prof.pool.push_back(e);
+    }
+    return g_prof.pool[g_prof.used++];
+}
+
+void prof_pre(const char* name, cudaStream_t s, cudaEvent_t* after) {
+    *after = nullptr;
+    if (!g_prof.on) return;
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    if (!g_prof.on) return;
+    cudaEvent_t a = prof_event_locked(), b = prof_event_locked();
+    if (!a || !b) return;
+    cudaEventRecord(a, s);
+    g_prof.recs.push_back({name, a, b});
+    *after = b;
+}
+
+#define MOE_LAUNCH(NAME, STREAM, ...)                                   \
+    do {                                                                \
+        cudaEvent_t moe_after_;                                         \
+        prof_pre(NAME, STREAM, &moe_after_);                            \
+        __VA_ARGS__;                                                    \
+        const cudaError_t moe_err_ = cudaGetLastError();                \
+        if (moe_after_) cudaEventRecord(moe_after_, STREAM);            \
+        g_launches.fetch_add(1, std::memory_order_relaxed);             \
+        if (moe_err_ != cudaSuccess) return MOE_ERR_CUDA;               \
+    } while (0)
+
+// ---------------------------------------------------------------------------------
+// device facts
+// ---------------------------------------------------------------------------------
+int current_device() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return dev;
+}
+
+int num_sms() {
+    static int cache[64] = {0};
+    const int dev = current_device();
+    if (dev < 0 || dev >= 64) return 148;
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (cols contiguous) read in boxes of 64 columns x
+// box_rows rows with the 128-byte swizzle; out-of-range rows read as zero.
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------------
+// validation
+// ---------------------------------------------------------------------------------
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_bf16_kind(const moe_config& c) {
+    return c.kind == MOE_EXPERT_GELU || c.kind == MOE_EXPERT_SWIGLU;
+}
+
+int64_t n1_of(const moe_config& c) {
+    return c.kind == MOE_EXPERT_LINEAR ? c.d : (c.kind == MOE_EXPERT_GELU ? c.F : 2ll * c.F);
+}
+
+moe_status check_cfg(const moe_config* c) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (c->T < 0 || c->E < 1 || c->E > 1024 || c->top_k < 1 || c->top_k > 32 || c->top_k > c->E)
+        return MOE_ERR_INVALID_ARG;
+    if (c->d < 8 || c->d % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)c->T * c->top_k >= (1ll << 31)) return MOE_ERR_INVALID_ARG;
+    if (!std::isfinite(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
+    if ((c->has_shared != 0 && c->has_shared != 1) || (c->add_residual != 0 && c->add_residual != 1))
+        return MOE_ERR_INVALID_ARG;
+    if (c->act_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    switch (c->kind) {
+        case MOE_EXPERT_LINEAR:
+            if (c->act_dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
+            break;
+        case MOE_EXPERT_GELU:
+        case MOE_EXPERT_SWIGLU:
+            if (c->act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+            if (c->d % 64 != 0 || c->F < 64 || c->F % 64 != 0) return MOE_ERR_INVALID_ARG;
+            if ((int64_t)c->E * n1_of(*c) >= (1ll << 31) || (int64_t)c->E * c->d >= (1ll << 31))
+                return MOE_ERR_INVALID_ARG;
+            break;
+        default:
+            return MOE_ERR_INVALID_ARG;
+    }
+    return MOE_OK;
+}
+
+int32_t capacity_of(const moe_config& c) {
+    if (!(c.capacity_factor > 0.0f)) return c.T;
+    double v = std::ceil((double)c.capacity_factor * (double)c.T * (double)c.top_k / (double)c.E);
+    if (v < 1.0) v = 1.0;
+    if (v > (double)c.T) v = (double)c.T;
+    return (int32_t)v;
+}
+
+// ---------------------------------------------------------------------------------
+// workspace layout (256-byte aligned regions, identical for every entry point)
+// ---------------------------------------------------------------------------------
+struct WsLayout {
+    size_t logits, idx, w, load, counts, offsets, blockcnt, blockoff, perm_token, perm_slot,
+        slot_dest, x_perm, mtile, shared_tab, h, hs, y, total;
+};
+
+WsLayout ws_layout(const moe_config& c) {
+    WsLayout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += (bytes + 255) & ~size_t(255);
+        return o;
+    };
+    const size_t T = (size_t)c.T, k = (size_t)c.top_k, E = (size_t)c.E, d = (size_t)c.d;
+    const size_t F = (size_t)std::max(c.F, 0);
+    const size_t Pmax = T * k;
+    const size_t nb = std::max<size_t>(1, (T + kDispTok - 1) / kDispTok);
+    const size_t es = c.act_dtype == MOE_BF16 ? 2 : 4;
+    L.logits = take(T * E * 4);
+    L.idx = take(Pmax * 4);
+    L.w = take(Pmax * 4);
+    L.load = take(E * 4);
+    L.counts = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.blockcnt = take(nb * E * 4);
+    L.blockoff = take(nb * E * 4);
+    L.perm_token = take(Pmax * 4);
+    L.perm_slot = take(Pmax * 4);
+    L.slot_dest = take(Pmax * 4);
+    L.x_perm = take(Pmax * d * es);
+    L.mtile = take((E + 1) * 4);
+    L.shared_tab = take(4 * 4);
+    L.h = take(is_bf16_kind(c) ? Pmax * F * 2 : 0);
+    L.hs = take(is_bf16_kind(c) && c.has_shared ? T * F * 2 : 0);
+    L.y = take((Pmax + (c.has_shared ? T : 0)) * d * 4);
+    L.total = off;
+    return L;
+}
+
+template <typename P>
+P* at(void* ws, size_t off) {
+    return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
+}
+
+// ---------------------------------------------------------------------------------
+// stage implementations (arguments already validated)
+// ---------------------------------------------------------------------------------
+moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const float* bias,
+                      float* logits, int32_t* idx, float* w, cudaStream_t s) {
+    const int T = c.T, E = c.E, d = c.d, k = c.top_k;
+    const dim3 grid((T + RT_BM - 1) / RT_BM, (E + RT_BN - 1) / RT_BN);
+    if (c.act_dtype == MOE_F32) {
+        MOE_LAUNCH("router_logits_f32", s,
+                   router_logits_kernel<float><<<grid, 256, 0, s>>>(
+                       static_cast<const float*>(x), Wg, bias, logits, T, d, E));
+    } else {
+        MOE_LAUNCH("router_logits_bf16", s,
+                   router_logits_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+                       static_cast<const __nv_bfloat16*>(x), Wg, bias, logits, T, d, E));
+    }
+    MOE_LAUNCH("topk_renorm", s,
+               topk_renorm_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, k, idx, w));
+    return MOE_OK;
+}
+
+moe_status dispatch_impl(const moe_config& c, const int32_t* idx, const void* x, int32_t* load,
+                         int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* perm_slot,
+                         int32_t* slot_dest, void* x_perm, int32_t* blockcnt, int32_t* blockoff,
+                         int32_t* mtile, cudaStream_t s) {
+    const int T = c.T, E = c.E, k = c.top_k;
+    const int cap = capacity_of(c);
+    const int nb = (T + kDispTok - 1) / kDispTok;
+    MOE_LAUNCH("dispatch_hist", s,
+               dispatch_hist_kernel<<<nb, 256, E * sizeof(int), s>>>(idx, T, k, E, blockcnt));
+    MOE_LAUNCH("dispatch_scan", s,
+               dispatch_scan_kernel<<<1, 1024, 0, s>>>(blockcnt, nb, E, cap, blockoff, load, counts,
+                                                       offsets, mtile));
+    MOE_LAUNCH("dispatch_rank", s,
+               dispatch_rank_kernel<<<nb, 256, kDispWarps * E * sizeof(int), s>>>(
+                   idx, T, k, E, cap, blockoff, offsets, perm_token, perm_slot, slot_dest));
+    if (x_perm) {
+        const int es = c.act_dtype == MOE_BF16 ? 2 : 4;
+        const long long Pmax = (long long)T * k;
+        const int blocks = (int)std::min<long long>((Pmax + 7) / 8, (long long)num_sms() * 16);
+        MOE_LAUNCH("gather_rows", s,
+                   gather_rows_kernel<<<std::max(blocks, 1), 256, 0, s>>>(
+                       static_cast<const uint8_t*>(x), perm_token, offsets + E,
+                       static_cast<uint8_t*>(x_perm), c.d * es));
+    }
+    return MOE_OK;
+}
+
+template <int EPI>
+const char* gemm_name() {
+    switch (EPI) {
+        case EPI_F32: return "grouped_gemm_f32";
+        case EPI_GELU_BF16: return "grouped_gemm_gelu";
+        case EPI_SWIGLU_BF16: return "grouped_gemm_swiglu";
+        default: return "grouped_gemm_scale";
+    }
+}
+
+template <int EPI>
+moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int64_t b_rows_total,
+                       int b_rows_per_group, int G, int N, const int32_t* row_offsets,
+                       const int32_t* mtile_offsets, void* out, long long ld_out, const float* bias,
+                       const float* topk_w, const int32_t* perm_token, const int32_t* perm_slot,
+                       int top_k, cudaStream_t s) {
+    if (a_rows <= 0 || G <= 0) return MOE_OK;
+    if (G > GM_MAX_GROUPS) return MOE_ERR_UNSUPPORTED;
+    CUtensorMap ta, tb;
+    if (!make_tmap_bf16(&ta, A, (uint64_t)a_rows, (uint64_t)K, GM_BM)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16(&tb, B, (uint64_t)b_rows_total, (uint64_t)K, GM_BN / 2)) return MOE_ERR_CUDA;
+    GemmParams p{};
+    p.G = G;
+    p.N = N;
+    p.K = K;
+    p.b_rows_per_group = b_rows_per_group;
+    p.up_offset = (EPI == EPI_SWIGLU_BF16) ? N : GM_BN / 2;
+    p.n_tiles = (EPI == EPI_SWIGLU_BF16) ? (N + 127) / 128 : (N + GM_BN - 1) / GM_BN;
+    p.row_offsets = row_offsets;
+    p.mtile_offsets = mtile_offsets;
+    p.out = out;
+    p.ld_out = ld_out;
+    p.bias = bias;
+    p.topk_w = topk_w;
+    p.perm_token = perm_token;
+    p.perm_slot = perm_slot;
+    p.top_k = top_k;
+    const int smem = gm_smem_bytes(G);
+    static std::once_flag attr_once[64];
+    static cudaError_t attr_err[64];
+    const int dev = current_device();
+    if (dev >= 0 && dev < 64) {
+        std::call_once(attr_once[dev], [&] {
+            attr_err[dev] = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 gm_smem_bytes(GM_MAX_GROUPS));
+        });
+        if (attr_err[dev] != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    const int grid = num_sms();
+    MOE_LAUNCH(gemm_name<EPI>(), s,
+               grouped_gemm_kernel<EPI><<<grid, GM_THREADS, smem, s>>>(ta, tb, p));
+    return MOE_OK;
+}
+
+#define MOE_TRY(expr)                       \
+    do {                                    \
+        const moe_status st_ = (expr);      \
+        if (st_ != MOE_OK) return st_;      \
+    } while (0)
+
+moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offsets,
+                    const moe_expert_weights& R, const moe_expert_weights* S, const void* x,
+                    const float* topk_w, const int32_t* perm_token, const int32_t* perm_slot,
+                    float* y, int32_t* mtile, bool mtile_ready, int32_t* shared_tab,
+                    __nv_bfloat16* h, __nv_bfloat16* hs, cudaStream_t s) {
+    const int T = c.T, E = c.E, d = c.d, k = c.top_k, F = c.F;
+    const long long Pmax = (long long)T * k;
+    float* y_shared = y + Pmax * d;
+    if (c.kind == MOE_EXPERT_LINEAR) {
+        const long long n = Pmax * d;
+        const int blocks = (int)std::max<long long>(1, std::min<long long>((n + 255) / 256, 65535));
+        MOE_LAUNCH("linear_expert", s,
+                   linear_expert_kernel<<<blocks, 256, 0, s>>>(
+                       static_cast<const float*>(x_perm), offsets, E,
+                       static_cast<const float*>(R.w1), R.b1, topk_w, perm_token, perm_slot, k, y,
+                       d, Pmax));
+        if (c.has_shared) {
+            MOE_LAUNCH("single_group_table", s,
+                       single_group_table_kernel<<<1, 32, 0, s>>>(T, shared_tab, shared_tab + 2));
+            const long long ns = (long long)T * d;
+            const int sb = (int)std::max<long long>(1, std::min<long long>((ns + 255) / 256, 65535));
+            MOE_LAUNCH("linear_expert", s,
+                       linear_expert_kernel<<<sb, 256, 0, s>>>(
+                           static_cast<const float*>(x), shared_tab, 1,
+                           static_cast<const float*>(S->w1), S->b1, nullptr, nullptr, nullptr, k,
+                           y_shared, d, T));
+        }
+        return MOE_OK;
+    }
+    if (!mtile_ready)
+        MOE_LAUNCH("mtile_table", s, mtile_table_kernel<<<1, 1024, 0, s>>>(offsets, E, mtile));
+    const int64_t N1 = n1_of(c);
+    if (c.kind == MOE_EXPERT_SWIGLU)
+        MOE_TRY(launch_gemm<EPI_SWIGLU_BF16>(x_perm, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
+                                             offsets, mtile, h, F, R.b1, nullptr, nullptr, nullptr,
+                                             k, s));
+    else
+        MOE_TRY(launch_gemm<EPI_GELU_BF16>(x_perm, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
+                                           offsets, mtile, h, F, R.b1, nullptr, nullptr, nullptr, k,
+                                           s));
+    MOE_TRY(launch_gemm<EPI_SCALE_F32>(h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets, mtile, y,
+                                       d, R.b2, topk_w, perm_token, perm_slot, k, s));
+    if (c.has_shared) {
+        MOE_LAUNCH("single_group_table", s,
+                   single_group_table_kernel<<<1, 32, 0, s>>>(T, shared_tab, shared_tab + 2));
+        if (c.kind == MOE_EXPERT_SWIGLU)
+            MOE_TRY(launch_gemm<EPI_SWIGLU_BF16>(x, T, d, S->w1, N1, (int)N1, 1, F, shared_tab,
+                                                 shared_tab + 2, hs, F, S->b1, nullptr, nullptr,
+                                                 nullptr, k, s));
+        else
+            MOE_TRY(launch_gemm<EPI_GELU_BF16>(x, T, d, S->w1, N1, (int)N1, 1, F, shared_tab,
+                                               shared_tab + 2, hs, F, S->b1, nullptr, nullptr,
+                                               nullptr, k, s));
+        MOE_TRY(launch_gemm<EPI_F32>(hs, T, F, S->w2, d, d, 1, d, shared_tab, shared_tab + 2,
+                                     y_shared, d, S->b2, nullptr, nullptr, nullptr, k, s));
+    }
+    return MOE_OK;
+}
+
+moe_status combine_impl(const moe_config& c, const void* x, const float* y,
+                        const int32_t* slot_dest, void* out, cudaStream_t s) {
+    const int T = c.T, d = c.d, k = c.top_k;
+    const long long Pmax = (long long)T * k;
+    const float* ysh = c.has_shared ? y + Pmax * d : nullptr;
+    int threads = std::min(256, ((d / 4 + 31) / 32) * 32);
+    threads = std::max(threads, 32);
+    if (c.act_dtype == MOE_F32)
+        MOE_LAUNCH("combine_f32", s,
+                   combine_kernel<float><<<T, threads, 0, s>>>(
+                       static_cast<const float*>(x), y, slot_dest, ysh, static_cast<float*>(out), d,
+                       k, c.add_residual));
+    else
+        MOE_LAUNCH("combine_bf16", s,
+                   combine_kernel<__nv_bfloat16><<<T, threads, 0, s>>>(
+                       static_cast<const __nv_bfloat16*>(x), y, slot_dest, ysh,
+                       static_cast<__nv_bfloat16*>(out), d, k, c.add_residual));
+    return MOE_OK;
+}
+
+moe_status check_weights(const moe_config& c, const moe_expert_weights* W) {
+    if (!W || !W->w1) return MOE_ERR_INVALID_ARG;
+    if (c.kind != MOE_EXPERT_LINEAR && !W->w2) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(W->w1) || !aligned16(W->w2) || !aligned16(W->b1) || !aligned16(W->b2))
+        return MOE_ERR_MISALIGNED;
+    return MOE_OK;
+}
+
+}  // namespace
+
+// =====================================================================================
+// exported C ABI
+// =====================================================================================
+extern "C" {
+
+size_t moe_workspace_size(const moe_config* cfg) {
+    if (check_cfg(cfg) != MOE_OK) return 0;
+    return ws_layout(*cfg).total;
+}
+
+int64_t moe_max_rows(const moe_config* cfg) {
+    if (check_cfg(cfg) != MOE_OK) return -1;
+    return (int64_t)cfg->T * cfg->top_k;
+}
+
+int32_t moe_capacity(const moe_config* cfg) {
+    if (check_cfg(cfg) != MOE_OK) return -1;
+    return capacity_of(*cfg);
+}
+
+moe_status moe_route(const moe_config* cfg, const void* x, const float* W_gate,
+                     const float* gate_bias, float* logits, int32_t* topk_idx, float* topk_w,
+                     void* ws, cudaStream_t stream) {
+    MOE_TRY(check_cfg(cfg));
+    const moe_config& c = *cfg;
+    if (c.T == 0) return MOE_OK;
+    if (!x || !W_gate || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+    if (!logits && !ws) return MOE_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(W_gate) || !aligned16(gate_bias) || !aligned16(logits) ||
+        !aligned16(topk_idx) || !aligned16(topk_w) || !aligned16(ws))
+        return MOE_ERR_MISALIGNED;
+    float* L = logits ? logits : at<float>(ws, ws_layout(c).logits);
+    return route_impl(c, x, W_gate, gate_bias, L, topk_idx, topk_w, stream);
+}
+
+moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const void* x,
+                        int32_t* load, int32_t* counts, int32_t* offsets, int32_t* perm_token,
+                        int32_t* perm_slot, int32_t* slot_dest, void* x_perm, void* ws,
+                        cudaStream_t stream) {
+    MOE_TRY(check_cfg(cfg));
+    const moe_config& c = *cfg;
+    if (c.T == 0) return MOE_OK;
+    if (!topk_idx || !load || !counts || !offsets || !perm_token || !perm_slot || !slot_dest)
+        return MOE_ERR_INVALID_ARG;
+    if (x_perm && !x) return MOE_ERR_INVALID_ARG;
+    if (!ws) return MOE_ERR_WORKSPACE;
+    const void* ptrs[] = {topk_idx, x, load, counts, offsets, perm_token, perm_slot, slot_dest,
+                          x_perm, ws};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    const WsLayout L = ws_layout(c);
+    return dispatch_impl(c, topk_idx, x, load, counts, offsets, perm_token, perm_slot, slot_dest,
+                         x_perm, at<int32_t>(ws, L.blockcnt), at<int32_t>(ws, L.blockoff), nullptr,
+                         stream);
+}
+
+moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                          const moe_expert_weights* routed, const moe_expert_weights* shared,
+                          const void* x, const float* topk_w, const int32_t* perm_token,
+                          const int32_t* perm_slot, float* y, void* ws, cudaStream_t stream) {
+    MOE_TRY(check_cfg(cfg));
+    const moe_config& c = *cfg;
+    if (c.T == 0) return MOE_OK;
+    if (!x_perm || !offsets || !topk_w || !perm_token || !perm_slot || !y) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_weights(c, routed));
+    if (c.has_shared) {
+        if (!x) return MOE_ERR_INVALID_ARG;
+        MOE_TRY(check_weights(c, shared));
+    }
+    if (!ws) return MOE_ERR_WORKSPACE;
+    const void* ptrs[] = {x_perm, offsets, x, topk_w, perm_token, perm_slot, y, ws};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    const WsLayout L = ws_layout(c);
+    return ffn_impl(c, x_perm, offsets, *routed, shared, x, topk_w, perm_token, perm_slot, y,
+                    at<int32_t>(ws, L.mtile), false, at<int32_t>(ws, L.shared_tab),
+                    at<__nv_bfloat16>(ws, L.h), at<__nv_bfloat16>(ws, L.hs), stream);
+}
+
+moe_status moe_combine(const moe_config* cfg, const void* x, const float* y,
+                       const int32_t* slot_dest, void* out, cudaStream_t stream) {
+    MOE_TRY(check_cfg(cfg));
+    const moe_config& c = *cfg;
+    if (c.T == 0) return MOE_OK;
+    if (!y || !slot_dest || !out || (c.add_residual && !x)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y) || !aligned16(slot_dest) || !aligned16(out))
+        return MOE_ERR_MISALIGNED;
+    return combine_impl(c, x, y, slot_dest, out, stream);
+}
+
+moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate,
+                       const float* gate_bias, const moe_expert_weights* routed,
+                       const moe_expert_weights* shared, void* out, int32_t* topk_idx,
+                       float* topk_w, int32_t* load, void* ws, size_t ws_bytes,
+                       cudaStream_t stream) {
+    MOE_TRY(check_cfg(cfg));
+    const moe_config& c = *cfg;
+    if (c.T == 0) return MOE_OK;
+    if (!x || !W_gate || !out) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_weights(c, routed));
+    if (c.has_shared) MOE_TRY(check_weights(c, shared));
+    const WsLayout L = ws_layout(c);
+    if (!ws || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    const void* ptrs[] = {x, W_gate, gate_bias, out, topk_idx, topk_w, load, ws};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    int32_t* idx = topk_idx ? topk_idx : at<int32_t>(ws, L.idx);
+    float* w = topk_w ? topk_w : at<float>(ws, L.w);
+    int32_t* ld = load ? load : at<int32_t>(ws, L.load);
+    int32_t* offsets = at<int32_t>(ws, L.offsets);
+    int32_t* perm_token = at<int32_t>(ws, L.perm_token);
+    int32_t* perm_slot = at<int32_t>(ws, L.perm_slot);
+    int32_t* slot_dest = at<int32_t>(ws, L.slot_dest);
+    void* x_perm = at<void>(ws, L.x_perm);
+    float* y = at<float>(ws, L.y);
+    int32_t* mtile = at<int32_t>(ws, L.mtile);
+    MOE_TRY(route_impl(c, x, W_gate, gate_bias, at<float>(ws, L.logits), idx, w, stream));
+    MOE_TRY(dispatch_impl(c, idx, x, ld, at<int32_t>(ws, L.counts), offsets, perm_token, perm_slot,
+                          slot_dest, x_perm, at<int32_t>(ws, L.blockcnt),
+                          at<int32_t>(ws, L.blockoff), mtile, stream));
+    MOE_TRY(ffn_impl(c, x_perm, offsets, *routed, shared, x, w, perm_token, perm_slot, y, mtile,
+                     true, at<int32_t>(ws, L.shared_tab), at<__nv_bfloat16>(ws, L.h),
+                     at<__nv_bfloat16>(ws, L.hs), stream));
+    return combine_impl(c, x, y, slot_dest, out, stream);
+}
+
+size_t moe_grouped_gemm_ws_size(int32_t G) {
+    if (G < 1 || G > 1024) return 0;
+    return (size_t)(G + 1) * 4;
+}
+
+moe_status moe_grouped_gemm(const void* A, int64_t a_rows, const void* B, int32_t G, int32_t N,
+                            int32_t K, const int32_t* row_offsets, float* D, void* ws,
+                            cudaStream_t stream) {
+    if (!A || !B || !row_offsets || !D) return MOE_ERR_INVALID_ARG;
+    if (G < 1 || G > 1024 || N < 64 || N % 64 != 0 || K < 64 || K % 64 != 0 || a_rows < 0 ||
+        a_rows >= (1ll << 31) || (int64_t)G * N >= (1ll << 31))
+        return MOE_ERR_INVALID_ARG;
+    if (!ws) return MOE_ERR_WORKSPACE;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(row_offsets) || !aligned16(D) || !aligned16(ws))
+        return MOE_ERR_MISALIGNED;
+    if (a_rows == 0) return MOE_OK;
+    int32_t* mtile = static_cast<int32_t*>(ws);
+    MOE_LAUNCH("mtile_table", stream,
+               mtile_table_kernel<<<1, 1024, 0, stream>>>(row_offsets, G, mtile));
+    return launch_gemm<EPI_F32>(A, a_rows, K, B, (int64_t)G * N, N, G, N, row_offsets, mtile, D, N,
+                                nullptr, nullptr, nullptr, nullptr, 1, stream);
+}
+
+moe_status moe_load_report(const int32_t* load_host, int32_t E, int32_t D, int32_t* assign,
+                           int64_t* dev_load, double* imbalance) {
+    if (!load_host || !assign || !dev_load || !imbalance || E < 1 || D < 1)
+        return MOE_ERR_INVALID_ARG;
+    int32_t mx = load_host[0], mn = load_host[0];
+    for (int e = 1; e < E; ++e) {
+        mx = std::max(mx, load_host[e]);
+        mn = std::min(mn, load_host[e]);
+    }
+    *imbalance = (double)mx / ((double)mn + 1e-6);
+    std::vector<int> order(E);
+    std::iota(order.begin(), order.end(), 0);
+    std::stable_sort(order.begin(), order.end(),
+                     [&](int a, int b) { return load_host[a] > load_host[b]; });
+    std::fill(dev_load, dev_load + D, 0);
+    for (int e : order) {
+        const int dv = (int)(std::min_element(dev_load, dev_load + D) - dev_load);
+        assign[e] = dv;
+        dev_load[dv] += load_host[e];
+    }
+    return MOE_OK;
+}
+
+moe_status moe_last_device_status(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_dev_error, sizeof(v)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (v) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(zero)) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    if (v & DEVERR_TIMEOUT) return MOE_ERR_TIMEOUT;
+    if (v & DEVERR_INDEX) return MOE_ERR_DEVICE_INDEX;
+    return MOE_OK;
+}
+
+const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+        case MOE_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+        case MOE_ERR_DEVICE_INDEX: return "expert id out of range in device data";
+    }
+    return "unknown status";
+}
+
+moe_status moe_profile_begin(void) {
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    g_prof.recs.clear();
+    g_prof.used = 0;
+    g_prof.on = true;
+    return MOE_OK;
+}
+
+int32_t moe_profile_end(moe_kernel_stat* stats, int32_t max_stats) {
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    g_prof.on = false;
+    std::vector<moe_kernel_stat> agg;
+    for (const ProfRec& r : g_prof.recs) {
+        if (cudaEventSynchronize(r.b) != cudaSuccess) return -1;
+        float ms = 0.0f;
+        if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) return -1;
+        auto it = std::find_if(agg.begin(), agg.end(),
+                               [&](const moe_kernel_stat& s) { return std::strcmp(s.name, r.name) == 0; });
+        if (it == agg.end()) agg.push_back({r.name, 1, (double)ms});
+        else {
+            it->launches += 1;
+            it->total_ms += ms;
+        }
+    }
+    g_prof.recs.clear();
+    g_prof.used = 0;
+    if (stats)
+        for (int i = 0; i < (int)agg.size() && i < max_stats; ++i) stats[i] = agg[i];
+    return (int32_t)agg.size();
+}
+
+uint64_t moe_kernel_launch_count(void) { return g_launches.load(); }
+
+moe_status moe_selftest_wait_timeout(int64_t budget_cycles, cudaStream_t stream) {
+    if (budget_cycles < 0 || budget_cycles > kWaitBudgetCycles) return MOE_ERR_INVALID_ARG;
+    MOE_LAUNCH("selftest_wait", stream, selftest_wait_kernel<<<1, 32, 0, stream>>>(budget_cycles));
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,37 @@
+"""MoELayer: holds a layer's configuration, weights and workspace (torch-owned
+device memory) and runs the whole forward through moe_forward."""
+
+import torch
+
+from . import api
+
+
+class MoELayer:
+    """One MoE layer. Tensors (all on one CUDA device, contiguous):
+    W_gate [d, E] fp32, gate_bias [E] fp32 or None, w1 [E, N1, d], b1 [E, N1] or None,
+    w2 [E, d, F] (not for LINEAR), b2 [E, d] or None, shared = (w1, b1, w2, b2) or None.
+    The workspace is sized for up to `max_tokens` tokens per call."""
+
+    def __init__(self, cfg, W_gate, gate_bias, w1, b1=None, w2=None, b2=None, shared=None):
+        self.cfg = cfg
+        self._keep = [W_gate, gate_bias, w1, b1, w2, b2, shared]
+        self.W_gate, self.gate_bias = W_gate, gate_bias
+        self.routed = api.weights(w1, b1, w2, b2)
+        self.shared = api.weights(*shared) if shared is not None else None
+        self.ws = torch.empty(api.workspace_size(cfg), dtype=torch.uint8, device=w1.device)
+
+    def config(self, T):
+        c = api.MoeConfig()
+        for f, _ in api.MoeConfig._fields_:
+            setattr(c, f, getattr(self.cfg, f))
+        c.T = T
+        return c
+
+    def __call__(self, x, out=None, topk_idx=None, topk_w=None, load=None, stream=None):
+        T = x.shape[0]
+        if T > self.cfg.T:
+            raise ValueError(f"{T} tokens exceed the layer's max_tokens {self.cfg.T}")
+        out = torch.empty_like(x) if out is None else out
+        api.forward(self.config(T), x, self.W_gate, self.gate_bias, self.routed, self.shared,
+                    out, self.ws, topk_idx=topk_idx, topk_w=topk_w, load=load, stream=stream)
+        return out
