@@ -189,6 +189,27 @@ moe_status moe_grouped_gemm(const void* A, int64_t a_rows, const void* B, int32_
                             int32_t N, int32_t K, const int32_t* row_offsets, float* D,
                             void* ws, cudaStream_t stream);
 
+/* moe_dispatch without a workspace: the pages have no counterpart to this entry
+ * point; it exists for callers that cannot allocate device memory when they call
+ * the layer, for example a plugin running inside a host framework that owns all
+ * device memory and exposes no allocator to it, or a latency-critical loop that
+ * must not take the implicit device synchronisation of cudaMalloc.
+ * Arguments and outputs are those of moe_dispatch minus `ws`; the caller still
+ * passes every input and output buffer. The dispatch scratch (2 * ceil(T/256) * E
+ * int32) lives in a 1 MiB static device array inside the library, held on every
+ * GPU that loads the library until the process exits. Problems with
+ * ceil(T/256) * E > 131072 are rejected with MOE_ERR_WORKSPACE (with E = 1024 that
+ * allows T <= 32768 tokens; with E = 256, T <= 131072). It calls no cudaMalloc, cudaFree or
+ * other allocating routine. Its first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress, with that device current), so make that
+ * first call before any stream capture. All calls share the one array: calls that
+ * overlap on the GPU (different streams, or different host threads) race on it and
+ * must be ordered by the caller. */
+moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_idx, const void* x,
+                                int32_t* load, int32_t* counts, int32_t* offsets,
+                                int32_t* perm_token, int32_t* perm_slot, int32_t* slot_dest,
+                                void* x_perm, cudaStream_t stream);
+
 /* Host-only load report [adv12 3.3 EPLB, 4.2 expert_imbalance, 4.3 eplb_rebalance]:
  * imbalance = max(load) / (min(load) + 1e-6); LPT placement of the E experts on D
  * devices (heaviest first, equal loads by ascending id, each to the currently

@@ -163,3 +163,14 @@ def kernel_launch_count():
 def selftest_wait_timeout(budget_cycles, stream=None):
     _check(C.load().moe_selftest_wait_timeout(int(budget_cycles), _stream(stream)),
            "moe_selftest_wait_timeout")
+
+
+def dispatch_noalloc(cfg, topk_idx, x, load, counts, offsets, perm_token, perm_slot, slot_dest,
+                     x_perm, stream=None):
+    """moe_dispatch without a workspace (scratch in the library's static device array)."""
+    fn = C.load().moe_dispatch_noalloc
+    fn.restype = ctypes.c_int32
+    fn.argtypes = [ctypes.POINTER(MoeConfig)] + [ctypes.c_void_p] * 10
+    _check(fn(ctypes.byref(cfg), _ptr(topk_idx), _ptr(x), _ptr(load), _ptr(counts),
+              _ptr(offsets), _ptr(perm_token), _ptr(perm_slot), _ptr(slot_dest), _ptr(x_perm),
+              _stream(stream)), "moe_dispatch_noalloc")

@@ -659,3 +659,61 @@ moe_status moe_selftest_wait_timeout(int64_t budget_cycles, cudaStream_t stream)
 }
 
 }  // extern "C"
+
+// =====================================================================================
+// moe_dispatch_noalloc: moe_dispatch with its scratch in a fixed static device array
+// =====================================================================================
+// The dispatch kernels need two tables of ceil(T/256) x E ints (per-chunk counts and
+// per-chunk rank bases). Here they live in this file-scope array instead of a caller
+// workspace. Every GPU that loads the library holds the array until the process
+// exits. Every word the kernels read is written earlier in the same call, so nothing
+// has to be cleared between calls.
+namespace {
+constexpr long long kNoallocScratchInts = 1ll << 18;   // 1 MiB
+}
+static __device__ __align__(256) int32_t g_noalloc_scratch[kNoallocScratchInts];
+
+namespace {
+std::mutex g_noalloc_mu;
+int32_t* g_noalloc_ptr[64] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once per
+// device with that device current (host code cannot use the symbol itself as a
+// device pointer).
+moe_status noalloc_scratch(int32_t** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+        g_noalloc_ptr[dev] = static_cast<int32_t*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return MOE_OK;
+}
+}  // namespace
+
+extern "C" moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_idx,
+                                           const void* x, int32_t* load, int32_t* counts,
+                                           int32_t* offsets, int32_t* perm_token,
+                                           int32_t* perm_slot, int32_t* slot_dest, void* x_perm,
+                                           cudaStream_t stream) {
+    MOE_TRY(check_cfg(cfg));
+    const moe_config& c = *cfg;
+    if (c.T == 0) return MOE_OK;
+    if (!topk_idx || !load || !counts || !offsets || !perm_token || !perm_slot || !slot_dest)
+        return MOE_ERR_INVALID_ARG;
+    if (x_perm && !x) return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {topk_idx, x, load, counts, offsets, perm_token, perm_slot, slot_dest,
+                          x_perm};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    const long long nb = ((long long)c.T + kDispTok - 1) / kDispTok;
+    if (2 * nb * (long long)c.E > kNoallocScratchInts) return MOE_ERR_WORKSPACE;
+    int32_t* scratch = nullptr;
+    MOE_TRY(noalloc_scratch(&scratch));
+    return dispatch_impl(c, topk_idx, x, load, counts, offsets, perm_token, perm_slot, slot_dest,
+                         x_perm, scratch, scratch + nb * c.E, nullptr, stream);
+}
