@@ -150,18 +150,32 @@ def kernel_algorithmic_cost(wl, name, P, touched):
     return 0.0, 0.0
 
 
-def kernel_sources_hash():
-    import glob
+KERNEL_FILES = {
+    "grouped_gemm": ["grouped_gemm.cuh", "common.cuh"],
+    "router": ["router.cuh", "common.cuh"],
+    "topk": ["router.cuh", "common.cuh"],
+    "dispatch": ["dispatch.cuh", "common.cuh"],
+    "gather": ["dispatch.cuh", "common.cuh"],
+    "combine": ["combine.cuh", "common.cuh"],
+    "linear": ["combine.cuh", "common.cuh"],
+}
+
+
+def kernel_sources_hash(kernel):
+    """Hash of the source files that define `kernel` (by name prefix)."""
+    files = next((v for k, v in KERNEL_FILES.items() if kernel.startswith(k)), None)
+    if files is None:
+        return None
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "top_routing_expert_renorm_b300", "csrc", "*"))):
-        with open(p, "rb") as f:
+    for fn in files:
+        with open(os.path.join(ROOT, "top_routing_expert_renorm_b300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel, workload):
-    """Per-launch DRAM bytes from a committed ncu summary, when it was taken on the
-    current kernel sources; else None."""
+    """Per-launch DRAM bytes (read + write) from a committed ncu summary, if that
+    summary was taken on the kernel's current sources; else None."""
     path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.txt")
     if not os.path.exists(path):
         return None
@@ -171,10 +185,10 @@ def recorded_traffic(kernel, workload):
             if ":" in line:
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
-    if vals.get("kernel_sources_sha") != kernel_sources_hash():
+    if vals.get("kernel_sources_sha") != kernel_sources_hash(kernel):
         return None
     try:
-        return float(vals["dram_bytes_per_step"])
+        return float(vals["dram_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
 
@@ -356,7 +370,7 @@ def run_ours(args, wl):
         roof = {"bound": "hbm", "achieved": by / t_step_s / 1e9, "peak": hbm, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     tr = recorded_traffic(dname, wl.name)
-    roof["traffic"] = None if tr is None else tr / (dlaunch / K)
+    roof["traffic"] = tr
     roof["kernel"] = dname
     roof["launches_per_step"] = dlaunch / K
     roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
