@@ -138,8 +138,14 @@ def kernel_algorithmic_cost(wl, name, P, touched):
         return 2.0 * P * F * d, touched * d * F * 2 + P * F * 2 + P * d * 4
     if name == "grouped_gemm_f32":        # shared expert down projection
         return 2.0 * T * F * d, d * F * 2 + T * F * 2 + T * d * 4
-    if name.startswith("router_logits"):
+    if name.startswith("router_logits") or name == "router_splitk":
         return 2.0 * T * d * E, T * d * es + d * E * 4 + T * E * 4
+    if name == "router_gemm_tc":          # algorithmic: the fp32 gate GEMM it computes
+        return 2.0 * T * d * E, T * d * es + 3 * d * E * 2 + T * 3 * E * 4
+    if name == "gate_split":
+        return 0.0, d * E * 4 + 3 * d * E * 2
+    if name == "topk_renorm":
+        return 0.0, T * E * 4 + T * wl.k * 8
     if name.startswith("combine"):
         rows = P + (T if wl.has_shared else 0)
         return 0.0, rows * d * 4 + T * d * es * (2 if wl.add_residual else 1) + T * wl.k * 4
@@ -152,6 +158,8 @@ def kernel_algorithmic_cost(wl, name, P, touched):
 
 KERNEL_FILES = {
     "grouped_gemm": ["grouped_gemm.cuh", "common.cuh"],
+    "router_gemm_tc": ["grouped_gemm.cuh", "common.cuh"],
+    "gate_split": ["router.cuh", "common.cuh"],
     "router": ["router.cuh", "common.cuh"],
     "topk": ["router.cuh", "common.cuh"],
     "dispatch": ["dispatch.cuh", "common.cuh"],

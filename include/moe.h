@@ -112,13 +112,16 @@ int32_t moe_capacity(const moe_config* cfg);
  *   x         [T, d]  act_dtype
  *   W_gate    [d, E]  fp32 (E contiguous)
  *   gate_bias [E]     fp32, nullable (added to the logits)
- *   logits    [T, E]  fp32 output, nullable (then kept in the workspace)
+ *   logits    [T, E]  fp32 output, nullable
  *   topk_idx  [T, k]  int32 output: experts ordered by logit descending, ties to
  *                     the lower expert id
  *   topk_w    [T, k]  fp32 output: exp(L_j - L_0) / sum_j' exp(L_j' - L_0) over the
  *                     k kept logits = softmax then divide by the kept sum
- *   ws        workspace (required when logits is NULL)
- * Logits are fp32 sums of fp32 products; selection is bit-reproducible given them. */
+ *   ws        workspace (required)
+ * Logits are fp32 sums of exact fp32 products x_i * W_gate[i, e] (bf16 activations with
+ * many tokens run on the tensor cores against W_gate split exactly into three bf16
+ * terms); partial sums are added in a fixed order, so results are reproducible run to
+ * run, and selection is bit-reproducible given the logits. */
 moe_status moe_route(const moe_config* cfg, const void* x, const float* W_gate,
                      const float* gate_bias, float* logits, int32_t* topk_idx, float* topk_w,
                      void* ws, cudaStream_t stream);

@@ -40,8 +40,8 @@ __global__ void __launch_bounds__(256) linear_expert_kernel(
 }
 
 // ---- combine: out[t] = (res ? x[t] : 0) + sum_j kept y[slot_dest[t,j]] (+ y_shared[t]) ----
-// One CTA per token, 4 columns per thread (16-byte loads of y). The k slot rows are
-// summed in slot order, so the result does not depend on scheduling.
+// The k slot rows are summed in slot order, so the result does not depend on
+// scheduling.
 template <typename OT>
 __device__ __forceinline__ void load4(const OT* p, float4& v);
 template <>
@@ -70,38 +70,51 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, const fl
     *reinterpret_cast<uint2*>(p) = u;
 }
 
+// One warp per token (grid-stride), each lane owning two float4 column groups per
+// pass, so a warp keeps 2 x k row loads in flight. slot_dest of the token is read
+// once by lanes 0..k-1 and broadcast by shuffles.
+__device__ __forceinline__ void add4(float4& a, const float4& v) {
+    a.x += v.x;
+    a.y += v.y;
+    a.z += v.z;
+    a.w += v.w;
+}
+
 template <typename OT>
 __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ x,
                                                       const float* __restrict__ y,
                                                       const int* __restrict__ slot_dest,
                                                       const float* __restrict__ y_shared,
-                                                      OT* __restrict__ out, int d, int k,
+                                                      OT* __restrict__ out, int T, int d, int k,
                                                       int add_residual) {
-    __shared__ int s_dest[32];
-    const long long t = blockIdx.x;
-    if (threadIdx.x < k) s_dest[threadIdx.x] = slot_dest[t * k + threadIdx.x];
-    __syncthreads();
-    for (int c = threadIdx.x * 4; c < d; c += blockDim.x * 4) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (add_residual) load4<OT>(x + t * d + c, acc);
-        for (int j = 0; j < k; ++j) {
-            const int r = s_dest[j];
-            if (r >= 0) {
-                const float4 v = *reinterpret_cast<const float4*>(y + (long long)r * d + c);
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long t = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T;
+         t += warps) {
+        const int mydest = lane < k ? slot_dest[t * k + lane] : -1;
+        for (int c0 = 0; c0 < d; c0 += 256) {
+            const int ca = c0 + lane * 4, cb = c0 + 128 + lane * 4;
+            const bool va = ca < d, vb = cb < d;
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+            if (add_residual) {
+                if (va) load4<OT>(x + t * d + ca, a);
+                if (vb) load4<OT>(x + t * d + cb, b);
             }
+            for (int j = 0; j < k; ++j) {
+                const int r = __shfl_sync(0xffffffffu, mydest, j);
+                if (r < 0) continue;
+                const float* yr = y + (long long)r * d;
+                if (va) add4(a, *reinterpret_cast<const float4*>(yr + ca));
+                if (vb) add4(b, *reinterpret_cast<const float4*>(yr + cb));
+            }
+            if (y_shared) {
+                const float* ys = y_shared + t * d;
+                if (va) add4(a, *reinterpret_cast<const float4*>(ys + ca));
+                if (vb) add4(b, *reinterpret_cast<const float4*>(ys + cb));
+            }
+            if (va) store4<OT>(out + t * d + ca, a);
+            if (vb) store4<OT>(out + t * d + cb, b);
         }
-        if (y_shared) {
-            const float4 v = *reinterpret_cast<const float4*>(y_shared + t * d + c);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
-        }
-        store4<OT>(out + t * d + c, acc);
     }
 }
 

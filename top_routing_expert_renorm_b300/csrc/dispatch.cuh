@@ -162,7 +162,8 @@ __global__ void __launch_bounds__(256) dispatch_rank_kernel(
 }
 
 // ---- x_perm[p] = x[perm_token[p]] for p < P = offsets[E]; one warp per row -----------
-// 16-byte vector copies; row_bytes is a multiple of 16.
+// 16-byte vector copies, four loads in flight per lane before their stores;
+// row_bytes is a multiple of 16.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restrict__ x,
                                                           const int* __restrict__ perm_token,
                                                           const int* __restrict__ total_rows,
@@ -170,12 +171,21 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
                                                           int row_bytes) {
     const int P = *total_rows;
     const int lane = threadIdx.x & 31;
-    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-    for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < P;
-         r += warps) {
-        const uint4* src = reinterpret_cast<const uint4*>(x + (long long)perm_token[r] * row_bytes);
-        uint4* dst = reinterpret_cast<uint4*>(x_perm + r * row_bytes);
-        for (int c = lane; c < row_bytes / 16; c += 32) dst[c] = __ldg(src + c);
+    const int nvec = row_bytes / 16;
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < P; r += warps) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)perm_token[r] * row_bytes);
+        uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * row_bytes);
+        int c = lane;
+        for (; c + 96 < nvec; c += 128) {
+            const uint4 a = __ldg(src + c), b = __ldg(src + c + 32), d = __ldg(src + c + 64),
+                        e = __ldg(src + c + 96);
+            dst[c] = a;
+            dst[c + 32] = b;
+            dst[c + 64] = d;
+            dst[c + 96] = e;
+        }
+        for (; c < nvec; c += 32) dst[c] = __ldg(src + c);
     }
 }
 

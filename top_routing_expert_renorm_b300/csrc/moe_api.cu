@@ -178,6 +178,49 @@ int32_t capacity_of(const moe_config& c) {
 // ---------------------------------------------------------------------------------
 // workspace layout (256-byte aligned regions, identical for every entry point)
 // ---------------------------------------------------------------------------------
+// Router scratch: raw partial logits (and, on the tensor-core path, the split gate
+// weights and the one-group tables). Paths: fp32 activations -> CUDA-core GEMM;
+// bf16 activations with T >= kRouterTensorMinT -> exact 3-way bf16 split on the tensor
+// cores; fewer bf16 tokens -> split-K CUDA-core kernel.
+constexpr int kRouterTensorMinT = 256;
+
+struct RouterPlan {
+    int path;                 // 1 fp32 CUDA core, 2 tensor cores, 3 split-K
+    int Ep;                   // padded experts per term (path 2)
+    int n_parts;
+    long long part_stride, row_stride;
+    size_t bg_bytes, d_bytes, scratch_bytes;
+};
+
+size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
+
+RouterPlan router_plan(const moe_config& c) {
+    RouterPlan r{};
+    const size_t T = (size_t)c.T, E = (size_t)c.E, d = (size_t)c.d;
+    if (c.act_dtype == MOE_F32) {
+        r.path = 1;
+        r.n_parts = 1;
+        r.row_stride = c.E;
+        r.scratch_bytes = al256(T * E * 4);
+    } else if (c.T >= kRouterTensorMinT) {
+        r.path = 2;
+        r.Ep = (c.E + kRouterPad - 1) / kRouterPad * kRouterPad;
+        r.n_parts = 3;
+        r.part_stride = r.Ep;
+        r.row_stride = 3ll * r.Ep;
+        r.bg_bytes = al256(3 * (size_t)r.Ep * d * 2);
+        r.d_bytes = al256(T * 3 * (size_t)r.Ep * 4);
+        r.scratch_bytes = r.bg_bytes + r.d_bytes + 256;
+    } else {
+        r.path = 3;
+        r.n_parts = (c.d + RS_K - 1) / RS_K;
+        r.part_stride = (long long)c.T * c.E;
+        r.row_stride = c.E;
+        r.scratch_bytes = al256((size_t)r.n_parts * T * E * 4);
+    }
+    return r;
+}
+
 struct WsLayout {
     size_t logits, idx, w, load, counts, offsets, blockcnt, blockoff, perm_token, perm_slot,
         slot_dest, x_perm, mtile, shared_tab, h, hs, y, total;
@@ -196,7 +239,7 @@ WsLayout ws_layout(const moe_config& c) {
     const size_t Pmax = T * k;
     const size_t nb = std::max<size_t>(1, (T + kDispTok - 1) / kDispTok);
     const size_t es = c.act_dtype == MOE_BF16 ? 2 : 4;
-    L.logits = take(T * E * 4);
+    L.logits = take(router_plan(c).scratch_bytes);   // router scratch
     L.idx = take(Pmax * 4);
     L.w = take(Pmax * 4);
     L.load = take(E * 4);
@@ -225,24 +268,6 @@ P* at(void* ws, size_t off) {
 // ---------------------------------------------------------------------------------
 // stage implementations (arguments already validated)
 // ---------------------------------------------------------------------------------
-moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const float* bias,
-                      float* logits, int32_t* idx, float* w, cudaStream_t s) {
-    const int T = c.T, E = c.E, d = c.d, k = c.top_k;
-    const dim3 grid((T + RT_BM - 1) / RT_BM, (E + RT_BN - 1) / RT_BN);
-    if (c.act_dtype == MOE_F32) {
-        MOE_LAUNCH("router_logits_f32", s,
-                   router_logits_kernel<float><<<grid, 256, 0, s>>>(
-                       static_cast<const float*>(x), Wg, bias, logits, T, d, E));
-    } else {
-        MOE_LAUNCH("router_logits_bf16", s,
-                   router_logits_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-                       static_cast<const __nv_bfloat16*>(x), Wg, bias, logits, T, d, E));
-    }
-    MOE_LAUNCH("topk_renorm", s,
-               topk_renorm_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, k, idx, w));
-    return MOE_OK;
-}
-
 moe_status dispatch_impl(const moe_config& c, const int32_t* idx, const void* x, int32_t* load,
                          int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* perm_slot,
                          int32_t* slot_dest, void* x_perm, int32_t* blockcnt, int32_t* blockoff,
@@ -285,7 +310,7 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
                        int b_rows_per_group, int G, int N, const int32_t* row_offsets,
                        const int32_t* mtile_offsets, void* out, long long ld_out, const float* bias,
                        const float* topk_w, const int32_t* perm_token, const int32_t* perm_slot,
-                       int top_k, cudaStream_t s) {
+                       int top_k, cudaStream_t s, const char* name = nullptr) {
     if (a_rows <= 0 || G <= 0) return MOE_OK;
     if (G > GM_MAX_GROUPS) return MOE_ERR_UNSUPPORTED;
     CUtensorMap ta, tb;
@@ -320,7 +345,7 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
         if (attr_err[dev] != cudaSuccess) return MOE_ERR_CUDA;
     }
     const int grid = num_sms();
-    MOE_LAUNCH(gemm_name<EPI>(), s,
+    MOE_LAUNCH(name ? name : gemm_name<EPI>(), s,
                grouped_gemm_kernel<EPI><<<grid, GM_THREADS, smem, s>>>(ta, tb, p));
     return MOE_OK;
 }
@@ -330,6 +355,40 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
         const moe_status st_ = (expr);      \
         if (st_ != MOE_OK) return st_;      \
     } while (0)
+
+moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const float* bias,
+                      float* logits, int32_t* idx, float* w, void* scratch, cudaStream_t s) {
+    const int T = c.T, E = c.E, d = c.d, k = c.top_k;
+    const RouterPlan rp = router_plan(c);
+    float* parts = static_cast<float*>(scratch);
+    if (rp.path == 1) {
+        const dim3 grid((T + RT_BM - 1) / RT_BM, (E + RT_BN - 1) / RT_BN);
+        MOE_LAUNCH("router_logits_f32", s,
+                   router_logits_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x),
+                                                                    Wg, parts, T, d, E));
+    } else if (rp.path == 2) {
+        __nv_bfloat16* Bg = static_cast<__nv_bfloat16*>(scratch);
+        parts = reinterpret_cast<float*>(static_cast<char*>(scratch) + rp.bg_bytes);
+        int32_t* tables =
+            reinterpret_cast<int32_t*>(static_cast<char*>(scratch) + rp.bg_bytes + rp.d_bytes);
+        const dim3 grid((d + 31) / 32, rp.Ep / 32);
+        MOE_LAUNCH("gate_split", s,
+                   gate_split_kernel<<<grid, 256, 0, s>>>(Wg, d, E, rp.Ep, Bg, T, tables));
+        MOE_TRY(launch_gemm<EPI_F32>(x, T, d, Bg, 3ll * rp.Ep, 3 * rp.Ep, 1, 3 * rp.Ep, tables,
+                                     tables + 2, parts, 3ll * rp.Ep, nullptr, nullptr, nullptr,
+                                     nullptr, 1, s, "router_gemm_tc"));
+    } else {
+        const dim3 grid((E + RS_E - 1) / RS_E, rp.n_parts, (T + RS_T - 1) / RS_T);
+        MOE_LAUNCH("router_splitk", s,
+                   router_splitk_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
+                                                             Wg, parts, T, d, E));
+    }
+    MOE_LAUNCH("topk_renorm", s,
+               topk_renorm_kernel<<<(T + 7) / 8, 256, 0, s>>>(parts, rp.n_parts, rp.part_stride,
+                                                              rp.row_stride, bias, logits, T, E,
+                                                              k, idx, w));
+    return MOE_OK;
+}
 
 moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offsets,
                     const moe_expert_weights& R, const moe_expert_weights* S, const void* x,
@@ -395,18 +454,18 @@ moe_status combine_impl(const moe_config& c, const void* x, const float* y,
     const int T = c.T, d = c.d, k = c.top_k;
     const long long Pmax = (long long)T * k;
     const float* ysh = c.has_shared ? y + Pmax * d : nullptr;
-    int threads = std::min(256, ((d / 4 + 31) / 32) * 32);
-    threads = std::max(threads, 32);
+    const int blocks = (int)std::max<long long>(1, std::min<long long>((T + 7) / 8,
+                                                                       (long long)num_sms() * 8));
     if (c.act_dtype == MOE_F32)
         MOE_LAUNCH("combine_f32", s,
-                   combine_kernel<float><<<T, threads, 0, s>>>(
-                       static_cast<const float*>(x), y, slot_dest, ysh, static_cast<float*>(out), d,
-                       k, c.add_residual));
+                   combine_kernel<float><<<blocks, 256, 0, s>>>(
+                       static_cast<const float*>(x), y, slot_dest, ysh, static_cast<float*>(out), T,
+                       d, k, c.add_residual));
     else
         MOE_LAUNCH("combine_bf16", s,
-                   combine_kernel<__nv_bfloat16><<<T, threads, 0, s>>>(
+                   combine_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
                        static_cast<const __nv_bfloat16*>(x), y, slot_dest, ysh,
-                       static_cast<__nv_bfloat16*>(out), d, k, c.add_residual));
+                       static_cast<__nv_bfloat16*>(out), T, d, k, c.add_residual));
     return MOE_OK;
 }
 
@@ -447,12 +506,12 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* W_gate,
     const moe_config& c = *cfg;
     if (c.T == 0) return MOE_OK;
     if (!x || !W_gate || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
-    if (!logits && !ws) return MOE_ERR_WORKSPACE;
+    if (!ws) return MOE_ERR_WORKSPACE;
     if (!aligned16(x) || !aligned16(W_gate) || !aligned16(gate_bias) || !aligned16(logits) ||
         !aligned16(topk_idx) || !aligned16(topk_w) || !aligned16(ws))
         return MOE_ERR_MISALIGNED;
-    float* L = logits ? logits : at<float>(ws, ws_layout(c).logits);
-    return route_impl(c, x, W_gate, gate_bias, L, topk_idx, topk_w, stream);
+    return route_impl(c, x, W_gate, gate_bias, logits, topk_idx, topk_w,
+                      at<void>(ws, ws_layout(c).logits), stream);
 }
 
 moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const void* x,
@@ -536,7 +595,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate
     void* x_perm = at<void>(ws, L.x_perm);
     float* y = at<float>(ws, L.y);
     int32_t* mtile = at<int32_t>(ws, L.mtile);
-    MOE_TRY(route_impl(c, x, W_gate, gate_bias, at<float>(ws, L.logits), idx, w, stream));
+    MOE_TRY(route_impl(c, x, W_gate, gate_bias, nullptr, idx, w, at<void>(ws, L.logits), stream));
     MOE_TRY(dispatch_impl(c, idx, x, ld, at<int32_t>(ws, L.counts), offsets, perm_token, perm_slot,
                           slot_dest, x_perm, at<int32_t>(ws, L.blockcnt),
                           at<int32_t>(ws, L.blockoff), mtile, stream));

@@ -7,7 +7,11 @@
 
 namespace moe {
 
-// ---- logits = x * W_gate (+ bias), fp32 CUDA-core GEMM -------------------------------
+// Every router path writes raw partial sums of x * W_gate; topk_renorm_kernel adds
+// the parts in a fixed order (plus the bias) to form the fp32 logits, so the
+// result does not depend on scheduling.
+
+// ---- path 1: x * W_gate, fp32 CUDA-core GEMM (fp32 activations) ------------------------
 // CTA tile 64 tokens x 64 experts, K step 16, 256 threads with a 4x4 register tile
 // each. x is converted to fp32 on the way into shared memory (exact for bf16).
 constexpr int RT_BM = 64, RT_BN = 64, RT_BK = 16;
@@ -15,7 +19,6 @@ constexpr int RT_BM = 64, RT_BN = 64, RT_BK = 16;
 template <typename XT>
 __global__ void __launch_bounds__(256) router_logits_kernel(const XT* __restrict__ x,
                                                             const float* __restrict__ Wg,
-                                                            const float* __restrict__ bias,
                                                             float* __restrict__ logits, int T,
                                                             int d, int E) {
     __shared__ float xs[RT_BK][RT_BM + 4];
@@ -68,7 +71,104 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const XT* __restrict
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int e = e0 + tx * 4 + j;
-            if (e < E) logits[t * E + e] = acc[i][j] + (bias ? bias[e] : 0.0f);
+            if (e < E) logits[t * E + e] = acc[i][j];
+        }
+    }
+}
+
+// ---- path 2: bf16 activations, many tokens: tensor cores on an exact 3-way split ------
+// Every fp32 gate weight v is split into three bf16 terms hi + mid + lo == v exactly
+// (hi = bf16(v), mid = bf16(v - hi), lo = v - hi - mid, which has at most 8 significant
+// bits). Products of a bf16 activation with each term are exact in fp32, so running
+// x [T, d] against B = [hi; mid; lo] ([3*Ep, d], K-major) on the bf16 tensor cores with
+// fp32 accumulation gives fp32-accurate logits. This kernel transposes W_gate [d, E]
+// into that layout (32x32 tiles through shared memory) and writes the one-group
+// row / M-tile tables of the GEMM.
+constexpr int kRouterPad = 32;   // experts are padded to Ep = round_up(E, 32) per term
+
+__global__ void __launch_bounds__(256) gate_split_kernel(const float* __restrict__ Wg, int d,
+                                                         int E, int Ep,
+                                                         __nv_bfloat16* __restrict__ Bg, int T,
+                                                         int* __restrict__ tables) {
+    __shared__ float tile[32][33];
+    const int k0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
+    for (int r = ty; r < 32; r += 8) {
+        const int k = k0 + r, e = e0 + tx;
+        tile[r][tx] = (k < d && e < E) ? Wg[(long long)k * E + e] : 0.0f;
+    }
+    __syncthreads();
+    for (int r = ty; r < 32; r += 8) {
+        const int e = e0 + r, k = k0 + tx;
+        if (e >= Ep || k >= d) continue;
+        const float v = tile[tx][r];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const float r1 = v - __bfloat162float(hi);
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+        Bg[(long long)e * d + k] = hi;
+        Bg[((long long)Ep + e) * d + k] = mid;
+        Bg[(2ll * Ep + e) * d + k] = lo;
+    }
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+        tables[0] = 0;                      // row offsets of the single group
+        tables[1] = T;
+        tables[2] = 0;                      // its M-tile offsets
+        tables[3] = (T + 127) / 128;
+    }
+}
+
+// ---- path 3: bf16 activations, few tokens: split-K CUDA-core kernel --------------------
+// CTA (256 threads) = 32 experts (lane) x a 256-long K slice (warp w takes 32 of it) x
+// up to 64 tokens (blockIdx.z chunk). Each thread accumulates its 32 K values for every
+// token; the 8 warps are then summed through shared memory in a fixed order and the
+// CTA writes one partial [slice][T][E]. Wide grids keep all SMs streaming W_gate.
+constexpr int RS_E = 32, RS_K = 256, RS_T = 64;
+
+__global__ void __launch_bounds__(256) router_splitk_kernel(const __nv_bfloat16* __restrict__ x,
+                                                            const float* __restrict__ Wg,
+                                                            float* __restrict__ parts, int T,
+                                                            int d, int E) {
+    __shared__ __nv_bfloat16 xs[RS_T][RS_K];
+    __shared__ float red[8][8][RS_E + 1];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int e = blockIdx.x * RS_E + lane;
+    const int k0 = blockIdx.y * RS_K;
+    const int t0 = blockIdx.z * RS_T;
+    const int nt = min(RS_T, T - t0);
+    for (int i = threadIdx.x; i < RS_T * RS_K; i += blockDim.x) {
+        const int t = i / RS_K, kk = i % RS_K;
+        xs[t][kk] = (t < nt && k0 + kk < d) ? x[(long long)(t0 + t) * d + k0 + kk]
+                                             : __float2bfloat16_rn(0.0f);
+    }
+    __syncthreads();
+    float acc[RS_T];
+#pragma unroll
+    for (int t = 0; t < RS_T; ++t) acc[t] = 0.0f;
+    for (int i = 0; i < 32; ++i) {
+        const int kk = w * 32 + i;
+        const int k = k0 + kk;
+        const float wv = (k < d && e < E) ? Wg[(long long)k * E + e] : 0.0f;
+#pragma unroll
+        for (int t = 0; t < RS_T; ++t)
+            if (t < nt) acc[t] = fmaf(__bfloat162float(xs[t][kk]), wv, acc[t]);
+    }
+    float* out = parts + (long long)blockIdx.y * T * E;
+#pragma unroll
+    for (int c = 0; c < RS_T / 8; ++c) {
+        __syncthreads();
+#pragma unroll
+        for (int t = 0; t < 8; ++t) red[w][t][lane] = acc[c * 8 + t];
+        __syncthreads();
+        for (int i = threadIdx.x; i < 8 * RS_E; i += blockDim.x) {
+            const int t = i / RS_E, l = i % RS_E;
+            const int tt = c * 8 + t, ee = blockIdx.x * RS_E + l;
+            if (tt < nt && ee < E) {
+                float s = 0.0f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) s += red[q][t][l];
+                out[(long long)(t0 + tt) * E + ee] = s;
+            }
         }
     }
 }
@@ -81,13 +181,19 @@ __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
     return be < 0 || v > bv || (v == bv && e < be);
 }
 
-__global__ void __launch_bounds__(256) topk_renorm_kernel(const float* __restrict__ logits, int T,
+// Logit (t, e) = sum_{p < n_parts} parts[p*part_stride + t*row_stride + e] (+ bias[e]),
+// summed in part order; written to `logits` [T, E] when that is non-null.
+__global__ void __launch_bounds__(256) topk_renorm_kernel(const float* __restrict__ parts,
+                                                          int n_parts, long long part_stride,
+                                                          long long row_stride,
+                                                          const float* __restrict__ bias,
+                                                          float* __restrict__ logits, int T,
                                                           int E, int k, int* __restrict__ idx,
                                                           float* __restrict__ w) {
     const int lane = threadIdx.x & 31;
     const long long t = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
-    const float* L = logits + t * E;
+    const float* L = parts + t * row_stride;
     float v[32];
     uint32_t avail = 0;
 #pragma unroll
@@ -95,7 +201,11 @@ __global__ void __launch_bounds__(256) topk_renorm_kernel(const float* __restric
         const int e = lane + 32 * i;
         v[i] = 0.0f;
         if (e < E) {
-            v[i] = L[e];
+            float s = L[e];
+            for (int p = 1; p < n_parts; ++p) s += L[p * part_stride + e];
+            if (bias) s += bias[e];
+            v[i] = s;
+            if (logits) logits[t * E + e] = s;
             avail |= 1u << i;
         }
     }
