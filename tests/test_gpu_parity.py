@@ -36,6 +36,13 @@ SMALL = {
     "hot_expert_cap": W("hot", T=400, d=64, E=8, k=2, F=128, kind="gelu", act="bf16", cf=0.5,
                         gate_bias="hot", add_residual=True),
     "max_E_max_k": W("mx", T=64, d=64, E=1024, k=32, F=64, kind="gelu", act="bf16"),
+    # few tokens against long K: the expert GEMMs run split-K (partials + reduction)
+    "split_swiglu_bias_shared": W("ssb", T=3, d=1024, E=8, k=2, F=512, kind="swiglu",
+                                  act="bf16", expert_bias=True, has_shared=True),
+    "split_gelu_cap_res": W("sgc", T=5, d=512, E=4, k=1, F=768, kind="gelu", act="bf16",
+                            cf=1.0, add_residual=True, expert_bias=True),
+    "split_swiglu_k8": W("ss8", T=2, d=2048, E=64, k=8, F=256, kind="swiglu", act="bf16",
+                         gate_dist="uniform"),
 }
 
 
@@ -153,6 +160,41 @@ def test_out_of_range_expert_id_is_skipped_and_reported():
     sd = to_np(outs[5])
     assert sd[5, 0] == -1 and sd[17, 0] == -1
     assert to_np(outs[0]).sum() == T * k - 2
+
+
+def test_out_of_range_expert_id_single_cta_dispatch():
+    # T <= 256 runs the whole dispatch in one CTA; it must skip and report bad ids too
+    wl = SMALL["swiglu_bias"]
+    cfg = moe.config_for(wl)
+    T, k, E = wl.T, wl.k, wl.E
+    g = torch.Generator(device="cpu").manual_seed(3)
+    idx = torch.randint(0, E, (T, k), dtype=torch.int32, generator=g)
+    idx[7, 1] = E + 5
+    idx[100, 0] = -1
+    ref = idx.clone()
+    ref[7, 1] = -1    # the oracle sees the bad slots as never routed
+    ref[100, 0] = -1
+    i32 = dict(dtype=torch.int32, device="cuda")
+    outs = [torch.empty(E, **i32), torch.empty(E, **i32), torch.empty(E + 1, **i32),
+            torch.empty(T * k, **i32), torch.empty(T * k, **i32), torch.empty(T, k, **i32)]
+    ws = torch.empty(moe.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    moe.dispatch(cfg, idx.cuda(), None, *outs, None, ws)
+    assert moe.last_device_status() == moe._capi.MOE_ERR_DEVICE_INDEX
+    sd = to_np(outs[5])
+    assert sd[7, 1] == -1 and sd[100, 0] == -1
+    ld = to_np(outs[0])
+    assert ld.sum() == T * k - 2
+    good = ref.numpy()
+    assert np.array_equal(ld, np.bincount(good[good >= 0], minlength=E))
+
+
+def test_split_k_is_used_for_few_tokens():
+    wl = SMALL["split_swiglu_bias_shared"]
+    moe.profile_begin()
+    GpuRun(wl).run()
+    stats = moe.profile_end()
+    assert "splitk_reduce_swiglu" in stats and "splitk_reduce_scale" in stats
+    assert "splitk_reduce_f32" in stats
 
 
 def test_profile_and_launch_count():

@@ -70,9 +70,13 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, const fl
     *reinterpret_cast<uint2*>(p) = u;
 }
 
-// One warp per token (grid-stride), each lane owning two float4 column groups per
-// pass, so a warp keeps 2 x k row loads in flight. slot_dest of the token is read
-// once by lanes 0..k-1 and broadcast by shuffles.
+// One warp per task = (token, span of `cpt` consecutive 256-column chunks), grid-stride:
+// whole tokens when there are many, single chunks when there are few, so that few
+// tokens still spread over many SMs. slot_dest of the token is read once per task by
+// lanes 0..k-1 and broadcast by shuffles; each lane owns two float4 column groups of a
+// chunk. Additions run in slot order and skip dropped slots (adding +0 would turn a
+// -0 residual into +0). The slot loop stays a plain loop: the kernel needs few
+// registers, so many warps per SM keep the HBM reads in flight.
 __device__ __forceinline__ void add4(float4& a, const float4& v) {
     a.x += v.x;
     a.y += v.y;
@@ -86,14 +90,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ x,
                                                       const int* __restrict__ slot_dest,
                                                       const float* __restrict__ y_shared,
                                                       OT* __restrict__ out, int T, int d, int k,
-                                                      int add_residual) {
+                                                      int add_residual, int cpt) {
     const int lane = threadIdx.x & 31;
+    const int chunks = (d + 255) / 256;
+    const int spans = (chunks + cpt - 1) / cpt;
+    const long long work = (long long)T * spans;
     const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-    for (long long t = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T;
-         t += warps) {
+    for (long long wi = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); wi < work;
+         wi += warps) {
+        const long long t = wi / spans;
+        const int sp = (int)(wi - t * spans);
         const int mydest = lane < k ? slot_dest[t * k + lane] : -1;
-        for (int c0 = 0; c0 < d; c0 += 256) {
-            const int ca = c0 + lane * 4, cb = c0 + 128 + lane * 4;
+        const int cend = min(chunks, (sp + 1) * cpt);
+        for (int ch = sp * cpt; ch < cend; ++ch) {
+            const int ca = ch * 256 + lane * 4, cb = ca + 128;
             const bool va = ca < d, vb = cb < d;
             float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
             if (add_residual) {

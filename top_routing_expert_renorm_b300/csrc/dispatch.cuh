@@ -65,15 +65,29 @@ __device__ __forceinline__ int block_excl_scan_1024(int v, int* s_warp /*[32]*/,
     return r;
 }
 
+// M-tile table from the per-group row counts (one group per thread of a 1024-thread
+// CTA): tables[0..G] = exclusive scan of ceil(rows/128). Every thread must call it (it
+// contains barriers); tables may be null.
+__device__ __forceinline__ void write_tile_tables(int rows, int g, int G, int* s_warp,
+                                                  int* __restrict__ tables) {
+    int tot;
+    const int off = block_excl_scan_1024((rows + kMTile - 1) / kMTile, s_warp, tot);
+    if (tables) {
+        if (g < G) tables[g] = off;
+        if (g == 0) tables[G] = tot;
+    }
+}
+
 // ---- one CTA: load, capacity, offsets, per-chunk rank bases, M-tile table ----------
 // blockoff[b][e] = assignments of e in chunks before b (rank base of chunk b).
 // mtile_offsets[e] = exclusive prefix sum over experts of ceil(counts/128).
 __global__ void __launch_bounds__(1024) dispatch_scan_kernel(
     const int* __restrict__ blockcnt, int nb, int E, int cap, int* __restrict__ blockoff,
     int* __restrict__ load, int* __restrict__ counts, int* __restrict__ offsets,
-    int* __restrict__ mtile_offsets) {
+    int* __restrict__ mtile_offsets, unsigned long long* __restrict__ counters, int n_counters) {
     __shared__ int s_warp[32];
     const int e = threadIdx.x;
+    if (counters && e < n_counters) counters[e] = 0ull;
     int kept = 0;
     if (e < E) {
         int run = 0;
@@ -91,13 +105,7 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(
     const int off = block_excl_scan_1024(kept, s_warp, total);
     if (e < E) offsets[e] = off;
     if (e == 0) offsets[E] = total;
-    const int tiles = (kept + kMTile - 1) / kMTile;
-    int ttot;
-    const int toff = block_excl_scan_1024(tiles, s_warp, ttot);
-    if (mtile_offsets) {
-        if (e < E) mtile_offsets[e] = toff;
-        if (e == 0) mtile_offsets[E] = ttot;
-    }
+    write_tile_tables(kept, e, E, s_warp, mtile_offsets);
 }
 
 // ---- stable rank + scatter of the kept assignments ------------------------------------
@@ -161,6 +169,98 @@ __global__ void __launch_bounds__(256) dispatch_rank_kernel(
     }
 }
 
+// ---- T <= kDispTok: the whole dispatch in one CTA of 1024 threads ----------------------
+// Warps 0..kDispWarps-1 count and then rank their contiguous runs of assignments exactly
+// as dispatch_rank_kernel does for a single chunk (rank base 0); all 1024 threads form
+// load, counts, offsets and the M-tile table in between. One launch instead of three,
+// with the same outputs and no scratch memory. Needs (kDispWarps + 1) * E ints of
+// dynamic shared memory.
+__global__ void __launch_bounds__(1024) dispatch_small_kernel(
+    const int* __restrict__ idx, int T, int k, int E, int cap, int* __restrict__ load,
+    int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ perm_token,
+    int* __restrict__ perm_slot, int* __restrict__ slot_dest, int* __restrict__ mtile_offsets,
+    unsigned long long* __restrict__ counters, int n_counters) {
+    extern __shared__ int dsm[];
+    if (counters && (int)threadIdx.x < n_counters) counters[threadIdx.x] = 0ull;
+    __shared__ int s_warp[32];
+    int* wcnt = dsm;                      // [kDispWarps][E] running counters
+    int* s_off = dsm + kDispWarps * E;    // [E] offsets
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < kDispWarps * E; i += blockDim.x) wcnt[i] = 0;
+    __syncthreads();
+    const long long n = (long long)T * k;
+    const long long seg = ((n + kDispWarps - 1) / kDispWarps + 31) / 32 * 32;
+    const bool ranker = wid < kDispWarps;
+    const long long wbeg = (long long)wid * seg;
+    const long long wend = min(wbeg + seg, n);
+    int* my = wcnt + (ranker ? wid : 0) * E;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    // pass 1: per-warp totals (out-of-range ids are reported once, here, and skipped)
+    if (ranker) {
+        for (long long base = wbeg; base < wend; base += 32) {
+            const long long i = base + lane;
+            int e = -1;
+            if (i < wend) {
+                e = idx[i];
+                if (e < 0 || e >= E) {
+                    raise_error(DEVERR_INDEX);
+                    e = -1;
+                }
+            }
+            const unsigned peers = __match_any_sync(0xffffffffu, e);
+            if (e >= 0 && (peers & lt_mask) == 0) my[e] += __popc(peers);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    // load, capacity, offsets; warp counters become rank bases
+    const int e = threadIdx.x;
+    int kept = 0;
+    if (e < E) {
+        int run = 0;
+        for (int w = 0; w < kDispWarps; ++w) {
+            const int c = wcnt[w * E + e];
+            wcnt[w * E + e] = run;
+            run += c;
+        }
+        load[e] = run;
+        kept = min(run, cap);
+        counts[e] = kept;
+    }
+    int total;
+    const int off = block_excl_scan_1024(kept, s_warp, total);
+    if (e < E) {
+        offsets[e] = off;
+        s_off[e] = off;
+    }
+    if (e == 0) offsets[E] = total;
+    write_tile_tables(kept, e, E, s_warp, mtile_offsets);
+    __syncthreads();
+    // pass 2: stable ranks and scatter
+    if (!ranker) return;
+    for (long long base = wbeg; base < wend; base += 32) {
+        const long long i = base + lane;
+        int ex = (i < wend) ? idx[i] : -1;
+        if (ex < 0 || ex >= E) ex = -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, ex);
+        int rank = 0;
+        if (ex >= 0) rank = my[ex] + __popc(peers & lt_mask);
+        __syncwarp();
+        if (ex >= 0 && (peers & lt_mask) == 0) my[ex] += __popc(peers);
+        __syncwarp();
+        if (i < wend) {
+            if (ex >= 0 && rank < cap) {
+                const int pos = s_off[ex] + rank;
+                perm_token[pos] = (int)(i / k);
+                perm_slot[pos] = (int)(i % k);
+                slot_dest[i] = pos;
+            } else {
+                slot_dest[i] = -1;
+            }
+        }
+    }
+}
+
 // ---- x_perm[p] = x[perm_token[p]] for p < P = offsets[E]; one warp per row -----------
 // 16-byte vector copies, four loads in flight per lane before their stores;
 // row_bytes is a multiple of 16.
@@ -190,21 +290,25 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
 }
 
 // ---- M-tile table from offsets (expert stage entry): single CTA of 1024 threads ----
+// The table kernels also zero the tile counters of the grouped-GEMM launches that
+// follow them (counters may be null).
 __global__ void __launch_bounds__(1024) mtile_table_kernel(const int* __restrict__ offsets, int G,
-                                                           int* __restrict__ mtile_offsets) {
+                                                           int* __restrict__ mtile_offsets,
+                                                           unsigned long long* __restrict__ counters,
+                                                           int n_counters) {
     __shared__ int s_warp[32];
     const int g = threadIdx.x;
-    int tiles = 0;
-    if (g < G) tiles = (offsets[g + 1] - offsets[g] + kMTile - 1) / kMTile;
-    int tot;
-    const int off = block_excl_scan_1024(tiles, s_warp, tot);
-    if (g < G) mtile_offsets[g] = off;
-    if (g == 0) mtile_offsets[G] = tot;
+    if (counters && g < n_counters) counters[g] = 0ull;
+    const int rows = (g < G) ? offsets[g + 1] - offsets[g] : 0;
+    write_tile_tables(rows, g, G, s_warp, mtile_offsets);
 }
 
 // Row and M-tile tables of a single group of `rows` rows (the shared expert).
 __global__ void single_group_table_kernel(int rows, int* __restrict__ row_offsets,
-                                          int* __restrict__ mtile_offsets) {
+                                          int* __restrict__ mtile_offsets,
+                                          unsigned long long* __restrict__ counters,
+                                          int n_counters) {
+    if (counters && (int)threadIdx.x < n_counters) counters[threadIdx.x] = 0ull;
     if (threadIdx.x == 0) {
         row_offsets[0] = 0;
         row_offsets[1] = rows;

@@ -15,7 +15,11 @@
 // allocation), warps 2-5 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
 // Tiles are ordered expert-major, then N block, then M block, so the CTAs working
 // at the same time share one weight slice (read once from HBM) while the
-// expert's activation rows stay in L2.
+// expert's activation rows stay in L2. CTAs take tiles dynamically from a global
+// counter: the first M tile of a weight slice streams it from HBM while its sibling
+// M tiles re-read it from L2, so tiles differ in cost and a fixed round-robin would
+// give some SMs most of the HBM traffic. The producer thread fetches the next tile
+// id and hands it to the MMA and epilogue warps through a small ring in shared memory.
 // For SwiGLU a tile's 256 B rows are 128 gate rows (n0..) and 128 up rows
 // (F+n0..) of the same expert, loaded as two TMA boxes, so the epilogue can form
 // silu(gate) * up for 128 output columns without repacking the weights.
@@ -42,6 +46,20 @@ struct GemmParams {
     const int* perm_token;
     const int* perm_slot;
     int top_k;
+    // split-K: every output tile is computed as k_splits units over consecutive ranges of
+    // kb_per_split K blocks; with partial != null each unit stores its raw fp32 sums at
+    // partial + split * part_stride + row * ld_part + column (columns as in B's rows, so
+    // a SwiGLU unit writes gate columns n and up columns F + n), and splitk_reduce_kernel
+    // applies the epilogue afterwards.
+    int k_splits;
+    int kb_per_split;
+    float* partial;
+    long long part_stride;
+    long long ld_part;
+    // Dynamic scheduling: a CTA takes unit blockIdx.x first, then gridDim.x + the value
+    // it fetched-and-incremented from this counter (zeroed by the kernel that writes
+    // the launch's tables). Null: static round-robin over the units.
+    unsigned long long* tile_counter;
 };
 
 constexpr int GM_BM = 128, GM_BN = 256, GM_BK = 64, GM_STAGES = 4;
@@ -51,24 +69,58 @@ constexpr int GM_STAGE_BYTES = GM_A_BYTES + GM_B_BYTES;
 constexpr int GM_THREADS = 192;
 constexpr int GM_TMEM_COLS = 512;
 constexpr int GM_MAX_GROUPS = 1025;
+constexpr int GM_TQ = 8;            // depth of the ring of scheduled unit ids
+constexpr int GM_HDR_BYTES = 512;   // barriers, TMEM address, abort flag, unit-id ring
 
 __host__ __device__ constexpr int gm_smem_bytes(int G) {
-    return 1024 + GM_STAGES * GM_STAGE_BYTES + 256 + 2 * (G + 1) * 4;
+    return 1024 + GM_STAGES * GM_STAGE_BYTES + GM_HDR_BYTES + 2 * (G + 1) * 4;
 }
 
-__device__ __forceinline__ void gm_decode(long long t, int G, int n_tiles, const int* s_mt, int& g,
-                                          int& mb, int& nb) {
-    int lo = 0, hi = G;   // s_mt[lo]*n_tiles <= t < s_mt[hi]*n_tiles
+// Work unit t -> (group g, M block mb, N block nb, K split ks). Units of one group are
+// ordered N block, then M block, then K split.
+__device__ __forceinline__ void gm_decode(long long t, int G, int n_tiles, int S, const int* s_mt,
+                                          int& g, int& mb, int& nb, int& ks) {
+    const long long per = (long long)n_tiles * S;   // units per M tile
+    int lo = 0, hi = G;   // s_mt[lo]*per <= t < s_mt[hi]*per
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if ((long long)s_mt[mid] * n_tiles <= t) lo = mid;
+        if ((long long)s_mt[mid] * per <= t) lo = mid;
         else hi = mid;
     }
     g = lo;
-    const long long local = t - (long long)s_mt[g] * n_tiles;
+    const long long local = t - (long long)s_mt[g] * per;
     const int mt = s_mt[g + 1] - s_mt[g];
-    nb = (int)(local / mt);
-    mb = (int)(local % mt);
+    const long long ms = (long long)mt * S;
+    nb = (int)(local / ms);
+    const int rem = (int)(local - (long long)nb * ms);
+    mb = rem / S;
+    ks = rem - mb * S;
+}
+
+// Raw fp32 accumulator of one unit -> its split-K partial rows.
+template <int EPI>
+__device__ __forceinline__ void gm_epilogue_partial(const GemmParams& p, uint32_t tb, int nb, int ks,
+                                                    bool row_ok, long long grow) {
+    float* prow = p.partial + (long long)ks * p.part_stride + grow * p.ld_part;
+    constexpr int chunks = GM_BN / 32;
+#pragma unroll 1
+    for (int c = 0; c < chunks; ++c) {
+        float v[32];
+        __syncwarp();
+        tmem_load_32cols(tb + c * 32, v);
+        int col;
+        if constexpr (EPI == EPI_SWIGLU_BF16)
+            col = (c < chunks / 2) ? nb * 128 + c * 32 : p.N + nb * 128 + (c - chunks / 2) * 32;
+        else
+            col = nb * GM_BN + c * 32;
+        const int lim = (EPI == EPI_SWIGLU_BF16) ? ((c < chunks / 2) ? p.N : 2 * p.N) : p.N;
+        if (row_ok && col < lim) {
+            float4* dst = reinterpret_cast<float4*>(prow + col);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+    }
 }
 
 template <int EPI>
@@ -177,16 +229,18 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
                                                ~static_cast<uintptr_t>(1023));
     uint8_t* tiles = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GM_STAGES * GM_STAGE_BYTES);
-    // barrier slots: full[0..3], empty[4..7], tfull[8..9], tempty[10..11], drain[12]
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 16);
-    volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 17);
-    int* s_ro = reinterpret_cast<int*>(bars + 32);
+    // barrier slots: full[0..3], empty[4..7], tfull[8..9], tempty[10..11], drain[12],
+    // unit-id ring full[16..23] / empty[24..31]
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 32);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 33);
+    volatile long long* s_unit = reinterpret_cast<volatile long long*>(bars + 40);   // [GM_TQ]
+    int* s_ro = reinterpret_cast<int*>(bars + GM_HDR_BYTES / 8);
     int* s_mt = s_ro + (p.G + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto bar = [&](int i) { return smem_addr(bars + i); };
     const int FULL = 0, EMPTY = GM_STAGES, TFULL = 2 * GM_STAGES, TEMPTY = 2 * GM_STAGES + 2,
-              DRAIN = 2 * GM_STAGES + 4;
+              DRAIN = 2 * GM_STAGES + 4, QFULL = 16, QEMPTY = 16 + GM_TQ;
 
     for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
         s_ro[i] = p.row_offsets[i];
@@ -202,6 +256,10 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
             mbar_init(bar(TEMPTY + a), 4);
         }
         mbar_init(bar(DRAIN), 1);
+        for (int i = 0; i < GM_TQ; ++i) {
+            mbar_init(bar(QFULL + i), 1);
+            mbar_init(bar(QEMPTY + i), 5);   // the MMA thread + four epilogue warps
+        }
         *s_abort = 0;
         mbar_fence_init();
         tma_prefetch_desc(&tmA);
@@ -215,7 +273,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
-    const long long total = (long long)s_mt[p.G] * p.n_tiles;
+    const long long total = (long long)s_mt[p.G] * p.n_tiles * p.k_splits;
     const int kblocks = p.K / GM_BK;
 
     if (warp == 0) {
@@ -227,14 +285,35 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
 #pragma unroll
             for (int s = 0; s < GM_STAGES; ++s) last_par[s] = -1;
             bool ok = true;
-            for (long long t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                int g, mb, nb;
-                gm_decode(t, p.G, p.n_tiles, s_mt, g, mb, nb);
+            int q = 0;
+            uint32_t qph = 0;
+            long long t = blockIdx.x;
+            while (true) {
+                // publish the next unit id (-1: no more work) to the MMA and epilogue warps
+                if (*s_abort || !mbar_wait(bar(QEMPTY + q), qph ^ 1)) {
+                    *s_abort = 1;
+                    break;
+                }
+                const long long pub = (ok && t < total) ? t : -1;
+                s_unit[q] = pub;
+                mbar_arrive(bar(QFULL + q));
+                if (++q == GM_TQ) {
+                    q = 0;
+                    qph ^= 1;
+                }
+                if (pub < 0) break;
+                const long long next =
+                    p.tile_counter ? (long long)gridDim.x + (long long)atomicAdd(p.tile_counter, 1ull)
+                                   : t + gridDim.x;
+                int g, mb, nb, ks;
+                gm_decode(t, p.G, p.n_tiles, p.k_splits, s_mt, g, mb, nb, ks);
+                const int kb0 = ks * p.kb_per_split;
+                const int kb1 = min(kblocks, kb0 + p.kb_per_split);
                 const int a_row = s_ro[g] + mb * GM_BM;
                 const int n0 = (EPI == EPI_SWIGLU_BF16) ? nb * 128 : nb * GM_BN;
                 const int b0 = g * p.b_rows_per_group + n0;
                 const int b1 = b0 + p.up_offset;
-                for (int kb = 0; kb < kblocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (*s_abort || !mbar_wait(bar(EMPTY + stage), ph ^ 1)) {
                         *s_abort = 1;
                         ok = false;
@@ -252,6 +331,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
                         ph ^= 1;
                     }
                 }
+                t = next;
             }
             // Every copy this thread started must have landed before the CTA exits.
             for (int s = 0; s < GM_STAGES; ++s)
@@ -263,15 +343,31 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
             constexpr uint32_t idesc = idesc_bf16_f32(GM_BM, GM_BN);
             int stage = 0, acc = 0;
             uint32_t ph = 0, aph = 0;
-            for (long long t = blockIdx.x; t < total; t += gridDim.x) {
+            int q = 0;
+            uint32_t qph = 0;
+            while (true) {
+                if (*s_abort || !mbar_wait(bar(QFULL + q), qph)) {
+                    *s_abort = 1;
+                    break;
+                }
+                const long long t = s_unit[q];
+                mbar_arrive(bar(QEMPTY + q));
+                if (++q == GM_TQ) {
+                    q = 0;
+                    qph ^= 1;
+                }
+                if (t < 0) break;
                 if (*s_abort || !mbar_wait(bar(TEMPTY + acc), aph ^ 1)) {
                     *s_abort = 1;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t dt = tmem_base + (uint32_t)(acc * GM_BN);
+                const long long within = t % p.k_splits;   // the unit's K split
+                const int kb0 = (int)within * p.kb_per_split;
+                const int kb1 = min(kblocks, kb0 + p.kb_per_split);
                 bool ok = true;
-                for (int kb = 0; kb < kblocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(bar(FULL + stage), ph)) {
                         *s_abort = 1;
                         ok = false;
@@ -283,7 +379,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < GM_BK / 16; ++kk)
                         umma_bf16(dt, sw128_kmajor_desc(sa + kk * 32), sw128_kmajor_desc(sb + kk * 32),
-                                  idesc, (kb | kk) != 0 ? 1u : 0u);
+                                  idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
                     umma_commit(bar(EMPTY + stage));
                     if (++stage == GM_STAGES) {
                         stage = 0;
@@ -304,9 +400,32 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         const int q = warp & 3;
         int acc = 0;
         uint32_t aph = 0;
-        for (long long t = blockIdx.x; t < total; t += gridDim.x) {
-            int g, mb, nb;
-            gm_decode(t, p.G, p.n_tiles, s_mt, g, mb, nb);
+        int uq = 0;
+        uint32_t uqph = 0;
+        while (true) {
+            long long t = -1;
+            int got = 1;
+            if (lane == 0) {
+                if (*s_abort || !mbar_wait(bar(QFULL + uq), uqph)) {
+                    got = 0;
+                } else {
+                    t = s_unit[uq];
+                    mbar_arrive(bar(QEMPTY + uq));
+                }
+            }
+            got = __shfl_sync(0xffffffffu, got, 0);
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (++uq == GM_TQ) {
+                uq = 0;
+                uqph ^= 1;
+            }
+            if (!got) {
+                if (lane == 0) *s_abort = 1;
+                break;
+            }
+            if (t < 0) break;
+            int g, mb, nb, ks;
+            gm_decode(t, p.G, p.n_tiles, p.k_splits, s_mt, g, mb, nb, ks);
             int ok = 1;
             if (lane == 0) ok = (!*s_abort && mbar_wait(bar(TFULL + acc), aph)) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -317,10 +436,12 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
             tc_fence_after();
             const int r_in = q * 32 + lane;
             const int rows_g = s_ro[g + 1] - s_ro[g];
-            const bool row_ok = mb * GM_BM + r_in < rows_g;
-            const long long grow = (long long)s_ro[g] + (long long)mb * GM_BM + r_in;
+            const int r_tile = mb * GM_BM + r_in;   // row within the group
+            const bool row_ok = r_tile < rows_g;
+            const long long grow = (long long)s_ro[g] + r_tile;
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * GM_BN);
-            gm_epilogue_tile<EPI>(p, tb, g, nb, row_ok, grow);
+            if (p.partial) gm_epilogue_partial<EPI>(p, tb, nb, ks, row_ok, grow);
+            else gm_epilogue_tile<EPI>(p, tb, g, nb, row_ok, grow);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(TEMPTY + acc));
@@ -335,6 +456,67 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem_base, GM_TMEM_COLS);
+    }
+}
+
+// ---- split-K reduction + epilogue ---------------------------------------------------
+// For rows r < rows_total[0] (the kept rows P) and output columns c (4 per thread):
+// sums the k_splits partials in split order, then applies the same epilogue as the
+// unsplit kernel (bias, GELU / SwiGLU -> bf16, or routing-weight scale -> fp32).
+template <int EPI>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmParams p,
+                                                            const int* __restrict__ rows_total) {
+    const int P = *rows_total;
+    const int nq = p.N / 4;
+    const long long work = (long long)P * nq;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < work;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long r = i / nq;
+        const int c = (int)(i - r * nq) * 4;
+        const float* src = p.partial + r * p.ld_part + c;
+        float4 a = *reinterpret_cast<const float4*>(src);
+        float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (EPI == EPI_SWIGLU_BF16) u = *reinterpret_cast<const float4*>(src + p.N);
+        for (int s = 1; s < p.k_splits; ++s) {
+            const float4 v = *reinterpret_cast<const float4*>(src + s * p.part_stride);
+            a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+            if constexpr (EPI == EPI_SWIGLU_BF16) {
+                const float4 w = *reinterpret_cast<const float4*>(src + s * p.part_stride + p.N);
+                u.x += w.x; u.y += w.y; u.z += w.z; u.w += w.w;
+            }
+        }
+        if (p.bias) {
+            int lo = 0, hi = p.G;   // row_offsets[lo] <= r < row_offsets[hi]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (p.row_offsets[mid] <= r) lo = mid;
+                else hi = mid;
+            }
+            const float* b = p.bias + (long long)lo * p.b_rows_per_group + c;
+            a.x += b[0]; a.y += b[1]; a.z += b[2]; a.w += b[3];
+            if constexpr (EPI == EPI_SWIGLU_BF16) {
+                const float* bu = b + p.up_offset;
+                u.x += bu[0]; u.y += bu[1]; u.z += bu[2]; u.w += bu[3];
+            }
+        }
+        if constexpr (EPI == EPI_SWIGLU_BF16 || EPI == EPI_GELU_BF16) {
+            float h0, h1, h2, h3;
+            if constexpr (EPI == EPI_SWIGLU_BF16) {
+                h0 = silu(a.x) * u.x; h1 = silu(a.y) * u.y; h2 = silu(a.z) * u.z; h3 = silu(a.w) * u.w;
+            } else {
+                h0 = gelu_erf(a.x); h1 = gelu_erf(a.y); h2 = gelu_erf(a.z); h3 = gelu_erf(a.w);
+            }
+            uint2 o;
+            o.x = pack_bf16x2(h0, h1);
+            o.y = pack_bf16x2(h2, h3);
+            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + r * p.ld_out + c) = o;
+        } else {
+            if constexpr (EPI == EPI_SCALE_F32) {
+                const float sc = p.topk_w[(long long)p.perm_token[r] * p.top_k + p.perm_slot[r]];
+                a.x *= sc; a.y *= sc; a.z *= sc; a.w *= sc;
+            }
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + r * p.ld_out + c) = a;
+        }
     }
 }
 

@@ -221,9 +221,88 @@ RouterPlan router_plan(const moe_config& c) {
     return r;
 }
 
+// ---------------------------------------------------------------------------------
+// split-K plan of one grouped-GEMM launch
+// ---------------------------------------------------------------------------------
+// When an upper bound on the launch's output tiles cannot fill the SMs twice, every
+// tile is cut along K into S units (at least 4 K blocks each) so that the units
+// spread over whole waves of SMs; S maximises the fraction of SM slots in use
+// (a larger S must win by 2 %). The plan depends only on the configuration, so the
+// workspace can hold its partial sums.
+struct SplitPlan {
+    int S = 1;
+    int kbs = 0;   // K blocks per split
+};
+
+SplitPlan split_plan(long long max_mtiles, int n_tiles, int K, int sms) {
+    SplitPlan sp;
+    const int KB = K / GM_BK;
+    sp.kbs = KB;
+    const long long tiles = max_mtiles * n_tiles;
+    if (tiles <= 0 || tiles >= 2ll * sms) return sp;
+    auto eff = [&](long long units) {
+        const long long waves = (units + sms - 1) / sms;
+        return (double)units / (double)(waves * sms);
+    };
+    double best = eff(tiles);
+    for (int S = 2; S <= 16; ++S) {
+        const int kbs = (KB + S - 1) / S;
+        if (kbs < 4) break;
+        const int Se = (KB + kbs - 1) / kbs;
+        const double e = eff(tiles * Se);
+        if (e > best + 0.02) {
+            best = e;
+            sp.S = Se;
+            sp.kbs = kbs;
+        }
+    }
+    return sp;
+}
+
+// Upper bound on the M tiles of the routed experts: sum_e ceil(n_e / 128) over the
+// non-empty experts <= P / 128 + min(E, P).
+long long routed_mtiles_bound(const moe_config& c) {
+    const long long Pmax = (long long)c.T * c.top_k;
+    return Pmax / kMTile + std::min<long long>(c.E, Pmax);
+}
+
+struct FfnPlan {
+    SplitPlan up, down, sh_up, sh_down;
+    size_t partial_floats = 0;   // largest partial buffer any of the four launches needs
+};
+
+FfnPlan ffn_plan(const moe_config& c) {
+    FfnPlan f;
+    if (!(c.kind == MOE_EXPERT_GELU || c.kind == MOE_EXPERT_SWIGLU)) return f;
+    const int sms = num_sms();
+    const long long Pmax = (long long)c.T * c.top_k;
+    const int up_nt = c.kind == MOE_EXPERT_SWIGLU ? (c.F + 127) / 128 : (c.F + GM_BN - 1) / GM_BN;
+    const int dn_nt = (c.d + GM_BN - 1) / GM_BN;
+    const long long N1 = c.kind == MOE_EXPERT_SWIGLU ? 2ll * c.F : c.F;
+    const long long mt = routed_mtiles_bound(c);
+    f.up = split_plan(mt, up_nt, c.d, sms);
+    f.down = split_plan(mt, dn_nt, c.F, sms);
+    auto need = [&](const SplitPlan& sp, long long rows, long long cols) {
+        if (sp.S > 1) f.partial_floats = std::max<size_t>(f.partial_floats, (size_t)(sp.S * rows * cols));
+    };
+    need(f.up, Pmax, N1);
+    need(f.down, Pmax, c.d);
+    if (c.has_shared) {
+        const long long smt = (c.T + kMTile - 1) / kMTile;
+        f.sh_up = split_plan(smt, up_nt, c.d, sms);
+        f.sh_down = split_plan(smt, dn_nt, c.F, sms);
+        need(f.sh_up, c.T, N1);
+        need(f.sh_down, c.T, c.d);
+    }
+    return f;
+}
+
+// Tile counters of the expert-stage grouped-GEMM launches (dynamic scheduling).
+enum { kCntUp = 0, kCntDown = 1, kCntSharedUp = 2, kCntSharedDown = 3, kNumCounters = 4 };
+
 struct WsLayout {
     size_t logits, idx, w, load, counts, offsets, blockcnt, blockoff, perm_token, perm_slot,
-        slot_dest, x_perm, mtile, shared_tab, h, hs, y, total;
+        slot_dest, x_perm, mtile, shared_tab, counters, h, hs, y, partial, total;
 };
 
 WsLayout ws_layout(const moe_config& c) {
@@ -253,9 +332,11 @@ WsLayout ws_layout(const moe_config& c) {
     L.x_perm = take(Pmax * d * es);
     L.mtile = take((E + 1) * 4);
     L.shared_tab = take(4 * 4);
+    L.counters = take(kNumCounters * 8);
     L.h = take(is_bf16_kind(c) ? Pmax * F * 2 : 0);
     L.hs = take(is_bf16_kind(c) && c.has_shared ? T * F * 2 : 0);
     L.y = take((Pmax + (c.has_shared ? T : 0)) * d * 4);
+    L.partial = take(ffn_plan(c).partial_floats * 4);
     L.total = off;
     return L;
 }
@@ -271,18 +352,26 @@ P* at(void* ws, size_t off) {
 moe_status dispatch_impl(const moe_config& c, const int32_t* idx, const void* x, int32_t* load,
                          int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* perm_slot,
                          int32_t* slot_dest, void* x_perm, int32_t* blockcnt, int32_t* blockoff,
-                         int32_t* mtile, cudaStream_t s) {
+                         int32_t* mtile, unsigned long long* counters, cudaStream_t s) {
+    // counters (nullable): the routed up/down GEMM tile counters, zeroed here
     const int T = c.T, E = c.E, k = c.top_k;
     const int cap = capacity_of(c);
     const int nb = (T + kDispTok - 1) / kDispTok;
+    if (nb == 1) {
+        MOE_LAUNCH("dispatch_small", s,
+                   dispatch_small_kernel<<<1, 1024, (kDispWarps + 1) * E * sizeof(int), s>>>(
+                       idx, T, k, E, cap, load, counts, offsets, perm_token, perm_slot,
+                       slot_dest, mtile, counters, 2));
+    } else {
     MOE_LAUNCH("dispatch_hist", s,
                dispatch_hist_kernel<<<nb, 256, E * sizeof(int), s>>>(idx, T, k, E, blockcnt));
     MOE_LAUNCH("dispatch_scan", s,
                dispatch_scan_kernel<<<1, 1024, 0, s>>>(blockcnt, nb, E, cap, blockoff, load, counts,
-                                                       offsets, mtile));
+                                                       offsets, mtile, counters, 2));
     MOE_LAUNCH("dispatch_rank", s,
                dispatch_rank_kernel<<<nb, 256, kDispWarps * E * sizeof(int), s>>>(
                    idx, T, k, E, cap, blockoff, offsets, perm_token, perm_slot, slot_dest));
+    }
     if (x_perm) {
         const int es = c.act_dtype == MOE_BF16 ? 2 : 4;
         const long long Pmax = (long long)T * k;
@@ -306,11 +395,25 @@ const char* gemm_name() {
 }
 
 template <int EPI>
+const char* reduce_name() {
+    switch (EPI) {
+        case EPI_F32: return "splitk_reduce_f32";
+        case EPI_GELU_BF16: return "splitk_reduce_gelu";
+        case EPI_SWIGLU_BF16: return "splitk_reduce_swiglu";
+        default: return "splitk_reduce_scale";
+    }
+}
+
+// One grouped-GEMM launch (plus, when sp.S > 1, the split-K reduction that applies the
+// epilogue). `partial` must hold sp.S * a_rows * (SwiGLU ? 2N : N) floats when split.
+template <int EPI>
 moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int64_t b_rows_total,
                        int b_rows_per_group, int G, int N, const int32_t* row_offsets,
                        const int32_t* mtile_offsets, void* out, long long ld_out, const float* bias,
                        const float* topk_w, const int32_t* perm_token, const int32_t* perm_slot,
-                       int top_k, cudaStream_t s, const char* name = nullptr) {
+                       int top_k, cudaStream_t s, const char* name = nullptr,
+                       SplitPlan sp = SplitPlan(), float* partial = nullptr,
+                       unsigned long long* counter = nullptr) {
     if (a_rows <= 0 || G <= 0) return MOE_OK;
     if (G > GM_MAX_GROUPS) return MOE_ERR_UNSUPPORTED;
     CUtensorMap ta, tb;
@@ -332,6 +435,13 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     p.perm_token = perm_token;
     p.perm_slot = perm_slot;
     p.top_k = top_k;
+    const bool split = sp.S > 1 && partial != nullptr;
+    p.k_splits = split ? sp.S : 1;
+    p.kb_per_split = split ? sp.kbs : K / GM_BK;
+    p.partial = split ? partial : nullptr;
+    p.ld_part = (EPI == EPI_SWIGLU_BF16) ? 2ll * N : N;
+    p.part_stride = (long long)a_rows * p.ld_part;
+    p.tile_counter = counter;
     const int smem = gm_smem_bytes(G);
     static std::once_flag attr_once[64];
     static cudaError_t attr_err[64];
@@ -347,12 +457,19 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     const int grid = num_sms();
     MOE_LAUNCH(name ? name : gemm_name<EPI>(), s,
                grouped_gemm_kernel<EPI><<<grid, GM_THREADS, smem, s>>>(ta, tb, p));
+    if (split) {
+        const long long work = a_rows * (long long)(N / 4);
+        const int blocks = (int)std::max<long long>(
+            1, std::min<long long>((work + 255) / 256, (long long)num_sms() * 8));
+        MOE_LAUNCH(reduce_name<EPI>(), s,
+                   splitk_reduce_kernel<EPI><<<blocks, 256, 0, s>>>(p, row_offsets + G));
+    }
     return MOE_OK;
 }
 
-#define MOE_TRY(expr)                       \
+#define MOE_TRY(...)                        \
     do {                                    \
-        const moe_status st_ = (expr);      \
+        const moe_status st_ = (__VA_ARGS__); \
         if (st_ != MOE_OK) return st_;      \
     } while (0)
 
@@ -373,18 +490,29 @@ moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const
             reinterpret_cast<int32_t*>(static_cast<char*>(scratch) + rp.bg_bytes + rp.d_bytes);
         const dim3 grid((d + 31) / 32, rp.Ep / 32);
         MOE_LAUNCH("gate_split", s,
-                   gate_split_kernel<<<grid, 256, 0, s>>>(Wg, d, E, rp.Ep, Bg, T, tables));
+                   gate_split_kernel<<<grid, 256, 0, s>>>(
+                       Wg, d, E, rp.Ep, Bg, T, tables,
+                       reinterpret_cast<unsigned long long*>(tables + 4)));
         MOE_TRY(launch_gemm<EPI_F32>(x, T, d, Bg, 3ll * rp.Ep, 3 * rp.Ep, 1, 3 * rp.Ep, tables,
                                      tables + 2, parts, 3ll * rp.Ep, nullptr, nullptr, nullptr,
-                                     nullptr, 1, s, "router_gemm_tc"));
+                                     nullptr, 1, s, "router_gemm_tc", SplitPlan(), nullptr,
+                                     reinterpret_cast<unsigned long long*>(tables + 4)));
     } else {
-        const dim3 grid((E + RS_E - 1) / RS_E, rp.n_parts, (T + RS_T - 1) / RS_T);
-        MOE_LAUNCH("router_splitk", s,
-                   router_splitk_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
-                                                             Wg, parts, T, d, E));
+        const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+        if (T <= 8) {
+            const dim3 grid((E + RS_E - 1) / RS_E, rp.n_parts, 1);
+            MOE_LAUNCH("router_splitk", s,
+                       router_splitk_kernel<8><<<grid, 256, 0, s>>>(xb, Wg, parts, T, d, E));
+        } else {
+            const dim3 grid((E + RS_E - 1) / RS_E, rp.n_parts, (T + 63) / 64);
+            MOE_LAUNCH("router_splitk", s,
+                       router_splitk_kernel<64><<<grid, 256, 0, s>>>(xb, Wg, parts, T, d, E));
+        }
     }
     MOE_LAUNCH("topk_renorm", s,
-               topk_renorm_kernel<<<(T + 7) / 8, 256, 0, s>>>(parts, rp.n_parts, rp.part_stride,
+               topk_renorm_kernel<<<(T + kTopkTok - 1) / kTopkTok, 256,
+                                    kTopkTok * E * sizeof(float), s>>>(parts, rp.n_parts,
+                                                                      rp.part_stride,
                                                               rp.row_stride, bias, logits, T, E,
                                                               k, idx, w));
     return MOE_OK;
@@ -394,8 +522,12 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
                     const moe_expert_weights& R, const moe_expert_weights* S, const void* x,
                     const float* topk_w, const int32_t* perm_token, const int32_t* perm_slot,
                     float* y, int32_t* mtile, bool mtile_ready, int32_t* shared_tab,
-                    __nv_bfloat16* h, __nv_bfloat16* hs, cudaStream_t s) {
+                    __nv_bfloat16* h, __nv_bfloat16* hs, float* partial,
+                    unsigned long long* counters, cudaStream_t s) {
+    // counters: kNumCounters tile counters; [kCntUp], [kCntDown] are already zero when
+    // mtile_ready (the dispatch kernel that wrote the M-tile table zeroed them)
     const int T = c.T, E = c.E, d = c.d, k = c.top_k, F = c.F;
+    const FfnPlan fp = ffn_plan(c);
     const long long Pmax = (long long)T * k;
     float* y_shared = y + Pmax * d;
     if (c.kind == MOE_EXPERT_LINEAR) {
@@ -408,7 +540,8 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
                        d, Pmax));
         if (c.has_shared) {
             MOE_LAUNCH("single_group_table", s,
-                       single_group_table_kernel<<<1, 32, 0, s>>>(T, shared_tab, shared_tab + 2));
+                       single_group_table_kernel<<<1, 32, 0, s>>>(T, shared_tab, shared_tab + 2,
+                                                                  nullptr, 0));
             const long long ns = (long long)T * d;
             const int sb = (int)std::max<long long>(1, std::min<long long>((ns + 255) / 256, 65535));
             MOE_LAUNCH("linear_expert", s,
@@ -420,31 +553,37 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
         return MOE_OK;
     }
     if (!mtile_ready)
-        MOE_LAUNCH("mtile_table", s, mtile_table_kernel<<<1, 1024, 0, s>>>(offsets, E, mtile));
+        MOE_LAUNCH("mtile_table", s,
+                   mtile_table_kernel<<<1, 1024, 0, s>>>(offsets, E, mtile, counters + kCntUp, 2));
     const int64_t N1 = n1_of(c);
     if (c.kind == MOE_EXPERT_SWIGLU)
         MOE_TRY(launch_gemm<EPI_SWIGLU_BF16>(x_perm, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
                                              offsets, mtile, h, F, R.b1, nullptr, nullptr, nullptr,
-                                             k, s));
+                                             k, s, nullptr, fp.up, partial, counters + kCntUp));
     else
         MOE_TRY(launch_gemm<EPI_GELU_BF16>(x_perm, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
                                            offsets, mtile, h, F, R.b1, nullptr, nullptr, nullptr, k,
-                                           s));
+                                           s, nullptr, fp.up, partial, counters + kCntUp));
     MOE_TRY(launch_gemm<EPI_SCALE_F32>(h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets, mtile, y,
-                                       d, R.b2, topk_w, perm_token, perm_slot, k, s));
+                                       d, R.b2, topk_w, perm_token, perm_slot, k, s, nullptr,
+                                       fp.down, partial, counters + kCntDown));
     if (c.has_shared) {
         MOE_LAUNCH("single_group_table", s,
-                   single_group_table_kernel<<<1, 32, 0, s>>>(T, shared_tab, shared_tab + 2));
+                   single_group_table_kernel<<<1, 32, 0, s>>>(T, shared_tab, shared_tab + 2,
+                                                              counters + kCntSharedUp, 2));
         if (c.kind == MOE_EXPERT_SWIGLU)
             MOE_TRY(launch_gemm<EPI_SWIGLU_BF16>(x, T, d, S->w1, N1, (int)N1, 1, F, shared_tab,
                                                  shared_tab + 2, hs, F, S->b1, nullptr, nullptr,
-                                                 nullptr, k, s));
+                                                 nullptr, k, s, nullptr, fp.sh_up, partial,
+                                                 counters + kCntSharedUp));
         else
             MOE_TRY(launch_gemm<EPI_GELU_BF16>(x, T, d, S->w1, N1, (int)N1, 1, F, shared_tab,
                                                shared_tab + 2, hs, F, S->b1, nullptr, nullptr,
-                                               nullptr, k, s));
+                                               nullptr, k, s, nullptr, fp.sh_up, partial,
+                                               counters + kCntSharedUp));
         MOE_TRY(launch_gemm<EPI_F32>(hs, T, F, S->w2, d, d, 1, d, shared_tab, shared_tab + 2,
-                                     y_shared, d, S->b2, nullptr, nullptr, nullptr, k, s));
+                                     y_shared, d, S->b2, nullptr, nullptr, nullptr, k, s, nullptr,
+                                     fp.sh_down, partial, counters + kCntSharedDown));
     }
     return MOE_OK;
 }
@@ -454,18 +593,23 @@ moe_status combine_impl(const moe_config& c, const void* x, const float* y,
     const int T = c.T, d = c.d, k = c.top_k;
     const long long Pmax = (long long)T * k;
     const float* ysh = c.has_shared ? y + Pmax * d : nullptr;
-    const int blocks = (int)std::max<long long>(1, std::min<long long>((T + 7) / 8,
+    // tasks of cpt 256-column chunks: whole tokens unless that leaves fewer than ~4096 tasks
+    const int chunks = (d + 255) / 256;
+    const int cpt = (int)std::max<long long>(
+        1, std::min<long long>(chunks, (long long)chunks * T / 4096));
+    const long long work = (long long)T * ((chunks + cpt - 1) / cpt);
+    const int blocks = (int)std::max<long long>(1, std::min<long long>((work + 7) / 8,
                                                                        (long long)num_sms() * 8));
     if (c.act_dtype == MOE_F32)
         MOE_LAUNCH("combine_f32", s,
                    combine_kernel<float><<<blocks, 256, 0, s>>>(
                        static_cast<const float*>(x), y, slot_dest, ysh, static_cast<float*>(out), T,
-                       d, k, c.add_residual));
+                       d, k, c.add_residual, cpt));
     else
         MOE_LAUNCH("combine_bf16", s,
                    combine_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
                        static_cast<const __nv_bfloat16*>(x), y, slot_dest, ysh,
-                       static_cast<__nv_bfloat16*>(out), T, d, k, c.add_residual));
+                       static_cast<__nv_bfloat16*>(out), T, d, k, c.add_residual, cpt));
     return MOE_OK;
 }
 
@@ -532,7 +676,7 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const vo
     const WsLayout L = ws_layout(c);
     return dispatch_impl(c, topk_idx, x, load, counts, offsets, perm_token, perm_slot, slot_dest,
                          x_perm, at<int32_t>(ws, L.blockcnt), at<int32_t>(ws, L.blockoff), nullptr,
-                         stream);
+                         nullptr, stream);
 }
 
 moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
@@ -555,7 +699,8 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32
     const WsLayout L = ws_layout(c);
     return ffn_impl(c, x_perm, offsets, *routed, shared, x, topk_w, perm_token, perm_slot, y,
                     at<int32_t>(ws, L.mtile), false, at<int32_t>(ws, L.shared_tab),
-                    at<__nv_bfloat16>(ws, L.h), at<__nv_bfloat16>(ws, L.hs), stream);
+                    at<__nv_bfloat16>(ws, L.h), at<__nv_bfloat16>(ws, L.hs),
+                    at<float>(ws, L.partial), at<unsigned long long>(ws, L.counters), stream);
 }
 
 moe_status moe_combine(const moe_config* cfg, const void* x, const float* y,
@@ -598,16 +743,22 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate
     MOE_TRY(route_impl(c, x, W_gate, gate_bias, nullptr, idx, w, at<void>(ws, L.logits), stream));
     MOE_TRY(dispatch_impl(c, idx, x, ld, at<int32_t>(ws, L.counts), offsets, perm_token, perm_slot,
                           slot_dest, x_perm, at<int32_t>(ws, L.blockcnt),
-                          at<int32_t>(ws, L.blockoff), mtile, stream));
+                          at<int32_t>(ws, L.blockoff), mtile,
+                          at<unsigned long long>(ws, L.counters), stream));
     MOE_TRY(ffn_impl(c, x_perm, offsets, *routed, shared, x, w, perm_token, perm_slot, y, mtile,
                      true, at<int32_t>(ws, L.shared_tab), at<__nv_bfloat16>(ws, L.h),
-                     at<__nv_bfloat16>(ws, L.hs), stream));
+                     at<__nv_bfloat16>(ws, L.hs), at<float>(ws, L.partial),
+                     at<unsigned long long>(ws, L.counters), stream));
     return combine_impl(c, x, y, slot_dest, out, stream);
 }
 
+// M-tile table ((G+1) int32), then the tile counter (8-byte aligned).
+// M-tile table ((G+1) int32), then the tile counter (8-byte aligned).
+size_t gg_counter_offset(int32_t G) { return ((size_t)(G + 1) * 4 + 7) & ~size_t(7); }
+
 size_t moe_grouped_gemm_ws_size(int32_t G) {
     if (G < 1 || G > 1024) return 0;
-    return (size_t)(G + 1) * 4;
+    return gg_counter_offset(G) + 8;
 }
 
 moe_status moe_grouped_gemm(const void* A, int64_t a_rows, const void* B, int32_t G, int32_t N,
@@ -622,10 +773,13 @@ moe_status moe_grouped_gemm(const void* A, int64_t a_rows, const void* B, int32_
         return MOE_ERR_MISALIGNED;
     if (a_rows == 0) return MOE_OK;
     int32_t* mtile = static_cast<int32_t*>(ws);
+    unsigned long long* counter =
+        reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + gg_counter_offset(G));
     MOE_LAUNCH("mtile_table", stream,
-               mtile_table_kernel<<<1, 1024, 0, stream>>>(row_offsets, G, mtile));
+               mtile_table_kernel<<<1, 1024, 0, stream>>>(row_offsets, G, mtile, counter, 1));
     return launch_gemm<EPI_F32>(A, a_rows, K, B, (int64_t)G * N, N, G, N, row_offsets, mtile, D, N,
-                                nullptr, nullptr, nullptr, nullptr, 1, stream);
+                                nullptr, nullptr, nullptr, nullptr, 1, stream, nullptr,
+                                SplitPlan(), nullptr, counter);
 }
 
 moe_status moe_load_report(const int32_t* load_host, int32_t E, int32_t D, int32_t* assign,
@@ -774,5 +928,5 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t*
     int32_t* scratch = nullptr;
     MOE_TRY(noalloc_scratch(&scratch));
     return dispatch_impl(c, topk_idx, x, load, counts, offsets, perm_token, perm_slot, slot_dest,
-                         x_perm, scratch, scratch + nb * c.E, nullptr, stream);
+                         x_perm, scratch, scratch + nb * c.E, nullptr, nullptr, stream);
 }

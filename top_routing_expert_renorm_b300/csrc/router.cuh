@@ -89,7 +89,8 @@ constexpr int kRouterPad = 32;   // experts are padded to Ep = round_up(E, 32) p
 __global__ void __launch_bounds__(256) gate_split_kernel(const float* __restrict__ Wg, int d,
                                                          int E, int Ep,
                                                          __nv_bfloat16* __restrict__ Bg, int T,
-                                                         int* __restrict__ tables) {
+                                                         int* __restrict__ tables,
+                                                         unsigned long long* __restrict__ counter) {
     __shared__ float tile[32][33];
     const int k0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
@@ -115,47 +116,53 @@ __global__ void __launch_bounds__(256) gate_split_kernel(const float* __restrict
         tables[1] = T;
         tables[2] = 0;                      // its M-tile offsets
         tables[3] = (T + 127) / 128;
+        *counter = 0ull;                    // tile counter of the router GEMM
     }
 }
 
 // ---- path 3: bf16 activations, few tokens: split-K CUDA-core kernel --------------------
 // CTA (256 threads) = 32 experts (lane) x a 256-long K slice (warp w takes 32 of it) x
-// up to 64 tokens (blockIdx.z chunk). Each thread accumulates its 32 K values for every
-// token; the 8 warps are then summed through shared memory in a fixed order and the
-// CTA writes one partial [slice][T][E]. Wide grids keep all SMs streaming W_gate.
-constexpr int RS_E = 32, RS_K = 256, RS_T = 64;
+// up to TT tokens (blockIdx.z chunk). Each thread first issues all 32 of its W_gate
+// loads, then accumulates its 32 K values for every token; the 8 warps are summed
+// through shared memory in a fixed order and the CTA writes one partial [slice][T][E].
+// Wide grids keep all SMs streaming W_gate.
+constexpr int RS_E = 32, RS_K = 256;
 
+template <int TT>
 __global__ void __launch_bounds__(256) router_splitk_kernel(const __nv_bfloat16* __restrict__ x,
                                                             const float* __restrict__ Wg,
                                                             float* __restrict__ parts, int T,
                                                             int d, int E) {
-    __shared__ __nv_bfloat16 xs[RS_T][RS_K];
+    __shared__ __nv_bfloat16 xs[TT][RS_K];
     __shared__ float red[8][8][RS_E + 1];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int e = blockIdx.x * RS_E + lane;
     const int k0 = blockIdx.y * RS_K;
-    const int t0 = blockIdx.z * RS_T;
-    const int nt = min(RS_T, T - t0);
-    for (int i = threadIdx.x; i < RS_T * RS_K; i += blockDim.x) {
+    const int t0 = blockIdx.z * TT;
+    const int nt = min(TT, T - t0);
+    float wv[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int k = k0 + w * 32 + i;
+        wv[i] = (k < d && e < E) ? __ldg(Wg + (long long)k * E + e) : 0.0f;
+    }
+    for (int i = threadIdx.x; i < TT * RS_K; i += blockDim.x) {
         const int t = i / RS_K, kk = i % RS_K;
         xs[t][kk] = (t < nt && k0 + kk < d) ? x[(long long)(t0 + t) * d + k0 + kk]
                                              : __float2bfloat16_rn(0.0f);
     }
     __syncthreads();
-    float acc[RS_T];
+    float acc[TT];
 #pragma unroll
-    for (int t = 0; t < RS_T; ++t) acc[t] = 0.0f;
-    for (int i = 0; i < 32; ++i) {
-        const int kk = w * 32 + i;
-        const int k = k0 + kk;
-        const float wv = (k < d && e < E) ? Wg[(long long)k * E + e] : 0.0f;
+    for (int t = 0; t < TT; ++t) {
+        float a = 0.0f;
 #pragma unroll
-        for (int t = 0; t < RS_T; ++t)
-            if (t < nt) acc[t] = fmaf(__bfloat162float(xs[t][kk]), wv, acc[t]);
+        for (int i = 0; i < 32; ++i) a = fmaf(__bfloat162float(xs[t][w * 32 + i]), wv[i], a);
+        acc[t] = a;
     }
     float* out = parts + (long long)blockIdx.y * T * E;
 #pragma unroll
-    for (int c = 0; c < RS_T / 8; ++c) {
+    for (int c = 0; c < TT / 8; ++c) {
         __syncthreads();
 #pragma unroll
         for (int t = 0; t < 8; ++t) red[w][t][lane] = acc[c * 8 + t];
@@ -183,6 +190,11 @@ __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
 
 // Logit (t, e) = sum_{p < n_parts} parts[p*part_stride + t*row_stride + e] (+ bias[e]),
 // summed in part order; written to `logits` [T, E] when that is non-null.
+// A CTA handles kTopkTok tokens: all 256 threads first form the CTA's logits in shared
+// memory (every (token, expert) sum issues its part loads in batches of 8, so few
+// round trips are exposed even with many parts), then warp w selects for token w.
+constexpr int kTopkTok = 8;
+
 __global__ void __launch_bounds__(256) topk_renorm_kernel(const float* __restrict__ parts,
                                                           int n_parts, long long part_stride,
                                                           long long row_stride,
@@ -190,10 +202,31 @@ __global__ void __launch_bounds__(256) topk_renorm_kernel(const float* __restric
                                                           float* __restrict__ logits, int T,
                                                           int E, int k, int* __restrict__ idx,
                                                           float* __restrict__ w) {
+    extern __shared__ float sL[];   // [kTopkTok][E]
     const int lane = threadIdx.x & 31;
-    const long long t = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (t >= T) return;
-    const float* L = parts + t * row_stride;
+    const long long t0 = (long long)blockIdx.x * kTopkTok;
+    const int nt = (int)min((long long)kTopkTok, (long long)T - t0);
+    for (int i = threadIdx.x; i < nt * E; i += blockDim.x) {
+        const int tt = i / E, e = i - tt * E;
+        const float* L = parts + (t0 + tt) * row_stride + e;
+        float s = L[0];
+        for (int p = 1; p < n_parts; p += 8) {
+            float v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = (p + q < n_parts) ? L[(p + q) * part_stride] : 0.0f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (p + q < n_parts) s += v[q];
+        }
+        if (bias) s += bias[e];
+        sL[i] = s;
+        if (logits) logits[(t0 + tt) * E + e] = s;
+    }
+    __syncthreads();
+    const int wt = threadIdx.x >> 5;
+    if (wt >= nt) return;
+    const long long t = t0 + wt;
+    const float* Ls = sL + wt * E;
     float v[32];
     uint32_t avail = 0;
 #pragma unroll
@@ -201,11 +234,7 @@ __global__ void __launch_bounds__(256) topk_renorm_kernel(const float* __restric
         const int e = lane + 32 * i;
         v[i] = 0.0f;
         if (e < E) {
-            float s = L[e];
-            for (int p = 1; p < n_parts; ++p) s += L[p * part_stride + e];
-            if (bias) s += bias[e];
-            v[i] = s;
-            if (logits) logits[t * E + e] = s;
+            v[i] = Ls[e];
             avail |= 1u << i;
         }
     }
