@@ -16,6 +16,7 @@ __global__ void __launch_bounds__(256) linear_expert_kernel(
     const float* __restrict__ W, const float* __restrict__ b, const float* __restrict__ topk_w,
     const int* __restrict__ perm_token, const int* __restrict__ perm_slot, int k,
     float* __restrict__ y, int d, long long max_rows) {
+    pdl_entry();
     const int P = row_offsets[G];
     const long long n = (long long)P * d;
     const long long stride = (long long)gridDim.x * blockDim.x;
@@ -91,6 +92,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ x,
                                                       const float* __restrict__ y_shared,
                                                       OT* __restrict__ out, int T, int d, int k,
                                                       int add_residual, int cpt) {
+    pdl_entry();
     const int lane = threadIdx.x & 31;
     const int chunks = (d + 255) / 256;
     const int spans = (chunks + cpt - 1) / cpt;

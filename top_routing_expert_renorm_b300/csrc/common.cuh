@@ -29,6 +29,23 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+// ---- programmatic dependent launch ----------------------------------------------------
+// Every kernel of the library is launched so that it may start while the kernel before
+// it in the stream finishes. pdl_wait() blocks until the preceding grid has completed
+// and its writes are visible; a kernel calls it before it reads anything an earlier
+// kernel wrote (or writes anything an earlier kernel reads). pdl_trigger(), called right
+// after, lets the next kernel be scheduled; since every kernel passes its own wait
+// before it triggers, a kernel that has started knows that all kernels two or more
+// launches back have completed. Launched without the attribute, both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_entry() {
+    pdl_wait();
+    pdl_trigger();
+}
+
 // ---- mbarrier -----------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -71,6 +88,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 // Self-test of the bounded wait: one thread waits on an mbarrier phase that nothing
 // completes, gives up after `budget` cycles and records DEVERR_TIMEOUT.
 __global__ void selftest_wait_kernel(long long budget) {
+    pdl_entry();
     __shared__ __align__(8) uint64_t bar;
     if (threadIdx.x == 0) {
         const uint32_t b = smem_addr(&bar);

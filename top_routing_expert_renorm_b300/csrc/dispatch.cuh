@@ -23,6 +23,7 @@ constexpr int kMTile = 128;      // rows per tensor-core M tile
 __global__ void __launch_bounds__(256) dispatch_hist_kernel(const int* __restrict__ idx, int T,
                                                             int k, int E,
                                                             int* __restrict__ blockcnt) {
+    pdl_entry();
     extern __shared__ int cnt[];
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
@@ -85,6 +86,7 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(
     const int* __restrict__ blockcnt, int nb, int E, int cap, int* __restrict__ blockoff,
     int* __restrict__ load, int* __restrict__ counts, int* __restrict__ offsets,
     int* __restrict__ mtile_offsets, unsigned long long* __restrict__ counters, int n_counters) {
+    pdl_entry();
     __shared__ int s_warp[32];
     const int e = threadIdx.x;
     if (counters && e < n_counters) counters[e] = 0ull;
@@ -113,6 +115,7 @@ __global__ void __launch_bounds__(256) dispatch_rank_kernel(
     const int* __restrict__ idx, int T, int k, int E, int cap, const int* __restrict__ blockoff,
     const int* __restrict__ offsets, int* __restrict__ perm_token, int* __restrict__ perm_slot,
     int* __restrict__ slot_dest) {
+    pdl_entry();
     extern __shared__ int wcnt[];   // [kDispWarps][E] running counters
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < kDispWarps * E; i += blockDim.x) wcnt[i] = 0;
@@ -180,6 +183,7 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(
     int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ perm_token,
     int* __restrict__ perm_slot, int* __restrict__ slot_dest, int* __restrict__ mtile_offsets,
     unsigned long long* __restrict__ counters, int n_counters) {
+    pdl_entry();
     extern __shared__ int dsm[];
     if (counters && (int)threadIdx.x < n_counters) counters[threadIdx.x] = 0ull;
     __shared__ int s_warp[32];
@@ -269,6 +273,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
                                                           const int* __restrict__ total_rows,
                                                           uint8_t* __restrict__ x_perm,
                                                           int row_bytes) {
+    pdl_entry();
     const int P = *total_rows;
     const int lane = threadIdx.x & 31;
     const int nvec = row_bytes / 16;
@@ -296,6 +301,7 @@ __global__ void __launch_bounds__(1024) mtile_table_kernel(const int* __restrict
                                                            int* __restrict__ mtile_offsets,
                                                            unsigned long long* __restrict__ counters,
                                                            int n_counters) {
+    pdl_entry();
     __shared__ int s_warp[32];
     const int g = threadIdx.x;
     if (counters && g < n_counters) counters[g] = 0ull;
@@ -308,6 +314,7 @@ __global__ void single_group_table_kernel(int rows, int* __restrict__ row_offset
                                           int* __restrict__ mtile_offsets,
                                           unsigned long long* __restrict__ counters,
                                           int n_counters) {
+    pdl_entry();
     if (counters && (int)threadIdx.x < n_counters) counters[threadIdx.x] = 0ull;
     if (threadIdx.x == 0) {
         row_offsets[0] = 0;

@@ -242,10 +242,6 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     const int FULL = 0, EMPTY = GM_STAGES, TFULL = 2 * GM_STAGES, TEMPTY = 2 * GM_STAGES + 2,
               DRAIN = 2 * GM_STAGES + 4, QFULL = 16, QEMPTY = 16 + GM_TQ;
 
-    for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
-        s_ro[i] = p.row_offsets[i];
-        s_mt[i] = p.mtile_offsets[i];
-    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < GM_STAGES; ++s) {
             mbar_init(bar(FULL + s), 1);
@@ -268,6 +264,13 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     if (warp == 1) {
         tmem_alloc(smem_addr(s_tmem), GM_TMEM_COLS);
         tmem_relinquish();
+    }
+    // Everything above is local set-up that may overlap the end of the preceding kernel;
+    // the tables and operands may be its outputs.
+    pdl_entry();
+    for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
+        s_ro[i] = p.row_offsets[i];
+        s_mt[i] = p.mtile_offsets[i];
     }
     tc_fence_before();
     __syncthreads();
@@ -466,6 +469,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
 template <int EPI>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmParams p,
                                                             const int* __restrict__ rows_total) {
+    pdl_entry();
     const int P = *rows_total;
     const int nq = p.N / 4;
     const long long work = (long long)P * nq;

@@ -10,6 +10,7 @@
 #include <cstring>
 #include <mutex>
 #include <numeric>
+#include <utility>
 #include <vector>
 
 #include "common.cuh"
@@ -60,12 +61,30 @@ void prof_pre(const char* name, cudaStream_t s, cudaEvent_t* after) {
     *after = b;
 }
 
+// Launches a kernel with programmatic stream serialization (see pdl_wait() in the
+// device code) and returns the launch status.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = block;
+    lc.dynamicSmemBytes = smem;
+    lc.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...);
+}
+
+// EXPR is a launch_k(...) call.
 #define MOE_LAUNCH(NAME, STREAM, ...)                                   \
     do {                                                                \
         cudaEvent_t moe_after_;                                         \
         prof_pre(NAME, STREAM, &moe_after_);                            \
-        __VA_ARGS__;                                                    \
-        const cudaError_t moe_err_ = cudaGetLastError();                \
+        const cudaError_t moe_err_ = (__VA_ARGS__);                     \
         if (moe_after_) cudaEventRecord(moe_after_, STREAM);            \
         g_launches.fetch_add(1, std::memory_order_relaxed);             \
         if (moe_err_ != cudaSuccess) return MOE_ERR_CUDA;               \
@@ -359,17 +378,17 @@ moe_status dispatch_impl(const moe_config& c, const int32_t* idx, const void* x,
     const int nb = (T + kDispTok - 1) / kDispTok;
     if (nb == 1) {
         MOE_LAUNCH("dispatch_small", s,
-                   dispatch_small_kernel<<<1, 1024, (kDispWarps + 1) * E * sizeof(int), s>>>(
+                   launch_k(dispatch_small_kernel, 1, 1024, (kDispWarps + 1) * E * sizeof(int), s,
                        idx, T, k, E, cap, load, counts, offsets, perm_token, perm_slot,
                        slot_dest, mtile, counters, 2));
     } else {
     MOE_LAUNCH("dispatch_hist", s,
-               dispatch_hist_kernel<<<nb, 256, E * sizeof(int), s>>>(idx, T, k, E, blockcnt));
+               launch_k(dispatch_hist_kernel, nb, 256, E * sizeof(int), s, idx, T, k, E, blockcnt));
     MOE_LAUNCH("dispatch_scan", s,
-               dispatch_scan_kernel<<<1, 1024, 0, s>>>(blockcnt, nb, E, cap, blockoff, load, counts,
+               launch_k(dispatch_scan_kernel, 1, 1024, 0, s, blockcnt, nb, E, cap, blockoff, load, counts,
                                                        offsets, mtile, counters, 2));
     MOE_LAUNCH("dispatch_rank", s,
-               dispatch_rank_kernel<<<nb, 256, kDispWarps * E * sizeof(int), s>>>(
+               launch_k(dispatch_rank_kernel, nb, 256, kDispWarps * E * sizeof(int), s,
                    idx, T, k, E, cap, blockoff, offsets, perm_token, perm_slot, slot_dest));
     }
     if (x_perm) {
@@ -377,7 +396,7 @@ moe_status dispatch_impl(const moe_config& c, const int32_t* idx, const void* x,
         const long long Pmax = (long long)T * k;
         const int blocks = (int)std::min<long long>((Pmax + 7) / 8, (long long)num_sms() * 16);
         MOE_LAUNCH("gather_rows", s,
-                   gather_rows_kernel<<<std::max(blocks, 1), 256, 0, s>>>(
+                   launch_k(gather_rows_kernel, std::max(blocks, 1), 256, 0, s,
                        static_cast<const uint8_t*>(x), perm_token, offsets + E,
                        static_cast<uint8_t*>(x_perm), c.d * es));
     }
@@ -456,13 +475,13 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     }
     const int grid = num_sms();
     MOE_LAUNCH(name ? name : gemm_name<EPI>(), s,
-               grouped_gemm_kernel<EPI><<<grid, GM_THREADS, smem, s>>>(ta, tb, p));
+               launch_k(grouped_gemm_kernel<EPI>, grid, GM_THREADS, smem, s, ta, tb, p));
     if (split) {
         const long long work = a_rows * (long long)(N / 4);
         const int blocks = (int)std::max<long long>(
             1, std::min<long long>((work + 255) / 256, (long long)num_sms() * 8));
         MOE_LAUNCH(reduce_name<EPI>(), s,
-                   splitk_reduce_kernel<EPI><<<blocks, 256, 0, s>>>(p, row_offsets + G));
+                   launch_k(splitk_reduce_kernel<EPI>, blocks, 256, 0, s, p, row_offsets + G));
     }
     return MOE_OK;
 }
@@ -481,7 +500,7 @@ moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const
     if (rp.path == 1) {
         const dim3 grid((T + RT_BM - 1) / RT_BM, (E + RT_BN - 1) / RT_BN);
         MOE_LAUNCH("router_logits_f32", s,
-                   router_logits_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x),
+                   launch_k(router_logits_kernel<float>, grid, 256, 0, s, static_cast<const float*>(x),
                                                                     Wg, parts, T, d, E));
     } else if (rp.path == 2) {
         __nv_bfloat16* Bg = static_cast<__nv_bfloat16*>(scratch);
@@ -490,7 +509,7 @@ moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const
             reinterpret_cast<int32_t*>(static_cast<char*>(scratch) + rp.bg_bytes + rp.d_bytes);
         const dim3 grid((d + 31) / 32, rp.Ep / 32);
         MOE_LAUNCH("gate_split", s,
-                   gate_split_kernel<<<grid, 256, 0, s>>>(
+                   launch_k(gate_split_kernel, grid, 256, 0, s,
                        Wg, d, E, rp.Ep, Bg, T, tables,
                        reinterpret_cast<unsigned long long*>(tables + 4)));
         MOE_TRY(launch_gemm<EPI_F32>(x, T, d, Bg, 3ll * rp.Ep, 3 * rp.Ep, 1, 3 * rp.Ep, tables,
@@ -502,16 +521,16 @@ moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const
         if (T <= 8) {
             const dim3 grid((E + RS_E - 1) / RS_E, rp.n_parts, 1);
             MOE_LAUNCH("router_splitk", s,
-                       router_splitk_kernel<8><<<grid, 256, 0, s>>>(xb, Wg, parts, T, d, E));
+                       launch_k(router_splitk_kernel<8>, grid, 256, 0, s, xb, Wg, parts, T, d, E));
         } else {
             const dim3 grid((E + RS_E - 1) / RS_E, rp.n_parts, (T + 63) / 64);
             MOE_LAUNCH("router_splitk", s,
-                       router_splitk_kernel<64><<<grid, 256, 0, s>>>(xb, Wg, parts, T, d, E));
+                       launch_k(router_splitk_kernel<64>, grid, 256, 0, s, xb, Wg, parts, T, d, E));
         }
     }
     MOE_LAUNCH("topk_renorm", s,
-               topk_renorm_kernel<<<(T + kTopkTok - 1) / kTopkTok, 256,
-                                    kTopkTok * E * sizeof(float), s>>>(parts, rp.n_parts,
+               launch_k(topk_renorm_kernel, (T + kTopkTok - 1) / kTopkTok, 256,
+                                    kTopkTok * E * sizeof(float), s, parts, rp.n_parts,
                                                                       rp.part_stride,
                                                               rp.row_stride, bias, logits, T, E,
                                                               k, idx, w));
@@ -534,18 +553,18 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
         const long long n = Pmax * d;
         const int blocks = (int)std::max<long long>(1, std::min<long long>((n + 255) / 256, 65535));
         MOE_LAUNCH("linear_expert", s,
-                   linear_expert_kernel<<<blocks, 256, 0, s>>>(
+                   launch_k(linear_expert_kernel, blocks, 256, 0, s,
                        static_cast<const float*>(x_perm), offsets, E,
                        static_cast<const float*>(R.w1), R.b1, topk_w, perm_token, perm_slot, k, y,
                        d, Pmax));
         if (c.has_shared) {
             MOE_LAUNCH("single_group_table", s,
-                       single_group_table_kernel<<<1, 32, 0, s>>>(T, shared_tab, shared_tab + 2,
+                       launch_k(single_group_table_kernel, 1, 32, 0, s, T, shared_tab, shared_tab + 2,
                                                                   nullptr, 0));
             const long long ns = (long long)T * d;
             const int sb = (int)std::max<long long>(1, std::min<long long>((ns + 255) / 256, 65535));
             MOE_LAUNCH("linear_expert", s,
-                       linear_expert_kernel<<<sb, 256, 0, s>>>(
+                       launch_k(linear_expert_kernel, sb, 256, 0, s,
                            static_cast<const float*>(x), shared_tab, 1,
                            static_cast<const float*>(S->w1), S->b1, nullptr, nullptr, nullptr, k,
                            y_shared, d, T));
@@ -554,7 +573,7 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
     }
     if (!mtile_ready)
         MOE_LAUNCH("mtile_table", s,
-                   mtile_table_kernel<<<1, 1024, 0, s>>>(offsets, E, mtile, counters + kCntUp, 2));
+                   launch_k(mtile_table_kernel, 1, 1024, 0, s, offsets, E, mtile, counters + kCntUp, 2));
     const int64_t N1 = n1_of(c);
     if (c.kind == MOE_EXPERT_SWIGLU)
         MOE_TRY(launch_gemm<EPI_SWIGLU_BF16>(x_perm, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
@@ -569,7 +588,7 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
                                        fp.down, partial, counters + kCntDown));
     if (c.has_shared) {
         MOE_LAUNCH("single_group_table", s,
-                   single_group_table_kernel<<<1, 32, 0, s>>>(T, shared_tab, shared_tab + 2,
+                   launch_k(single_group_table_kernel, 1, 32, 0, s, T, shared_tab, shared_tab + 2,
                                                               counters + kCntSharedUp, 2));
         if (c.kind == MOE_EXPERT_SWIGLU)
             MOE_TRY(launch_gemm<EPI_SWIGLU_BF16>(x, T, d, S->w1, N1, (int)N1, 1, F, shared_tab,
@@ -602,12 +621,12 @@ moe_status combine_impl(const moe_config& c, const void* x, const float* y,
                                                                        (long long)num_sms() * 8));
     if (c.act_dtype == MOE_F32)
         MOE_LAUNCH("combine_f32", s,
-                   combine_kernel<float><<<blocks, 256, 0, s>>>(
+                   launch_k(combine_kernel<float>, blocks, 256, 0, s,
                        static_cast<const float*>(x), y, slot_dest, ysh, static_cast<float*>(out), T,
                        d, k, c.add_residual, cpt));
     else
         MOE_LAUNCH("combine_bf16", s,
-                   combine_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+                   launch_k(combine_kernel<__nv_bfloat16>, blocks, 256, 0, s,
                        static_cast<const __nv_bfloat16*>(x), y, slot_dest, ysh,
                        static_cast<__nv_bfloat16*>(out), T, d, k, c.add_residual, cpt));
     return MOE_OK;
@@ -776,7 +795,7 @@ moe_status moe_grouped_gemm(const void* A, int64_t a_rows, const void* B, int32_
     unsigned long long* counter =
         reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + gg_counter_offset(G));
     MOE_LAUNCH("mtile_table", stream,
-               mtile_table_kernel<<<1, 1024, 0, stream>>>(row_offsets, G, mtile, counter, 1));
+               launch_k(mtile_table_kernel, 1, 1024, 0, stream, row_offsets, G, mtile, counter, 1));
     return launch_gemm<EPI_F32>(A, a_rows, K, B, (int64_t)G * N, N, G, N, row_offsets, mtile, D, N,
                                 nullptr, nullptr, nullptr, nullptr, 1, stream, nullptr,
                                 SplitPlan(), nullptr, counter);
@@ -867,7 +886,7 @@ uint64_t moe_kernel_launch_count(void) { return g_launches.load(); }
 
 moe_status moe_selftest_wait_timeout(int64_t budget_cycles, cudaStream_t stream) {
     if (budget_cycles < 0 || budget_cycles > kWaitBudgetCycles) return MOE_ERR_INVALID_ARG;
-    MOE_LAUNCH("selftest_wait", stream, selftest_wait_kernel<<<1, 32, 0, stream>>>(budget_cycles));
+    MOE_LAUNCH("selftest_wait", stream, launch_k(selftest_wait_kernel, 1, 32, 0, stream, budget_cycles));
     return MOE_OK;
 }
 

@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const XT* __restrict
                                                             const float* __restrict__ Wg,
                                                             float* __restrict__ logits, int T,
                                                             int d, int E) {
+    pdl_entry();
     __shared__ float xs[RT_BK][RT_BM + 4];
     __shared__ float ws[RT_BK][RT_BN + 4];
     const int tid = threadIdx.x;
@@ -91,6 +92,7 @@ __global__ void __launch_bounds__(256) gate_split_kernel(const float* __restrict
                                                          __nv_bfloat16* __restrict__ Bg, int T,
                                                          int* __restrict__ tables,
                                                          unsigned long long* __restrict__ counter) {
+    pdl_entry();
     __shared__ float tile[32][33];
     const int k0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
@@ -140,12 +142,15 @@ __global__ void __launch_bounds__(256) router_splitk_kernel(const __nv_bfloat16*
     const int k0 = blockIdx.y * RS_K;
     const int t0 = blockIdx.z * TT;
     const int nt = min(TT, T - t0);
+    // W_gate is a layer input no kernel of the library writes: its loads may start
+    // before the preceding kernel has finished; x may be that kernel's output.
     float wv[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const int k = k0 + w * 32 + i;
         wv[i] = (k < d && e < E) ? __ldg(Wg + (long long)k * E + e) : 0.0f;
     }
+    pdl_entry();
     for (int i = threadIdx.x; i < TT * RS_K; i += blockDim.x) {
         const int t = i / RS_K, kk = i % RS_K;
         xs[t][kk] = (t < nt && k0 + kk < d) ? x[(long long)(t0 + t) * d + k0 + kk]
@@ -202,6 +207,7 @@ __global__ void __launch_bounds__(256) topk_renorm_kernel(const float* __restric
                                                           float* __restrict__ logits, int T,
                                                           int E, int k, int* __restrict__ idx,
                                                           float* __restrict__ w) {
+    pdl_entry();
     extern __shared__ float sL[];   // [kTopkTok][E]
     const int lane = threadIdx.x & 31;
     const long long t0 = (long long)blockIdx.x * kTopkTok;
