@@ -136,6 +136,11 @@ def kernel_algorithmic_cost(wl, name, P, touched):
         return fl, by
     if name == "grouped_gemm_scale":
         return 2.0 * P * F * d, touched * d * F * 2 + P * F * 2 + P * d * 4
+    if name == "grouped_gemm_combine1":   # top-1 down projection writing the layer output
+        return 2.0 * P * F * d, (touched * d * F * 2 + P * F * 2 + P * d * es
+                                 + (P * d * es if wl.add_residual else 0))
+    if name == "copy_dropped":            # dropped tokens (T - P of them) leave as x or 0
+        return 0.0, T * wl.k * 4 + (T - P) * d * es * (2 if wl.add_residual else 1)
     if name == "grouped_gemm_f32":        # shared expert down projection
         return 2.0 * T * F * d, d * F * 2 + T * F * 2 + T * d * 4
     if name.startswith("router_logits") or name == "router_splitk":

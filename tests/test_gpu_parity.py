@@ -43,6 +43,9 @@ SMALL = {
                             cf=1.0, add_residual=True, expert_bias=True),
     "split_swiglu_k8": W("ss8", T=2, d=2048, E=64, k=8, F=256, kind="swiglu", act="bf16",
                          gate_dist="uniform"),
+    # top-1 without residual and with drops: the fused combine writes dropped tokens as 0
+    "top1_drop_no_residual": W("t1d", T=300, d=128, E=4, k=1, F=192, kind="gelu", act="bf16",
+                               cf=0.5, expert_bias=True),
 }
 
 
@@ -104,6 +107,14 @@ def test_dropped_tokens_leave_as_x_bit_exact():
     assert dropped.sum() > 0
     x = to_np(r.inp["x"])
     assert np.array_equal(to_np(r.out)[dropped], x[dropped])
+
+
+@pytest.mark.parametrize("name", ["gelu_cap_res", "top1_drop_no_residual", "one_expert"])
+def test_top1_fused_combine_matches_staged_path_bitwise(name):
+    # moe_forward fuses the combine into the down projection for top-1 layers without a
+    # shared expert; the staged entry points do not. The fp32 operations are the same.
+    r = GpuRun(SMALL[name]).run()
+    assert np.array_equal(to_np(r.out), to_np(r.out_stages))
 
 
 def test_forward_is_deterministic():

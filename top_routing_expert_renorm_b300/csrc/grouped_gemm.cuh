@@ -28,7 +28,15 @@
 
 namespace moe {
 
-enum EpiKind : int { EPI_F32 = 0, EPI_GELU_BF16 = 1, EPI_SWIGLU_BF16 = 2, EPI_SCALE_F32 = 3 };
+enum EpiKind : int {
+    EPI_F32 = 0,
+    EPI_GELU_BF16 = 1,
+    EPI_SWIGLU_BF16 = 2,
+    EPI_SCALE_F32 = 3,
+    // top-1 layers without a shared expert: the down projection is also the combine,
+    // out[t] = [resid[t] +] w * (acc + b) in bf16 at t = perm_token[row]
+    EPI_COMBINE1_BF16 = 4
+};
 
 struct GemmParams {
     int G;                     // groups
@@ -46,6 +54,7 @@ struct GemmParams {
     const int* perm_token;
     const int* perm_slot;
     int top_k;
+    const __nv_bfloat16* resid;   // EPI_COMBINE1_BF16: residual x [T, ld_out], nullable
     // split-K: every output tile is computed as k_splits units over consecutive ranges of
     // kb_per_split K blocks; with partial != null each unit stores its raw fp32 sums at
     // partial + split * part_stride + row * ld_part + column (columns as in B's rows, so
@@ -176,6 +185,58 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
                         a1 += brow[col + 2 * i + 1];
                     }
                     packed[i] = pack_bf16x2(gelu_erf(a0), gelu_erf(a1));
+                }
+                uint4* dst = reinterpret_cast<uint4*>(orow + col);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                        packed[4 * i + 3]);
+            }
+        }
+    } else if constexpr (EPI == EPI_COMBINE1_BF16) {
+        // Same fp32 operations, in the same order, as the scale epilogue followed by the
+        // combine kernel: y = (acc + b) * w, then out = resid + y (or 0 + y), rounded once.
+        const int n0 = nb * GM_BN;
+        long long tok = 0;
+        float scale = 0.0f;
+        if (row_ok) {
+            tok = p.perm_token[grow];
+            scale = p.topk_w[tok * p.top_k + p.perm_slot[grow]];
+        }
+        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) + tok * p.ld_out;
+        const __nv_bfloat16* xrow = p.resid ? p.resid + tok * p.ld_out : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+            float v[32];
+            __syncwarp();
+            tmem_load_32cols(tb + c * 32, v);
+            const int col = n0 + c * 32;
+            if (row_ok && col < p.N) {
+                uint32_t xin[16];
+                if (xrow) {
+                    const uint4* xs = reinterpret_cast<const uint4*>(xrow + col);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4 u = xs[i];
+                        xin[4 * i] = u.x;
+                        xin[4 * i + 1] = u.y;
+                        xin[4 * i + 2] = u.z;
+                        xin[4 * i + 3] = u.w;
+                    }
+                }
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float y0 = (v[2 * i] + (brow ? brow[col + 2 * i] : 0.0f)) * scale;
+                    float y1 = (v[2 * i + 1] + (brow ? brow[col + 2 * i + 1] : 0.0f)) * scale;
+                    float a0 = 0.0f, a1 = 0.0f;
+                    if (xrow) {
+                        const __nv_bfloat162 xx = *reinterpret_cast<const __nv_bfloat162*>(&xin[i]);
+                        const float2 xf = __bfloat1622float2(xx);
+                        a0 = xf.x;
+                        a1 = xf.y;
+                    }
+                    packed[i] = pack_bf16x2(a0 + y0, a1 + y1);
                 }
                 uint4* dst = reinterpret_cast<uint4*>(orow + col);
 #pragma unroll

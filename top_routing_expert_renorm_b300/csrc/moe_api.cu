@@ -409,6 +409,7 @@ const char* gemm_name() {
         case EPI_F32: return "grouped_gemm_f32";
         case EPI_GELU_BF16: return "grouped_gemm_gelu";
         case EPI_SWIGLU_BF16: return "grouped_gemm_swiglu";
+        case EPI_COMBINE1_BF16: return "grouped_gemm_combine1";
         default: return "grouped_gemm_scale";
     }
 }
@@ -432,7 +433,7 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
                        const float* topk_w, const int32_t* perm_token, const int32_t* perm_slot,
                        int top_k, cudaStream_t s, const char* name = nullptr,
                        SplitPlan sp = SplitPlan(), float* partial = nullptr,
-                       unsigned long long* counter = nullptr) {
+                       unsigned long long* counter = nullptr, const void* resid = nullptr) {
     if (a_rows <= 0 || G <= 0) return MOE_OK;
     if (G > GM_MAX_GROUPS) return MOE_ERR_UNSUPPORTED;
     CUtensorMap ta, tb;
@@ -461,6 +462,7 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     p.ld_part = (EPI == EPI_SWIGLU_BF16) ? 2ll * N : N;
     p.part_stride = (long long)a_rows * p.ld_part;
     p.tile_counter = counter;
+    p.resid = static_cast<const __nv_bfloat16*>(resid);
     const int smem = gm_smem_bytes(G);
     static std::once_flag attr_once[64];
     static cudaError_t attr_err[64];
@@ -542,7 +544,9 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
                     const float* topk_w, const int32_t* perm_token, const int32_t* perm_slot,
                     float* y, int32_t* mtile, bool mtile_ready, int32_t* shared_tab,
                     __nv_bfloat16* h, __nv_bfloat16* hs, float* partial,
-                    unsigned long long* counters, cudaStream_t s) {
+                    unsigned long long* counters, cudaStream_t s, void* fused_out = nullptr) {
+    // fused_out (top-1, no shared expert, unsplit down projection): the down projection
+    // writes the layer output [T, d] directly (combine fused); y is not written
     // counters: kNumCounters tile counters; [kCntUp], [kCntDown] are already zero when
     // mtile_ready (the dispatch kernel that wrote the M-tile table zeroed them)
     const int T = c.T, E = c.E, d = c.d, k = c.top_k, F = c.F;
@@ -583,9 +587,15 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
         MOE_TRY(launch_gemm<EPI_GELU_BF16>(x_perm, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
                                            offsets, mtile, h, F, R.b1, nullptr, nullptr, nullptr, k,
                                            s, nullptr, fp.up, partial, counters + kCntUp));
-    MOE_TRY(launch_gemm<EPI_SCALE_F32>(h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets, mtile, y,
-                                       d, R.b2, topk_w, perm_token, perm_slot, k, s, nullptr,
-                                       fp.down, partial, counters + kCntDown));
+    if (fused_out)
+        MOE_TRY(launch_gemm<EPI_COMBINE1_BF16>(h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets,
+                                               mtile, fused_out, d, R.b2, topk_w, perm_token,
+                                               perm_slot, k, s, nullptr, SplitPlan(), nullptr,
+                                               counters + kCntDown, c.add_residual ? x : nullptr));
+    else
+        MOE_TRY(launch_gemm<EPI_SCALE_F32>(h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets,
+                                           mtile, y, d, R.b2, topk_w, perm_token, perm_slot, k, s,
+                                           nullptr, fp.down, partial, counters + kCntDown));
     if (c.has_shared) {
         MOE_LAUNCH("single_group_table", s,
                    launch_k(single_group_table_kernel, 1, 32, 0, s, T, shared_tab, shared_tab + 2,
@@ -759,6 +769,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate
     void* x_perm = at<void>(ws, L.x_perm);
     float* y = at<float>(ws, L.y);
     int32_t* mtile = at<int32_t>(ws, L.mtile);
+    // Top-1 layers without a shared expert write the output from the down projection.
+    const bool fuse1 = is_bf16_kind(c) && c.top_k == 1 && !c.has_shared && ffn_plan(c).down.S == 1;
     MOE_TRY(route_impl(c, x, W_gate, gate_bias, nullptr, idx, w, at<void>(ws, L.logits), stream));
     MOE_TRY(dispatch_impl(c, idx, x, ld, at<int32_t>(ws, L.counts), offsets, perm_token, perm_slot,
                           slot_dest, x_perm, at<int32_t>(ws, L.blockcnt),
@@ -767,7 +779,16 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate
     MOE_TRY(ffn_impl(c, x_perm, offsets, *routed, shared, x, w, perm_token, perm_slot, y, mtile,
                      true, at<int32_t>(ws, L.shared_tab), at<__nv_bfloat16>(ws, L.h),
                      at<__nv_bfloat16>(ws, L.hs), at<float>(ws, L.partial),
-                     at<unsigned long long>(ws, L.counters), stream));
+                     at<unsigned long long>(ws, L.counters), stream, fuse1 ? out : nullptr));
+    if (fuse1) {
+        const int blocks = (int)std::max<long long>(
+            1, std::min<long long>((c.T + 7) / 8, (long long)num_sms() * 8));
+        MOE_LAUNCH("copy_dropped", stream,
+                   launch_k(copy_dropped_kernel<__nv_bfloat16>, blocks, 256, 0, stream,
+                            static_cast<const __nv_bfloat16*>(x), slot_dest,
+                            static_cast<__nv_bfloat16*>(out), c.T, c.d, c.add_residual));
+        return MOE_OK;
+    }
     return combine_impl(c, x, y, slot_dest, out, stream);
 }
 
