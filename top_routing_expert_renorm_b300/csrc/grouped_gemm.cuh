@@ -35,7 +35,11 @@ enum EpiKind : int {
     EPI_SCALE_F32 = 3,
     // top-1 layers without a shared expert: the down projection is also the combine,
     // out[t] = [resid[t] +] w * (acc + b) in bf16 at t = perm_token[row]
-    EPI_COMBINE1_BF16 = 4
+    EPI_COMBINE1_BF16 = 4,
+    // router with E <= 64: accumulator columns [p*Ep, p*Ep + E) are the three bf16-split
+    // terms of x * W_gate; the epilogue forms the logits, selects the top k and writes the
+    // renormalised weights (the top-k kernel is not launched)
+    EPI_ROUTER_TOPK = 5
 };
 
 struct GemmParams {
@@ -55,6 +59,9 @@ struct GemmParams {
     const int* perm_slot;
     int top_k;
     const __nv_bfloat16* resid;   // EPI_COMBINE1_BF16: residual x [T, ld_out], nullable
+    int* r_idx;                   // EPI_ROUTER_TOPK: top-k ids [T, top_k]
+    float* r_w;                   //                  renormalised weights [T, top_k]
+    int r_E, r_Ep;                //                  experts, padded experts per term (32 | 64)
     // split-K: every output tile is computed as k_splits units over consecutive ranges of
     // kb_per_split K blocks; with partial != null each unit stores its raw fp32 sums at
     // partial + split * part_stride + row * ld_part + column (columns as in B's rows, so
@@ -191,6 +198,67 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
                 for (int i = 0; i < 4; ++i)
                     dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
                                         packed[4 * i + 3]);
+            }
+        }
+    } else if constexpr (EPI == EPI_ROUTER_TOPK) {
+        // Logit e = term0 + term1 + term2 (+ bias[e]), then k rounds of arg-max (logit
+        // descending, lower id on ties) and w_j = exp(L_j - L_0) / sum_j' exp(L_j' - L_0)
+        // summed in slot order: the same fp32 operations as topk_renorm_kernel.
+        constexpr int MAXE = 64;
+        const int Ep = p.r_Ep, E = p.r_E, k = p.top_k;
+        float L[MAXE];
+#pragma unroll
+        for (int c = 0; c < MAXE / 32; ++c) {
+            if (c * 32 < Ep) {
+                float a[32], b[32], d3[32];
+                __syncwarp();
+                tmem_load_32cols(tb + c * 32, a);
+                tmem_load_32cols(tb + Ep + c * 32, b);
+                tmem_load_32cols(tb + 2 * Ep + c * 32, d3);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) L[c * 32 + i] = a[i] + b[i] + d3[i];
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) L[c * 32 + i] = 0.0f;
+            }
+        }
+        if (row_ok) {
+            if (p.bias) {
+#pragma unroll
+                for (int e = 0; e < MAXE; ++e)
+                    if (e < E) L[e] += p.bias[e];
+            }
+            if (p.out) {
+                float* lrow = reinterpret_cast<float*>(p.out) + grow * p.ld_out;
+#pragma unroll
+                for (int e = 0; e < MAXE; ++e)
+                    if (e < E) lrow[e] = L[e];
+            }
+            uint64_t taken = 0;
+            float vals[32];
+            int ids[32];
+            for (int j = 0; j < k; ++j) {
+                float bv = 0.0f;
+                int be = -1;
+#pragma unroll
+                for (int e = 0; e < MAXE; ++e)
+                    if (e < E && !((taken >> e) & 1ull) && (be < 0 || L[e] > bv)) {
+                        bv = L[e];
+                        be = e;
+                    }
+                taken |= 1ull << be;
+                vals[j] = bv;
+                ids[j] = be;
+            }
+            float ex[32];
+            float ssum = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                ex[j] = expf(vals[j] - vals[0]);
+                ssum += ex[j];
+            }
+            for (int j = 0; j < k; ++j) {
+                p.r_idx[grow * k + j] = ids[j];
+                p.r_w[grow * k + j] = ex[j] / ssum;
             }
         }
     } else if constexpr (EPI == EPI_COMBINE1_BF16) {

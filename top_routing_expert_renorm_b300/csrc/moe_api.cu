@@ -228,7 +228,9 @@ RouterPlan router_plan(const moe_config& c) {
         r.part_stride = r.Ep;
         r.row_stride = 3ll * r.Ep;
         r.bg_bytes = al256(3 * (size_t)r.Ep * d * 2);
-        r.d_bytes = al256(T * 3 * (size_t)r.Ep * 4);
+        // partial logits only when the three terms do not fit one accumulator (E > 64);
+        // otherwise the GEMM epilogue selects the top k itself
+        r.d_bytes = r.Ep <= 64 ? 0 : al256(T * 3 * (size_t)r.Ep * 4);
         r.scratch_bytes = r.bg_bytes + r.d_bytes + 256;
     } else {
         r.path = 3;
@@ -410,6 +412,7 @@ const char* gemm_name() {
         case EPI_GELU_BF16: return "grouped_gemm_gelu";
         case EPI_SWIGLU_BF16: return "grouped_gemm_swiglu";
         case EPI_COMBINE1_BF16: return "grouped_gemm_combine1";
+        case EPI_ROUTER_TOPK: return "router_gemm_topk";
         default: return "grouped_gemm_scale";
     }
 }
@@ -433,7 +436,8 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
                        const float* topk_w, const int32_t* perm_token, const int32_t* perm_slot,
                        int top_k, cudaStream_t s, const char* name = nullptr,
                        SplitPlan sp = SplitPlan(), float* partial = nullptr,
-                       unsigned long long* counter = nullptr, const void* resid = nullptr) {
+                       unsigned long long* counter = nullptr, const void* resid = nullptr,
+                       int* r_idx = nullptr, float* r_w = nullptr, int r_E = 0, int r_Ep = 0) {
     if (a_rows <= 0 || G <= 0) return MOE_OK;
     if (G > GM_MAX_GROUPS) return MOE_ERR_UNSUPPORTED;
     CUtensorMap ta, tb;
@@ -463,6 +467,10 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     p.part_stride = (long long)a_rows * p.ld_part;
     p.tile_counter = counter;
     p.resid = static_cast<const __nv_bfloat16*>(resid);
+    p.r_idx = r_idx;
+    p.r_w = r_w;
+    p.r_E = r_E;
+    p.r_Ep = r_Ep;
     const int smem = gm_smem_bytes(G);
     static std::once_flag attr_once[64];
     static cudaError_t attr_err[64];
@@ -514,6 +522,13 @@ moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const
                    launch_k(gate_split_kernel, grid, 256, 0, s,
                        Wg, d, E, rp.Ep, Bg, T, tables,
                        reinterpret_cast<unsigned long long*>(tables + 4)));
+        if (rp.Ep <= 64) {   // the three terms fit one 256-column accumulator: fused top-k
+            MOE_TRY(launch_gemm<EPI_ROUTER_TOPK>(
+                x, T, d, Bg, 3ll * rp.Ep, 3 * rp.Ep, 1, 3 * rp.Ep, tables, tables + 2, logits, E,
+                bias, nullptr, nullptr, nullptr, k, s, nullptr, SplitPlan(), nullptr,
+                reinterpret_cast<unsigned long long*>(tables + 4), nullptr, idx, w, E, rp.Ep));
+            return MOE_OK;
+        }
         MOE_TRY(launch_gemm<EPI_F32>(x, T, d, Bg, 3ll * rp.Ep, 3 * rp.Ep, 1, 3 * rp.Ep, tables,
                                      tables + 2, parts, 3ll * rp.Ep, nullptr, nullptr, nullptr,
                                      nullptr, 1, s, "router_gemm_tc", SplitPlan(), nullptr,
