@@ -65,6 +65,9 @@ def test_noalloc_dispatch_matches_workspace_dispatch_on_consecutive_calls():
         Workload("na_b", T=3000, d=256, E=64, k=8, F=128, kind="swiglu", act="bf16", cf=1.0,
                  gate_bias="zipf"),
         Workload("na_c", T=96, d=16, E=5, k=2, F=16, kind="linear", act="f32", cf=0.75),
+        # more assignments and experts than one CTA dispatches: the per-chunk count and
+        # rank-base tables live in the static array
+        Workload("na_d", T=9000, d=64, E=512, k=8, F=64, kind="gelu", act="bf16", cf=1.0),
     ]
     routed = [(_route(wl), wl) for wl in cases]
     # a, b, c, then a again: each call runs over what the previous one left behind

@@ -172,13 +172,22 @@ __global__ void __launch_bounds__(256) dispatch_rank_kernel(
     }
 }
 
-// ---- T <= kDispTok: the whole dispatch in one CTA of 1024 threads ----------------------
-// Warps 0..kDispWarps-1 count and then rank their contiguous runs of assignments exactly
-// as dispatch_rank_kernel does for a single chunk (rank base 0); all 1024 threads form
-// load, counts, offsets and the M-tile table in between. One launch instead of three,
-// with the same outputs and no scratch memory. Needs (kDispWarps + 1) * E ints of
-// dynamic shared memory.
-__global__ void __launch_bounds__(1024) dispatch_small_kernel(
+// ---- the whole dispatch in one CTA of 1024 threads -------------------------------------
+// For n = T*k <= kOneCtaMaxAssign and E <= kOneCtaMaxE (one launch instead of three).
+// Warp w owns the contiguous run of assignments [w*seg, (w+1)*seg) (seg a multiple of 32)
+// and reads its ids in batches of kOneCtaBatch rounds (all loads of a batch in flight
+// together). Pass 1 counts each warp's run per expert (__match_any_sync groups); the
+// warp counters then become rank bases in warp order, while all threads form load,
+// counts, offsets and the M-tile table; pass 2 ranks and scatters. Ranks are stable in
+// token order, as in the three-kernel path, and no scratch memory is used. Needs
+// (32 + 1) * E ints of dynamic shared memory.
+constexpr int kOneCtaBatch = 16;
+// One CTA ranks about 8k assignments in the time the three-kernel path takes; beyond
+// a few thousand the parallel path wins.
+constexpr int kOneCtaMaxAssign = 4096;
+constexpr int kOneCtaMaxE = 320;
+
+__global__ void __launch_bounds__(1024) dispatch_one_cta_kernel(
     const int* __restrict__ idx, int T, int k, int E, int cap, int* __restrict__ load,
     int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ perm_token,
     int* __restrict__ perm_slot, int* __restrict__ slot_dest, int* __restrict__ mtile_offsets,
@@ -187,30 +196,41 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(
     extern __shared__ int dsm[];
     if (counters && (int)threadIdx.x < n_counters) counters[threadIdx.x] = 0ull;
     __shared__ int s_warp[32];
-    int* wcnt = dsm;                      // [kDispWarps][E] running counters
-    int* s_off = dsm + kDispWarps * E;    // [E] offsets
+    int* wcnt = dsm;            // [32][E] running counters
+    int* s_off = dsm + 32 * E;  // [E] offsets
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < kDispWarps * E; i += blockDim.x) wcnt[i] = 0;
-    __syncthreads();
+    for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
     const long long n = (long long)T * k;
-    const long long seg = ((n + kDispWarps - 1) / kDispWarps + 31) / 32 * 32;
-    const bool ranker = wid < kDispWarps;
+    const int seg = (int)(((n + 31) / 32 + 31) / 32 * 32);   // assignments per warp
+    const int rounds = seg / 32;
     const long long wbeg = (long long)wid * seg;
     const long long wend = min(wbeg + seg, n);
-    int* my = wcnt + (ranker ? wid : 0) * E;
+    int* my = wcnt + wid * E;
     const unsigned lt_mask = (1u << lane) - 1u;
-    // pass 1: per-warp totals (out-of-range ids are reported once, here, and skipped)
-    if (ranker) {
-        for (long long base = wbeg; base < wend; base += 32) {
-            const long long i = base + lane;
+    // ids of rounds r0 .. r0+kOneCtaBatch-1 of this lane (-1 past the run or out of range)
+    auto load_batch = [&](int r0, int (&ids)[kOneCtaBatch], bool report) {
+#pragma unroll
+        for (int j = 0; j < kOneCtaBatch; ++j) {
+            const long long i = wbeg + (long long)(r0 + j) * 32 + lane;
             int e = -1;
-            if (i < wend) {
+            if (r0 + j < rounds && i < wend) {
                 e = idx[i];
                 if (e < 0 || e >= E) {
-                    raise_error(DEVERR_INDEX);
+                    if (report) raise_error(DEVERR_INDEX);
                     e = -1;
                 }
             }
+            ids[j] = e;
+        }
+    };
+    __syncthreads();
+    // pass 1: per-warp totals (out-of-range ids are reported once, here, and skipped)
+    for (int r0 = 0; r0 < rounds; r0 += kOneCtaBatch) {
+        int ids[kOneCtaBatch];
+        load_batch(r0, ids, true);
+#pragma unroll
+        for (int j = 0; j < kOneCtaBatch; ++j) {
+            const int e = ids[j];
             const unsigned peers = __match_any_sync(0xffffffffu, e);
             if (e >= 0 && (peers & lt_mask) == 0) my[e] += __popc(peers);
             __syncwarp();
@@ -222,7 +242,7 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(
     int kept = 0;
     if (e < E) {
         int run = 0;
-        for (int w = 0; w < kDispWarps; ++w) {
+        for (int w = 0; w < 32; ++w) {
             const int c = wcnt[w * E + e];
             wcnt[w * E + e] = run;
             run += c;
@@ -238,28 +258,37 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(
         s_off[e] = off;
     }
     if (e == 0) offsets[E] = total;
-    write_tile_tables(kept, e, E, s_warp, mtile_offsets);
+    const int tiles = (kept + kMTile - 1) / kMTile;
+    int ttot;
+    const int toff = block_excl_scan_1024(tiles, s_warp, ttot);
+    if (mtile_offsets) {
+        if (e < E) mtile_offsets[e] = toff;
+        if (e == 0) mtile_offsets[E] = ttot;
+    }
     __syncthreads();
     // pass 2: stable ranks and scatter
-    if (!ranker) return;
-    for (long long base = wbeg; base < wend; base += 32) {
-        const long long i = base + lane;
-        int ex = (i < wend) ? idx[i] : -1;
-        if (ex < 0 || ex >= E) ex = -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, ex);
-        int rank = 0;
-        if (ex >= 0) rank = my[ex] + __popc(peers & lt_mask);
-        __syncwarp();
-        if (ex >= 0 && (peers & lt_mask) == 0) my[ex] += __popc(peers);
-        __syncwarp();
-        if (i < wend) {
-            if (ex >= 0 && rank < cap) {
-                const int pos = s_off[ex] + rank;
-                perm_token[pos] = (int)(i / k);
-                perm_slot[pos] = (int)(i % k);
-                slot_dest[i] = pos;
-            } else {
-                slot_dest[i] = -1;
+    for (int r0 = 0; r0 < rounds; r0 += kOneCtaBatch) {
+        int ids[kOneCtaBatch];
+        load_batch(r0, ids, false);
+#pragma unroll
+        for (int j = 0; j < kOneCtaBatch; ++j) {
+            const long long i = wbeg + (long long)(r0 + j) * 32 + lane;
+            const int ex = ids[j];
+            const unsigned peers = __match_any_sync(0xffffffffu, ex);
+            int rank = 0;
+            if (ex >= 0) rank = my[ex] + __popc(peers & lt_mask);
+            __syncwarp();
+            if (ex >= 0 && (peers & lt_mask) == 0) my[ex] += __popc(peers);
+            __syncwarp();
+            if (r0 + j < rounds && i < wend) {
+                if (ex >= 0 && rank < cap) {
+                    const int pos = s_off[ex] + rank;
+                    perm_token[pos] = (int)(i / k);
+                    perm_slot[pos] = (int)(i % k);
+                    slot_dest[i] = pos;
+                } else {
+                    slot_dest[i] = -1;
+                }
             }
         }
     }

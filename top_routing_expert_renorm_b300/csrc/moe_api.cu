@@ -378,11 +378,11 @@ moe_status dispatch_impl(const moe_config& c, const int32_t* idx, const void* x,
     const int T = c.T, E = c.E, k = c.top_k;
     const int cap = capacity_of(c);
     const int nb = (T + kDispTok - 1) / kDispTok;
-    if (nb == 1) {
-        MOE_LAUNCH("dispatch_small", s,
-                   launch_k(dispatch_small_kernel, 1, 1024, (kDispWarps + 1) * E * sizeof(int), s,
-                       idx, T, k, E, cap, load, counts, offsets, perm_token, perm_slot,
-                       slot_dest, mtile, counters, 2));
+    if ((long long)T * k <= kOneCtaMaxAssign && E <= kOneCtaMaxE) {
+        MOE_LAUNCH("dispatch_one_cta", s,
+                   launch_k(dispatch_one_cta_kernel, 1, 1024, 33 * E * sizeof(int), s, idx, T, k,
+                            E, cap, load, counts, offsets, perm_token, perm_slot, slot_dest,
+                            mtile, counters, 2));
     } else {
     MOE_LAUNCH("dispatch_hist", s,
                launch_k(dispatch_hist_kernel, nb, 256, E * sizeof(int), s, idx, T, k, E, blockcnt));
