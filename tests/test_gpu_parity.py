@@ -148,6 +148,29 @@ def test_layer_object_matches_forward():
     assert out2.shape == (50, wl.d)
 
 
+@pytest.mark.parametrize("name", ["swiglu_k8_cap_shared", "gelu_cap_res", "split_swiglu_bias_shared"])
+def test_captured_graph_matches_direct_forward(name):
+    wl = SMALL[name]
+    r = GpuRun(wl).run()
+    inp = r.inp
+    layer = moe.MoELayer(r.cfg, inp["wg"], inp["gate_bias"], inp["w1"], inp["b1"], inp["w2"],
+                         inp["b2"], inp["shared"])
+    x = inp["x"].clone()
+    out = torch.empty_like(x)
+    graph = layer.capture(x, out)
+    out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, r.out)
+    # new contents of the captured input buffer: the replay follows them
+    x.copy_(inp["x"].flip(0))
+    graph.replay()
+    direct = layer(inp["x"].flip(0).contiguous())
+    torch.cuda.synchronize()
+    assert torch.equal(out, direct)
+    assert moe.last_device_status() == 0
+
+
 def test_bounded_wait_timeout_is_reported():
     assert moe.last_device_status() == 0
     moe.selftest_wait_timeout(200000)

@@ -27,6 +27,20 @@ class MoELayer:
         c.T = T
         return c
 
+    def capture(self, x, out, stream=None):
+        """Record one forward of x -> out (fixed buffers) into a CUDA graph and return it;
+        graph.replay() then runs the whole layer with a single launch from the host,
+        on torch's current stream. x and out must stay allocated while the graph is used.
+        One direct forward runs first so that the library's one-time set-up (device
+        attribute queries, kernel attributes) happens outside the capture."""
+        import torch
+        self(x, out=out, stream=stream)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self(x, out=out)
+        return graph
+
     def __call__(self, x, out=None, topk_idx=None, topk_w=None, load=None, stream=None):
         T = x.shape[0]
         if T > self.cfg.T:
