@@ -21,6 +21,9 @@
 //   [SafeSM]   "MoE 混合专家架构", section 4.2 数值稳定性 (max-subtracted softmax).
 //   [Merged]   "MoE 混合专家架构", section 5.2 专家融合与并行 (stacked W1, silu on the W1 slice).
 //   [LPT]      adv12 sections 3.3 EPLB and 4.3 eplb_rebalance; 4.2 expert_imbalance; Q3.
+//   [Hier]     "MoE 并行", 通信瓶颈 table, row Hierarchical Routing (pick groups first, then
+//              experts); adv12 section 5 (DeepSeek-V3: device-limited routing, each token's
+//              experts lie on at most M devices).
 //
 // Readings where the pages are silent or disagree (each one is listed in the design notes):
 //   * selection is done on logits with ties broken toward the lower expert id;
@@ -29,7 +32,9 @@
 //   * over-capacity assignments are dropped in ascending token order and add 0;
 //   * GELU is the exact-erf form; SwiGLU gate rows are [0,F) of W1, up rows [F,2F);
 //   * the hidden activation h is rounded to bf16 when the weights are bf16;
-//   * the shared expert has weight 1 for every token.
+//   * the shared expert has weight 1 for every token;
+//   * group-limited routing scores a group by its best expert logit (the pages name the
+//     two steps but not the score).
 //
 // Parity status: every exported function is pinned by the CPU test suite against
 // values printed on the pages, closed forms, or brute force on tiny inputs,
@@ -136,6 +141,54 @@ void oracle_topk_renorm(const float* logits, int T, int E, int k, int32_t* idx, 
             taken[best] = 1;
             idx[(long long)t * k + j] = best;
         }
+        double l0 = (double)L[idx[(long long)t * k]];
+        double s = 0.0;
+        for (int j = 0; j < k; ++j) s += std::exp((double)L[idx[(long long)t * k + j]] - l0);
+        for (int j = 0; j < k; ++j)
+            w[(long long)t * k + j] = (float)(std::exp((double)L[idx[(long long)t * k + j]] - l0) / s);
+    }
+}
+
+// Group-limited routing [Hier]: experts are split into n_group groups of E / n_group
+// consecutive ids. First the topk_group groups whose best expert logit is highest are
+// chosen (ties to the lower group id); then the k experts with the highest logits among
+// the chosen groups' experts (ties to the lower id); the kept weights are renormalised
+// as in oracle_topk_renorm.
+void oracle_topk_renorm_grouped(const float* logits, int T, int E, int k, int n_group,
+                                int topk_group, int32_t* idx, float* w) {
+    const int gsize = E / n_group;
+    for (int t = 0; t < T; ++t) {
+        const float* L = logits + (long long)t * E;
+        // step 1: score of each group = its best expert logit
+        std::vector<float> gscore(n_group);
+        for (int g = 0; g < n_group; ++g) {
+            float m = L[g * gsize];
+            for (int e = g * gsize + 1; e < (g + 1) * gsize; ++e)
+                if (L[e] > m) m = L[e];
+            gscore[g] = m;
+        }
+        // step 2: the topk_group best groups
+        std::vector<char> chosen(n_group, 0);
+        for (int j = 0; j < topk_group; ++j) {
+            int best = -1;
+            for (int g = 0; g < n_group; ++g) {
+                if (chosen[g]) continue;
+                if (best < 0 || gscore[g] > gscore[best]) best = g;
+            }
+            chosen[best] = 1;
+        }
+        // step 3: the k best experts of the chosen groups
+        std::vector<char> taken(E, 0);
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e] || !chosen[e / gsize]) continue;
+                if (best < 0 || L[e] > L[best]) best = e;
+            }
+            taken[best] = 1;
+            idx[(long long)t * k + j] = best;
+        }
+        // step 4: renormalised weights of the kept experts
         double l0 = (double)L[idx[(long long)t * k]];
         double s = 0.0;
         for (int j = 0; j < k; ++j) s += std::exp((double)L[idx[(long long)t * k + j]] - l0);

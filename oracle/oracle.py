@@ -33,6 +33,8 @@ def lib():
         L.oracle_gate_logits.argtypes = [vp, i32, vp, vp, i32, i32, i32, vp, i32, vp]
         L.oracle_topk_renorm.restype = None
         L.oracle_topk_renorm.argtypes = [vp, i32, i32, i32, vp, vp]
+        L.oracle_topk_renorm_grouped.restype = None
+        L.oracle_topk_renorm_grouped.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp]
         L.oracle_load.restype = None
         L.oracle_load.argtypes = [vp, i32, i32, i32, vp]
         L.oracle_capacity.restype = ctypes.c_int32
@@ -95,13 +97,19 @@ def gate_logits(x, Wg, bias=None, rows=None):
     return out
 
 
-def topk_renorm(logits, k):
-    """Top-k expert ids (logit desc, id asc) and renormalised weights, [T, k] each."""
+def topk_renorm(logits, k, n_group=0, topk_group=0):
+    """Top-k expert ids (logit desc, id asc) and renormalised weights, [T, k] each.
+    With n_group > 0 the selection is group-limited: only the experts of the topk_group
+    groups with the best expert logit are candidates."""
     logits = np.ascontiguousarray(logits, np.float32)
     T, E = logits.shape
     idx = np.empty((T, k), np.int32)
     w = np.empty((T, k), np.float32)
-    lib().oracle_topk_renorm(_p(logits), T, E, k, _p(idx), _p(w))
+    if n_group > 0:
+        lib().oracle_topk_renorm_grouped(_p(logits), T, E, k, n_group, topk_group, _p(idx),
+                                         _p(w))
+    else:
+        lib().oracle_topk_renorm(_p(logits), T, E, k, _p(idx), _p(w))
     return idx, w
 
 

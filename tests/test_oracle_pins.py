@@ -420,3 +420,82 @@ def test_load_sums_to_T_times_k():
         k = int(rng.integers(1, E + 1))
         idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
         assert orc.load(idx, E).sum() == T * k
+
+
+# --------------------------------------------------------------------------
+# group-limited routing ["MoE 并行" 通信瓶颈 table, Hierarchical Routing: groups
+# first, then experts; adv12 section 5: each token's experts on at most M devices]
+# --------------------------------------------------------------------------
+
+def _brute_grouped(L, k, n_group, topk_group):
+    """Enumerate every choice of topk_group groups and every k-subset of their experts.
+    The chosen groups are the subset whose (group best logit, -group id) pairs, sorted
+    descending, are lexicographically largest; the experts are the k-subset of those
+    groups' experts whose (logit, -id) pairs, sorted descending, are largest."""
+    E = L.shape[0]
+    gs = E // n_group
+    gkey = [(float(L[g * gs:(g + 1) * gs].max()), -g) for g in range(n_group)]
+    best_groups = max(itertools.combinations(range(n_group), topk_group),
+                      key=lambda c: sorted((gkey[g] for g in c), reverse=True))
+    cand = [e for e in range(E) if e // gs in best_groups]
+    best = max(itertools.combinations(cand, k),
+               key=lambda c: sorted(((float(L[e]), -e) for e in c), reverse=True))
+    return sorted(best, key=lambda e: (-float(L[e]), e))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_grouped_topk_equals_brute_force(seed):
+    rng = np.random.default_rng(100 + seed)
+    for E, n_group, topk_group, k in ((8, 4, 2, 3), (12, 3, 1, 2), (8, 2, 1, 4), (12, 4, 3, 5)):
+        # a coarse grid of values makes ties (within and across groups) common
+        L = (rng.integers(-4, 5, size=(6, E)) / 4.0).astype(np.float32)
+        idx, w = orc.topk_renorm(L, k, n_group, topk_group)
+        for t in range(L.shape[0]):
+            assert list(idx[t]) == _brute_grouped(L[t], k, n_group, topk_group)
+            ex = np.exp(L[t, idx[t]].astype(np.float64) - L[t, idx[t][0]])
+            assert np.allclose(w[t], ex / ex.sum(), rtol=1e-6, atol=0)
+
+
+@pytest.mark.parametrize("E,k,n_group,topk_group", [
+    (16, 3, 1, 1),     # one group holds every expert
+    (16, 3, 4, 4),     # every group kept
+    (16, 3, 16, 3),    # groups of one expert, as many groups kept as experts needed
+    (32, 8, 32, 12),
+])
+def test_grouped_topk_reduces_to_plain_topk(E, k, n_group, topk_group):
+    rng = np.random.default_rng(E + k)
+    L = rng.standard_normal((50, E)).astype(np.float32)
+    a = orc.topk_renorm(L, k, n_group, topk_group)
+    b = orc.topk_renorm(L, k)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_grouped_topk_worked_example():
+    # Four groups of two experts, keep two groups, top 3. Group best logits are
+    # 0.9 (g0), 0.85 (g1), 0.86 (g2), 0.2 (g3), so groups 0 and 2 are kept and the
+    # third expert is 1 (0.1, lower id than expert 5 at 0.1) - not expert 2 (0.85),
+    # which plain top-3 would take. (Derived by hand from the two steps above.)
+    L = np.array([[0.9, 0.1, 0.85, 0.84, 0.86, 0.1, 0.2, 0.1]], np.float32)
+    idx, _ = orc.topk_renorm(L, 3, 4, 2)
+    assert idx[0].tolist() == [0, 4, 1]
+    assert orc.topk_renorm(L, 3)[0][0].tolist() == [0, 4, 2]
+
+
+def test_grouped_topk_keeps_experts_within_the_chosen_groups():
+    rng = np.random.default_rng(7)
+    E, k, n_group, topk_group = 256, 8, 8, 4
+    L = rng.standard_normal((200, E)).astype(np.float32)
+    idx, _ = orc.topk_renorm(L, k, n_group, topk_group)
+    gs = E // n_group
+    for t in range(200):
+        groups = set(int(e) // gs for e in idx[t])
+        assert len(groups) <= topk_group
+        gbest = L[t].reshape(n_group, gs).max(axis=1)
+        chosen_min = min(gbest[g] for g in groups)
+        # every group with a better best logit than the weakest chosen group is used
+        # or was out-competed inside the chosen groups: its best expert is not above the
+        # k-th kept logit
+        kth = L[t, idx[t][-1]]
+        for g in range(n_group):
+            if g not in groups and gbest[g] > chosen_min:
+                assert gbest[g] <= kth
