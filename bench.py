@@ -227,7 +227,7 @@ def cpu_oracle_sample(wl, sample_tokens, seed=0):
     Wg, gb = wl.wg_host(), wl.gate_bias_host()
     t0 = time.perf_counter()
     L = orc.gate_logits(x, Wg, gb)
-    idx, w = orc.topk_renorm(L, wl.k)
+    idx, w = orc.topk_renorm(L, wl.k, wl.n_group, wl.topk_group)
     cap = orc.capacity(np.float32(wl.cf), wl.T, wl.k, wl.E)
     counts, offsets, pt, ps, sd = orc.dispatch(idx, wl.E, cap)
     t_route = time.perf_counter() - t0
@@ -482,6 +482,7 @@ def run_ours(args, wl):
         "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "top_k": wl.k,
                    "F": wl.F, "kind": wl.kind, "capacity_factor": wl.cf,
                    "shared_expert": wl.has_shared, "residual": wl.add_residual,
+                   "expert_groups": [wl.n_group, wl.topk_group] if wl.n_group else None,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"flushed between steps ({args.flush_mib} MiB write)",
                    "kept_rows_P": P, "touched_experts": touched},

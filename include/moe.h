@@ -82,6 +82,13 @@ typedef struct {
     int32_t has_shared;        /* 1: one always-on shared expert of the same kind, weight 1 */
     int32_t add_residual;      /* 1: out = x + combine (tokens whose every slot overflowed
                                   the capacity leave the layer as x, bit for bit) */
+    int32_t n_group;           /* 0: plain top-k. Else group-limited routing ["MoE 并行" 通信瓶颈,
+                                  Hierarchical Routing; adv12 5, device-limited routing]: the
+                                  E experts form n_group groups of E/n_group consecutive ids
+                                  (n_group divides E, at most 32) ... */
+    int32_t topk_group;        /* ... only the topk_group groups with the highest best-expert
+                                  logit (ties to the lower group id) supply the top k;
+                                  1 <= topk_group <= n_group, k <= topk_group * E / n_group */
 } moe_config;
 
 /* One set of stacked expert weights (nn.Linear [out, in] layout, K contiguous).

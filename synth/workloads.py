@@ -39,6 +39,8 @@ class Workload:
     gate_dist: str = "normal"   # "normal" | "uniform"
     gate_bias: str = "none"     # "none" | "zipf" | "hot" (+20 on expert 0: one expert takes all)
     expert_bias: bool = False
+    n_group: int = 0            # group-limited routing: expert groups (0 = plain top-k)
+    topk_group: int = 0         # groups kept per token
     seed: int = 0
     note: str = ""
 
@@ -209,6 +211,10 @@ WORKLOADS = {
     "deepseek": Workload("deepseek", T=8192, d=7168, E=256, k=8, F=2048, kind="swiglu",
                          act="bf16", cf=1.0, has_shared=True,
                          note="DeepSeek-V3-shaped: 256 routed + 1 shared SwiGLU experts, top-8, cf 1.0"),
+    "deepseek_grouped": Workload("deepseek_grouped", T=8192, d=7168, E=256, k=8, F=2048,
+                                 kind="swiglu", act="bf16", cf=1.0, has_shared=True, n_group=8,
+                                 topk_group=4,
+                                 note="DeepSeek-V3-shaped, group-limited routing: 8 groups, 4 kept"),
     "deepseek_cf125": Workload("deepseek_cf125", T=8192, d=7168, E=256, k=8, F=2048,
                                kind="swiglu", act="bf16", cf=1.25, has_shared=True,
                                note="DeepSeek-V3-shaped, capacity factor 1.25"),

@@ -105,7 +105,7 @@ def check_logits(wl, x_host, rows, L_gpu_rows):
 def check_routing(r):
     """idx bit-exact and w within 2e-6 against the oracle fed the GPU logits."""
     L = to_np(r.logits)
-    idx_ref, w_ref = orc.topk_renorm(L, r.wl.k)
+    idx_ref, w_ref = orc.topk_renorm(L, r.wl.k, r.wl.n_group, r.wl.topk_group)
     idx = to_np(r.idx)
     assert np.array_equal(idx, idx_ref), f"{(idx != idx_ref).sum()} top-k ids differ"
     w = to_np(r.w)

@@ -84,7 +84,11 @@ def test_workspace_and_rows(lib):
     dict(top_k=0), dict(top_k=5, E=4), dict(E=0), dict(E=1025), dict(d=12), dict(d=4),
     dict(T=-1), dict(top_k=33, E=64), dict(F=96), dict(F=0), dict(d=72),
     dict(T=2 ** 28, top_k=8), dict(capacity_factor=float("nan")), dict(kind=7),
-    dict(act_dtype=3), dict(has_shared=2), dict(add_residual=-1)])
+    dict(act_dtype=3), dict(has_shared=2), dict(add_residual=-1),
+    # group-limited routing: groups must divide E, keep 1..n_group groups, hold k experts
+    dict(n_group=3, topk_group=1), dict(n_group=2, topk_group=0), dict(n_group=2, topk_group=3),
+    dict(n_group=64, topk_group=1, E=64), dict(n_group=4, topk_group=1, top_k=2),
+    dict(n_group=-1, topk_group=1)])
 def test_invalid_configs_rejected(lib, bad):
     base = dict(T=64, d=128, E=4, top_k=2, F=128, capacity_factor=0.0, act_dtype=C.MOE_BF16,
                 kind=C.MOE_EXPERT_GELU, has_shared=0, add_residual=0)
@@ -95,6 +99,13 @@ def test_invalid_configs_rejected(lib, bad):
     fake = ctypes.c_void_p(1 << 20)
     st = lib.moe_route(ctypes.byref(cfg), fake, fake, None, fake, fake, fake, fake, None)
     assert st in (C.MOE_ERR_INVALID_ARG, C.MOE_ERR_UNSUPPORTED)
+
+
+def test_grouped_routing_configs_accepted(lib):
+    for n_group, topk_group, E, k in ((2, 1, 4, 2), (4, 2, 4, 2), (8, 4, 256, 8), (32, 1, 32, 1)):
+        cfg = api.make_config(64, 128, E, k, 128, 0.0, "gelu", True, n_group=n_group,
+                              topk_group=topk_group)
+        assert api.workspace_size(cfg) > 0
 
 
 def test_unsupported_dtype_kind_pairs(lib):

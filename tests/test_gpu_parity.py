@@ -43,6 +43,11 @@ SMALL = {
                             cf=1.0, add_residual=True, expert_bias=True),
     "split_swiglu_k8": W("ss8", T=2, d=2048, E=64, k=8, F=256, kind="swiglu", act="bf16",
                          gate_dist="uniform"),
+    # group-limited routing: tensor-core router (T >= 256) and split-K router (few tokens)
+    "grouped_tc": W("gtc", T=300, d=128, E=32, k=4, F=128, kind="swiglu", act="bf16",
+                    n_group=8, topk_group=2, has_shared=True),
+    "grouped_small_T": W("gst", T=40, d=256, E=64, k=6, F=64, kind="gelu", act="bf16",
+                         n_group=16, topk_group=3, cf=1.0),
     # top-1 without residual and with drops: the fused combine writes dropped tokens as 0
     "top1_drop_no_residual": W("t1d", T=300, d=128, E=4, k=1, F=192, kind="gelu", act="bf16",
                                cf=0.5, expert_bias=True),
@@ -127,6 +132,7 @@ def test_forward_is_deterministic():
 
 @pytest.mark.parametrize("name,sample", [
     ("switch", 32), ("mixtral", 8), ("deepseek", 4), ("deepseek_cf125", 4),
+    ("deepseek_grouped", 4),
     ("decode1", None), ("decode8", 4), ("decode64", 4),
 ])
 def test_full_size_sampled(name, sample):

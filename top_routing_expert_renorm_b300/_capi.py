@@ -29,7 +29,8 @@ class MoeConfig(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("F", ctypes.c_int32),
                 ("capacity_factor", ctypes.c_float), ("act_dtype", ctypes.c_int32),
                 ("kind", ctypes.c_int32), ("has_shared", ctypes.c_int32),
-                ("add_residual", ctypes.c_int32)]
+                ("add_residual", ctypes.c_int32), ("n_group", ctypes.c_int32),
+                ("topk_group", ctypes.c_int32)]
 
 
 class MoeExpertWeights(ctypes.Structure):

@@ -40,19 +40,21 @@ def _stream(stream):
 
 
 def make_config(T, d, E, top_k, F=0, capacity_factor=0.0, kind="gelu", bf16=True,
-                has_shared=False, add_residual=False):
+                has_shared=False, add_residual=False, n_group=0, topk_group=0):
     kinds = {"linear": C.MOE_EXPERT_LINEAR, "gelu": C.MOE_EXPERT_GELU,
              "swiglu": C.MOE_EXPERT_SWIGLU}
     return MoeConfig(T=T, d=d, E=E, top_k=top_k, F=F, capacity_factor=capacity_factor,
                      act_dtype=C.MOE_BF16 if bf16 else C.MOE_F32, kind=kinds[kind],
-                     has_shared=int(bool(has_shared)), add_residual=int(bool(add_residual)))
+                     has_shared=int(bool(has_shared)), add_residual=int(bool(add_residual)),
+                     n_group=n_group, topk_group=topk_group)
 
 
 def config_for(workload, T=None):
     """MoeConfig of a synth.Workload (optionally with another token count)."""
     return make_config(T if T is not None else workload.T, workload.d, workload.E, workload.k,
                        workload.F if workload.kind != "linear" else 0, workload.cf,
-                       workload.kind, workload.bf16, workload.has_shared, workload.add_residual)
+                       workload.kind, workload.bf16, workload.has_shared, workload.add_residual,
+                       workload.n_group, workload.topk_group)
 
 
 def weights(w1, b1=None, w2=None, b2=None):

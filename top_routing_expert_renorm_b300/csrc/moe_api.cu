@@ -169,6 +169,11 @@ moe_status check_cfg(const moe_config* c) {
     if ((c->has_shared != 0 && c->has_shared != 1) || (c->add_residual != 0 && c->add_residual != 1))
         return MOE_ERR_INVALID_ARG;
     if (c->act_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (c->n_group != 0) {
+        if (c->n_group < 1 || c->n_group > 32 || c->E % c->n_group != 0) return MOE_ERR_INVALID_ARG;
+        if (c->topk_group < 1 || c->topk_group > c->n_group) return MOE_ERR_INVALID_ARG;
+        if ((int64_t)c->top_k > (int64_t)c->topk_group * (c->E / c->n_group)) return MOE_ERR_INVALID_ARG;
+    }
     switch (c->kind) {
         case MOE_EXPERT_LINEAR:
             if (c->act_dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
@@ -230,7 +235,7 @@ RouterPlan router_plan(const moe_config& c) {
         r.bg_bytes = al256(3 * (size_t)r.Ep * d * 2);
         // partial logits only when the three terms do not fit one accumulator (E > 64);
         // otherwise the GEMM epilogue selects the top k itself
-        r.d_bytes = r.Ep <= 64 ? 0 : al256(T * 3 * (size_t)r.Ep * 4);
+        r.d_bytes = (r.Ep <= 64 && c.n_group == 0) ? 0 : al256(T * 3 * (size_t)r.Ep * 4);
         r.scratch_bytes = r.bg_bytes + r.d_bytes + 256;
     } else {
         r.path = 3;
@@ -522,7 +527,7 @@ moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const
                    launch_k(gate_split_kernel, grid, 256, 0, s,
                        Wg, d, E, rp.Ep, Bg, T, tables,
                        reinterpret_cast<unsigned long long*>(tables + 4)));
-        if (rp.Ep <= 64) {   // the three terms fit one 256-column accumulator: fused top-k
+        if (rp.Ep <= 64 && c.n_group == 0) {   // the three terms fit one accumulator: fused top-k
             MOE_TRY(launch_gemm<EPI_ROUTER_TOPK>(
                 x, T, d, Bg, 3ll * rp.Ep, 3 * rp.Ep, 1, 3 * rp.Ep, tables, tables + 2, logits, E,
                 bias, nullptr, nullptr, nullptr, k, s, nullptr, SplitPlan(), nullptr,
@@ -547,10 +552,8 @@ moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const
     }
     MOE_LAUNCH("topk_renorm", s,
                launch_k(topk_renorm_kernel, (T + kTopkTok - 1) / kTopkTok, 256,
-                                    kTopkTok * E * sizeof(float), s, parts, rp.n_parts,
-                                                                      rp.part_stride,
-                                                              rp.row_stride, bias, logits, T, E,
-                                                              k, idx, w));
+                        kTopkTok * E * sizeof(float), s, parts, rp.n_parts, rp.part_stride,
+                        rp.row_stride, bias, logits, T, E, k, c.n_group, c.topk_group, idx, w));
     return MOE_OK;
 }
 

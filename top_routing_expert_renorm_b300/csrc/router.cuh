@@ -205,7 +205,8 @@ __global__ void __launch_bounds__(256) topk_renorm_kernel(const float* __restric
                                                           long long row_stride,
                                                           const float* __restrict__ bias,
                                                           float* __restrict__ logits, int T,
-                                                          int E, int k, int* __restrict__ idx,
+                                                          int E, int k, int n_group,
+                                                          int topk_group, int* __restrict__ idx,
                                                           float* __restrict__ w) {
     pdl_entry();
     extern __shared__ float sL[];   // [kTopkTok][E]
@@ -242,6 +243,38 @@ __global__ void __launch_bounds__(256) topk_renorm_kernel(const float* __restric
         if (e < E) {
             v[i] = Ls[e];
             avail |= 1u << i;
+        }
+    }
+    if (n_group > 0) {
+        // Group-limited routing: lane g < n_group scores group g by its best logit; the
+        // topk_group best groups (ties to the lower group id) are kept and every expert
+        // of the other groups leaves the candidate set.
+        const int gsize = E / n_group;
+        float gbest = 0.0f;
+        if (lane < n_group) {
+            gbest = Ls[lane * gsize];
+            for (int e = lane * gsize + 1; e < (lane + 1) * gsize; ++e) gbest = fmaxf(gbest, Ls[e]);
+        }
+        uint32_t gavail = (lane < n_group) ? 1u : 0u, chosen = 0;
+        for (int j = 0; j < topk_group; ++j) {
+            float bv = gbest;
+            int bg = gavail ? lane : -1;
+#pragma unroll
+            for (int off = 16; off; off >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                const int og = __shfl_xor_sync(0xffffffffu, bg, off);
+                if (og >= 0 && better(ov, og, bv, bg)) {
+                    bv = ov;
+                    bg = og;
+                }
+            }
+            chosen |= 1u << bg;
+            if (bg == lane) gavail = 0;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !((chosen >> (e / gsize)) & 1u)) avail &= ~(1u << i);
         }
     }
     float my_v = 0.0f, l0 = 0.0f;
