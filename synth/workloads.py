@@ -218,6 +218,11 @@ WORKLOADS = {
     "deepseek_cf125": Workload("deepseek_cf125", T=8192, d=7168, E=256, k=8, F=2048,
                                kind="swiglu", act="bf16", cf=1.25, has_shared=True,
                                note="DeepSeek-V3-shaped, capacity factor 1.25"),
+    # per-expert shapes of the DeepSeek-V3-shaped layer with 32 experts and 1024 tokens
+    # (256 rows per expert at capacity 1.0): small enough for multi-pass profiler captures
+    "deepseek_e32": Workload("deepseek_e32", T=1024, d=7168, E=32, k=8, F=2048, kind="swiglu",
+                             act="bf16", cf=1.0, has_shared=True,
+                             note="DeepSeek-V3 expert shapes, 32 experts (for profiling)"),
     "decode1": Workload("decode1", T=1, d=7168, E=256, k=8, F=2048, kind="swiglu", act="bf16",
                         gate_dist="uniform", note="decode, 1 token"),
     "decode8": Workload("decode8", T=8, d=7168, E=256, k=8, F=2048, kind="swiglu", act="bf16",
