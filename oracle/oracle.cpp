@@ -21,6 +21,8 @@
 //   [SafeSM]   "MoE 混合专家架构", section 4.2 数值稳定性 (max-subtracted softmax).
 //   [Merged]   "MoE 混合专家架构", section 5.2 专家融合与并行 (stacked W1, silu on the W1 slice).
 //   [LPT]      adv12 sections 3.3 EPLB and 4.3 eplb_rebalance; 4.2 expert_imbalance; Q3.
+//   [Quant]    "MoE 混合专家架构", section 5.3 量化支持 (expert weights may be stored as INT8 /
+//              INT4 with an acceptable accuracy loss).
 //   [Hier]     "MoE 并行", 通信瓶颈 table, row Hierarchical Routing (pick groups first, then
 //              experts); adv12 section 5 (DeepSeek-V3: device-limited routing, each token's
 //              experts lie on at most M devices).
@@ -34,7 +36,9 @@
 //   * the hidden activation h is rounded to bf16 when the weights are bf16;
 //   * the shared expert has weight 1 for every token;
 //   * group-limited routing scores a group by its best expert logit (the pages name the
-//     two steps but not the score).
+//     two steps but not the score);
+//   * INT8 experts are weight-only, symmetric, one absmax scale per weight row (the pages
+//     name INT8 / INT4 but no scheme).
 //
 // Parity status: every exported function is pinned by the CPU test suite against
 // values printed on the pages, closed forms, or brute force on tiny inputs,
@@ -289,6 +293,66 @@ void oracle_expert_row(int kind, const void* x_row, int x_dtype,
     for (int o = 0; o < d; ++o) {
         double acc = 0.0;
         for (int f = 0; f < F; ++f) acc += load_elem(w2, w_dtype, (long long)o * F + f) * h[f];
+        if (b2) acc += (double)b2[o];
+        y[o] = acc;
+    }
+}
+
+// Weight-only INT8 experts [Quant]: every weight row n (an output channel of W1 or W2)
+// is stored as int8 codes q[n][k] and one fp32 scale s[n]; the expert computes with the
+// dequantised weights s[n] * q[n][k] (formed exactly in double).
+//   quantize: s = max_k |w[n][k]| / 127, q = round-half-even(w / s) clamped to [-127, 127],
+//   both in fp32 arithmetic (a floating-point decision that yields an integer code is made
+//   in the precision the kernel uses); an all-zero row has s = 0 and q = 0.
+void oracle_quantize_rows_i8(const uint16_t* w_bf16, long long rows, int cols, int8_t* q,
+                             float* scale) {
+    for (long long r = 0; r < rows; ++r) {
+        float m = 0.0f;
+        for (int c = 0; c < cols; ++c) {
+            const float v = std::fabs((float)bf16_bits_to_double(w_bf16[r * cols + c]));
+            if (v > m) m = v;
+        }
+        const float sc = m / 127.0f;
+        scale[r] = sc;
+        for (int c = 0; c < cols; ++c) {
+            float qv = 0.0f;
+            if (sc > 0.0f) {
+                const float v = (float)bf16_bits_to_double(w_bf16[r * cols + c]);
+                qv = std::nearbyint(v / sc);   // default rounding mode: nearest, ties to even
+                if (qv > 127.0f) qv = 127.0f;
+                if (qv < -127.0f) qv = -127.0f;
+            }
+            q[r * cols + c] = (int8_t)qv;
+        }
+    }
+}
+
+// O8 with INT8 weights: as oracle_expert_row for GELU / SWIGLU, the weight of row n,
+// column c being s[n] * q[n][c]. h is rounded to bf16 (the activations are bf16).
+void oracle_expert_row_q8(int kind, const void* x_row, int x_dtype, const int8_t* q1,
+                          const float* s1, const float* b1, const int8_t* q2, const float* s2,
+                          const float* b2, int d, int F, double* y) {
+    auto w1 = [&](long long r, int c) { return (double)s1[r] * (double)q1[r * d + c]; };
+    auto w2 = [&](long long r, int c) { return (double)s2[r] * (double)q2[r * F + c]; };
+    std::vector<double> h(F);
+    for (int f = 0; f < F; ++f) {
+        double a = 0.0;
+        for (int c = 0; c < d; ++c) a += w1(f, c) * load_elem(x_row, x_dtype, c);
+        if (b1) a += (double)b1[f];
+        double hv;
+        if (kind == ORC_GELU) {
+            hv = gelu_exact(a);
+        } else {
+            double u = 0.0;
+            for (int c = 0; c < d; ++c) u += w1(F + f, c) * load_elem(x_row, x_dtype, c);
+            if (b1) u += (double)b1[F + f];
+            hv = silu(a) * u;
+        }
+        h[f] = bf16_bits_to_double(double_to_bf16_rne(hv));
+    }
+    for (int o = 0; o < d; ++o) {
+        double acc = 0.0;
+        for (int f = 0; f < F; ++f) acc += w2(o, f) * h[f];
         if (b2) acc += (double)b2[o];
         y[o] = acc;
     }

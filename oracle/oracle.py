@@ -43,6 +43,10 @@ def lib():
         L.oracle_dispatch.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
         L.oracle_expert_row.restype = None
         L.oracle_expert_row.argtypes = [i32, vp, i32, vp, vp, vp, vp, i32, i32, i32, vp]
+        L.oracle_quantize_rows_i8.restype = None
+        L.oracle_quantize_rows_i8.argtypes = [vp, ctypes.c_longlong, i32, vp, vp]
+        L.oracle_expert_row_q8.restype = None
+        L.oracle_expert_row_q8.argtypes = [i32, vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, vp]
         L.oracle_combine_row.restype = None
         L.oracle_combine_row.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, i32]
         L.oracle_forward.restype = None
@@ -209,3 +213,27 @@ def load_report(load_arr, D):
                              ctypes.byref(imb), ctypes.byref(vl), ctypes.byref(vn))
     return dict(assign=assign, dev_load=dev, naive_load=naive, imbalance=imb.value,
                 var_lpt=vl.value, var_naive=vn.value)
+
+
+def quantize_rows_i8(w_bf16):
+    """Per-row absmax INT8 codes [rows, cols] int8 and fp32 scales [rows] of a bf16 matrix
+    (uint16 bit patterns, any leading shape; rows = all but the last axis)."""
+    w = np.ascontiguousarray(w_bf16, np.uint16)
+    cols = w.shape[-1]
+    rows = w.size // cols
+    q = np.empty(w.shape, np.int8)
+    s = np.empty(w.shape[:-1], np.float32)
+    lib().oracle_quantize_rows_i8(_p(w), rows, cols, _p(q), _p(s))
+    return q, s
+
+
+def expert_row_q8(kind, x_row, q1, s1, b1, q2, s2, b2, d, F):
+    """One token through one GELU / SWIGLU expert with INT8 weights (dequantised s*q)."""
+    x_row = np.ascontiguousarray(x_row)
+    xd = BF16 if x_row.dtype == np.uint16 else F32
+    y = np.empty(d, np.float64)
+    lib().oracle_expert_row_q8(kind, _p(x_row), xd, _p(np.ascontiguousarray(q1, np.int8)),
+                               _p(np.ascontiguousarray(s1, np.float32)), _p(b1),
+                               _p(np.ascontiguousarray(q2, np.int8)),
+                               _p(np.ascontiguousarray(s2, np.float32)), _p(b2), d, F, _p(y))
+    return y

@@ -499,3 +499,77 @@ def test_grouped_topk_keeps_experts_within_the_chosen_groups():
         for g in range(n_group):
             if g not in groups and gbest[g] > chosen_min:
                 assert gbest[g] <= kth
+
+
+# --------------------------------------------------------------------------
+# weight-only INT8 experts ["MoE 混合专家架构" 5.3 量化支持: expert weights in INT8 / INT4]
+# reading: one symmetric absmax scale per weight row, s = max|w| / 127, q = rne(w / s)
+# --------------------------------------------------------------------------
+
+def _bf16_bits(values):
+    f = np.asarray(values, np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def test_quantize_rows_on_the_grid_are_exact():
+    # rows whose entries are integers m times a power of two, with max |m| = 127: the
+    # scale is that power of two and the codes are the integers themselves
+    rng = np.random.default_rng(1)
+    m = rng.integers(-127, 128, size=(6, 40))
+    m[:, 3] = 127 * np.array([1, -1, 1, -1, 1, -1])
+    scales = 2.0 ** np.array([-7, -3, 0, 2, -12, -1])
+    w = _bf16_bits(m * scales[:, None])
+    q, s = orc.quantize_rows_i8(w)
+    assert np.array_equal(s, scales.astype(np.float32))
+    assert np.array_equal(q.astype(np.int64), m)
+
+
+def test_quantize_rows_bound_max_and_zero_row():
+    rng = np.random.default_rng(2)
+    vals = rng.standard_normal((50, 64)).astype(np.float32) * rng.uniform(0.01, 10, (50, 1))
+    vals[7] = 0.0
+    w = _bf16_bits(vals)
+    wf = bf16_bits_to_f64(w)
+    q, s = orc.quantize_rows_i8(w)
+    assert s[7] == 0.0 and not q[7].any()
+    for r in range(50):
+        if r == 7:
+            continue
+        amax = np.abs(wf[r]).max()
+        assert s[r] == np.float32(np.float32(amax) / np.float32(127.0))
+        assert np.abs(q[r]).max() == 127                 # the largest entry maps to +-127
+        err = np.abs(wf[r] - s[r].astype(np.float64) * q[r])
+        # nearest code, up to the fp32 rounding of w / s (half an ulp of a value below 128)
+        assert (err <= s[r] * (0.5 + 2.0 ** -17)).all()
+
+
+def test_quantize_rows_ties_go_to_even():
+    # scale 2^-6 (the row holds 127 * 2^-6); 2.5 * 2^-6 and 3.5 * 2^-6 lie halfway between codes
+    w = _bf16_bits([[127 * 2.0 ** -6, 2.5 * 2.0 ** -6, 3.5 * 2.0 ** -6, -2.5 * 2.0 ** -6]])
+    q, s = orc.quantize_rows_i8(w)
+    assert s[0] == 2.0 ** -6
+    assert q[0].tolist() == [127, 2, 4, -2]
+
+
+@pytest.mark.parametrize("kind,F", [(orc.GELU, 48), (orc.SWIGLU, 32)])
+def test_int8_expert_equals_bf16_expert_on_exactly_representable_weights(kind, F):
+    # power-of-two scales: every s * q is a bf16 value, so the INT8 expert must agree
+    # bit for bit with the (pinned) bf16 expert given those weights
+    rng = np.random.default_rng(kind + F)
+    d = 24
+    N1 = F if kind == orc.GELU else 2 * F
+    q1 = rng.integers(-127, 128, (N1, d)).astype(np.int8)
+    q2 = rng.integers(-127, 128, (d, F)).astype(np.int8)
+    s1 = (2.0 ** rng.integers(-12, -4, N1)).astype(np.float32)
+    s2 = (2.0 ** rng.integers(-12, -4, d)).astype(np.float32)
+    b1 = rng.standard_normal(N1).astype(np.float32)
+    b2 = rng.standard_normal(d).astype(np.float32)
+    w1 = _bf16_bits(s1[:, None] * q1.astype(np.float32))
+    w2 = _bf16_bits(s2[:, None] * q2.astype(np.float32))
+    assert np.array_equal(bf16_bits_to_f64(w1), s1[:, None].astype(np.float64) * q1)
+    for t in range(4):
+        x = _bf16_bits(rng.standard_normal(d))
+        a = orc.expert_row_q8(kind, x, q1, s1, b1, q2, s2, b2, d, F)
+        b = orc.expert_row(kind, x, w1, b1, w2, b2, d, F)
+        assert np.array_equal(a, b)
