@@ -126,18 +126,22 @@ def kernel_algorithmic_cost(wl, name, P, touched):
     es = 2 if wl.bf16 else 4
     T, d, F, E = wl.T, wl.d, wl.F, wl.E
     N1 = wl.N1
+    name = name.replace("_q8", "")          # INT8-weight kernels: same algorithm
+    we = 1 if wl.int8 else 2               # bytes per expert weight
+    sc1 = 4 * N1 if wl.int8 else 0         # per-row scales of one expert
+    sc2 = 4 * d if wl.int8 else 0
     up = {"grouped_gemm_gelu", "grouped_gemm_swiglu"}
     if name in up:
         fl = 2.0 * P * d * N1
-        by = touched * N1 * d * 2 + P * d * 2 + P * F * 2
+        by = touched * (N1 * d * we + sc1) + P * d * 2 + P * F * 2
         if wl.has_shared:
             fl += 2.0 * T * d * N1
-            by += N1 * d * 2 + T * d * 2 + T * F * 2
+            by += N1 * d * we + sc1 + T * d * 2 + T * F * 2
         return fl, by
     if name == "grouped_gemm_scale":
-        return 2.0 * P * F * d, touched * d * F * 2 + P * F * 2 + P * d * 4
+        return 2.0 * P * F * d, touched * (d * F * we + sc2) + P * F * 2 + P * d * 4
     if name == "grouped_gemm_combine1":   # top-1 down projection writing the layer output
-        return 2.0 * P * F * d, (touched * d * F * 2 + P * F * 2 + P * d * es
+        return 2.0 * P * F * d, (touched * (d * F * we + sc2) + P * F * 2 + P * d * es
                                  + (P * d * es if wl.add_residual else 0))
     if name == "copy_dropped":            # dropped tokens (T - P of them) leave as x or 0
         return 0.0, T * wl.k * 4 + (T - P) * d * es * (2 if wl.add_residual else 1)
@@ -164,6 +168,7 @@ def kernel_algorithmic_cost(wl, name, P, touched):
 
 
 KERNEL_FILES = {
+    "grouped_gemm_q8": ["grouped_gemm_q8.cuh", "grouped_gemm.cuh", "common.cuh"],
     "grouped_gemm": ["grouped_gemm.cuh", "common.cuh"],
     "router_gemm_tc": ["grouped_gemm.cuh", "common.cuh"],
     "router_gemm_topk": ["grouped_gemm.cuh", "common.cuh"],
@@ -232,9 +237,17 @@ def cpu_oracle_sample(wl, sample_tokens, seed=0):
     counts, offsets, pt, ps, sd = orc.dispatch(idx, wl.E, cap)
     t_route = time.perf_counter() - t0
     need = sorted({int(idx[t, j]) for t in rows for j in range(wl.k) if sd[t, j] >= 0})
-    Wc = {e: (wl.w1_host(e), wl.b1_host(e), wl.w2_host(e), wl.b2_host(e)) for e in need}
-    shared = ((wl.w1_host(0, True), wl.b1_host(0, True), wl.w2_host(0, True),
-               wl.b2_host(0, True)) if wl.has_shared else None)
+
+    def expert_fn(e, shared=False):
+        w1, b1, w2, b2 = (wl.w1_host(e, shared), wl.b1_host(e, shared), wl.w2_host(e, shared),
+                          wl.b2_host(e, shared))
+        if wl.int8:
+            q1, s1 = orc.quantize_rows_i8(w1)
+            q2, s2 = orc.quantize_rows_i8(w2)
+            return lambda xr: orc.expert_row_q8(wl.kind_code, xr, q1, s1, b1, q2, s2, b2, wl.d, wl.F)
+        return lambda xr: orc.expert_row(wl.kind_code, xr, w1, b1, w2, b2, wl.d, wl.F)
+    Wc = {e: expert_fn(e) for e in need}
+    shared = expert_fn(0, True) if wl.has_shared else None
     t0 = time.perf_counter()
     for t in rows:
         xr = np.ascontiguousarray(x[t])
@@ -242,9 +255,8 @@ def cpu_oracle_sample(wl, sample_tokens, seed=0):
         kept = (sd[t] >= 0).astype(np.int32)
         for j in range(wl.k):
             if kept[j]:
-                w1, b1, w2, b2 = Wc[int(idx[t, j])]
-                ys[j] = orc.expert_row(wl.kind_code, xr, w1, b1, w2, b2, wl.d, wl.F)
-        ysh = orc.expert_row(wl.kind_code, xr, *shared, wl.d, wl.F) if shared else None
+                ys[j] = Wc[int(idx[t, j])](xr)
+        ysh = shared(xr) if shared else None
         orc.combine_row(xr, wl.add_residual, w[t], kept, ys, ysh,
                         orc.BF16 if wl.bf16 else orc.F32)
     t_ffn = time.perf_counter() - t0
@@ -320,6 +332,11 @@ def run_ours(args, wl):
     cfg = moe.config_for(wl)
     layer = moe.MoELayer(cfg, inp["wg"], inp["gate_bias"], inp["w1"], inp["b1"], inp["w2"],
                          inp["b2"], inp["shared"])
+    if wl.int8:
+        # the layer holds the INT8 codes; the bf16 originals are no longer needed
+        inp["w1"] = inp["w2"] = inp["shared"] = None
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
     x = inp["x"]
     out = torch.empty_like(x)
     load = torch.empty(wl.E, dtype=torch.int32, device=dev)
@@ -483,6 +500,7 @@ def run_ours(args, wl):
                    "F": wl.F, "kind": wl.kind, "capacity_factor": wl.cf,
                    "shared_expert": wl.has_shared, "residual": wl.add_residual,
                    "expert_groups": [wl.n_group, wl.topk_group] if wl.n_group else None,
+                   "expert_weights": "int8 codes + fp32 row scales" if wl.int8 else "bf16",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"flushed between steps ({args.flush_mib} MiB write)",
                    "kept_rows_P": P, "touched_experts": touched},

@@ -59,7 +59,7 @@ typedef enum {
     MOE_ERR_DEVICE_INDEX = 7   /* a kernel saw an expert id outside [0,E) and skipped it */
 } moe_status;
 
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_I8 = 2 } moe_dtype;
 
 /* Expert FFN forms.
  *  LINEAR : y = W1 x + b1; W1 [E][d][d] fp32 (the tutorial's nn.Linear(d, d) experts).
@@ -89,6 +89,11 @@ typedef struct {
     int32_t topk_group;        /* ... only the topk_group groups with the highest best-expert
                                   logit (ties to the lower group id) supply the top k;
                                   1 <= topk_group <= n_group, k <= topk_group * E / n_group */
+    int32_t w_dtype;           /* 0 (or act_dtype): weights in act_dtype. MOE_I8 (GELU/SWIGLU
+                                  only): weight-only INT8 experts ["MoE 混合专家架构" 5.3 量化支持]:
+                                  w1/w2 hold int8 codes q and s1/s2 one fp32 scale per weight
+                                  row; the experts compute with s[n] * q[n][k] (see
+                                  moe_quantize_i8). Routed and shared experts alike. */
 } moe_config;
 
 /* One set of stacked expert weights (nn.Linear [out, in] layout, K contiguous).
@@ -99,6 +104,8 @@ typedef struct {
     const float* b1;
     const void* w2;
     const float* b2;
+    const float* s1;   /* w_dtype == MOE_I8: scales [E][N1] of the w1 rows, else ignored */
+    const float* s2;   /* w_dtype == MOE_I8: scales [E][d] of the w2 rows, else ignored */
 } moe_expert_weights;
 
 /* Bytes of scratch needed by any entry point below for this configuration
@@ -219,6 +226,15 @@ moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_idx, 
                                 int32_t* load, int32_t* counts, int32_t* offsets,
                                 int32_t* perm_token, int32_t* perm_slot, int32_t* slot_dest,
                                 void* x_perm, cudaStream_t stream);
+
+/* Weight-only INT8 codes of bf16 weights [the reading of "MoE 混合专家架构" 5.3 used by
+ * MOE_I8 experts]: for every row r of w [rows, cols] (bf16, cols a multiple of 8):
+ *   scale[r] = max_c |w[r][c]| / 127   (fp32)
+ *   q[r][c]  = round-half-even(w[r][c] / scale[r]) clamped to [-127, 127]   (fp32 division)
+ * and scale 0 / codes 0 for an all-zero row. q [rows, cols] int8 and scale [rows] fp32 are
+ * caller-owned device buffers. Stacked expert weights [E][N][K] are E*N rows of K. */
+moe_status moe_quantize_i8(const void* w, int64_t rows, int32_t cols, int8_t* q, float* scale,
+                           cudaStream_t stream);
 
 /* Host-only load report [adv12 3.3 EPLB, 4.2 expert_imbalance, 4.3 eplb_rebalance]:
  * imbalance = max(load) / (min(load) + 1e-6); LPT placement of the E experts on D

@@ -65,8 +65,18 @@ class GpuRun:
         self.x_perm = torch.empty(Pmax, d, dtype=inp["x"].dtype, device=self.dev)
         moe.dispatch(cfg, self.idx, inp["x"], self.load, self.counts, self.offsets,
                      self.perm_token, self.perm_slot, self.slot_dest, self.x_perm, ws)
-        routed = moe.weights(inp["w1"], inp["b1"], inp["w2"], inp["b2"])
-        shared = moe.weights(*inp["shared"]) if inp["shared"] is not None else None
+        if wl.int8:
+            # INT8 experts: codes and row scales from the library's quantiser
+            self.q = moe.quantize_weights(inp["w1"], inp["w2"])
+            routed = moe.weights(self.q[0], inp["b1"], self.q[2], inp["b2"], self.q[1], self.q[3])
+            shared = None
+            if inp["shared"] is not None:
+                sw1, sb1, sw2, sb2 = inp["shared"]
+                self.sq = moe.quantize_weights(sw1, sw2)
+                shared = moe.weights(self.sq[0], sb1, self.sq[2], sb2, self.sq[1], self.sq[3])
+        else:
+            routed = moe.weights(inp["w1"], inp["b1"], inp["w2"], inp["b2"])
+            shared = moe.weights(*inp["shared"]) if inp["shared"] is not None else None
         self.y = torch.empty(Pmax + (T if wl.has_shared else 0), d, **f32)
         moe.expert_ffn(cfg, self.x_perm, self.offsets, routed, shared, inp["x"], self.w,
                        self.perm_token, self.perm_slot, self.y, ws)
@@ -132,6 +142,28 @@ def check_dispatch(r, idx_ref):
     return cap, sd, P
 
 
+def _expert_fn(wl, e, shared=False):
+    """Oracle expert of the workload: bf16 weights, or their INT8 codes for INT8 layers."""
+    w1, b1, w2, b2 = (wl.w1_host(e, shared), wl.b1_host(e, shared), wl.w2_host(e, shared),
+                      wl.b2_host(e, shared))
+    if wl.int8:
+        q1, s1 = orc.quantize_rows_i8(w1)
+        q2, s2 = orc.quantize_rows_i8(w2)
+        return lambda xr: orc.expert_row_q8(wl.kind_code, xr, q1, s1, b1, q2, s2, b2, wl.d, wl.F)
+    return lambda xr: orc.expert_row(wl.kind_code, xr, w1, b1, w2, b2, wl.d, wl.F)
+
+
+def check_quantized_weights(r, experts):
+    """The library's INT8 codes and scales equal the oracle's, bit for bit."""
+    wl = r.wl
+    q1, s1, q2, s2 = r.q
+    for e in experts:
+        oq1, os1 = orc.quantize_rows_i8(wl.w1_host(e))
+        oq2, os2 = orc.quantize_rows_i8(wl.w2_host(e))
+        assert np.array_equal(to_np(q1[e]), oq1) and np.array_equal(to_np(s1[e]), os1)
+        assert np.array_equal(to_np(q2[e]), oq2) and np.array_equal(to_np(s2[e]), os2)
+
+
 def oracle_rows(wl, x_host_rows, rows, idx_ref, w_ref, sd, cache):
     """Oracle outputs for the given tokens, with routing fed from the GPU logits."""
     out = []
@@ -143,16 +175,13 @@ def oracle_rows(wl, x_host_rows, rows, idx_ref, w_ref, sd, cache):
             if kept[j]:
                 e = int(idx_ref[t, j])
                 if e not in cache:
-                    cache[e] = (wl.w1_host(e), wl.b1_host(e), wl.w2_host(e), wl.b2_host(e))
-                w1, b1, w2, b2 = cache[e]
-                ys[j] = orc.expert_row(wl.kind_code, xr, w1, b1, w2, b2, wl.d, wl.F)
+                    cache[e] = _expert_fn(wl, e)
+                ys[j] = cache[e](xr)
         ysh = None
         if wl.has_shared:
             if "shared" not in cache:
-                cache["shared"] = (wl.w1_host(0, True), wl.b1_host(0, True),
-                                   wl.w2_host(0, True), wl.b2_host(0, True))
-            sw1, sb1, sw2, sb2 = cache["shared"]
-            ysh = orc.expert_row(wl.kind_code, xr, sw1, sb1, sw2, sb2, wl.d, wl.F)
+                cache["shared"] = _expert_fn(wl, 0, True)
+            ysh = cache["shared"](xr)
         out.append(orc.combine_row(xr, wl.add_residual, w_ref[t], kept, ys, ysh,
                                    orc.BF16 if wl.bf16 else orc.F32))
     return np.stack(out)
@@ -194,6 +223,9 @@ def full_check(wl, sample=None, seed=0):
     pt = to_np(r.perm_token)[:P]
     chk = np.arange(0, P, max(1, P // 512))
     assert np.array_equal(xp[chk], x_all[pt[chk]])
+    if wl.int8:
+        used = sorted({int(e) for e in idx_ref[rows].ravel()})
+        check_quantized_weights(r, used[:8])
     ref = oracle_rows(wl, x_rows, rows, idx_ref, w_ref, sd, {})
     stats = check_outputs(wl, to_np(r.out)[rows], ref)
     check_outputs(wl, to_np(r.out_stages)[rows], ref)

@@ -88,7 +88,10 @@ def test_workspace_and_rows(lib):
     # group-limited routing: groups must divide E, keep 1..n_group groups, hold k experts
     dict(n_group=3, topk_group=1), dict(n_group=2, topk_group=0), dict(n_group=2, topk_group=3),
     dict(n_group=64, topk_group=1, E=64), dict(n_group=4, topk_group=1, top_k=2),
-    dict(n_group=-1, topk_group=1)])
+    dict(n_group=-1, topk_group=1),
+    # weight dtype: the activation dtype or INT8 codes (GELU / SwiGLU experts only)
+    dict(w_dtype=5), dict(w_dtype=-1),
+    dict(w_dtype=C.MOE_I8, kind=C.MOE_EXPERT_LINEAR, act_dtype=C.MOE_F32)])
 def test_invalid_configs_rejected(lib, bad):
     base = dict(T=64, d=128, E=4, top_k=2, F=128, capacity_factor=0.0, act_dtype=C.MOE_BF16,
                 kind=C.MOE_EXPERT_GELU, has_shared=0, add_residual=0)
@@ -106,6 +109,27 @@ def test_grouped_routing_configs_accepted(lib):
         cfg = api.make_config(64, 128, E, k, 128, 0.0, "gelu", True, n_group=n_group,
                               topk_group=topk_group)
         assert api.workspace_size(cfg) > 0
+
+
+def test_int8_weights_need_scales(lib):
+    cfg = api.make_config(64, 128, 4, 2, 128, 0.0, "swiglu", True, int8_weights=True)
+    assert cfg.w_dtype == C.MOE_I8 and api.workspace_size(cfg) > 0
+    ok = ctypes.c_void_p(1 << 20)
+    bad = ctypes.c_void_p((1 << 20) + 4)
+    r = ctypes.byref(cfg)
+    ws = 1 << 40
+    w = C.MoeExpertWeights(w1=ok, b1=None, w2=ok, b2=None, s1=ok, s2=None)
+    assert lib.moe_forward(r, ok, ok, None, ctypes.byref(w), None, ok, None, None, None, ok,
+                           ws, None) == C.MOE_ERR_INVALID_ARG
+    w = C.MoeExpertWeights(w1=ok, b1=None, w2=ok, b2=None, s1=ok, s2=bad)
+    assert lib.moe_forward(r, ok, ok, None, ctypes.byref(w), None, ok, None, None, None, ok,
+                           ws, None) == C.MOE_ERR_MISALIGNED
+    # the quantiser's own argument checks (no launch)
+    assert lib.moe_quantize_i8(ok, 4, 12, ok, ok, None) == C.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_i8(ok, -1, 64, ok, ok, None) == C.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_i8(None, 4, 64, ok, ok, None) == C.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_i8(ok, 4, 64, bad, ok, None) == C.MOE_ERR_MISALIGNED
+    assert lib.moe_quantize_i8(ok, 0, 64, ok, ok, None) == C.MOE_OK
 
 
 def test_unsupported_dtype_kind_pairs(lib):

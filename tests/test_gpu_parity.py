@@ -51,6 +51,19 @@ SMALL = {
     # top-1 without residual and with drops: the fused combine writes dropped tokens as 0
     "top1_drop_no_residual": W("t1d", T=300, d=128, E=4, k=1, F=192, kind="gelu", act="bf16",
                                cf=0.5, expert_bias=True),
+    # weight-only INT8 experts: codes widened in shared memory, scales in the epilogue
+    "i8_gelu_bias_k2": W("q8g", T=333, d=192, E=6, k=2, F=256, kind="gelu", act="bf16",
+                         expert_bias=True, int8=True),
+    "i8_swiglu_zipf_shared": W("q8s", T=700, d=192, E=6, k=2, F=192, kind="swiglu",
+                               act="bf16", gate_bias="zipf", has_shared=True, int8=True),
+    "i8_top1_cap_res": W("q8t", T=1000, d=128, E=4, k=1, F=320, kind="gelu", act="bf16",
+                         cf=1.25, add_residual=True, int8=True),
+    "i8_k8_cap": W("q8k", T=260, d=256, E=32, k=8, F=128, kind="swiglu", act="bf16", cf=1.0,
+                   int8=True),
+    "i8_split_swiglu_bias_shared": W("q8ss", T=3, d=1024, E=8, k=2, F=512, kind="swiglu",
+                                     act="bf16", expert_bias=True, has_shared=True, int8=True),
+    "i8_split_gelu_cap_res": W("q8sg", T=5, d=512, E=4, k=1, F=768, kind="gelu", act="bf16",
+                               cf=1.0, add_residual=True, expert_bias=True, int8=True),
 }
 
 
@@ -114,7 +127,8 @@ def test_dropped_tokens_leave_as_x_bit_exact():
     assert np.array_equal(to_np(r.out)[dropped], x[dropped])
 
 
-@pytest.mark.parametrize("name", ["gelu_cap_res", "top1_drop_no_residual", "one_expert"])
+@pytest.mark.parametrize("name", ["gelu_cap_res", "top1_drop_no_residual", "one_expert",
+                                  "i8_top1_cap_res"])
 def test_top1_fused_combine_matches_staged_path_bitwise(name):
     # moe_forward fuses the combine into the down projection for top-1 layers without a
     # shared expert; the staged entry points do not. The fp32 operations are the same.
@@ -134,6 +148,7 @@ def test_forward_is_deterministic():
     ("switch", 32), ("mixtral", 8), ("deepseek", 4), ("deepseek_cf125", 4),
     ("deepseek_grouped", 4),
     ("decode1", None), ("decode8", 4), ("decode64", 4),
+    ("decode1_i8", None), ("decode8_i8", 4), ("decode64_i8", 4),
 ])
 def test_full_size_sampled(name, sample):
     r, stats = full_check(get(name), sample=sample, seed=1)
@@ -226,6 +241,43 @@ def test_out_of_range_expert_id_single_cta_dispatch():
     assert ld.sum() == T * k - 2
     good = ref.numpy()
     assert np.array_equal(ld, np.bincount(good[good >= 0], minlength=E))
+
+
+def test_int8_quantiser_matches_oracle_bitwise():
+    import oracle as orc
+    g = torch.Generator(device="cpu").manual_seed(11)
+    w = (torch.randn(37, 192, generator=g) * torch.rand(37, 1, generator=g) * 4)
+    w[3] = 0.0                        # all-zero row: scale 0, codes 0
+    w[5, :] = 0.25                    # constant row: every code 127
+    w[6] = 0.0
+    w[6, 7] = -1e-30                  # one tiny value among zeros: code -127
+    w = w.to(torch.bfloat16)
+    q = torch.empty(w.shape, dtype=torch.int8, device="cuda")
+    s = torch.empty(37, dtype=torch.float32, device="cuda")
+    moe.quantize_i8(w.cuda(), q, s)
+    oq, os_ = orc.quantize_rows_i8(to_np(w))
+    assert np.array_equal(to_np(q), oq)
+    assert np.array_equal(to_np(s), os_)
+    assert (to_np(q)[5] == 127).all() and (to_np(q)[3] == 0).all() and to_np(s)[3] == 0
+    assert to_np(q)[6, 7] == -127
+
+
+def test_int8_layer_object_quantises_bf16_weights():
+    wl = SMALL["i8_swiglu_zipf_shared"]
+    r = GpuRun(wl).run()
+    inp = r.inp
+    layer = moe.MoELayer(r.cfg, inp["wg"], inp["gate_bias"], inp["w1"], inp["b1"], inp["w2"],
+                         inp["b2"], inp["shared"])
+    assert torch.equal(layer(inp["x"]), r.out)
+
+
+def test_int8_uses_the_int8_kernel():
+    wl = SMALL["i8_split_swiglu_bias_shared"]
+    moe.profile_begin()
+    GpuRun(wl).run()
+    stats = moe.profile_end()
+    assert any(n.startswith("grouped_gemm_q8_") for n in stats)
+    assert not any(n.startswith("grouped_gemm_") and "_q8_" not in n for n in stats)
 
 
 def test_split_k_is_used_for_few_tokens():

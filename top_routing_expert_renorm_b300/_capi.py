@@ -20,7 +20,7 @@ MOE_ERR_TIMEOUT = 6
 MOE_ERR_DEVICE_INDEX = 7
 
 # moe_dtype / moe_expert_kind
-MOE_F32, MOE_BF16 = 0, 1
+MOE_F32, MOE_BF16, MOE_I8 = 0, 1, 2
 MOE_EXPERT_LINEAR, MOE_EXPERT_GELU, MOE_EXPERT_SWIGLU = 0, 1, 2
 
 
@@ -30,12 +30,12 @@ class MoeConfig(ctypes.Structure):
                 ("capacity_factor", ctypes.c_float), ("act_dtype", ctypes.c_int32),
                 ("kind", ctypes.c_int32), ("has_shared", ctypes.c_int32),
                 ("add_residual", ctypes.c_int32), ("n_group", ctypes.c_int32),
-                ("topk_group", ctypes.c_int32)]
+                ("topk_group", ctypes.c_int32), ("w_dtype", ctypes.c_int32)]
 
 
 class MoeExpertWeights(ctypes.Structure):
     _fields_ = [("w1", ctypes.c_void_p), ("b1", ctypes.c_void_p), ("w2", ctypes.c_void_p),
-                ("b2", ctypes.c_void_p)]
+                ("b2", ctypes.c_void_p), ("s1", ctypes.c_void_p), ("s2", ctypes.c_void_p)]
 
 
 class MoeKernelStat(ctypes.Structure):
@@ -70,6 +70,7 @@ def load():
         "moe_grouped_gemm_ws_size": (sz, [i32]),
         "moe_grouped_gemm": (i32, [vp, i64, vp, i32, i32, i32, vp, vp, vp, vp]),
         "moe_load_report": (i32, [vp, i32, i32, vp, vp, vp]),
+        "moe_quantize_i8": (i32, [vp, i64, i32, vp, vp, vp]),
         "moe_last_device_status": (i32, [vp]),
         "moe_status_string": (ctypes.c_char_p, [i32]),
         "moe_profile_begin": (i32, []),

@@ -54,6 +54,9 @@ struct GemmParams {
     void* out;                 // D rows, same row numbering as A
     long long ld_out;          // elements per output row
     const float* bias;         // [G][b_rows_per_group] fp32 or null
+    const float* w_scale;      // [G][b_rows_per_group] fp32 per weight row (INT8 weights), or
+                               // null: column n of the accumulator is multiplied by its row's
+                               // scale before the bias and the epilogue
     const float* topk_w;       // EPI_SCALE_F32: row r scaled by topk_w[perm_token[r]*k + perm_slot[r]]
     const int* perm_token;
     const int* perm_slot;
@@ -143,6 +146,7 @@ template <int EPI>
 __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t tb, int g, int nb,
                                                  bool row_ok, long long grow) {
     const float* brow = p.bias ? p.bias + (long long)g * p.b_rows_per_group : nullptr;
+    const float* srow = p.w_scale ? p.w_scale + (long long)g * p.b_rows_per_group : nullptr;
     if constexpr (EPI == EPI_SWIGLU_BF16) {
         const int n0 = nb * 128;
         __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) + grow * p.ld_out;
@@ -154,6 +158,13 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
             tmem_load_32cols(tb + 128 + c * 32, uv);
             const int col = n0 + c * 32;
             if (row_ok && col < p.N) {
+                if (srow) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        gv[i] *= srow[col + i];
+                        uv[i] *= srow[p.up_offset + col + i];
+                    }
+                }
                 uint32_t packed[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -183,6 +194,10 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
             tmem_load_32cols(tb + c * 32, v);
             const int col = n0 + c * 32;
             if (row_ok && col < p.N) {
+                if (srow) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= srow[col + i];
+                }
                 uint32_t packed[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -280,6 +295,10 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
             tmem_load_32cols(tb + c * 32, v);
             const int col = n0 + c * 32;
             if (row_ok && col < p.N) {
+                if (srow) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= srow[col + i];
+                }
                 uint32_t xin[16];
                 if (xrow) {
                     const uint4* xs = reinterpret_cast<const uint4*>(xrow + col);
@@ -328,6 +347,10 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
             tmem_load_32cols(tb + c * 32, v);
             const int col = n0 + c * 32;
             if (row_ok && col < p.N) {
+                if (srow) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= srow[col + i];
+                }
                 float4* dst = reinterpret_cast<float4*>(orow + col);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -616,6 +639,22 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmParams p,
             if constexpr (EPI == EPI_SWIGLU_BF16) {
                 const float4 w = *reinterpret_cast<const float4*>(src + s * p.part_stride + p.N);
                 u.x += w.x; u.y += w.y; u.z += w.z; u.w += w.w;
+            }
+        }
+        if (p.bias || p.w_scale) {
+            int lo = 0, hi = p.G;   // row_offsets[lo] <= r < row_offsets[hi]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (p.row_offsets[mid] <= r) lo = mid;
+                else hi = mid;
+            }
+            if (p.w_scale) {
+                const float* sc = p.w_scale + (long long)lo * p.b_rows_per_group + c;
+                a.x *= sc[0]; a.y *= sc[1]; a.z *= sc[2]; a.w *= sc[3];
+                if constexpr (EPI == EPI_SWIGLU_BF16) {
+                    const float* su = sc + p.up_offset;
+                    u.x *= su[0]; u.y *= su[1]; u.z *= su[2]; u.w *= su[3];
+                }
             }
         }
         if (p.bias) {

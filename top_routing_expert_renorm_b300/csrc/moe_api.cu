@@ -17,6 +17,7 @@
 #include "router.cuh"
 #include "dispatch.cuh"
 #include "grouped_gemm.cuh"
+#include "grouped_gemm_q8.cuh"
 #include "combine.cuh"
 
 using namespace moe;
@@ -146,6 +147,20 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t co
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D int8 tensor [rows, cols] read in boxes of 64 bytes x box_rows rows, unswizzled
+// (the INT8 GEMM widens the codes itself into the swizzled bf16 layout).
+bool make_tmap_i8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------------------------
 // validation
 // ---------------------------------------------------------------------------------
@@ -169,6 +184,10 @@ moe_status check_cfg(const moe_config* c) {
     if ((c->has_shared != 0 && c->has_shared != 1) || (c->add_residual != 0 && c->add_residual != 1))
         return MOE_ERR_INVALID_ARG;
     if (c->act_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (c->w_dtype != 0 && c->w_dtype != c->act_dtype) {
+        if (c->w_dtype != MOE_I8) return MOE_ERR_INVALID_ARG;
+        if (c->kind != MOE_EXPERT_GELU && c->kind != MOE_EXPERT_SWIGLU) return MOE_ERR_UNSUPPORTED;
+    }
     if (c->n_group != 0) {
         if (c->n_group < 1 || c->n_group > 32 || c->E % c->n_group != 0) return MOE_ERR_INVALID_ARG;
         if (c->topk_group < 1 || c->topk_group > c->n_group) return MOE_ERR_INVALID_ARG;
@@ -423,6 +442,17 @@ const char* gemm_name() {
 }
 
 template <int EPI>
+const char* gemm_q8_name() {
+    switch (EPI) {
+        case EPI_F32: return "grouped_gemm_q8_f32";
+        case EPI_GELU_BF16: return "grouped_gemm_q8_gelu";
+        case EPI_SWIGLU_BF16: return "grouped_gemm_q8_swiglu";
+        case EPI_COMBINE1_BF16: return "grouped_gemm_q8_combine1";
+        default: return "grouped_gemm_q8_scale";
+    }
+}
+
+template <int EPI>
 const char* reduce_name() {
     switch (EPI) {
         case EPI_F32: return "splitk_reduce_f32";
@@ -442,12 +472,16 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
                        int top_k, cudaStream_t s, const char* name = nullptr,
                        SplitPlan sp = SplitPlan(), float* partial = nullptr,
                        unsigned long long* counter = nullptr, const void* resid = nullptr,
-                       int* r_idx = nullptr, float* r_w = nullptr, int r_E = 0, int r_Ep = 0) {
+                       int* r_idx = nullptr, float* r_w = nullptr, int r_E = 0, int r_Ep = 0,
+                       const float* w_scale = nullptr) {
+    // w_scale != null: B holds int8 codes, one fp32 scale per B row (INT8 kernel)
     if (a_rows <= 0 || G <= 0) return MOE_OK;
     if (G > GM_MAX_GROUPS) return MOE_ERR_UNSUPPORTED;
     CUtensorMap ta, tb;
     if (!make_tmap_bf16(&ta, A, (uint64_t)a_rows, (uint64_t)K, GM_BM)) return MOE_ERR_CUDA;
-    if (!make_tmap_bf16(&tb, B, (uint64_t)b_rows_total, (uint64_t)K, GM_BN / 2)) return MOE_ERR_CUDA;
+    if (w_scale ? !make_tmap_i8(&tb, B, (uint64_t)b_rows_total, (uint64_t)K, GM_BN / 2)
+                : !make_tmap_bf16(&tb, B, (uint64_t)b_rows_total, (uint64_t)K, GM_BN / 2))
+        return MOE_ERR_CUDA;
     GemmParams p{};
     p.G = G;
     p.N = N;
@@ -476,6 +510,7 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     p.r_w = r_w;
     p.r_E = r_E;
     p.r_Ep = r_Ep;
+    p.w_scale = w_scale;
     const int smem = gm_smem_bytes(G);
     static std::once_flag attr_once[64];
     static cudaError_t attr_err[64];
@@ -489,8 +524,24 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
         if (attr_err[dev] != cudaSuccess) return MOE_ERR_CUDA;
     }
     const int grid = num_sms();
-    MOE_LAUNCH(name ? name : gemm_name<EPI>(), s,
-               launch_k(grouped_gemm_kernel<EPI>, grid, GM_THREADS, smem, s, ta, tb, p));
+    if (w_scale) {
+        static std::once_flag q8_once[64];
+        static cudaError_t q8_err[64];
+        if (dev >= 0 && dev < 64) {
+            std::call_once(q8_once[dev], [&] {
+                q8_err[dev] = cudaFuncSetAttribute(grouped_gemm_q8_kernel<EPI>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   gm_q8_smem_bytes(GM_MAX_GROUPS));
+            });
+            if (q8_err[dev] != cudaSuccess) return MOE_ERR_CUDA;
+        }
+        MOE_LAUNCH(name ? name : gemm_q8_name<EPI>(), s,
+                   launch_k(grouped_gemm_q8_kernel<EPI>, grid, GM_Q8_THREADS, gm_q8_smem_bytes(G), s,
+                            ta, tb, p));
+    } else {
+        MOE_LAUNCH(name ? name : gemm_name<EPI>(), s,
+                   launch_k(grouped_gemm_kernel<EPI>, grid, GM_THREADS, smem, s, ta, tb, p));
+    }
     if (split) {
         const long long work = a_rows * (long long)(N / 4);
         const int blocks = (int)std::max<long long>(
@@ -597,23 +648,31 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
         MOE_LAUNCH("mtile_table", s,
                    launch_k(mtile_table_kernel, 1, 1024, 0, s, offsets, E, mtile, counters + kCntUp, 2));
     const int64_t N1 = n1_of(c);
+    // INT8 weights: per-row scales select the INT8 kernel
+    const bool q8 = c.w_dtype == MOE_I8;
+    const float* rs1 = q8 ? R.s1 : nullptr;
+    const float* rs2 = q8 ? R.s2 : nullptr;
     if (c.kind == MOE_EXPERT_SWIGLU)
         MOE_TRY(launch_gemm<EPI_SWIGLU_BF16>(x_perm, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
                                              offsets, mtile, h, F, R.b1, nullptr, nullptr, nullptr,
-                                             k, s, nullptr, fp.up, partial, counters + kCntUp));
+                                             k, s, nullptr, fp.up, partial, counters + kCntUp,
+                                             nullptr, nullptr, nullptr, 0, 0, rs1));
     else
         MOE_TRY(launch_gemm<EPI_GELU_BF16>(x_perm, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
                                            offsets, mtile, h, F, R.b1, nullptr, nullptr, nullptr, k,
-                                           s, nullptr, fp.up, partial, counters + kCntUp));
+                                           s, nullptr, fp.up, partial, counters + kCntUp, nullptr,
+                                           nullptr, nullptr, 0, 0, rs1));
     if (fused_out)
         MOE_TRY(launch_gemm<EPI_COMBINE1_BF16>(h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets,
                                                mtile, fused_out, d, R.b2, topk_w, perm_token,
                                                perm_slot, k, s, nullptr, SplitPlan(), nullptr,
-                                               counters + kCntDown, c.add_residual ? x : nullptr));
+                                               counters + kCntDown, c.add_residual ? x : nullptr,
+                                               nullptr, nullptr, 0, 0, rs2));
     else
         MOE_TRY(launch_gemm<EPI_SCALE_F32>(h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets,
                                            mtile, y, d, R.b2, topk_w, perm_token, perm_slot, k, s,
-                                           nullptr, fp.down, partial, counters + kCntDown));
+                                           nullptr, fp.down, partial, counters + kCntDown, nullptr,
+                                           nullptr, nullptr, 0, 0, rs2));
     if (c.has_shared) {
         MOE_LAUNCH("single_group_table", s,
                    launch_k(single_group_table_kernel, 1, 32, 0, s, T, shared_tab, shared_tab + 2,
@@ -622,15 +681,18 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
             MOE_TRY(launch_gemm<EPI_SWIGLU_BF16>(x, T, d, S->w1, N1, (int)N1, 1, F, shared_tab,
                                                  shared_tab + 2, hs, F, S->b1, nullptr, nullptr,
                                                  nullptr, k, s, nullptr, fp.sh_up, partial,
-                                                 counters + kCntSharedUp));
+                                                 counters + kCntSharedUp, nullptr, nullptr,
+                                                 nullptr, 0, 0, q8 ? S->s1 : nullptr));
         else
             MOE_TRY(launch_gemm<EPI_GELU_BF16>(x, T, d, S->w1, N1, (int)N1, 1, F, shared_tab,
                                                shared_tab + 2, hs, F, S->b1, nullptr, nullptr,
                                                nullptr, k, s, nullptr, fp.sh_up, partial,
-                                               counters + kCntSharedUp));
+                                               counters + kCntSharedUp, nullptr, nullptr, nullptr,
+                                               0, 0, q8 ? S->s1 : nullptr));
         MOE_TRY(launch_gemm<EPI_F32>(hs, T, F, S->w2, d, d, 1, d, shared_tab, shared_tab + 2,
                                      y_shared, d, S->b2, nullptr, nullptr, nullptr, k, s, nullptr,
-                                     fp.sh_down, partial, counters + kCntSharedDown));
+                                     fp.sh_down, partial, counters + kCntSharedDown, nullptr,
+                                     nullptr, nullptr, 0, 0, q8 ? S->s2 : nullptr));
     }
     return MOE_OK;
 }
@@ -663,7 +725,9 @@ moe_status combine_impl(const moe_config& c, const void* x, const float* y,
 moe_status check_weights(const moe_config& c, const moe_expert_weights* W) {
     if (!W || !W->w1) return MOE_ERR_INVALID_ARG;
     if (c.kind != MOE_EXPERT_LINEAR && !W->w2) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(W->w1) || !aligned16(W->w2) || !aligned16(W->b1) || !aligned16(W->b2))
+    if (c.w_dtype == MOE_I8 && (!W->s1 || !W->s2)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(W->w1) || !aligned16(W->w2) || !aligned16(W->b1) || !aligned16(W->b2) ||
+        !aligned16(W->s1) || !aligned16(W->s2))
         return MOE_ERR_MISALIGNED;
     return MOE_OK;
 }
@@ -838,6 +902,19 @@ moe_status moe_grouped_gemm(const void* A, int64_t a_rows, const void* B, int32_
     return launch_gemm<EPI_F32>(A, a_rows, K, B, (int64_t)G * N, N, G, N, row_offsets, mtile, D, N,
                                 nullptr, nullptr, nullptr, nullptr, 1, stream, nullptr,
                                 SplitPlan(), nullptr, counter);
+}
+
+moe_status moe_quantize_i8(const void* w, int64_t rows, int32_t cols, int8_t* q, float* scale,
+                           cudaStream_t stream) {
+    if (!w || !q || !scale || rows < 0 || cols < 8 || cols % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(q) || !aligned16(scale)) return MOE_ERR_MISALIGNED;
+    if (rows == 0) return MOE_OK;
+    const int blocks = (int)std::max<long long>(
+        1, std::min<long long>((rows + 7) / 8, (long long)num_sms() * 16));
+    MOE_LAUNCH("quantize_i8", stream,
+               launch_k(quantize_rows_i8_kernel, blocks, 256, 0, stream,
+                        static_cast<const __nv_bfloat16*>(w), (long long)rows, (int)cols, q, scale));
+    return MOE_OK;
 }
 
 moe_status moe_load_report(const int32_t* load_host, int32_t E, int32_t D, int32_t* assign,

@@ -9,14 +9,23 @@ from . import api
 class MoELayer:
     """One MoE layer. Tensors (all on one CUDA device, contiguous):
     W_gate [d, E] fp32, gate_bias [E] fp32 or None, w1 [E, N1, d], b1 [E, N1] or None,
-    w2 [E, d, F] (not for LINEAR), b2 [E, d] or None, shared = (w1, b1, w2, b2) or None.
+    w2 [E, d, F] (not for LINEAR), b2 [E, d] or None, shared = (w1, b1, w2, b2[, s1, s2]) or
+    None; with INT8 experts w1 / w2 hold int8 codes and s1 [E, N1] / s2 [E, d] their scales.
     The workspace is sized for up to `max_tokens` tokens per call."""
 
-    def __init__(self, cfg, W_gate, gate_bias, w1, b1=None, w2=None, b2=None, shared=None):
+    def __init__(self, cfg, W_gate, gate_bias, w1, b1=None, w2=None, b2=None, shared=None,
+                 s1=None, s2=None):
+        import torch
         self.cfg = cfg
-        self._keep = [W_gate, gate_bias, w1, b1, w2, b2, shared]
+        if cfg.w_dtype == api.C.MOE_I8 and w1.dtype == torch.bfloat16:
+            # bf16 weights for an INT8 layer: quantise them once (codes + per-row scales)
+            w1, s1, w2, s2 = api.quantize_weights(w1, w2)
+            if shared is not None:
+                sw1, ss1, sw2, ss2 = api.quantize_weights(shared[0], shared[2])
+                shared = (sw1, shared[1], sw2, shared[3], ss1, ss2)
+        self._keep = [W_gate, gate_bias, w1, b1, w2, b2, shared, s1, s2]
         self.W_gate, self.gate_bias = W_gate, gate_bias
-        self.routed = api.weights(w1, b1, w2, b2)
+        self.routed = api.weights(w1, b1, w2, b2, s1, s2)
         self.shared = api.weights(*shared) if shared is not None else None
         self.ws = torch.empty(api.workspace_size(cfg), dtype=torch.uint8, device=w1.device)
 
