@@ -19,6 +19,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -126,7 +127,7 @@ def kernel_algorithmic_cost(wl, name, P, touched):
     es = 2 if wl.bf16 else 4
     T, d, F, E = wl.T, wl.d, wl.F, wl.E
     N1 = wl.N1
-    name = name.replace("_q8", "")          # INT8-weight kernels: same algorithm
+    name = re.sub(r"_q8t?_", "_", name)     # INT8-weight kernels: same algorithm
     we = 1 if wl.int8 else 2               # bytes per expert weight
     sc1 = 4 * N1 if wl.int8 else 0         # per-row scales of one expert
     sc2 = 4 * d if wl.int8 else 0
@@ -146,7 +147,7 @@ def kernel_algorithmic_cost(wl, name, P, touched):
     if name == "copy_dropped":            # dropped tokens (T - P of them) leave as x or 0
         return 0.0, T * wl.k * 4 + (T - P) * d * es * (2 if wl.add_residual else 1)
     if name == "grouped_gemm_f32":        # shared expert down projection
-        return 2.0 * T * F * d, d * F * 2 + T * F * 2 + T * d * 4
+        return 2.0 * T * F * d, d * F * we + sc2 + T * F * 2 + T * d * 4
     if name.startswith("router_logits") or name == "router_splitk":
         return 2.0 * T * d * E, T * d * es + d * E * 4 + T * E * 4
     if name == "router_gemm_tc":          # algorithmic: the fp32 gate GEMM it computes
@@ -168,6 +169,8 @@ def kernel_algorithmic_cost(wl, name, P, touched):
 
 
 KERNEL_FILES = {
+    "grouped_gemm_q8t": ["grouped_gemm_q8t.cuh", "grouped_gemm_q8.cuh", "grouped_gemm.cuh",
+                         "common.cuh"],
     "grouped_gemm_q8": ["grouped_gemm_q8.cuh", "grouped_gemm.cuh", "common.cuh"],
     "grouped_gemm": ["grouped_gemm.cuh", "common.cuh"],
     "router_gemm_tc": ["grouped_gemm.cuh", "common.cuh"],

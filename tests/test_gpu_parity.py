@@ -64,6 +64,19 @@ SMALL = {
                                      act="bf16", expert_bias=True, has_shared=True, int8=True),
     "i8_split_gelu_cap_res": W("q8sg", T=5, d=512, E=4, k=1, F=768, kind="gelu", act="bf16",
                                cf=1.0, add_residual=True, expert_bias=True, int8=True),
+    # INT8 with few rows per expert: the weight-streaming kernel (32-row activation tiles);
+    # ragged feature tiles, experts and a shared expert spanning two activation tiles
+    "i8t_swiglu_bias_shared": W("q8t1", T=24, d=256, E=16, k=4, F=192, kind="swiglu",
+                                act="bf16", expert_bias=True, has_shared=True, int8=True),
+    "i8t_gelu_two_tiles": W("q8t2", T=64, d=192, E=4, k=2, F=320, kind="gelu", act="bf16",
+                            expert_bias=True, has_shared=True, int8=True),
+    "i8t_hot_cap_res": W("q8t3", T=40, d=128, E=8, k=1, F=128, kind="gelu", act="bf16",
+                         cf=0.5, gate_bias="hot", add_residual=True, int8=True),
+    "i8t_hot_one_expert": W("q8t4", T=48, d=128, E=8, k=1, F=128, kind="swiglu", act="bf16",
+                            gate_bias="hot", int8=True),
+    # K = 64: one half-filled 128-code K block (zero codes and activations past the end)
+    "i8t_k64": W("q8t5", T=10, d=64, E=4, k=2, F=64, kind="swiglu", act="bf16",
+                 expert_bias=True, has_shared=True, int8=True),
 }
 
 
@@ -271,13 +284,16 @@ def test_int8_layer_object_quantises_bf16_weights():
     assert torch.equal(layer(inp["x"]), r.out)
 
 
-def test_int8_uses_the_int8_kernel():
-    wl = SMALL["i8_split_swiglu_bias_shared"]
+@pytest.mark.parametrize("name,prefix", [("i8_split_swiglu_bias_shared", "grouped_gemm_q8t_"),
+                                         ("i8t_gelu_two_tiles", "grouped_gemm_q8t_"),
+                                         ("i8_swiglu_zipf_shared", "grouped_gemm_q8_")])
+def test_int8_uses_the_int8_kernels(name, prefix):
+    # few rows per expert: the weight-streaming kernel; otherwise the shared-memory one
     moe.profile_begin()
-    GpuRun(wl).run()
+    GpuRun(SMALL[name]).run()
     stats = moe.profile_end()
-    assert any(n.startswith("grouped_gemm_q8_") for n in stats)
-    assert not any(n.startswith("grouped_gemm_") and "_q8_" not in n for n in stats)
+    gemms = [n for n in stats if n.startswith("grouped_gemm_")]
+    assert gemms and all(n.startswith(prefix) for n in gemms), gemms
 
 
 def test_split_k_is_used_for_few_tokens():

@@ -18,6 +18,7 @@
 #include "dispatch.cuh"
 #include "grouped_gemm.cuh"
 #include "grouped_gemm_q8.cuh"
+#include "grouped_gemm_q8t.cuh"
 #include "combine.cuh"
 
 using namespace moe;
@@ -147,17 +148,18 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t co
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D int8 tensor [rows, cols] read in boxes of 64 bytes x box_rows rows, unswizzled
-// (the INT8 GEMM widens the codes itself into the swizzled bf16 layout).
-bool make_tmap_i8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// 2-D int8 tensor [rows, cols] read in boxes of box_cols bytes x box_rows rows, unswizzled
+// or swizzled (the INT8 GEMMs widen the codes themselves).
+bool make_tmap_i8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                  uint32_t box_cols = 64, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols};
-    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -279,9 +281,11 @@ struct SplitPlan {
     int kbs = 0;   // K blocks per split
 };
 
-SplitPlan split_plan(long long max_mtiles, int n_tiles, int K, int sms) {
+SplitPlan split_plan(long long max_mtiles, int n_tiles, int K, int sms, int bk = GM_BK) {
+    // bk: K elements per block of the kernel that runs (GM_BK, or QT_BK for the
+    // weight-streaming INT8 kernel)
     SplitPlan sp;
-    const int KB = K / GM_BK;
+    const int KB = (K + bk - 1) / bk;
     sp.kbs = KB;
     const long long tiles = max_mtiles * n_tiles;
     if (tiles <= 0 || tiles >= 2ll * sms) return sp;
@@ -304,11 +308,20 @@ SplitPlan split_plan(long long max_mtiles, int n_tiles, int K, int sms) {
     return sp;
 }
 
-// Upper bound on the M tiles of the routed experts: sum_e ceil(n_e / 128) over the
-// non-empty experts <= P / 128 + min(E, P).
+// INT8 experts with few rows per group run the weight-streaming kernel
+// (grouped_gemm_q8t_kernel: operands swapped, 32-row activation tiles): the routed
+// experts when they average at most 32 rows, the shared expert up to 64 tokens.
+bool q8t_routed(const moe_config& c) {
+    return c.w_dtype == MOE_I8 && (long long)c.T * c.top_k <= 32ll * c.E;
+}
+bool q8t_shared(const moe_config& c) { return c.w_dtype == MOE_I8 && c.T <= 64; }
+
+// Upper bound on the M tiles of the routed experts: sum_e ceil(n_e / m) over the
+// non-empty experts <= P / m + min(E, P), m = 128 rows (32 for the weight-streaming
+// INT8 kernel).
 long long routed_mtiles_bound(const moe_config& c) {
     const long long Pmax = (long long)c.T * c.top_k;
-    return Pmax / kMTile + std::min<long long>(c.E, Pmax);
+    return Pmax / (q8t_routed(c) ? QT_NT : kMTile) + std::min<long long>(c.E, Pmax);
 }
 
 struct FfnPlan {
@@ -325,17 +338,20 @@ FfnPlan ffn_plan(const moe_config& c) {
     const int dn_nt = (c.d + GM_BN - 1) / GM_BN;
     const long long N1 = c.kind == MOE_EXPERT_SWIGLU ? 2ll * c.F : c.F;
     const long long mt = routed_mtiles_bound(c);
-    f.up = split_plan(mt, up_nt, c.d, sms);
-    f.down = split_plan(mt, dn_nt, c.F, sms);
+    const int rbk = q8t_routed(c) ? QT_BK : GM_BK;
+    f.up = split_plan(mt, up_nt, c.d, sms, rbk);
+    f.down = split_plan(mt, dn_nt, c.F, sms, rbk);
     auto need = [&](const SplitPlan& sp, long long rows, long long cols) {
         if (sp.S > 1) f.partial_floats = std::max<size_t>(f.partial_floats, (size_t)(sp.S * rows * cols));
     };
     need(f.up, Pmax, N1);
     need(f.down, Pmax, c.d);
     if (c.has_shared) {
-        const long long smt = (c.T + kMTile - 1) / kMTile;
-        f.sh_up = split_plan(smt, up_nt, c.d, sms);
-        f.sh_down = split_plan(smt, dn_nt, c.F, sms);
+        const int sm = q8t_shared(c) ? QT_NT : kMTile;
+        const long long smt = (c.T + sm - 1) / sm;
+        const int sbk = q8t_shared(c) ? QT_BK : GM_BK;
+        f.sh_up = split_plan(smt, up_nt, c.d, sms, sbk);
+        f.sh_down = split_plan(smt, dn_nt, c.F, sms, sbk);
         need(f.sh_up, c.T, N1);
         need(f.sh_down, c.T, c.d);
     }
@@ -453,6 +469,20 @@ const char* gemm_q8_name() {
 }
 
 template <int EPI>
+const char* gemm_q8t_name() {
+    switch (EPI) {
+        case EPI_F32: return "grouped_gemm_q8t_f32";
+        case EPI_GELU_BF16: return "grouped_gemm_q8t_gelu";
+        case EPI_SWIGLU_BF16: return "grouped_gemm_q8t_swiglu";
+        default: return "grouped_gemm_q8t_scale";
+    }
+}
+
+constexpr bool q8t_supports(int epi) {
+    return epi == EPI_F32 || epi == EPI_GELU_BF16 || epi == EPI_SWIGLU_BF16 || epi == EPI_SCALE_F32;
+}
+
+template <int EPI>
 const char* reduce_name() {
     switch (EPI) {
         case EPI_F32: return "splitk_reduce_f32";
@@ -473,14 +503,20 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
                        SplitPlan sp = SplitPlan(), float* partial = nullptr,
                        unsigned long long* counter = nullptr, const void* resid = nullptr,
                        int* r_idx = nullptr, float* r_w = nullptr, int r_E = 0, int r_Ep = 0,
-                       const float* w_scale = nullptr) {
-    // w_scale != null: B holds int8 codes, one fp32 scale per B row (INT8 kernel)
+                       const float* w_scale = nullptr, bool swap_ab = false) {
+    // w_scale != null: B holds int8 codes, one fp32 scale per B row (INT8 kernels); with
+    // swap_ab the weight-streaming INT8 kernel for few rows per group runs
     if (a_rows <= 0 || G <= 0) return MOE_OK;
     if (G > GM_MAX_GROUPS) return MOE_ERR_UNSUPPORTED;
+    swap_ab = swap_ab && w_scale != nullptr;
+    if (swap_ab && !q8t_supports(EPI)) return MOE_ERR_UNSUPPORTED;
     CUtensorMap ta, tb;
-    if (!make_tmap_bf16(&ta, A, (uint64_t)a_rows, (uint64_t)K, GM_BM)) return MOE_ERR_CUDA;
-    if (w_scale ? !make_tmap_i8(&tb, B, (uint64_t)b_rows_total, (uint64_t)K, GM_BN / 2)
-                : !make_tmap_bf16(&tb, B, (uint64_t)b_rows_total, (uint64_t)K, GM_BN / 2))
+    if (!make_tmap_bf16(&ta, A, (uint64_t)a_rows, (uint64_t)K, swap_ab ? QT_NT : GM_BM))
+        return MOE_ERR_CUDA;
+    if (swap_ab ? !make_tmap_i8(&tb, B, (uint64_t)b_rows_total, (uint64_t)K, GM_BN / 2, QT_BK,
+                                CU_TENSOR_MAP_SWIZZLE_128B)
+        : w_scale ? !make_tmap_i8(&tb, B, (uint64_t)b_rows_total, (uint64_t)K, GM_BN / 2)
+                  : !make_tmap_bf16(&tb, B, (uint64_t)b_rows_total, (uint64_t)K, GM_BN / 2))
         return MOE_ERR_CUDA;
     GemmParams p{};
     p.G = G;
@@ -500,7 +536,7 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     p.top_k = top_k;
     const bool split = sp.S > 1 && partial != nullptr;
     p.k_splits = split ? sp.S : 1;
-    p.kb_per_split = split ? sp.kbs : K / GM_BK;
+    p.kb_per_split = split ? sp.kbs : (swap_ab ? (K + QT_BK - 1) / QT_BK : K / GM_BK);
     p.partial = split ? partial : nullptr;
     p.ld_part = (EPI == EPI_SWIGLU_BF16) ? 2ll * N : N;
     p.part_stride = (long long)a_rows * p.ld_part;
@@ -524,7 +560,23 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
         if (attr_err[dev] != cudaSuccess) return MOE_ERR_CUDA;
     }
     const int grid = num_sms();
-    if (w_scale) {
+    if (swap_ab) {
+        if constexpr (q8t_supports(EPI)) {
+            static std::once_flag qt_once[64];
+            static cudaError_t qt_err[64];
+            if (dev >= 0 && dev < 64) {
+                std::call_once(qt_once[dev], [&] {
+                    qt_err[dev] = cudaFuncSetAttribute(grouped_gemm_q8t_kernel<EPI>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       gm_q8t_smem_bytes(GM_MAX_GROUPS));
+                });
+                if (qt_err[dev] != cudaSuccess) return MOE_ERR_CUDA;
+            }
+            MOE_LAUNCH(name ? name : gemm_q8t_name<EPI>(), s,
+                       launch_k(grouped_gemm_q8t_kernel<EPI>, grid, QT_THREADS, gm_q8t_smem_bytes(G),
+                                s, ta, tb, p));
+        }
+    } else if (w_scale) {
         static std::once_flag q8_once[64];
         static cudaError_t q8_err[64];
         if (dev >= 0 && dev < 64) {
@@ -652,16 +704,17 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
     const bool q8 = c.w_dtype == MOE_I8;
     const float* rs1 = q8 ? R.s1 : nullptr;
     const float* rs2 = q8 ? R.s2 : nullptr;
+    const bool swap_r = q8t_routed(c), swap_s = q8t_shared(c);
     if (c.kind == MOE_EXPERT_SWIGLU)
         MOE_TRY(launch_gemm<EPI_SWIGLU_BF16>(x_perm, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
                                              offsets, mtile, h, F, R.b1, nullptr, nullptr, nullptr,
                                              k, s, nullptr, fp.up, partial, counters + kCntUp,
-                                             nullptr, nullptr, nullptr, 0, 0, rs1));
+                                             nullptr, nullptr, nullptr, 0, 0, rs1, swap_r));
     else
         MOE_TRY(launch_gemm<EPI_GELU_BF16>(x_perm, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
                                            offsets, mtile, h, F, R.b1, nullptr, nullptr, nullptr, k,
                                            s, nullptr, fp.up, partial, counters + kCntUp, nullptr,
-                                           nullptr, nullptr, 0, 0, rs1));
+                                           nullptr, nullptr, 0, 0, rs1, swap_r));
     if (fused_out)
         MOE_TRY(launch_gemm<EPI_COMBINE1_BF16>(h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets,
                                                mtile, fused_out, d, R.b2, topk_w, perm_token,
@@ -672,7 +725,7 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
         MOE_TRY(launch_gemm<EPI_SCALE_F32>(h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets,
                                            mtile, y, d, R.b2, topk_w, perm_token, perm_slot, k, s,
                                            nullptr, fp.down, partial, counters + kCntDown, nullptr,
-                                           nullptr, nullptr, 0, 0, rs2));
+                                           nullptr, nullptr, 0, 0, rs2, swap_r));
     if (c.has_shared) {
         MOE_LAUNCH("single_group_table", s,
                    launch_k(single_group_table_kernel, 1, 32, 0, s, T, shared_tab, shared_tab + 2,
@@ -682,17 +735,17 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
                                                  shared_tab + 2, hs, F, S->b1, nullptr, nullptr,
                                                  nullptr, k, s, nullptr, fp.sh_up, partial,
                                                  counters + kCntSharedUp, nullptr, nullptr,
-                                                 nullptr, 0, 0, q8 ? S->s1 : nullptr));
+                                                 nullptr, 0, 0, q8 ? S->s1 : nullptr, swap_s));
         else
             MOE_TRY(launch_gemm<EPI_GELU_BF16>(x, T, d, S->w1, N1, (int)N1, 1, F, shared_tab,
                                                shared_tab + 2, hs, F, S->b1, nullptr, nullptr,
                                                nullptr, k, s, nullptr, fp.sh_up, partial,
                                                counters + kCntSharedUp, nullptr, nullptr, nullptr,
-                                               0, 0, q8 ? S->s1 : nullptr));
+                                               0, 0, q8 ? S->s1 : nullptr, swap_s));
         MOE_TRY(launch_gemm<EPI_F32>(hs, T, F, S->w2, d, d, 1, d, shared_tab, shared_tab + 2,
                                      y_shared, d, S->b2, nullptr, nullptr, nullptr, k, s, nullptr,
                                      fp.sh_down, partial, counters + kCntSharedDown, nullptr,
-                                     nullptr, nullptr, 0, 0, q8 ? S->s2 : nullptr));
+                                     nullptr, nullptr, 0, 0, q8 ? S->s2 : nullptr, swap_s));
     }
     return MOE_OK;
 }
@@ -852,7 +905,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate
     float* y = at<float>(ws, L.y);
     int32_t* mtile = at<int32_t>(ws, L.mtile);
     // Top-1 layers without a shared expert write the output from the down projection.
-    const bool fuse1 = is_bf16_kind(c) && c.top_k == 1 && !c.has_shared && ffn_plan(c).down.S == 1;
+    const bool fuse1 = is_bf16_kind(c) && c.top_k == 1 && !c.has_shared && !q8t_routed(c) &&
+                       ffn_plan(c).down.S == 1;
     MOE_TRY(route_impl(c, x, W_gate, gate_bias, nullptr, idx, w, at<void>(ws, L.logits), stream));
     MOE_TRY(dispatch_impl(c, idx, x, ld, at<int32_t>(ws, L.counts), offsets, perm_token, perm_slot,
                           slot_dest, x_perm, at<int32_t>(ws, L.blockcnt),
