@@ -26,6 +26,11 @@
 //   [Hier]     "MoE 并行", 通信瓶颈 table, row Hierarchical Routing (pick groups first, then
 //              experts); adv12 section 5 (DeepSeek-V3: device-limited routing, each token's
 //              experts lie on at most M devices).
+//   [Reroute]  "MoE 并行", 推理时的负载均衡 (dynamic re-routing: a token whose expert is over
+//              its limit goes to the next expert); "MoE 混合专家架构" section 4.2 (capacity
+//              check that redistributes the excess tokens of a full expert).
+//   [OvfShared] "MoE 并行" Q4 (inference: capacity limit, overflow tokens go to the shared
+//              expert) and Q5; adv12 Q2 option 2 (overflow routed to the shared expert).
 //
 // Readings where the pages are silent or disagree (each one is listed in the design notes):
 //   * selection is done on logits with ties broken toward the lower expert id;
@@ -38,7 +43,12 @@
 //   * group-limited routing scores a group by its best expert logit (the pages name the
 //     two steps but not the score);
 //   * INT8 experts are weight-only, symmetric, one absmax scale per weight row (the pages
-//     name INT8 / INT4 but no scheme).
+//     name INT8 / INT4 but no scheme);
+//   * overflow to the shared expert: a dropped slot's weight is added to the (always-on)
+//     shared expert's weight of that token;
+//   * re-routing: one round; a token's dropped slots, in slot order, go to its next-ranked
+//     experts (ranks k, k+1, ...) and keep their weights; each expert accepts them in token
+//     order while it has room under the capacity; rejected slots stay dropped.
 //
 // Parity status: every exported function is pinned by the CPU test suite against
 // values printed on the pages, closed forms, or brute force on tiny inputs,
@@ -254,6 +264,113 @@ void oracle_dispatch(const int32_t* idx, int T, int k, int E, int cap,
         }
 }
 
+// Next-ranked experts for re-routing [Reroute]: cand[t][0..m) are the experts at
+// positions k .. k+m-1 of token t's ranking (logit descending, id ascending), or -1 where
+// the ranking has fewer experts. With n_group > 0 the ranking covers only the experts of
+// the topk_group chosen groups (chosen as in oracle_topk_renorm_grouped).
+void oracle_rank_candidates(const float* logits, int T, int E, int k, int n_group, int topk_group,
+                            int m, int32_t* cand) {
+    for (int t = 0; t < T; ++t) {
+        const float* L = logits + (long long)t * E;
+        std::vector<char> allowed(E, 1);
+        if (n_group > 0) {
+            const int gsize = E / n_group;
+            std::vector<float> gscore(n_group);
+            for (int g = 0; g < n_group; ++g) {
+                float mx = L[g * gsize];
+                for (int e = g * gsize + 1; e < (g + 1) * gsize; ++e)
+                    if (L[e] > mx) mx = L[e];
+                gscore[g] = mx;
+            }
+            std::vector<char> chosen(n_group, 0);
+            for (int j = 0; j < topk_group; ++j) {
+                int best = -1;
+                for (int g = 0; g < n_group; ++g) {
+                    if (chosen[g]) continue;
+                    if (best < 0 || gscore[g] > gscore[best]) best = g;
+                }
+                chosen[best] = 1;
+            }
+            for (int e = 0; e < E; ++e) allowed[e] = chosen[e / gsize];
+        }
+        std::vector<char> taken(E, 0);
+        for (int pos = 0; pos < k + m; ++pos) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e] || !allowed[e]) continue;
+                if (best < 0 || L[e] > L[best]) best = e;
+            }
+            if (best >= 0) taken[best] = 1;
+            if (pos >= k) cand[(long long)t * m + (pos - k)] = best;
+        }
+    }
+}
+
+// Dispatch with one round of re-routing [Reroute], [Capacity].
+// Round 0 is oracle_dispatch's rule: per expert, assignments in ascending token order,
+// the r-th kept iff r < cap. Round 1: the dropped slots of token t, in slot order, propose
+// to cand[t][0], cand[t][1], ... (k candidates per token; -1 = none); each expert takes its
+// proposals in ascending (token, slot) order while its round-0 rows plus the proposals it
+// has taken stay below cap. Expert e's rows are its round-0 rows (token order) followed by
+// its round-1 rows (token order). route_idx[t][j] is the expert that processes slot
+// (t, j) (the original one unless re-routed); slot_dest as in oracle_dispatch.
+void oracle_dispatch_reroute(const int32_t* idx, const int32_t* cand, int T, int k, int E, int cap,
+                             int32_t* counts, int32_t* offsets, int32_t* perm_token,
+                             int32_t* perm_slot, int32_t* slot_dest, int32_t* route_idx) {
+    const long long n = (long long)T * k;
+    // round 0: ranks in token order
+    std::vector<int> r0(n, -1);
+    std::vector<int> kept0(E, 0), seen(E, 0);
+    for (long long s = 0; s < n; ++s) {
+        const int e = idx[s];
+        if (seen[e] < cap) {
+            r0[s] = seen[e];
+            kept0[e] += 1;
+        }
+        seen[e] += 1;
+    }
+    // round 1: proposals of the dropped slots, accepted in token order while there is room
+    std::vector<int> prop(n, -1), r1(n, -1), acc1(E, 0);
+    for (int t = 0; t < T; ++t) {
+        int m = 0;
+        for (int j = 0; j < k; ++j) {
+            const long long s = (long long)t * k + j;
+            if (r0[s] >= 0) continue;
+            prop[s] = cand[(long long)t * k + m];
+            m += 1;
+        }
+    }
+    for (long long s = 0; s < n; ++s) {
+        const int e = prop[s];
+        if (e < 0) continue;
+        if (kept0[e] + acc1[e] < cap) {
+            r1[s] = acc1[e];
+            acc1[e] += 1;
+        }
+    }
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) {
+        counts[e] = kept0[e] + acc1[e];
+        offsets[e + 1] = offsets[e] + counts[e];
+    }
+    for (long long s = 0; s < n; ++s) {
+        const int t = (int)(s / k), j = (int)(s % k);
+        int pos = -1;
+        route_idx[s] = idx[s];
+        if (r0[s] >= 0) {
+            pos = offsets[idx[s]] + r0[s];
+        } else if (r1[s] >= 0) {
+            pos = offsets[prop[s]] + kept0[prop[s]] + r1[s];
+            route_idx[s] = prop[s];
+        }
+        slot_dest[s] = pos;
+        if (pos >= 0) {
+            perm_token[pos] = t;
+            perm_slot[pos] = j;
+        }
+    }
+}
+
 // O8 one token through one expert [Steps] (expert_e(x)), [Merged] (stacked W1 slice).
 //   LINEAR: y = W1 x + b1                (W1 [d][d]; the tiny tutorial expert)
 //   GELU:   h = gelu(W1 x + b1), y = W2 h + b2         (W1 [F][d], W2 [d][F])
@@ -359,19 +476,31 @@ void oracle_expert_row_q8(int kind, const void* x_row, int x_dtype, const int8_t
 }
 
 // O9 combine for one token [Agg], [Steps] step 4, [Capacity] (overflow -> residual):
-// out = (add_residual ? x : 0) + sum_{j kept, ascending} w_j * y_j + (shared ? ys : 0),
+// out = (add_residual ? x : 0) + sum_{j kept, ascending} w_j * y_j + (shared ? a * ys : 0),
 // accumulated in double, rounded once to out_dtype. ys may be NULL.
 // ys_k holds k rows of d values; kept[j] == 0 marks a dropped slot.
-void oracle_combine_row(const void* x_row, int x_dtype, int add_residual, int d, int k,
-                        const float* w, const int32_t* kept, const double* ys_k,
-                        const double* ys_shared, void* out_row, int out_dtype) {
+// a = 1, or with overflow_to_shared [OvfShared] a = 1 + sum_{j dropped} w_j.
+void oracle_combine_row_ovf(const void* x_row, int x_dtype, int add_residual, int d, int k,
+                            const float* w, const int32_t* kept, const double* ys_k,
+                            const double* ys_shared, int overflow_to_shared, void* out_row,
+                            int out_dtype) {
+    double a = 1.0;
+    if (overflow_to_shared)
+        for (int j = 0; j < k; ++j)
+            if (!kept[j]) a += (double)w[j];
     for (int c = 0; c < d; ++c) {
         double acc = add_residual ? load_elem(x_row, x_dtype, c) : 0.0;
         for (int j = 0; j < k; ++j)
             if (kept[j]) acc += (double)w[j] * ys_k[(long long)j * d + c];
-        if (ys_shared) acc += ys_shared[c];
+        if (ys_shared) acc += a * ys_shared[c];
         store_out(out_row, out_dtype, c, acc);
     }
+}
+void oracle_combine_row(const void* x_row, int x_dtype, int add_residual, int d, int k,
+                        const float* w, const int32_t* kept, const double* ys_k,
+                        const double* ys_shared, void* out_row, int out_dtype) {
+    oracle_combine_row_ovf(x_row, x_dtype, add_residual, d, k, w, kept, ys_k, ys_shared, 0,
+                           out_row, out_dtype);
 }
 
 // Whole forward for inputs held entirely in host memory (small problems).
@@ -380,18 +509,28 @@ void oracle_combine_row(const void* x_row, int x_dtype, int add_residual, int d,
 // N1 = d (LINEAR), F (GELU), 2F (SWIGLU). Shared expert (nullable): one such expert.
 // Outputs: out [T][d]; idx, w [T][k]; logits [T][E]; load [E]; counts [E];
 // offsets [E+1]; perm_token, perm_slot [T*k]; slot_dest [T*k].
+// overflow: 0 = dropped slots add 0; 1 = their weight goes to the shared expert
+// [OvfShared]; 2 = one re-routing round to the next-ranked experts [Reroute] (idx then
+// holds the expert that processes each slot). load is always the raw top-k bincount.
 void oracle_forward(int kind, int T, int d, int E, int k, int F, double cf, int add_residual,
                     const void* x, int x_dtype, const float* Wg, const float* gate_bias,
                     const void* w1, const float* b1, const void* w2, const float* b2,
                     const void* sw1, const float* sb1, const void* sw2, const float* sb2,
                     int w_dtype, void* out, float* logits, int32_t* idx, float* w,
                     int32_t* load, int32_t* counts, int32_t* offsets, int32_t* perm_token,
-                    int32_t* perm_slot, int32_t* slot_dest) {
+                    int32_t* perm_slot, int32_t* slot_dest, int overflow) {
     oracle_gate_logits(x, x_dtype, Wg, gate_bias, T, d, E, nullptr, 0, logits);
     oracle_topk_renorm(logits, T, E, k, idx, w);
     oracle_load(idx, T, k, E, load);
     int cap = oracle_capacity(cf, T, k, E);
-    oracle_dispatch(idx, T, k, E, cap, counts, offsets, perm_token, perm_slot, slot_dest);
+    if (overflow == 2) {
+        std::vector<int32_t> cand((size_t)T * k), orig(idx, idx + (size_t)T * k);
+        oracle_rank_candidates(logits, T, E, k, 0, 0, k, cand.data());
+        oracle_dispatch_reroute(orig.data(), cand.data(), T, k, E, cap, counts, offsets,
+                                perm_token, perm_slot, slot_dest, idx);
+    } else {
+        oracle_dispatch(idx, T, k, E, cap, counts, offsets, perm_token, perm_slot, slot_dest);
+    }
     long long N1 = (kind == ORC_LINEAR) ? d : (kind == ORC_GELU ? F : 2LL * F);
     long long w1_per = N1 * d, w2_per = (kind == ORC_LINEAR) ? 0 : (long long)d * F;
     long long esz = (w_dtype == ORC_F32) ? 4 : 2;
@@ -411,9 +550,9 @@ void oracle_forward(int kind, int T, int d, int E, int k, int F, double cf, int 
                               b2 ? b2 + (long long)e * d : nullptr, w_dtype, d, F, &ys[(size_t)j * d]);
         }
         if (sw1) oracle_expert_row(kind, xr, x_dtype, sw1, sb1, sw2, sb2, w_dtype, d, F, ysh.data());
-        oracle_combine_row(xr, x_dtype, add_residual, d, k, w + (long long)t * k, kept.data(),
-                           ys.data(), sw1 ? ysh.data() : nullptr,
-                           (char*)out + (long long)t * d * xsz, x_dtype);
+        oracle_combine_row_ovf(xr, x_dtype, add_residual, d, k, w + (long long)t * k, kept.data(),
+                               ys.data(), sw1 ? ysh.data() : nullptr, overflow == 1,
+                               (char*)out + (long long)t * d * xsz, x_dtype);
     }
 }
 

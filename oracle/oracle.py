@@ -41,6 +41,10 @@ def lib():
         L.oracle_capacity.argtypes = [dbl, i32, i32, i32]
         L.oracle_dispatch.restype = None
         L.oracle_dispatch.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
+        L.oracle_rank_candidates.restype = None
+        L.oracle_rank_candidates.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp]
+        L.oracle_dispatch_reroute.restype = None
+        L.oracle_dispatch_reroute.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         L.oracle_expert_row.restype = None
         L.oracle_expert_row.argtypes = [i32, vp, i32, vp, vp, vp, vp, i32, i32, i32, vp]
         L.oracle_quantize_rows_i8.restype = None
@@ -49,10 +53,12 @@ def lib():
         L.oracle_expert_row_q8.argtypes = [i32, vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, vp]
         L.oracle_combine_row.restype = None
         L.oracle_combine_row.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, i32]
+        L.oracle_combine_row_ovf.restype = None
+        L.oracle_combine_row_ovf.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, i32, vp, i32]
         L.oracle_forward.restype = None
         L.oracle_forward.argtypes = ([i32, i32, i32, i32, i32, i32, dbl, i32,
                                       vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
-                                      i32] + [vp] * 10)
+                                      i32] + [vp] * 10 + [i32])
         L.oracle_load_report.restype = None
         L.oracle_load_report.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, vp]
         _lib = L
@@ -153,7 +159,10 @@ def expert_row(kind, x_row, w1, b1, w2, b2, d, F):
     return y
 
 
-def combine_row(x_row, add_residual, w, kept, ys_k, ys_shared, out_dtype):
+def combine_row(x_row, add_residual, w, kept, ys_k, ys_shared, out_dtype,
+                overflow_to_shared=False):
+    """One token's output; with overflow_to_shared the dropped slots' weights are added to
+    the shared expert's weight (1 + sum of dropped w)."""
     x_row = np.ascontiguousarray(x_row)
     d = x_row.shape[0]
     k = len(w)
@@ -162,16 +171,49 @@ def combine_row(x_row, add_residual, w, kept, ys_k, ys_shared, out_dtype):
     ys_k = np.ascontiguousarray(ys_k, np.float64)
     ysh = None if ys_shared is None else np.ascontiguousarray(ys_shared, np.float64)
     out = np.empty(d, np.float32 if out_dtype == F32 else np.uint16)
-    lib().oracle_combine_row(_p(x_row), _dt(x_row), int(add_residual), d, k, _p(w), _p(kept),
-                             _p(ys_k), _p(ysh), _p(out), out_dtype)
+    lib().oracle_combine_row_ovf(_p(x_row), _dt(x_row), int(add_residual), d, k, _p(w), _p(kept),
+                                 _p(ys_k), _p(ysh), int(bool(overflow_to_shared)), _p(out),
+                                 out_dtype)
     return out
 
 
+def rank_candidates(logits, k, m, n_group=0, topk_group=0):
+    """[T, m] experts at ranking positions k .. k+m-1 of each token (-1 past the end);
+    with n_group > 0 only the experts of the chosen groups are ranked."""
+    logits = np.ascontiguousarray(logits, np.float32)
+    T, E = logits.shape
+    cand = np.empty((T, m), np.int32)
+    lib().oracle_rank_candidates(_p(logits), T, E, k, n_group, topk_group, m, _p(cand))
+    return cand
+
+
+def dispatch_reroute(idx, cand, E, cap):
+    """Dispatch with one re-routing round. cand [T, k] are each token's next-ranked
+    experts. Returns counts, offsets, perm_token[P], perm_slot[P], slot_dest[T,k] and
+    route_idx[T,k] (the expert that processes each slot)."""
+    idx = np.ascontiguousarray(idx, np.int32)
+    cand = np.ascontiguousarray(cand, np.int32)
+    T, k = idx.shape
+    assert cand.shape == (T, k)
+    counts = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    pt = np.full(T * k, -1, np.int32)
+    ps = np.full(T * k, -1, np.int32)
+    sd = np.empty((T, k), np.int32)
+    ri = np.empty((T, k), np.int32)
+    lib().oracle_dispatch_reroute(_p(idx), _p(cand), T, k, E, int(cap), _p(counts), _p(offsets),
+                                  _p(pt), _p(ps), _p(sd), _p(ri))
+    P = int(offsets[E])
+    return counts, offsets, pt[:P].copy(), ps[:P].copy(), sd, ri
+
+
 def forward(kind, x, Wg, gate_bias, w1, b1, w2, b2, k, F, cf=0.0, add_residual=False,
-            shared=None):
+            shared=None, overflow=0):
     """Whole-layer forward for host-resident inputs. Returns a dict of every output.
 
     shared: None or (sw1, sb1, sw2, sb2) for one always-on expert of the same kind.
+    overflow: 0 drop, 1 dropped weight to the shared expert, 2 one re-routing round
+    (idx then holds the expert that processes each slot).
     """
     T, d = x.shape
     E = Wg.shape[1]
@@ -192,7 +234,7 @@ def forward(kind, x, Wg, gate_bias, w1, b1, w2, b2, k, F, cf=0.0, add_residual=F
                          _p(x), xdt, _p(np.ascontiguousarray(Wg, np.float32)), _p(gate_bias),
                          _p(w1), _p(b1), _p(w2), _p(b2), _p(sw1), _p(sb1), _p(sw2), _p(sb2),
                          wdt, _p(out), _p(logits), _p(idx), _p(w), _p(ld), _p(counts),
-                         _p(offsets), _p(pt), _p(ps), _p(sd))
+                         _p(offsets), _p(pt), _p(ps), _p(sd), int(overflow))
     P = int(offsets[E])
     return dict(out=out, logits=logits, idx=idx, w=w, load=ld, counts=counts,
                 offsets=offsets, perm_token=pt[:P].copy(), perm_slot=ps[:P].copy(),

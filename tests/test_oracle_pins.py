@@ -573,3 +573,199 @@ def test_int8_expert_equals_bf16_expert_on_exactly_representable_weights(kind, F
         a = orc.expert_row_q8(kind, x, q1, s1, b1, q2, s2, b2, d, F)
         b = orc.expert_row(kind, x, w1, b1, w2, b2, d, F)
         assert np.array_equal(a, b)
+
+
+# --------------------------------------------------------------------------
+# overflow variants: re-routing to the next-ranked expert, overflow weight to the
+# shared expert ("MoE 并行" 推理时的负载均衡 and Q4; adv12 Q2)
+# --------------------------------------------------------------------------
+
+def _random_logits(T, E, seed, hot=()):
+    L = rand((T, E), seed, 3, 1.0)
+    for e in hot:
+        L[:, e] += 2.0          # a few popular experts, so that capacity bites
+    return np.ascontiguousarray(L, np.float32)
+
+
+def test_rank_candidates_match_a_sort():
+    L = _random_logits(40, 12, 5)
+    L[3, 4] = L[3, 7]           # a tie: the lower id ranks first
+    for k, m in ((1, 1), (2, 2), (3, 3), (5, 7)):
+        cand = orc.rank_candidates(L, k, m)
+        for t in range(40):
+            order = sorted(range(12), key=lambda e: (-float(L[t, e]), e))
+            want = (order[k:k + m] + [-1] * m)[:m]
+            assert cand[t].tolist() == want
+    # group-limited: only the chosen groups' experts are ranked
+    n_group, topk_group, k = 4, 2, 2
+    cand = orc.rank_candidates(L, k, 4, n_group, topk_group)
+    gs = 12 // n_group
+    for t in range(40):
+        gscore = [max(float(L[t, e]) for e in range(g * gs, (g + 1) * gs)) for g in range(n_group)]
+        groups = sorted(range(n_group), key=lambda g: (-gscore[g], g))[:topk_group]
+        pool = [e for e in range(12) if e // gs in groups]
+        order = sorted(pool, key=lambda e: (-float(L[t, e]), e))
+        assert cand[t].tolist() == order[k:k + 4]           # 6 experts in the pool, 4 asked
+        idx, _ = orc.topk_renorm(L[t:t + 1], k, n_group, topk_group)
+        assert idx[0].tolist() == order[:k]                 # consistent with the top-k
+
+
+def test_reroute_hand_example_top1():
+    # four tokens all prefer expert 0 (capacity 1); their second choices are 1, 1, 2, 1.
+    # Round 0 keeps token 0 on expert 0. Round 1: tokens 1 and 3 ask expert 1 (token 1
+    # first in token order takes its only row), token 2 asks expert 2 (accepted).
+    L = np.array([[3, 2, 1], [3, 2, 1], [3, 1, 2], [3, 2, 1]], np.float32)
+    idx, _ = orc.topk_renorm(L, 1)
+    cand = orc.rank_candidates(L, 1, 1)
+    assert cand[:, 0].tolist() == [1, 1, 2, 1]
+    counts, offsets, pt, ps, sd, ri = orc.dispatch_reroute(idx, cand, 3, 1)
+    assert counts.tolist() == [1, 1, 1] and offsets.tolist() == [0, 1, 2, 3]
+    assert pt.tolist() == [0, 1, 2] and ps.tolist() == [0, 0, 0]
+    assert sd[:, 0].tolist() == [0, 1, 2, -1]
+    assert ri[:, 0].tolist() == [0, 1, 2, 0]
+
+
+def test_reroute_hand_example_two_dropped_slots():
+    # E=4, k=2, capacity 1, every token ranks experts 0 > 1 > 2 > 3. Token 0 keeps 0 and
+    # 1; tokens 1 and 2 drop both slots. Round 1: slot 0 of a token asks its third-ranked
+    # expert (2), slot 1 its fourth (3); token 1 gets both rows, token 2 is rejected.
+    L = np.tile(np.array([[4, 3, 2, 1]], np.float32), (3, 1))
+    idx, _ = orc.topk_renorm(L, 2)
+    cand = orc.rank_candidates(L, 2, 2)
+    assert cand.tolist() == [[2, 3]] * 3
+    counts, offsets, pt, ps, sd, ri = orc.dispatch_reroute(idx, cand, 4, 1)
+    assert counts.tolist() == [1, 1, 1, 1]
+    assert pt.tolist() == [0, 0, 1, 1] and ps.tolist() == [0, 1, 0, 1]
+    assert sd.tolist() == [[0, 1], [2, 3], [-1, -1]]
+    assert ri.tolist() == [[0, 1], [2, 3], [0, 1]]
+
+
+def test_reroute_cannot_create_capacity_printed_loads():
+    # adv12 Q2 / section 3.2: loads [38, 34, 29, 27] at capacity 20. Every expert is over
+    # capacity, so no re-routed slot finds room: 80 rows kept, 18 + 14 + 9 + 7 = 48 dropped.
+    loads = [38, 34, 29, 27]
+    idx = np.concatenate([np.full(n, e, np.int32) for e, n in enumerate(loads)])
+    rng = np.random.default_rng(0)
+    idx = rng.permutation(idx).reshape(-1, 1)
+    T = idx.shape[0]
+    L = np.zeros((T, 4), np.float32)
+    L[np.arange(T), idx[:, 0]] = 1.0
+    cand = orc.rank_candidates(L, 1, 1)
+    counts, offsets, pt, ps, sd, ri = orc.dispatch_reroute(idx, cand, 4, 20)
+    assert counts.tolist() == [20, 20, 20, 20]
+    assert int((sd < 0).sum()) == 48
+    c0, o0, pt0, ps0, sd0 = orc.dispatch(idx, 4, 20)
+    assert np.array_equal(sd, sd0) and np.array_equal(pt, pt0)
+
+
+def test_reroute_without_capacity_is_plain_dispatch():
+    L = _random_logits(60, 8, 7, hot=(1, 2))
+    for k in (1, 2, 3):
+        idx, _ = orc.topk_renorm(L, k)
+        cand = orc.rank_candidates(L, k, k)
+        r = orc.dispatch_reroute(idx, cand, 8, 60)
+        p = orc.dispatch(idx, 8, 60)
+        for a, b in zip(r[:5], p):
+            assert np.array_equal(a, b)
+        assert np.array_equal(r[5], idx)
+
+
+@pytest.mark.parametrize("T,E,k,cap,seed", [(200, 16, 4, 40, 1), (300, 8, 1, 30, 2),
+                                            (150, 32, 8, 30, 3), (64, 6, 3, 20, 4)])
+def test_reroute_invariants(T, E, k, cap, seed):
+    L = _random_logits(T, E, seed, hot=(0, 3 % E))
+    idx, _ = orc.topk_renorm(L, k)
+    cand = orc.rank_candidates(L, k, k)
+    counts, offsets, pt, ps, sd, ri = orc.dispatch_reroute(idx, cand, E, cap)
+    c0, o0, pt0, ps0, sd0 = orc.dispatch(idx, E, cap)
+    P = int(offsets[E])
+    assert (counts <= cap).all() and P == int(counts.sum())
+    assert P >= int(c0.sum())                                # never fewer rows than dropping
+    kept0 = sd0 >= 0
+    assert ((sd >= 0) | ~kept0).all()                       # round-0 rows stay
+    assert np.array_equal(ri[kept0], idx[kept0])
+    proposals = {}
+    for t in range(T):
+        m = 0
+        for j in range(k):
+            if kept0[t, j]:
+                continue
+            want = int(cand[t, m])
+            m += 1
+            if sd[t, j] >= 0:
+                assert ri[t, j] == want                     # re-routed to its next candidate
+            else:
+                assert ri[t, j] == idx[t, j]
+            if want >= 0:
+                proposals.setdefault(want, []).append((t, j, sd[t, j] >= 0))
+        kept_e = [int(ri[t, j]) for j in range(k) if sd[t, j] >= 0]
+        assert len(kept_e) == len(set(kept_e))              # a token meets an expert once
+    for e, props in proposals.items():
+        accepted = [a for (_, _, a) in props]
+        # accepted in token order while there is room: a prefix, as long as the room
+        n_acc = sum(accepted)
+        assert accepted == [True] * n_acc + [False] * (len(props) - n_acc)
+        assert n_acc == min(len(props), cap - int(c0[e]))
+    # rows of each expert: round-0 rows in token order, then round-1 rows in token order
+    for e in range(E):
+        rows = list(zip(pt[offsets[e]:offsets[e + 1]], ps[offsets[e]:offsets[e + 1]]))
+        r0 = [(t, j) for (t, j) in rows if kept0[t, j]]
+        r1 = [(t, j) for (t, j) in rows if not kept0[t, j]]
+        assert rows == r0 + r1 and r0 == sorted(r0) and r1 == sorted(r1)
+    for t in range(T):
+        for j in range(k):
+            if sd[t, j] >= 0:
+                assert pt[sd[t, j]] == t and ps[sd[t, j]] == j
+
+
+def test_overflow_to_shared_expert():
+    kind, T, d, E, k, F = orc.LINEAR, 24, 8, 4, 2, 8
+    x, Wg, W = small_problem(kind, T, d, E, k, F, seed=9, bf16=False, shared=True)
+    gb = np.array([3.0, 0, 0, 0], np.float32)        # expert 0 is every token's first choice
+    sh = W["shared"]
+    W["shared"] = (sh[0], rand((d,), 9, 9, 0.1), None, None)
+    common = dict(cf=0.5, add_residual=True, shared=W["shared"])
+    r0 = orc.forward(kind, x, Wg, gb, W["w1"], W["b1"], None, None, k, F, overflow=0, **common)
+    r1 = orc.forward(kind, x, Wg, gb, W["w1"], W["b1"], None, None, k, F, overflow=1, **common)
+    assert np.array_equal(r0["slot_dest"], r1["slot_dest"])
+    dropped = r0["slot_dest"] < 0
+    assert dropped.any() and dropped.all(axis=1).any()
+    X = x.astype(np.float64)
+    S = X @ W["shared"][0].astype(np.float64).T + W["shared"][1].astype(np.float64)
+    a = (r0["w"].astype(np.float64) * dropped).sum(axis=1, keepdims=True)
+    # the dropped weight multiplies the shared expert: out1 - out0 = a * S
+    diff = r1["out"].astype(np.float64) - r0["out"].astype(np.float64)
+    tol = 4e-7 * (np.abs(r0["out"]).astype(np.float64) + np.abs(a * S) + 1e-6)
+    assert (np.abs(diff - a * S) <= tol).all()
+    # a fully dropped token: its weights sum to 1, so it leaves as x + 2 * S(x)
+    full = dropped.all(axis=1)
+    want = X[full] + 2.0 * S[full]
+    assert np.allclose(r1["out"][full], want, rtol=2e-6, atol=1e-6)
+    # without capacity nothing is dropped and the variants agree bit for bit
+    r0n = orc.forward(kind, x, Wg, gb, W["w1"], W["b1"], None, None, k, F, overflow=0,
+                      add_residual=True, shared=W["shared"])
+    r1n = orc.forward(kind, x, Wg, gb, W["w1"], W["b1"], None, None, k, F, overflow=1,
+                      add_residual=True, shared=W["shared"])
+    assert np.array_equal(r0n["out"], r1n["out"])
+
+
+def test_reroute_forward_matches_dense_mixture_of_processing_experts():
+    # the forward with re-routing equals a dense sum over experts where each kept slot's
+    # weight sits on the expert that processes it (route_idx)
+    kind, T, d, E, k, F = orc.LINEAR, 40, 8, 6, 2, 8
+    x, Wg, W = small_problem(kind, T, d, E, k, F, seed=13, bf16=False, biases=True)
+    gb = np.array([2.0, 1.5, 0, 0, 0, 0], np.float32)
+    r = orc.forward(kind, x, Wg, gb, W["w1"], W["b1"], None, None, k, F, cf=0.75, overflow=2)
+    base = orc.forward(kind, x, Wg, gb, W["w1"], W["b1"], None, None, k, F, cf=0.75)
+    assert int((r["slot_dest"] >= 0).sum()) > int((base["slot_dest"] >= 0).sum())
+    X = x.astype(np.float64)
+    M = np.zeros((T, E))
+    for t in range(T):
+        for j in range(k):
+            if r["slot_dest"][t, j] >= 0:
+                M[t, r["idx"][t, j]] += float(r["w"][t, j])
+    out = np.zeros((T, d))
+    for e in range(E):
+        out += M[:, [e]] * (X @ W["w1"][e].astype(np.float64).T + W["b1"][e].astype(np.float64))
+    assert np.allclose(r["out"], out, rtol=2e-6, atol=1e-6)
+    assert np.array_equal(r["load"], base["load"])          # load is the raw top-k bincount
