@@ -237,7 +237,11 @@ def cpu_oracle_sample(wl, sample_tokens, seed=0):
     L = orc.gate_logits(x, Wg, gb)
     idx, w = orc.topk_renorm(L, wl.k, wl.n_group, wl.topk_group)
     cap = orc.capacity(np.float32(wl.cf), wl.T, wl.k, wl.E)
-    counts, offsets, pt, ps, sd = orc.dispatch(idx, wl.E, cap)
+    if wl.overflow == "reroute":
+        cand = orc.rank_candidates(L, wl.k, wl.k, wl.n_group, wl.topk_group)
+        counts, offsets, pt, ps, sd, idx = orc.dispatch_reroute(idx, cand, wl.E, cap)
+    else:
+        counts, offsets, pt, ps, sd = orc.dispatch(idx, wl.E, cap)
     t_route = time.perf_counter() - t0
     need = sorted({int(idx[t, j]) for t in rows for j in range(wl.k) if sd[t, j] >= 0})
 
@@ -261,7 +265,8 @@ def cpu_oracle_sample(wl, sample_tokens, seed=0):
                 ys[j] = Wc[int(idx[t, j])](xr)
         ysh = shared(xr) if shared else None
         orc.combine_row(xr, wl.add_residual, w[t], kept, ys, ysh,
-                        orc.BF16 if wl.bf16 else orc.F32)
+                        orc.BF16 if wl.bf16 else orc.F32,
+                        overflow_to_shared=wl.overflow == "shared")
     t_ffn = time.perf_counter() - t0
     per_token = t_route / wl.T + t_ffn / S
     desc = (f"routing+dispatch of all {wl.T} tokens ({t_route:.2f} s) + expert FFN and "
@@ -504,6 +509,7 @@ def run_ours(args, wl):
                    "shared_expert": wl.has_shared, "residual": wl.add_residual,
                    "expert_groups": [wl.n_group, wl.topk_group] if wl.n_group else None,
                    "expert_weights": "int8 codes + fp32 row scales" if wl.int8 else "bf16",
+                   "overflow": wl.overflow,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"flushed between steps ({args.flush_mib} MiB write)",
                    "kept_rows_P": P, "touched_experts": touched},

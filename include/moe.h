@@ -69,6 +69,20 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_I8 = 2 } moe_dtype;
  * rounded to bf16 before the second GEMM. LINEAR runs in fp32. */
 typedef enum { MOE_EXPERT_LINEAR = 0, MOE_EXPERT_GELU = 1, MOE_EXPERT_SWIGLU = 2 } moe_expert_kind;
 
+/* What happens to an assignment (t, j) beyond its expert's capacity.
+ *  DROP    : it contributes 0 ["MoE 并行" Capacity Factor: overflow takes the residual path;
+ *            adv12 Q2 option 1].
+ *  SHARED  : its weight w_tj moves to the shared expert, whose weight for token t becomes
+ *            1 + sum of the token's dropped w ["MoE 并行" Q4, Q5; adv12 Q2 option 2].
+ *            Needs has_shared.
+ *  REROUTE : one re-routing round ["MoE 并行" 推理时的负载均衡, dynamic re-routing to the next
+ *            expert; "MoE 混合专家架构" 4.2 capacity check]: token t's dropped slots, in slot
+ *            order, propose to its experts ranked k, k+1, ... (same order and, with
+ *            group-limited routing, the same groups as the top k) keeping their weights;
+ *            each expert accepts proposals in token order while its round-0 rows plus the
+ *            accepted ones stay below the capacity; the rest stay dropped. */
+typedef enum { MOE_OVERFLOW_DROP = 0, MOE_OVERFLOW_SHARED = 1, MOE_OVERFLOW_REROUTE = 2 } moe_overflow;
+
 typedef struct {
     int32_t T;                 /* tokens (rows of x); 0 is a valid no-op */
     int32_t d;                 /* model width; multiple of 8 (of 64 for GELU/SWIGLU) */
@@ -94,6 +108,7 @@ typedef struct {
                                   w1/w2 hold int8 codes q and s1/s2 one fp32 scale per weight
                                   row; the experts compute with s[n] * q[n][k] (see
                                   moe_quantize_i8). Routed and shared experts alike. */
+    int32_t overflow;          /* moe_overflow; 0 = MOE_OVERFLOW_DROP */
 } moe_config;
 
 /* One set of stacked expert weights (nn.Linear [out, in] layout, K contiguous).
@@ -135,7 +150,9 @@ int32_t moe_capacity(const moe_config* cfg);
  * Logits are fp32 sums of exact fp32 products x_i * W_gate[i, e] (bf16 activations with
  * many tokens run on the tensor cores against W_gate split exactly into three bf16
  * terms); partial sums are added in a fixed order, so results are reproducible run to
- * run, and selection is bit-reproducible given the logits. */
+ * run, and selection is bit-reproducible given the logits.
+ * With MOE_OVERFLOW_REROUTE it also stores each token's experts ranked k .. 2k-1 in ws,
+ * where moe_dispatch reads them. */
 moe_status moe_route(const moe_config* cfg, const void* x, const float* W_gate,
                      const float* gate_bias, float* logits, int32_t* topk_idx, float* topk_w,
                      void* ws, cudaStream_t stream);
@@ -153,7 +170,12 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* W_gate,
  *                     (assignments beyond the capacity are dropped in token order)
  *   x_perm     [T*k, d] act_dtype output, nullable: x_perm[p] = x[perm_token[p]]
  *   ws         workspace
- * Everything is deterministic (no order-dependent atomics). */
+ * Everything is deterministic (no order-dependent atomics).
+ * MOE_OVERFLOW_REROUTE: ws must hold what moe_route wrote for the same tokens (the
+ * next-ranked experts). counts = kept rows after re-routing; expert e's rows are its
+ * round-0 rows (token order) followed by the re-routed rows it accepted (token order);
+ * slot_dest points re-routed slots at their new expert's rows; load stays the top-k
+ * bincount before capacity. */
 moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const void* x,
                         int32_t* load, int32_t* counts, int32_t* offsets, int32_t* perm_token,
                         int32_t* perm_slot, int32_t* slot_dest, void* x_perm, void* ws,
@@ -178,12 +200,14 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32
 
 /* Combine ["MOE 学习笔记" 输出聚合示例; "MoE 并行" Result Gather + 加权组合].
  *   out[t] = (add_residual ? x[t] : 0) + sum_{j = 0..k-1, slot kept} y[slot_dest[t,j]]
- *            + (has_shared ? y[T*k + t] : 0)
- * summed in fp32 in that order and rounded once to act_dtype.
+ *            + (has_shared ? a_t * y[T*k + t] : 0)
+ * summed in fp32 in that order and rounded once to act_dtype; a_t = 1, or with
+ * MOE_OVERFLOW_SHARED a_t = 1 + sum of topk_w[t, j] over the dropped slots (fp32, slot order).
  *   x [T, d] (read iff add_residual), y as written by moe_expert_ffn, slot_dest [T, k],
- *   out [T, d] act_dtype output. */
+ *   topk_w [T, k] (read iff MOE_OVERFLOW_SHARED, else nullable), out [T, d] act_dtype output. */
 moe_status moe_combine(const moe_config* cfg, const void* x, const float* y,
-                       const int32_t* slot_dest, void* out, cudaStream_t stream);
+                       const int32_t* slot_dest, const float* topk_w, void* out,
+                       cudaStream_t stream);
 
 /* The whole layer: route -> dispatch -> expert FFNs -> combine, stream-ordered, no
  * host synchronisation. out [T, d] act_dtype. Optional outputs (nullable):
@@ -221,7 +245,8 @@ moe_status moe_grouped_gemm(const void* A, int64_t a_rows, const void* B, int32_
  * device address (cudaGetSymbolAddress, with that device current), so make that
  * first call before any stream capture. All calls share the one array: calls that
  * overlap on the GPU (different streams, or different host threads) race on it and
- * must be ordered by the caller. */
+ * must be ordered by the caller. MOE_OVERFLOW_REROUTE needs the workspace moe_route
+ * wrote and is rejected here with MOE_ERR_UNSUPPORTED. */
 moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_idx, const void* x,
                                 int32_t* load, int32_t* counts, int32_t* offsets,
                                 int32_t* perm_token, int32_t* perm_slot, int32_t* slot_dest,

@@ -42,6 +42,7 @@ class Workload:
     int8: bool = False          # weight-only INT8 experts (codes + per-row scales)
     n_group: int = 0            # group-limited routing: expert groups (0 = plain top-k)
     topk_group: int = 0         # groups kept per token
+    overflow: str = "drop"      # over-capacity slots: "drop" | "shared" | "reroute"
     seed: int = 0
     note: str = ""
 
@@ -220,6 +221,10 @@ WORKLOADS = {
                                  kind="swiglu", act="bf16", cf=1.0, has_shared=True, n_group=8,
                                  topk_group=4,
                                  note="DeepSeek-V3-shaped, group-limited routing: 8 groups, 4 kept"),
+    "deepseek_reroute": Workload("deepseek_reroute", T=8192, d=7168, E=256, k=8, F=2048,
+                                 kind="swiglu", act="bf16", cf=1.0, has_shared=True,
+                                 overflow="reroute",
+                                 note="DeepSeek-V3-shaped, cf 1.0, over-capacity slots re-routed"),
     "deepseek_cf125": Workload("deepseek_cf125", T=8192, d=7168, E=256, k=8, F=2048,
                                kind="swiglu", act="bf16", cf=1.25, has_shared=True,
                                note="DeepSeek-V3-shaped, capacity factor 1.25"),

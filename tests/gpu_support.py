@@ -81,7 +81,7 @@ class GpuRun:
         moe.expert_ffn(cfg, self.x_perm, self.offsets, routed, shared, inp["x"], self.w,
                        self.perm_token, self.perm_slot, self.y, ws)
         self.out_stages = torch.empty_like(inp["x"])
-        moe.combine(cfg, inp["x"], self.y, self.slot_dest, self.out_stages)
+        moe.combine(cfg, inp["x"], self.y, self.slot_dest, self.out_stages, topk_w=self.w)
         # the fused entry point on a fresh workspace
         ws2 = torch.empty_like(ws)
         self.out = torch.empty_like(inp["x"])
@@ -126,10 +126,18 @@ def check_routing(r):
 
 
 def check_dispatch(r, idx_ref):
+    """Dispatch outputs bit-exact against the oracle fed the GPU's routing. Returns the
+    capacity, slot_dest, P and the expert that processes each slot (re-routing moves
+    dropped slots to the token's next-ranked experts)."""
     wl = r.wl
     cap = orc.capacity(np.float32(wl.cf), wl.T, wl.k, wl.E)
     assert moe.capacity(r.cfg) == cap
-    counts, offsets, pt, ps, sd = orc.dispatch(idx_ref, wl.E, cap)
+    if wl.overflow == "reroute":
+        cand = orc.rank_candidates(to_np(r.logits), wl.k, wl.k, wl.n_group, wl.topk_group)
+        counts, offsets, pt, ps, sd, route_idx = orc.dispatch_reroute(idx_ref, cand, wl.E, cap)
+    else:
+        counts, offsets, pt, ps, sd = orc.dispatch(idx_ref, wl.E, cap)
+        route_idx = idx_ref
     ld = orc.load(idx_ref, wl.E)
     assert np.array_equal(to_np(r.load), ld)
     assert np.array_equal(to_np(r.load_f), ld)
@@ -139,7 +147,7 @@ def check_dispatch(r, idx_ref):
     assert np.array_equal(to_np(r.perm_token)[:P], pt)
     assert np.array_equal(to_np(r.perm_slot)[:P], ps)
     assert np.array_equal(to_np(r.slot_dest), sd)
-    return cap, sd, P
+    return cap, sd, P, route_idx
 
 
 def _expert_fn(wl, e, shared=False):
@@ -165,7 +173,8 @@ def check_quantized_weights(r, experts):
 
 
 def oracle_rows(wl, x_host_rows, rows, idx_ref, w_ref, sd, cache):
-    """Oracle outputs for the given tokens, with routing fed from the GPU logits."""
+    """Oracle outputs for the given tokens, with routing fed from the GPU logits; idx_ref
+    names the expert that processes each kept slot."""
     out = []
     for t_i, t in enumerate(rows):
         xr = np.ascontiguousarray(x_host_rows[t_i])
@@ -183,7 +192,8 @@ def oracle_rows(wl, x_host_rows, rows, idx_ref, w_ref, sd, cache):
                 cache["shared"] = _expert_fn(wl, 0, True)
             ysh = cache["shared"](xr)
         out.append(orc.combine_row(xr, wl.add_residual, w_ref[t], kept, ys, ysh,
-                                   orc.BF16 if wl.bf16 else orc.F32))
+                                   orc.BF16 if wl.bf16 else orc.F32,
+                                   overflow_to_shared=wl.overflow == "shared"))
     return np.stack(out)
 
 
@@ -217,7 +227,7 @@ def full_check(wl, sample=None, seed=0):
         x_rows = x_all[rows]
     check_logits(wl, x_all, rows, to_np(r.logits)[rows])
     idx_ref, w_ref = check_routing(r)
-    cap, sd, P = check_dispatch(r, idx_ref)
+    cap, sd, P, route_idx = check_dispatch(r, idx_ref)
     # gathered rows are exact copies
     xp = to_np(r.x_perm)[:P]
     pt = to_np(r.perm_token)[:P]
@@ -226,7 +236,7 @@ def full_check(wl, sample=None, seed=0):
     if wl.int8:
         used = sorted({int(e) for e in idx_ref[rows].ravel()})
         check_quantized_weights(r, used[:8])
-    ref = oracle_rows(wl, x_rows, rows, idx_ref, w_ref, sd, {})
+    ref = oracle_rows(wl, x_rows, rows, route_idx, w_ref, sd, {})
     stats = check_outputs(wl, to_np(r.out)[rows], ref)
     check_outputs(wl, to_np(r.out_stages)[rows], ref)
     return r, stats

@@ -91,7 +91,9 @@ def test_workspace_and_rows(lib):
     dict(n_group=-1, topk_group=1),
     # weight dtype: the activation dtype or INT8 codes (GELU / SwiGLU experts only)
     dict(w_dtype=5), dict(w_dtype=-1),
-    dict(w_dtype=C.MOE_I8, kind=C.MOE_EXPERT_LINEAR, act_dtype=C.MOE_F32)])
+    dict(w_dtype=C.MOE_I8, kind=C.MOE_EXPERT_LINEAR, act_dtype=C.MOE_F32),
+    # overflow policy: 0..2; the dropped weight can only go to a shared expert that exists
+    dict(overflow=3), dict(overflow=-1), dict(overflow=C.MOE_OVERFLOW_SHARED)])
 def test_invalid_configs_rejected(lib, bad):
     base = dict(T=64, d=128, E=4, top_k=2, F=128, capacity_factor=0.0, act_dtype=C.MOE_BF16,
                 kind=C.MOE_EXPERT_GELU, has_shared=0, add_residual=0)
@@ -132,6 +134,25 @@ def test_int8_weights_need_scales(lib):
     assert lib.moe_quantize_i8(ok, 0, 64, ok, ok, None) == C.MOE_OK
 
 
+def test_overflow_policies(lib):
+    for ov in ("drop", "shared", "reroute"):
+        cfg = api.make_config(64, 128, 8, 2, 128, 1.0, "swiglu", True, has_shared=True,
+                              overflow=ov)
+        assert api.workspace_size(cfg) > 0
+    # re-routing keeps candidates and proposals in the workspace
+    base = api.make_config(300, 128, 8, 2, 128, 1.0, "swiglu", True)
+    rr = api.make_config(300, 128, 8, 2, 128, 1.0, "swiglu", True, overflow="reroute")
+    assert api.workspace_size(rr) >= api.workspace_size(base) + 2 * 300 * 2 * 4
+    ok = ctypes.c_void_p(1 << 20)
+    # moe_dispatch_noalloc has no workspace to read the candidates from
+    assert lib.moe_dispatch_noalloc(ctypes.byref(rr), ok, ok, ok, ok, ok, ok, ok, ok, None,
+                                    None) == C.MOE_ERR_UNSUPPORTED
+    # the shared-overflow combine needs the routing weights
+    sh = api.make_config(64, 128, 8, 2, 128, 1.0, "swiglu", True, has_shared=True,
+                         overflow="shared")
+    assert lib.moe_combine(ctypes.byref(sh), ok, ok, ok, None, ok, None) == C.MOE_ERR_INVALID_ARG
+
+
 def test_unsupported_dtype_kind_pairs(lib):
     for kind, dt in [(C.MOE_EXPERT_LINEAR, C.MOE_BF16), (C.MOE_EXPERT_GELU, C.MOE_F32),
                      (C.MOE_EXPERT_SWIGLU, C.MOE_F32)]:
@@ -150,7 +171,7 @@ def test_misaligned_and_missing_pointers(lib):
     assert lib.moe_route(r, bad, ok, None, ok, ok, ok, ok, None) == C.MOE_ERR_MISALIGNED
     assert lib.moe_route(r, None, ok, None, ok, ok, ok, ok, None) == C.MOE_ERR_INVALID_ARG
     assert lib.moe_route(r, ok, ok, None, None, ok, ok, None, None) == C.MOE_ERR_WORKSPACE
-    assert lib.moe_combine(r, ok, ok, ok, bad, None) == C.MOE_ERR_MISALIGNED
+    assert lib.moe_combine(r, ok, ok, ok, None, bad, None) == C.MOE_ERR_MISALIGNED
     w = C.MoeExpertWeights(w1=ok, b1=None, w2=None, b2=None)   # GELU needs w2
     assert lib.moe_forward(r, ok, ok, None, ctypes.byref(w), None, ok, None, None, None, ok,
                            1 << 40, None) == C.MOE_ERR_INVALID_ARG
@@ -164,7 +185,7 @@ def test_zero_tokens_is_a_noop(lib):
     cfg = api.make_config(0, 128, 4, 2, 128, 0.0, "gelu", True)
     r = ctypes.byref(cfg)
     assert lib.moe_route(r, None, None, None, None, None, None, None, None) == C.MOE_OK
-    assert lib.moe_combine(r, None, None, None, None, None) == C.MOE_OK
+    assert lib.moe_combine(r, None, None, None, None, None, None) == C.MOE_OK
     assert api.kernel_launch_count() == 0
 
 

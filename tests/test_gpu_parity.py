@@ -74,6 +74,22 @@ SMALL = {
                          cf=0.5, gate_bias="hot", add_residual=True, int8=True),
     "i8t_hot_one_expert": W("q8t4", T=48, d=128, E=8, k=1, F=128, kind="swiglu", act="bf16",
                             gate_bias="hot", int8=True),
+    # overflow variants: one re-routing round to the next-ranked experts, or the dropped
+    # weight moved to the shared expert
+    "reroute_k2_zipf": W("rr1", T=300, d=128, E=8, k=2, F=128, kind="gelu", act="bf16",
+                         cf=0.75, gate_bias="zipf", overflow="reroute"),
+    "reroute_top1_hot_res": W("rr2", T=500, d=128, E=4, k=1, F=192, kind="gelu", act="bf16",
+                              cf=0.5, gate_bias="hot", add_residual=True, overflow="reroute"),
+    "reroute_grouped_small_T": W("rr3", T=40, d=256, E=64, k=6, F=64, kind="gelu",
+                                 act="bf16", n_group=16, topk_group=3, cf=1.0,
+                                 overflow="reroute"),
+    "reroute_k8_shared": W("rr4", T=260, d=256, E=32, k=8, F=128, kind="swiglu", act="bf16",
+                           cf=0.5, has_shared=True, overflow="reroute"),
+    "ovf_shared_k2_res": W("os1", T=300, d=128, E=8, k=2, F=128, kind="swiglu", act="bf16",
+                           cf=0.5, has_shared=True, gate_bias="zipf", add_residual=True,
+                           overflow="shared"),
+    "ovf_shared_hot_k1": W("os2", T=200, d=64, E=8, k=1, F=64, kind="gelu", act="bf16",
+                           cf=0.5, gate_bias="hot", has_shared=True, overflow="shared"),
     # K = 64: one half-filled 128-code K block (zero codes and activations past the end)
     "i8t_k64": W("q8t5", T=10, d=64, E=4, k=2, F=64, kind="swiglu", act="bf16",
                  expert_bias=True, has_shared=True, int8=True),
@@ -161,7 +177,7 @@ def test_forward_is_deterministic():
     ("switch", 32), ("mixtral", 8), ("deepseek", 4), ("deepseek_cf125", 4),
     ("deepseek_grouped", 4),
     ("decode1", None), ("decode8", 4), ("decode64", 4),
-    ("decode1_i8", None), ("decode8_i8", 4), ("decode64_i8", 4),
+    ("decode1_i8", None), ("decode8_i8", 4), ("decode64_i8", 4), ("deepseek_reroute", 4),
 ])
 def test_full_size_sampled(name, sample):
     r, stats = full_check(get(name), sample=sample, seed=1)
@@ -254,6 +270,19 @@ def test_out_of_range_expert_id_single_cta_dispatch():
     assert ld.sum() == T * k - 2
     good = ref.numpy()
     assert np.array_equal(ld, np.bincount(good[good >= 0], minlength=E))
+
+
+@pytest.mark.parametrize("name", ["reroute_top1_hot_res", "reroute_k2_zipf"])
+def test_reroute_keeps_more_rows_than_dropping(name):
+    wl = SMALL[name]
+    r = GpuRun(wl).run()
+    plain = GpuRun(wl.with_(overflow="drop")).run()
+    kept_rr = int((to_np(r.slot_dest) >= 0).sum())
+    kept = int((to_np(plain.slot_dest) >= 0).sum())
+    assert kept_rr > kept
+    assert np.array_equal(to_np(r.load), to_np(plain.load))      # load: top-k before capacity
+    cap = moe.capacity(r.cfg)
+    assert (to_np(r.counts) <= cap).all()
 
 
 def test_int8_quantiser_matches_oracle_bitwise():

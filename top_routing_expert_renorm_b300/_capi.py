@@ -22,6 +22,7 @@ MOE_ERR_DEVICE_INDEX = 7
 # moe_dtype / moe_expert_kind
 MOE_F32, MOE_BF16, MOE_I8 = 0, 1, 2
 MOE_EXPERT_LINEAR, MOE_EXPERT_GELU, MOE_EXPERT_SWIGLU = 0, 1, 2
+MOE_OVERFLOW_DROP, MOE_OVERFLOW_SHARED, MOE_OVERFLOW_REROUTE = 0, 1, 2
 
 
 class MoeConfig(ctypes.Structure):
@@ -30,7 +31,8 @@ class MoeConfig(ctypes.Structure):
                 ("capacity_factor", ctypes.c_float), ("act_dtype", ctypes.c_int32),
                 ("kind", ctypes.c_int32), ("has_shared", ctypes.c_int32),
                 ("add_residual", ctypes.c_int32), ("n_group", ctypes.c_int32),
-                ("topk_group", ctypes.c_int32), ("w_dtype", ctypes.c_int32)]
+                ("topk_group", ctypes.c_int32), ("w_dtype", ctypes.c_int32),
+                ("overflow", ctypes.c_int32)]
 
 
 class MoeExpertWeights(ctypes.Structure):
@@ -65,7 +67,7 @@ def load():
         "moe_route": (i32, [cfgp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "moe_dispatch": (i32, [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "moe_expert_ffn": (i32, [cfgp, vp, vp, wp, wp, vp, vp, vp, vp, vp, vp, vp]),
-        "moe_combine": (i32, [cfgp, vp, vp, vp, vp, vp]),
+        "moe_combine": (i32, [cfgp, vp, vp, vp, vp, vp, vp]),
         "moe_forward": (i32, [cfgp, vp, vp, vp, wp, wp, vp, vp, vp, vp, vp, sz, vp]),
         "moe_grouped_gemm_ws_size": (sz, [i32]),
         "moe_grouped_gemm": (i32, [vp, i64, vp, i32, i32, i32, vp, vp, vp, vp]),

@@ -39,15 +39,21 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+OVERFLOW = {"drop": C.MOE_OVERFLOW_DROP, "shared": C.MOE_OVERFLOW_SHARED,
+            "reroute": C.MOE_OVERFLOW_REROUTE}
+
+
 def make_config(T, d, E, top_k, F=0, capacity_factor=0.0, kind="gelu", bf16=True,
-                has_shared=False, add_residual=False, n_group=0, topk_group=0, int8_weights=False):
+                has_shared=False, add_residual=False, n_group=0, topk_group=0, int8_weights=False,
+                overflow="drop"):
+    """overflow: "drop", "shared" (dropped weight to the shared expert) or "reroute"."""
     kinds = {"linear": C.MOE_EXPERT_LINEAR, "gelu": C.MOE_EXPERT_GELU,
              "swiglu": C.MOE_EXPERT_SWIGLU}
     return MoeConfig(T=T, d=d, E=E, top_k=top_k, F=F, capacity_factor=capacity_factor,
                      act_dtype=C.MOE_BF16 if bf16 else C.MOE_F32, kind=kinds[kind],
                      has_shared=int(bool(has_shared)), add_residual=int(bool(add_residual)),
                      n_group=n_group, topk_group=topk_group,
-                     w_dtype=C.MOE_I8 if int8_weights else 0)
+                     w_dtype=C.MOE_I8 if int8_weights else 0, overflow=OVERFLOW[overflow])
 
 
 def config_for(workload, T=None):
@@ -55,7 +61,8 @@ def config_for(workload, T=None):
     return make_config(T if T is not None else workload.T, workload.d, workload.E, workload.k,
                        workload.F if workload.kind != "linear" else 0, workload.cf,
                        workload.kind, workload.bf16, workload.has_shared, workload.add_residual,
-                       workload.n_group, workload.topk_group, workload.int8)
+                       workload.n_group, workload.topk_group, workload.int8,
+                       workload.overflow)
 
 
 def weights(w1, b1=None, w2=None, b2=None, s1=None, s2=None):
@@ -120,9 +127,10 @@ def expert_ffn(cfg, x_perm, offsets, routed, shared, x, topk_w, perm_token, perm
                                    _ptr(y), _ptr(ws), _stream(stream)), "moe_expert_ffn")
 
 
-def combine(cfg, x, y, slot_dest, out, stream=None):
-    _check(C.load().moe_combine(ctypes.byref(cfg), _ptr(x), _ptr(y), _ptr(slot_dest), _ptr(out),
-                                _stream(stream)), "moe_combine")
+def combine(cfg, x, y, slot_dest, out, topk_w=None, stream=None):
+    """topk_w is read when the layer sends overflow weight to the shared expert."""
+    _check(C.load().moe_combine(ctypes.byref(cfg), _ptr(x), _ptr(y), _ptr(slot_dest),
+                                _ptr(topk_w), _ptr(out), _stream(stream)), "moe_combine")
 
 
 def forward(cfg, x, W_gate, gate_bias, routed, shared, out, ws, topk_idx=None, topk_w=None,

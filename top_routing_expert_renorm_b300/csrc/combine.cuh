@@ -84,12 +84,19 @@ __device__ __forceinline__ void add4(float4& a, const float4& v) {
     a.z += v.z;
     a.w += v.w;
 }
+__device__ __forceinline__ void fma4(float4& a, float s, const float4& v) {
+    a.x = fmaf(s, v.x, a.x);
+    a.y = fmaf(s, v.y, a.y);
+    a.z = fmaf(s, v.z, a.z);
+    a.w = fmaf(s, v.w, a.w);
+}
 
 template <typename OT>
 __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ x,
                                                       const float* __restrict__ y,
                                                       const int* __restrict__ slot_dest,
                                                       const float* __restrict__ y_shared,
+                                                      const float* __restrict__ ovf_w,
                                                       OT* __restrict__ out, int T, int d, int k,
                                                       int add_residual, int cpt) {
     pdl_entry();
@@ -103,6 +110,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ x,
         const long long t = wi / spans;
         const int sp = (int)(wi - t * spans);
         const int mydest = lane < k ? slot_dest[t * k + lane] : -1;
+        // overflow to the shared expert: its weight is 1 + the dropped slots' weights,
+        // summed in fp32 in slot order
+        float a_sh = 1.0f;
+        if (ovf_w) {
+            const float wd = (lane < k && mydest < 0) ? ovf_w[t * k + lane] : 0.0f;
+            for (int j = 0; j < k; ++j) a_sh += __shfl_sync(0xffffffffu, wd, j);
+        }
         const int cend = min(chunks, (sp + 1) * cpt);
         for (int ch = sp * cpt; ch < cend; ++ch) {
             const int ca = ch * 256 + lane * 4, cb = ca + 128;
@@ -121,8 +135,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ x,
             }
             if (y_shared) {
                 const float* ys = y_shared + t * d;
-                if (va) add4(a, *reinterpret_cast<const float4*>(ys + ca));
-                if (vb) add4(b, *reinterpret_cast<const float4*>(ys + cb));
+                if (ovf_w) {
+                    if (va) fma4(a, a_sh, *reinterpret_cast<const float4*>(ys + ca));
+                    if (vb) fma4(b, a_sh, *reinterpret_cast<const float4*>(ys + cb));
+                } else {
+                    if (va) add4(a, *reinterpret_cast<const float4*>(ys + ca));
+                    if (vb) add4(b, *reinterpret_cast<const float4*>(ys + cb));
+                }
             }
             if (va) store4<OT>(out + t * d + ca, a);
             if (vb) store4<OT>(out + t * d + cb, b);

@@ -111,10 +111,20 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(
 }
 
 // ---- stable rank + scatter of the kept assignments ------------------------------------
+// MODE kRankScatter: rank the ids of `idx` and scatter the kept ones (rank < cap).
+// Re-routing ["MoE 并行" 推理时的负载均衡: an over-limit token goes to the next expert]:
+// MODE kRankStatus ranks the original ids and only records slot_dest[i] = round-0 rank
+// (kept), -1 (dropped) or -2 (invalid id, skipped as in the plain dispatch); MODE kRankReroute ranks the proposals `idx` = prop (the
+// dropped slots' next-ranked experts, -1 for none) and scatters every slot: a round-0
+// row of expert e at offsets[e] + its round-0 rank, an accepted proposal (rank <
+// cap - cnt0[e]) after the cnt0[e] round-0 rows of its new expert.
+enum { kRankScatter = 0, kRankStatus = 1, kRankReroute = 2 };
+
+template <int MODE>
 __global__ void __launch_bounds__(256) dispatch_rank_kernel(
     const int* __restrict__ idx, int T, int k, int E, int cap, const int* __restrict__ blockoff,
     const int* __restrict__ offsets, int* __restrict__ perm_token, int* __restrict__ perm_slot,
-    int* __restrict__ slot_dest) {
+    int* __restrict__ slot_dest, const int* __restrict__ orig_idx, const int* __restrict__ cnt0) {
     pdl_entry();
     extern __shared__ int wcnt[];   // [kDispWarps][E] running counters
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -160,16 +170,61 @@ __global__ void __launch_bounds__(256) dispatch_rank_kernel(
         if (e >= 0 && (peers & lt_mask) == 0) my[e] += __popc(peers);
         __syncwarp();
         if (i < wend) {
-            if (e >= 0 && rank < cap) {
-                const int pos = offsets[e] + rank;
-                perm_token[pos] = (int)(i / k);
-                perm_slot[pos] = (int)(i % k);
-                slot_dest[i] = pos;
+            if constexpr (MODE == kRankStatus) {
+                slot_dest[i] = (e >= 0) ? (rank < cap ? rank : -1) : -2;   // -2: invalid id
             } else {
-                slot_dest[i] = -1;
+                int pos = -1;
+                if constexpr (MODE == kRankScatter) {
+                    if (e >= 0 && rank < cap) pos = offsets[e] + rank;
+                } else {
+                    const int r0 = slot_dest[i];
+                    if (r0 >= 0) pos = offsets[orig_idx[i]] + r0;
+                    else if (e >= 0 && rank < cap - cnt0[e]) pos = offsets[e] + cnt0[e] + rank;
+                }
+                if (pos >= 0) {
+                    perm_token[pos] = (int)(i / k);
+                    perm_slot[pos] = (int)(i % k);
+                }
+                slot_dest[i] = pos;
             }
         }
     }
+}
+
+// ---- re-routing: proposals of the dropped slots and their per-chunk histogram ----------
+// slot_dest holds the round-0 status (rank, -1 dropped, -2 invalid). Token t's dropped
+// slots, in slot
+// order, take cand[t][0], cand[t][1], ... (its experts ranked k, k+1, ...; -1 = none):
+// prop[t*k + j] = that expert, -1 for kept slots. blockcnt[b][e] = proposals of chunk b
+// to expert e.
+__global__ void __launch_bounds__(256) reroute_propose_kernel(const int* __restrict__ slot_dest,
+                                                              const int* __restrict__ cand, int T,
+                                                              int k, int E, int* __restrict__ prop,
+                                                              int* __restrict__ blockcnt) {
+    pdl_entry();
+    extern __shared__ int cnt[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    const int t_end = min((blockIdx.x + 1) * kDispTok, T);
+    for (int t = blockIdx.x * kDispTok + threadIdx.x; t < t_end; t += blockDim.x) {
+        int m = 0;
+        for (int j = 0; j < k; ++j) {
+            const long long i = (long long)t * k + j;
+            int e = -1;
+            if (slot_dest[i] == -1) {
+                e = cand[(long long)t * k + m];
+                ++m;
+                if (e >= E) {
+                    raise_error(DEVERR_INDEX);
+                    e = -1;
+                }
+                if (e >= 0) atomicAdd(&cnt[e], 1);   // shared-memory count, order-free
+            }
+            prop[i] = e < 0 ? -1 : e;
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) blockcnt[(long long)blockIdx.x * E + e] = cnt[e];
 }
 
 // ---- the whole dispatch in one CTA of 1024 threads -------------------------------------
@@ -321,6 +376,39 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
         }
         for (; c < nvec; c += 32) dst[c] = __ldg(src + c);
     }
+}
+
+// ---- re-routing: room, final counts, offsets, M-tile table (one CTA, expert/thread) ----
+// counts[e] holds the round-0 counts on entry (saved to cnt0); expert e accepts
+// min(proposals, cap - cnt0[e]) proposals; blockoff[b][e] becomes the rank base of chunk
+// b's proposals. Also zeroes the expert GEMMs' tile counters.
+__global__ void __launch_bounds__(1024) reroute_scan_kernel(
+    const int* __restrict__ blockcnt, int nb, int E, int cap, int* __restrict__ blockoff,
+    int* __restrict__ counts, int* __restrict__ cnt0, int* __restrict__ offsets,
+    int* __restrict__ mtile_offsets, unsigned long long* __restrict__ counters, int n_counters) {
+    pdl_entry();
+    __shared__ int s_warp[32];
+    const int e = threadIdx.x;
+    if (counters && e < n_counters) counters[e] = 0ull;
+    int kept = 0;
+    if (e < E) {
+        int run = 0;
+        for (int b = 0; b < nb; ++b) {
+            const long long i = (long long)b * E + e;
+            const int c = blockcnt[i];
+            blockoff[i] = run;
+            run += c;
+        }
+        const int c0 = counts[e];
+        cnt0[e] = c0;
+        kept = c0 + min(run, max(0, cap - c0));
+        counts[e] = kept;
+    }
+    int total;
+    const int off = block_excl_scan_1024(kept, s_warp, total);
+    if (e < E) offsets[e] = off;
+    if (e == 0) offsets[E] = total;
+    write_tile_tables(kept, e, E, s_warp, mtile_offsets);
 }
 
 // ---- M-tile table from offsets (expert stage entry): single CTA of 1024 threads ----

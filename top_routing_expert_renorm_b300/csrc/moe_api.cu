@@ -190,6 +190,8 @@ moe_status check_cfg(const moe_config* c) {
         if (c->w_dtype != MOE_I8) return MOE_ERR_INVALID_ARG;
         if (c->kind != MOE_EXPERT_GELU && c->kind != MOE_EXPERT_SWIGLU) return MOE_ERR_UNSUPPORTED;
     }
+    if (c->overflow < MOE_OVERFLOW_DROP || c->overflow > MOE_OVERFLOW_REROUTE) return MOE_ERR_INVALID_ARG;
+    if (c->overflow == MOE_OVERFLOW_SHARED && !c->has_shared) return MOE_ERR_INVALID_ARG;
     if (c->n_group != 0) {
         if (c->n_group < 1 || c->n_group > 32 || c->E % c->n_group != 0) return MOE_ERR_INVALID_ARG;
         if (c->topk_group < 1 || c->topk_group > c->n_group) return MOE_ERR_INVALID_ARG;
@@ -239,6 +241,13 @@ struct RouterPlan {
 
 size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
 
+// The tensor-core router selects the top k in its GEMM epilogue when the three terms of
+// the padded experts fit one accumulator, routing is plain top-k and no re-routing
+// candidates are needed.
+bool router_fused_topk(const moe_config& c, int Ep) {
+    return Ep <= 64 && c.n_group == 0 && c.overflow != MOE_OVERFLOW_REROUTE;
+}
+
 RouterPlan router_plan(const moe_config& c) {
     RouterPlan r{};
     const size_t T = (size_t)c.T, E = (size_t)c.E, d = (size_t)c.d;
@@ -256,7 +265,7 @@ RouterPlan router_plan(const moe_config& c) {
         r.bg_bytes = al256(3 * (size_t)r.Ep * d * 2);
         // partial logits only when the three terms do not fit one accumulator (E > 64);
         // otherwise the GEMM epilogue selects the top k itself
-        r.d_bytes = (r.Ep <= 64 && c.n_group == 0) ? 0 : al256(T * 3 * (size_t)r.Ep * 4);
+        r.d_bytes = router_fused_topk(c, r.Ep) ? 0 : al256(T * 3 * (size_t)r.Ep * 4);
         r.scratch_bytes = r.bg_bytes + r.d_bytes + 256;
     } else {
         r.path = 3;
@@ -362,7 +371,8 @@ FfnPlan ffn_plan(const moe_config& c) {
 enum { kCntUp = 0, kCntDown = 1, kCntSharedUp = 2, kCntSharedDown = 3, kNumCounters = 4 };
 
 struct WsLayout {
-    size_t logits, idx, w, load, counts, offsets, blockcnt, blockoff, perm_token, perm_slot,
+    size_t logits, idx, w, load, counts, offsets, blockcnt, blockoff, cand, prop, cnt0,
+        perm_token, perm_slot,
         slot_dest, x_perm, mtile, shared_tab, counters, h, hs, y, partial, total;
 };
 
@@ -387,6 +397,10 @@ WsLayout ws_layout(const moe_config& c) {
     L.offsets = take((E + 1) * 4);
     L.blockcnt = take(nb * E * 4);
     L.blockoff = take(nb * E * 4);
+    const bool rr = c.overflow == MOE_OVERFLOW_REROUTE;
+    L.cand = take(rr ? Pmax * 4 : 0);
+    L.prop = take(rr ? Pmax * 4 : 0);
+    L.cnt0 = take(rr ? E * 4 : 0);
     L.perm_token = take(Pmax * 4);
     L.perm_slot = take(Pmax * 4);
     L.slot_dest = take(Pmax * 4);
@@ -413,12 +427,38 @@ P* at(void* ws, size_t off) {
 moe_status dispatch_impl(const moe_config& c, const int32_t* idx, const void* x, int32_t* load,
                          int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* perm_slot,
                          int32_t* slot_dest, void* x_perm, int32_t* blockcnt, int32_t* blockoff,
-                         int32_t* mtile, unsigned long long* counters, cudaStream_t s) {
+                         int32_t* mtile, unsigned long long* counters, cudaStream_t s,
+                         const int32_t* cand = nullptr, int32_t* prop = nullptr,
+                         int32_t* cnt0 = nullptr) {
     // counters (nullable): the routed up/down GEMM tile counters, zeroed here
+    // cand, prop, cnt0: re-routing candidates (from the router) and scratch
     const int T = c.T, E = c.E, k = c.top_k;
     const int cap = capacity_of(c);
     const int nb = (T + kDispTok - 1) / kDispTok;
-    if ((long long)T * k <= kOneCtaMaxAssign && E <= kOneCtaMaxE) {
+    const int rsm = kDispWarps * E * sizeof(int);
+    if (c.overflow == MOE_OVERFLOW_REROUTE) {
+        if (!cand || !prop || !cnt0) return MOE_ERR_UNSUPPORTED;
+        // round 0 (ranks only), proposals of the dropped slots, room and offsets, then
+        // ranks of the proposals and the scatter of every slot
+        MOE_LAUNCH("dispatch_hist", s,
+                   launch_k(dispatch_hist_kernel, nb, 256, E * sizeof(int), s, idx, T, k, E,
+                            blockcnt));
+        MOE_LAUNCH("dispatch_scan", s,
+                   launch_k(dispatch_scan_kernel, 1, 1024, 0, s, blockcnt, nb, E, cap, blockoff,
+                            load, counts, offsets, nullptr, nullptr, 0));
+        MOE_LAUNCH("dispatch_rank_status", s,
+                   launch_k(dispatch_rank_kernel<kRankStatus>, nb, 256, rsm, s, idx, T, k, E, cap,
+                            blockoff, offsets, perm_token, perm_slot, slot_dest, nullptr, nullptr));
+        MOE_LAUNCH("reroute_propose", s,
+                   launch_k(reroute_propose_kernel, nb, 256, E * sizeof(int), s, slot_dest, cand,
+                            T, k, E, prop, blockcnt));
+        MOE_LAUNCH("reroute_scan", s,
+                   launch_k(reroute_scan_kernel, 1, 1024, 0, s, blockcnt, nb, E, cap, blockoff,
+                            counts, cnt0, offsets, mtile, counters, 2));
+        MOE_LAUNCH("dispatch_rank_reroute", s,
+                   launch_k(dispatch_rank_kernel<kRankReroute>, nb, 256, rsm, s, prop, T, k, E,
+                            cap, blockoff, offsets, perm_token, perm_slot, slot_dest, idx, cnt0));
+    } else if ((long long)T * k <= kOneCtaMaxAssign && E <= kOneCtaMaxE) {
         MOE_LAUNCH("dispatch_one_cta", s,
                    launch_k(dispatch_one_cta_kernel, 1, 1024, 33 * E * sizeof(int), s, idx, T, k,
                             E, cap, load, counts, offsets, perm_token, perm_slot, slot_dest,
@@ -430,8 +470,9 @@ moe_status dispatch_impl(const moe_config& c, const int32_t* idx, const void* x,
                launch_k(dispatch_scan_kernel, 1, 1024, 0, s, blockcnt, nb, E, cap, blockoff, load, counts,
                                                        offsets, mtile, counters, 2));
     MOE_LAUNCH("dispatch_rank", s,
-               launch_k(dispatch_rank_kernel, nb, 256, kDispWarps * E * sizeof(int), s,
-                   idx, T, k, E, cap, blockoff, offsets, perm_token, perm_slot, slot_dest));
+               launch_k(dispatch_rank_kernel<kRankScatter>, nb, 256, rsm, s,
+                   idx, T, k, E, cap, blockoff, offsets, perm_token, perm_slot, slot_dest, nullptr,
+                   nullptr));
     }
     if (x_perm) {
         const int es = c.act_dtype == MOE_BF16 ? 2 : 4;
@@ -611,7 +652,10 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     } while (0)
 
 moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const float* bias,
-                      float* logits, int32_t* idx, float* w, void* scratch, cudaStream_t s) {
+                      float* logits, int32_t* idx, float* w, void* scratch, int32_t* cand,
+                      cudaStream_t s) {
+    // cand: the re-routing candidates [T, k] (written iff overflow == REROUTE)
+    if (c.overflow != MOE_OVERFLOW_REROUTE) cand = nullptr;
     const int T = c.T, E = c.E, d = c.d, k = c.top_k;
     const RouterPlan rp = router_plan(c);
     float* parts = static_cast<float*>(scratch);
@@ -630,7 +674,7 @@ moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const
                    launch_k(gate_split_kernel, grid, 256, 0, s,
                        Wg, d, E, rp.Ep, Bg, T, tables,
                        reinterpret_cast<unsigned long long*>(tables + 4)));
-        if (rp.Ep <= 64 && c.n_group == 0) {   // the three terms fit one accumulator: fused top-k
+        if (router_fused_topk(c, rp.Ep)) {   // the three terms fit one accumulator: fused top-k
             MOE_TRY(launch_gemm<EPI_ROUTER_TOPK>(
                 x, T, d, Bg, 3ll * rp.Ep, 3 * rp.Ep, 1, 3 * rp.Ep, tables, tables + 2, logits, E,
                 bias, nullptr, nullptr, nullptr, k, s, nullptr, SplitPlan(), nullptr,
@@ -656,7 +700,8 @@ moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const
     MOE_LAUNCH("topk_renorm", s,
                launch_k(topk_renorm_kernel, (T + kTopkTok - 1) / kTopkTok, 256,
                         kTopkTok * E * sizeof(float), s, parts, rp.n_parts, rp.part_stride,
-                        rp.row_stride, bias, logits, T, E, k, c.n_group, c.topk_group, idx, w));
+                        rp.row_stride, bias, logits, T, E, k, c.n_group, c.topk_group, idx, w,
+                        cand));
     return MOE_OK;
 }
 
@@ -751,7 +796,9 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
 }
 
 moe_status combine_impl(const moe_config& c, const void* x, const float* y,
-                        const int32_t* slot_dest, void* out, cudaStream_t s) {
+                        const int32_t* slot_dest, const float* topk_w, void* out, cudaStream_t s) {
+    // topk_w: read iff overflow == SHARED (the dropped slots' weights join the shared expert)
+    const float* ovf_w = (c.overflow == MOE_OVERFLOW_SHARED && c.has_shared) ? topk_w : nullptr;
     const int T = c.T, d = c.d, k = c.top_k;
     const long long Pmax = (long long)T * k;
     const float* ysh = c.has_shared ? y + Pmax * d : nullptr;
@@ -765,12 +812,12 @@ moe_status combine_impl(const moe_config& c, const void* x, const float* y,
     if (c.act_dtype == MOE_F32)
         MOE_LAUNCH("combine_f32", s,
                    launch_k(combine_kernel<float>, blocks, 256, 0, s,
-                       static_cast<const float*>(x), y, slot_dest, ysh, static_cast<float*>(out), T,
-                       d, k, c.add_residual, cpt));
+                       static_cast<const float*>(x), y, slot_dest, ysh, ovf_w,
+                       static_cast<float*>(out), T, d, k, c.add_residual, cpt));
     else
         MOE_LAUNCH("combine_bf16", s,
                    launch_k(combine_kernel<__nv_bfloat16>, blocks, 256, 0, s,
-                       static_cast<const __nv_bfloat16*>(x), y, slot_dest, ysh,
+                       static_cast<const __nv_bfloat16*>(x), y, slot_dest, ysh, ovf_w,
                        static_cast<__nv_bfloat16*>(out), T, d, k, c.add_residual, cpt));
     return MOE_OK;
 }
@@ -818,8 +865,9 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* W_gate,
     if (!aligned16(x) || !aligned16(W_gate) || !aligned16(gate_bias) || !aligned16(logits) ||
         !aligned16(topk_idx) || !aligned16(topk_w) || !aligned16(ws))
         return MOE_ERR_MISALIGNED;
-    return route_impl(c, x, W_gate, gate_bias, logits, topk_idx, topk_w,
-                      at<void>(ws, ws_layout(c).logits), stream);
+    const WsLayout L = ws_layout(c);
+    return route_impl(c, x, W_gate, gate_bias, logits, topk_idx, topk_w, at<void>(ws, L.logits),
+                      at<int32_t>(ws, L.cand), stream);
 }
 
 moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const void* x,
@@ -840,7 +888,8 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const vo
     const WsLayout L = ws_layout(c);
     return dispatch_impl(c, topk_idx, x, load, counts, offsets, perm_token, perm_slot, slot_dest,
                          x_perm, at<int32_t>(ws, L.blockcnt), at<int32_t>(ws, L.blockoff), nullptr,
-                         nullptr, stream);
+                         nullptr, stream, at<int32_t>(ws, L.cand), at<int32_t>(ws, L.prop),
+                         at<int32_t>(ws, L.cnt0));
 }
 
 moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
@@ -868,14 +917,17 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32
 }
 
 moe_status moe_combine(const moe_config* cfg, const void* x, const float* y,
-                       const int32_t* slot_dest, void* out, cudaStream_t stream) {
+                       const int32_t* slot_dest, const float* topk_w, void* out,
+                       cudaStream_t stream) {
     MOE_TRY(check_cfg(cfg));
     const moe_config& c = *cfg;
     if (c.T == 0) return MOE_OK;
     if (!y || !slot_dest || !out || (c.add_residual && !x)) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(y) || !aligned16(slot_dest) || !aligned16(out))
+    if (c.overflow == MOE_OVERFLOW_SHARED && !topk_w) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y) || !aligned16(slot_dest) || !aligned16(topk_w) ||
+        !aligned16(out))
         return MOE_ERR_MISALIGNED;
-    return combine_impl(c, x, y, slot_dest, out, stream);
+    return combine_impl(c, x, y, slot_dest, topk_w, out, stream);
 }
 
 moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate,
@@ -907,11 +959,13 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate
     // Top-1 layers without a shared expert write the output from the down projection.
     const bool fuse1 = is_bf16_kind(c) && c.top_k == 1 && !c.has_shared && !q8t_routed(c) &&
                        ffn_plan(c).down.S == 1;
-    MOE_TRY(route_impl(c, x, W_gate, gate_bias, nullptr, idx, w, at<void>(ws, L.logits), stream));
+    MOE_TRY(route_impl(c, x, W_gate, gate_bias, nullptr, idx, w, at<void>(ws, L.logits),
+                       at<int32_t>(ws, L.cand), stream));
     MOE_TRY(dispatch_impl(c, idx, x, ld, at<int32_t>(ws, L.counts), offsets, perm_token, perm_slot,
                           slot_dest, x_perm, at<int32_t>(ws, L.blockcnt),
                           at<int32_t>(ws, L.blockoff), mtile,
-                          at<unsigned long long>(ws, L.counters), stream));
+                          at<unsigned long long>(ws, L.counters), stream, at<int32_t>(ws, L.cand),
+                          at<int32_t>(ws, L.prop), at<int32_t>(ws, L.cnt0)));
     MOE_TRY(ffn_impl(c, x_perm, offsets, *routed, shared, x, w, perm_token, perm_slot, y, mtile,
                      true, at<int32_t>(ws, L.shared_tab), at<__nv_bfloat16>(ws, L.h),
                      at<__nv_bfloat16>(ws, L.hs), at<float>(ws, L.partial),
@@ -925,7 +979,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate
                             static_cast<__nv_bfloat16*>(out), c.T, c.d, c.add_residual));
         return MOE_OK;
     }
-    return combine_impl(c, x, y, slot_dest, out, stream);
+    return combine_impl(c, x, y, slot_dest, w, out, stream);
 }
 
 // M-tile table ((G+1) int32), then the tile counter (8-byte aligned).
@@ -1104,6 +1158,7 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t*
                                            cudaStream_t stream) {
     MOE_TRY(check_cfg(cfg));
     const moe_config& c = *cfg;
+    if (c.overflow == MOE_OVERFLOW_REROUTE) return MOE_ERR_UNSUPPORTED;   // needs moe_route's ws
     if (c.T == 0) return MOE_OK;
     if (!topk_idx || !load || !counts || !offsets || !perm_token || !perm_slot || !slot_dest)
         return MOE_ERR_INVALID_ARG;

@@ -198,6 +198,8 @@ __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
 // A CTA handles kTopkTok tokens: all 256 threads first form the CTA's logits in shared
 // memory (every (token, expert) sum issues its part loads in batches of 8, so few
 // round trips are exposed even with many parts), then warp w selects for token w.
+// cand (nullable, re-routing): the experts ranked k .. 2k-1 by the same order and within
+// the same candidate set, -1 where the set has fewer experts.
 constexpr int kTopkTok = 8;
 
 __global__ void __launch_bounds__(256) topk_renorm_kernel(const float* __restrict__ parts,
@@ -207,7 +209,8 @@ __global__ void __launch_bounds__(256) topk_renorm_kernel(const float* __restric
                                                           float* __restrict__ logits, int T,
                                                           int E, int k, int n_group,
                                                           int topk_group, int* __restrict__ idx,
-                                                          float* __restrict__ w) {
+                                                          float* __restrict__ w,
+                                                          int* __restrict__ cand) {
     pdl_entry();
     extern __shared__ float sL[];   // [kTopkTok][E]
     const int lane = threadIdx.x & 31;
@@ -277,11 +280,11 @@ __global__ void __launch_bounds__(256) topk_renorm_kernel(const float* __restric
             if (e < E && !((chosen >> (e / gsize)) & 1u)) avail &= ~(1u << i);
         }
     }
-    float my_v = 0.0f, l0 = 0.0f;
-    int my_e = 0;
-    for (int j = 0; j < k; ++j) {
-        float bv = 0.0f;
-        int be = -1;
+    // best remaining candidate (logit descending, id ascending) over the warp; it leaves
+    // the candidate set. be = -1 when the set is empty.
+    auto pick = [&](float& bv, int& be) {
+        bv = 0.0f;
+        be = -1;
 #pragma unroll
         for (int i = 0; i < 32; ++i)
             if ((avail >> i) & 1u)
@@ -298,12 +301,29 @@ __global__ void __launch_bounds__(256) topk_renorm_kernel(const float* __restric
                 be = oe;
             }
         }
-        if ((be & 31) == lane) avail &= ~(1u << (be >> 5));
+        if (be >= 0 && (be & 31) == lane) avail &= ~(1u << (be >> 5));
+    };
+    float my_v = 0.0f, l0 = 0.0f;
+    int my_e = 0;
+    for (int j = 0; j < k; ++j) {
+        float bv;
+        int be;
+        pick(bv, be);
         if (lane == j) {
             my_v = bv;
             my_e = be;
         }
         if (j == 0) l0 = bv;
+    }
+    if (cand) {
+        int my_c = -1;
+        for (int j = 0; j < k; ++j) {
+            float bv;
+            int be;
+            pick(bv, be);
+            if (lane == j) my_c = be;
+        }
+        if (lane < k) cand[t * k + lane] = my_c;
     }
     const float ex = (lane < k) ? expf(my_v - l0) : 0.0f;
     float s = 0.0f;
