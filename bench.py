@@ -319,6 +319,23 @@ def run_reference(args, wl):
 # ---------------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------------
+def max_over_ranks(ms, world, device):
+    """The job's time is the slowest replica's: MAX all-reduce over the ranks (a no-op on
+    one rank). `device` is where the process group's backend keeps its tensors."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(T, steps, world, total_ms):
+    """Whole-job throughput: every replica processes T tokens per step (weak scaling)."""
+    return T * steps * world / (total_ms / 1000.0)
+
+
 def run_ours(args, wl):
     import torch
     import torch.distributed as dist
@@ -395,15 +412,11 @@ def run_ours(args, wl):
         dist.barrier()
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     st = moe.last_device_status()
     if st != 0:
         raise RuntimeError(f"device status after timing: {moe.status_string(st)}")
-    value = wl.T * K * world / (total_ms / 1000.0)
+    value = job_tokens_per_s(wl.T, K, world, total_ms)
 
     # ---- roofline of the dominant kernel ----
     peaks, peak_src = load_peaks()
@@ -477,13 +490,9 @@ def run_ours(args, wl):
         pipelined(K)
         t1.record(down)
         torch.cuda.synchronize()
-        e2e_ms = t0.elapsed_time(t1)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
         nb = x.numel() * x.element_size()
-        e2e = {"value": wl.T * K * world / (e2e_ms / 1000.0), "unit": "tokens/s",
+        e2e = {"value": job_tokens_per_s(wl.T, K, world, e2e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": nb, "d2h_bytes_per_step": out.numel() * out.element_size(),
                "overlap": "uploads/downloads on their own streams, double-buffered",
                "launch": "MoELayer.capture CUDA graph per buffer pair, replayed every step"}
