@@ -144,8 +144,6 @@ def kernel_algorithmic_cost(wl, name, P, touched):
     if name == "grouped_gemm_combine1":   # top-1 down projection writing the layer output
         return 2.0 * P * F * d, (touched * (d * F * we + sc2) + P * F * 2 + P * d * es
                                  + (P * d * es if wl.add_residual else 0))
-    if name == "copy_dropped":            # dropped tokens (T - P of them) leave as x or 0
-        return 0.0, T * wl.k * 4 + (T - P) * d * es * (2 if wl.add_residual else 1)
     if name == "grouped_gemm_f32":        # shared expert down projection
         return 2.0 * T * F * d, d * F * we + sc2 + T * F * 2 + T * d * 4
     if name.startswith("router_logits") or name == "router_splitk":
@@ -176,7 +174,6 @@ KERNEL_FILES = {
     "router_gemm_tc": ["grouped_gemm.cuh", "common.cuh"],
     "router_gemm_topk": ["grouped_gemm.cuh", "common.cuh"],
     "splitk_reduce": ["grouped_gemm.cuh", "common.cuh"],
-    "copy_dropped": ["combine.cuh", "common.cuh"],
     "gate_split": ["router.cuh", "common.cuh"],
     "router": ["router.cuh", "common.cuh"],
     "topk": ["router.cuh", "common.cuh"],

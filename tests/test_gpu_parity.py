@@ -51,6 +51,12 @@ SMALL = {
     # top-1 without residual and with drops: the fused combine writes dropped tokens as 0
     "top1_drop_no_residual": W("t1d", T=300, d=128, E=4, k=1, F=192, kind="gelu", act="bf16",
                                cf=0.5, expert_bias=True),
+    # more than 4096 assignments: the dispatch runs as separate kernels and takes its
+    # histogram from the fused router top-k; top-1 also writes dropped rows in the scatter
+    "top1_hist_by_router": W("hbr1", T=4200, d=128, E=8, k=1, F=128, kind="gelu", act="bf16",
+                             cf=1.0, add_residual=True),
+    "k2_hist_by_router": W("hbr2", T=2100, d=128, E=16, k=2, F=128, kind="swiglu",
+                           act="bf16", cf=1.0, gate_bias="zipf"),
     # weight-only INT8 experts: codes widened in shared memory, scales in the epilogue
     "i8_gelu_bias_k2": W("q8g", T=333, d=192, E=6, k=2, F=256, kind="gelu", act="bf16",
                          expert_bias=True, int8=True),
@@ -157,7 +163,7 @@ def test_dropped_tokens_leave_as_x_bit_exact():
 
 
 @pytest.mark.parametrize("name", ["gelu_cap_res", "top1_drop_no_residual", "one_expert",
-                                  "i8_top1_cap_res"])
+                                  "i8_top1_cap_res", "top1_hist_by_router"])
 def test_top1_fused_combine_matches_staged_path_bitwise(name):
     # moe_forward fuses the combine into the down projection for top-1 layers without a
     # shared expert; the staged entry points do not. The fp32 operations are the same.

@@ -149,26 +149,4 @@ __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ x,
     }
 }
 
-// ---- top-1 layers with the combine fused into the down projection: tokens whose slot
-// was dropped by the capacity leave as (add_residual ? x : 0), bit for bit as the
-// combine kernel writes them. One warp per token (grid-stride), 16-byte copies.
-template <typename OT>
-__global__ void __launch_bounds__(256) copy_dropped_kernel(const OT* __restrict__ x,
-                                                           const int* __restrict__ slot_dest,
-                                                           OT* __restrict__ out, int T, int d,
-                                                           int add_residual) {
-    pdl_entry();
-    const int lane = threadIdx.x & 31;
-    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-    const int nvec = d * (int)sizeof(OT) / 16;
-    for (long long t = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T;
-         t += warps) {
-        if (slot_dest[t] >= 0) continue;
-        uint4* dst = reinterpret_cast<uint4*>(out + t * d);
-        const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
-        for (int c = lane; c < nvec; c += 32)
-            dst[c] = add_residual ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-    }
-}
-
 }  // namespace moe

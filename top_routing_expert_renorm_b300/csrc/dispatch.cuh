@@ -16,6 +16,33 @@
 namespace moe {
 
 constexpr int kDispTok = 256;    // tokens per dispatch chunk (one CTA)
+
+// Top-1 layers whose combine runs in the down projection's epilogue: the dispatch writes
+// the output row of every dropped token itself, as x (with the residual) or 0, bit for bit
+// what the combine writes for a token without kept slots ["MoE 并行" Capacity Factor:
+// overflow takes the residual path]. out == nullptr: nothing to write.
+struct DroppedRows {
+    const uint8_t* x;
+    uint8_t* out;
+    int row_bytes;   // multiple of 16
+    int add_residual;
+};
+
+// Slots i = base + lane (k = 1: slot i is token i) whose bit is set in `dropped`: the
+// warp copies each row in 16-byte vectors.
+__device__ __forceinline__ void write_dropped_rows(const DroppedRows& dr, unsigned dropped,
+                                                   long long base, int lane) {
+    const int nvec = dr.row_bytes / 16;
+    while (dropped) {
+        const int l = __ffs(dropped) - 1;
+        dropped &= dropped - 1;
+        const long long t = base + l;
+        uint4* dst = reinterpret_cast<uint4*>(dr.out + t * dr.row_bytes);
+        const uint4* src = reinterpret_cast<const uint4*>(dr.x + t * dr.row_bytes);
+        for (int c = lane; c < nvec; c += 32)
+            dst[c] = dr.add_residual ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
 constexpr int kDispWarps = 8;
 constexpr int kMTile = 128;      // rows per tensor-core M tile
 
@@ -124,7 +151,8 @@ template <int MODE>
 __global__ void __launch_bounds__(256) dispatch_rank_kernel(
     const int* __restrict__ idx, int T, int k, int E, int cap, const int* __restrict__ blockoff,
     const int* __restrict__ offsets, int* __restrict__ perm_token, int* __restrict__ perm_slot,
-    int* __restrict__ slot_dest, const int* __restrict__ orig_idx, const int* __restrict__ cnt0) {
+    int* __restrict__ slot_dest, const int* __restrict__ orig_idx, const int* __restrict__ cnt0,
+    DroppedRows dr) {
     pdl_entry();
     extern __shared__ int wcnt[];   // [kDispWarps][E] running counters
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -161,6 +189,7 @@ __global__ void __launch_bounds__(256) dispatch_rank_kernel(
     // pass 3: ranks and scatter
     for (long long base = wbeg; base < wend; base += 32) {
         const long long i = base + lane;
+        bool dropped = false;
         int e = (i < wend) ? idx[i] : -1;
         if (e >= E) e = -1;
         const unsigned peers = __match_any_sync(0xffffffffu, e);
@@ -186,7 +215,11 @@ __global__ void __launch_bounds__(256) dispatch_rank_kernel(
                     perm_slot[pos] = (int)(i % k);
                 }
                 slot_dest[i] = pos;
+                if (dr.out) dropped = pos < 0;
             }
+        }
+        if constexpr (MODE != kRankStatus) {
+            if (dr.out) write_dropped_rows(dr, __ballot_sync(0xffffffffu, dropped), base, lane);
         }
     }
 }
@@ -246,7 +279,7 @@ __global__ void __launch_bounds__(1024) dispatch_one_cta_kernel(
     const int* __restrict__ idx, int T, int k, int E, int cap, int* __restrict__ load,
     int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ perm_token,
     int* __restrict__ perm_slot, int* __restrict__ slot_dest, int* __restrict__ mtile_offsets,
-    unsigned long long* __restrict__ counters, int n_counters) {
+    unsigned long long* __restrict__ counters, int n_counters, DroppedRows dr) {
     pdl_entry();
     extern __shared__ int dsm[];
     if (counters && (int)threadIdx.x < n_counters) counters[threadIdx.x] = 0ull;
@@ -335,6 +368,7 @@ __global__ void __launch_bounds__(1024) dispatch_one_cta_kernel(
             __syncwarp();
             if (ex >= 0 && (peers & lt_mask) == 0) my[ex] += __popc(peers);
             __syncwarp();
+            bool dropped = false;
             if (r0 + j < rounds && i < wend) {
                 if (ex >= 0 && rank < cap) {
                     const int pos = s_off[ex] + rank;
@@ -343,8 +377,12 @@ __global__ void __launch_bounds__(1024) dispatch_one_cta_kernel(
                     slot_dest[i] = pos;
                 } else {
                     slot_dest[i] = -1;
+                    dropped = true;
                 }
             }
+            if (dr.out)
+                write_dropped_rows(dr, __ballot_sync(0xffffffffu, dropped),
+                                   wbeg + (long long)(r0 + j) * 32, lane);
         }
     }
 }

@@ -65,6 +65,8 @@ struct GemmParams {
     int* r_idx;                   // EPI_ROUTER_TOPK: top-k ids [T, top_k]
     float* r_w;                   //                  renormalised weights [T, top_k]
     int r_E, r_Ep;                //                  experts, padded experts per term (32 | 64)
+    int* r_hist;                  //                  nullable [T / r_hist_chunk][r_E]: selected
+    int r_hist_chunk;             //                  experts per chunk of tokens (zeroed before)
     // split-K: every output tile is computed as k_splits units over consecutive ranges of
     // kb_per_split K blocks; with partial != null each unit stores its raw fp32 sums at
     // partial + split * part_stride + row * ld_part + column (columns as in B's rows, so
@@ -275,6 +277,10 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
                 p.r_idx[grow * k + j] = ids[j];
                 p.r_w[grow * k + j] = ex[j] / ssum;
             }
+            // the dispatch's per-chunk expert histogram (order-free counts)
+            if (p.r_hist)
+                for (int j = 0; j < k; ++j)
+                    atomicAdd(p.r_hist + (grow / p.r_hist_chunk) * E + ids[j], 1);
         }
     } else if constexpr (EPI == EPI_COMBINE1_BF16) {
         // Same fp32 operations, in the same order, as the scale epilogue followed by the

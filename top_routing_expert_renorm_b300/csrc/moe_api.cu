@@ -241,6 +241,12 @@ struct RouterPlan {
 
 size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
 
+// The whole dispatch in one CTA (few assignments and experts, no re-routing).
+bool dispatch_one_cta(const moe_config& c) {
+    return (long long)c.T * c.top_k <= kOneCtaMaxAssign && c.E <= kOneCtaMaxE &&
+           c.overflow != MOE_OVERFLOW_REROUTE;
+}
+
 // The tensor-core router selects the top k in its GEMM epilogue when the three terms of
 // the padded experts fit one accumulator, routing is plain top-k and no re-routing
 // candidates are needed.
@@ -429,9 +435,13 @@ moe_status dispatch_impl(const moe_config& c, const int32_t* idx, const void* x,
                          int32_t* slot_dest, void* x_perm, int32_t* blockcnt, int32_t* blockoff,
                          int32_t* mtile, unsigned long long* counters, cudaStream_t s,
                          const int32_t* cand = nullptr, int32_t* prop = nullptr,
-                         int32_t* cnt0 = nullptr) {
+                         int32_t* cnt0 = nullptr, DroppedRows dr = DroppedRows{},
+                         bool hist_ready = false) {
+    // hist_ready: blockcnt already holds the per-chunk histogram (filled by the router)
     // counters (nullable): the routed up/down GEMM tile counters, zeroed here
     // cand, prop, cnt0: re-routing candidates (from the router) and scratch
+    // dr: top-1 layers with the combine fused into the down projection write the output
+    //     rows of dropped tokens here
     const int T = c.T, E = c.E, k = c.top_k;
     const int cap = capacity_of(c);
     const int nb = (T + kDispTok - 1) / kDispTok;
@@ -448,7 +458,8 @@ moe_status dispatch_impl(const moe_config& c, const int32_t* idx, const void* x,
                             load, counts, offsets, nullptr, nullptr, 0));
         MOE_LAUNCH("dispatch_rank_status", s,
                    launch_k(dispatch_rank_kernel<kRankStatus>, nb, 256, rsm, s, idx, T, k, E, cap,
-                            blockoff, offsets, perm_token, perm_slot, slot_dest, nullptr, nullptr));
+                            blockoff, offsets, perm_token, perm_slot, slot_dest, nullptr, nullptr,
+                            DroppedRows{}));
         MOE_LAUNCH("reroute_propose", s,
                    launch_k(reroute_propose_kernel, nb, 256, E * sizeof(int), s, slot_dest, cand,
                             T, k, E, prop, blockcnt));
@@ -457,22 +468,24 @@ moe_status dispatch_impl(const moe_config& c, const int32_t* idx, const void* x,
                             counts, cnt0, offsets, mtile, counters, 2));
         MOE_LAUNCH("dispatch_rank_reroute", s,
                    launch_k(dispatch_rank_kernel<kRankReroute>, nb, 256, rsm, s, prop, T, k, E,
-                            cap, blockoff, offsets, perm_token, perm_slot, slot_dest, idx, cnt0));
-    } else if ((long long)T * k <= kOneCtaMaxAssign && E <= kOneCtaMaxE) {
+                            cap, blockoff, offsets, perm_token, perm_slot, slot_dest, idx, cnt0, dr));
+    } else if (dispatch_one_cta(c)) {
         MOE_LAUNCH("dispatch_one_cta", s,
                    launch_k(dispatch_one_cta_kernel, 1, 1024, 33 * E * sizeof(int), s, idx, T, k,
                             E, cap, load, counts, offsets, perm_token, perm_slot, slot_dest,
-                            mtile, counters, 2));
+                            mtile, counters, 2, dr));
     } else {
-    MOE_LAUNCH("dispatch_hist", s,
-               launch_k(dispatch_hist_kernel, nb, 256, E * sizeof(int), s, idx, T, k, E, blockcnt));
+    if (!hist_ready)
+        MOE_LAUNCH("dispatch_hist", s,
+                   launch_k(dispatch_hist_kernel, nb, 256, E * sizeof(int), s, idx, T, k, E,
+                            blockcnt));
     MOE_LAUNCH("dispatch_scan", s,
                launch_k(dispatch_scan_kernel, 1, 1024, 0, s, blockcnt, nb, E, cap, blockoff, load, counts,
                                                        offsets, mtile, counters, 2));
     MOE_LAUNCH("dispatch_rank", s,
                launch_k(dispatch_rank_kernel<kRankScatter>, nb, 256, rsm, s,
                    idx, T, k, E, cap, blockoff, offsets, perm_token, perm_slot, slot_dest, nullptr,
-                   nullptr));
+                   nullptr, dr));
     }
     if (x_perm) {
         const int es = c.act_dtype == MOE_BF16 ? 2 : 4;
@@ -544,7 +557,8 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
                        SplitPlan sp = SplitPlan(), float* partial = nullptr,
                        unsigned long long* counter = nullptr, const void* resid = nullptr,
                        int* r_idx = nullptr, float* r_w = nullptr, int r_E = 0, int r_Ep = 0,
-                       const float* w_scale = nullptr, bool swap_ab = false) {
+                       const float* w_scale = nullptr, bool swap_ab = false,
+                       int* r_hist = nullptr) {
     // w_scale != null: B holds int8 codes, one fp32 scale per B row (INT8 kernels); with
     // swap_ab the weight-streaming INT8 kernel for few rows per group runs
     if (a_rows <= 0 || G <= 0) return MOE_OK;
@@ -588,6 +602,8 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     p.r_E = r_E;
     p.r_Ep = r_Ep;
     p.w_scale = w_scale;
+    p.r_hist = r_hist;
+    p.r_hist_chunk = kDispTok;
     const int smem = gm_smem_bytes(G);
     static std::once_flag attr_once[64];
     static cudaError_t attr_err[64];
@@ -653,8 +669,10 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
 
 moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const float* bias,
                       float* logits, int32_t* idx, float* w, void* scratch, int32_t* cand,
-                      cudaStream_t s) {
+                      cudaStream_t s, int32_t* hist = nullptr) {
     // cand: the re-routing candidates [T, k] (written iff overflow == REROUTE)
+    // hist: the dispatch's per-chunk histogram [ceil(T / kDispTok)][E], filled by the fused
+    //       top-k epilogue when non-null (the caller checks router_fills_hist)
     if (c.overflow != MOE_OVERFLOW_REROUTE) cand = nullptr;
     const int T = c.T, E = c.E, d = c.d, k = c.top_k;
     const RouterPlan rp = router_plan(c);
@@ -673,12 +691,14 @@ moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const
         MOE_LAUNCH("gate_split", s,
                    launch_k(gate_split_kernel, grid, 256, 0, s,
                        Wg, d, E, rp.Ep, Bg, T, tables,
-                       reinterpret_cast<unsigned long long*>(tables + 4)));
+                       reinterpret_cast<unsigned long long*>(tables + 4), hist,
+                       hist ? (int)(((T + kDispTok - 1) / kDispTok) * (long long)E) : 0));
         if (router_fused_topk(c, rp.Ep)) {   // the three terms fit one accumulator: fused top-k
             MOE_TRY(launch_gemm<EPI_ROUTER_TOPK>(
                 x, T, d, Bg, 3ll * rp.Ep, 3 * rp.Ep, 1, 3 * rp.Ep, tables, tables + 2, logits, E,
                 bias, nullptr, nullptr, nullptr, k, s, nullptr, SplitPlan(), nullptr,
-                reinterpret_cast<unsigned long long*>(tables + 4), nullptr, idx, w, E, rp.Ep));
+                reinterpret_cast<unsigned long long*>(tables + 4), nullptr, idx, w, E, rp.Ep,
+                nullptr, false, hist));
             return MOE_OK;
         }
         MOE_TRY(launch_gemm<EPI_F32>(x, T, d, Bg, 3ll * rp.Ep, 3 * rp.Ep, 1, 3 * rp.Ep, tables,
@@ -959,26 +979,27 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate
     // Top-1 layers without a shared expert write the output from the down projection.
     const bool fuse1 = is_bf16_kind(c) && c.top_k == 1 && !c.has_shared && !q8t_routed(c) &&
                        ffn_plan(c).down.S == 1;
+    // The fused router top-k also counts the dispatch histogram when the dispatch runs as
+    // separate kernels (one kernel fewer).
+    const RouterPlan rp = router_plan(c);
+    const bool hist_by_router = rp.path == 2 && router_fused_topk(c, rp.Ep) && !dispatch_one_cta(c);
     MOE_TRY(route_impl(c, x, W_gate, gate_bias, nullptr, idx, w, at<void>(ws, L.logits),
-                       at<int32_t>(ws, L.cand), stream));
+                       at<int32_t>(ws, L.cand), stream,
+                       hist_by_router ? at<int32_t>(ws, L.blockcnt) : nullptr));
     MOE_TRY(dispatch_impl(c, idx, x, ld, at<int32_t>(ws, L.counts), offsets, perm_token, perm_slot,
                           slot_dest, x_perm, at<int32_t>(ws, L.blockcnt),
                           at<int32_t>(ws, L.blockoff), mtile,
                           at<unsigned long long>(ws, L.counters), stream, at<int32_t>(ws, L.cand),
-                          at<int32_t>(ws, L.prop), at<int32_t>(ws, L.cnt0)));
+                          at<int32_t>(ws, L.prop), at<int32_t>(ws, L.cnt0),
+                          fuse1 ? DroppedRows{static_cast<const uint8_t*>(x),
+                                              static_cast<uint8_t*>(out), c.d * 2, c.add_residual}
+                                : DroppedRows{},
+                          hist_by_router));
     MOE_TRY(ffn_impl(c, x_perm, offsets, *routed, shared, x, w, perm_token, perm_slot, y, mtile,
                      true, at<int32_t>(ws, L.shared_tab), at<__nv_bfloat16>(ws, L.h),
                      at<__nv_bfloat16>(ws, L.hs), at<float>(ws, L.partial),
                      at<unsigned long long>(ws, L.counters), stream, fuse1 ? out : nullptr));
-    if (fuse1) {
-        const int blocks = (int)std::max<long long>(
-            1, std::min<long long>((c.T + 7) / 8, (long long)num_sms() * 8));
-        MOE_LAUNCH("copy_dropped", stream,
-                   launch_k(copy_dropped_kernel<__nv_bfloat16>, blocks, 256, 0, stream,
-                            static_cast<const __nv_bfloat16*>(x), slot_dest,
-                            static_cast<__nv_bfloat16*>(out), c.T, c.d, c.add_residual));
-        return MOE_OK;
-    }
+    if (fuse1) return MOE_OK;   // dropped tokens were written by the dispatch
     return combine_impl(c, x, y, slot_dest, w, out, stream);
 }
 
