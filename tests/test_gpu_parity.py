@@ -331,6 +331,20 @@ def test_int8_uses_the_int8_kernels(name, prefix):
     assert gemms and all(n.startswith(prefix) for n in gemms), gemms
 
 
+@pytest.mark.parametrize("name,gathers", [("swiglu_k8_cap_shared", True), ("max_E_max_k", True),
+                                          ("gelu_bias_k2", False)])
+def test_forward_gathers_rows_in_the_gemm_for_many_slots(name, gathers):
+    # k >= 4: moe_forward's up projection reads rows of x through perm_token itself (no
+    # row-gather kernel); the staged path still materialises x_perm. Both match the oracle
+    # (full_check in test_small_parity) and each other.
+    wl = SMALL[name]
+    moe.profile_begin()
+    r = GpuRun(wl).run()
+    stats = moe.profile_end()
+    assert stats["gather_rows"][0] == (1 if gathers else 2)    # staged path (+ forward)
+    assert np.array_equal(to_np(r.out), to_np(r.out_stages))
+
+
 def test_split_k_is_used_for_few_tokens():
     wl = SMALL["split_swiglu_bias_shared"]
     moe.profile_begin()

@@ -230,6 +230,12 @@ __device__ __forceinline__ void tmem_store_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy
+// accesses (tensor-core operand reads) once the thread has synchronised with the reader.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---- small numeric helpers ---------------------------------------------------------
 __device__ __forceinline__ float gelu_erf(float a) {
     return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f));

@@ -60,6 +60,11 @@ struct GemmParams {
     const float* topk_w;       // EPI_SCALE_F32: row r scaled by topk_w[perm_token[r]*k + perm_slot[r]]
     const int* perm_token;
     const int* perm_slot;
+    // Gathered A (nullable): row r of A is row a_gather[r] of a_src (a_row_bytes per row);
+    // the CTA then has 128 more threads that load A with cp.async instead of TMA
+    const int* a_gather;
+    const uint8_t* a_src;
+    long long a_row_bytes;
     int top_k;
     const __nv_bfloat16* resid;   // EPI_COMBINE1_BF16: residual x [T, ld_out], nullable
     int* r_idx;                   // EPI_ROUTER_TOPK: top-k ids [T, top_k]
@@ -88,6 +93,7 @@ constexpr int GM_A_BYTES = GM_BM * GM_BK * 2;     // 16 KB
 constexpr int GM_B_BYTES = GM_BN * GM_BK * 2;     // 32 KB
 constexpr int GM_STAGE_BYTES = GM_A_BYTES + GM_B_BYTES;
 constexpr int GM_THREADS = 192;
+constexpr int GM_GATHER_THREADS = 128;    // extra warps 6..9 that gather A rows
 constexpr int GM_TMEM_COLS = 512;
 constexpr int GM_MAX_GROUPS = 1025;
 constexpr int GM_TQ = 8;            // depth of the ring of scheduled unit ids
@@ -378,8 +384,23 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
     }
 }
 
+// 16-byte global -> shared copy that zero-fills when src_bytes is 0 (rows past a group).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+constexpr int GM_GATHER_DEPTH = 2;   // stages a gather thread keeps in flight before arriving
+
 template <int EPI>
-__global__ void __launch_bounds__(GM_THREADS, 1)
+__global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -400,9 +421,10 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
     const int FULL = 0, EMPTY = GM_STAGES, TFULL = 2 * GM_STAGES, TEMPTY = 2 * GM_STAGES + 2,
               DRAIN = 2 * GM_STAGES + 4, QFULL = 16, QEMPTY = 16 + GM_TQ;
 
+    const bool gather = p.a_gather != nullptr;
     if (threadIdx.x == 0) {
         for (int s = 0; s < GM_STAGES; ++s) {
-            mbar_init(bar(FULL + s), 1);
+            mbar_init(bar(FULL + s), gather ? 5 : 1);   // + the four gather warps
             mbar_init(bar(EMPTY + s), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -412,7 +434,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
         mbar_init(bar(DRAIN), 1);
         for (int i = 0; i < GM_TQ; ++i) {
             mbar_init(bar(QFULL + i), 1);
-            mbar_init(bar(QEMPTY + i), 5);   // the MMA thread + four epilogue warps
+            mbar_init(bar(QEMPTY + i), gather ? 9 : 5);   // MMA, 4 epilogue (+ 4 gather) warps
         }
         *s_abort = 0;
         mbar_fence_init();
@@ -481,8 +503,8 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
                         break;
                     }
                     const uint32_t sa = smem_addr(tiles + stage * GM_STAGE_BYTES);
-                    mbar_arrive_expect_tx(bar(FULL + stage), GM_STAGE_BYTES);
-                    tma_load_2d(sa, &tmA, bar(FULL + stage), kb * GM_BK, a_row);
+                    mbar_arrive_expect_tx(bar(FULL + stage), gather ? GM_B_BYTES : GM_STAGE_BYTES);
+                    if (!gather) tma_load_2d(sa, &tmA, bar(FULL + stage), kb * GM_BK, a_row);
                     tma_load_2d(sa + GM_A_BYTES, &tmB, bar(FULL + stage), kb * GM_BK, b0);
                     tma_load_2d(sa + GM_A_BYTES + GM_B_BYTES / 2, &tmB, bar(FULL + stage),
                                 kb * GM_BK, b1);
@@ -556,6 +578,91 @@ __global__ void __launch_bounds__(GM_THREADS, 1)
             umma_commit(bar(DRAIN));
             mbar_wait(bar(DRAIN), 0);
         }
+    } else if (warp >= 6) {
+        // ---------------- A rows gathered with cp.async (warps 6..9) ----------------
+        // Thread a copies 16-byte chunk (a & 7) of rows (a >> 3) + 16 i, i = 0..7, of each
+        // K block into the 128-byte-swizzled A tile. A stage's copies are waited for (and
+        // made visible to the tensor core) GM_GATHER_DEPTH stages later, then the warp
+        // arrives on the stage's FULL barrier.
+        const int a = threadIdx.x - GM_THREADS;
+        const int chunk = a & 7, r0 = a >> 3;
+        int stage = 0;
+        uint32_t ph = 0;
+        int q = 0;
+        uint32_t qph = 0;
+        int pend[GM_GATHER_DEPTH + 1];
+        int npend = 0;
+        auto release_oldest = [&]() {   // the oldest pending stage has landed: FULL
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(FULL + pend[0]));
+#pragma unroll
+            for (int i = 0; i < GM_GATHER_DEPTH; ++i) pend[i] = pend[i + 1];
+            --npend;
+        };
+        bool ok = true;
+        while (ok) {
+            long long t = -1;
+            int got = 1;
+            if (lane == 0) {
+                if (*s_abort || !mbar_wait(bar(QFULL + q), qph)) {
+                    *s_abort = 1;
+                    got = 0;
+                } else {
+                    t = s_unit[q];
+                    mbar_arrive(bar(QEMPTY + q));
+                }
+            }
+            if (++q == GM_TQ) {
+                q = 0;
+                qph ^= 1;
+            }
+            got = __shfl_sync(0xffffffffu, got, 0);
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (!got || t < 0) break;
+            int g, mb, nb, ks;
+            gm_decode(t, p.G, p.n_tiles, p.k_splits, s_mt, g, mb, nb, ks);
+            const int kb0 = ks * p.kb_per_split;
+            const int kb1 = min(kblocks, kb0 + p.kb_per_split);
+            const int rows_g = s_ro[g + 1] - s_ro[g];
+            const uint8_t* src[8];
+            uint32_t nbytes[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = mb * GM_BM + r0 + 16 * i;
+                const bool valid = r < rows_g;
+                const long long tok = valid ? (long long)p.a_gather[s_ro[g] + r] : 0;
+                src[i] = p.a_src + tok * p.a_row_bytes + chunk * 16;
+                nbytes[i] = valid ? 16u : 0u;
+            }
+            for (int kb = kb0; kb < kb1; ++kb) {
+                const bool w_ok = !*s_abort && mbar_wait(bar(EMPTY + stage), ph ^ 1);
+                if (!__all_sync(0xffffffffu, w_ok)) {
+                    if (lane == 0) *s_abort = 1;
+                    ok = false;
+                    break;
+                }
+                const uint32_t sa = smem_addr(tiles + stage * GM_STAGE_BYTES);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = r0 + 16 * i;
+                    cp_async_16(sa + r * 128 + ((chunk ^ (r & 7)) << 4), src[i] + kb * GM_BK * 2,
+                                nbytes[i]);
+                }
+                cp_async_commit();
+                pend[npend++] = stage;
+                if (npend > GM_GATHER_DEPTH) {
+                    cp_async_wait<GM_GATHER_DEPTH>();
+                    release_oldest();
+                }
+                if (++stage == GM_STAGES) {
+                    stage = 0;
+                    ph ^= 1;
+                }
+            }
+        }
+        cp_async_wait<0>();
+        while (npend > 0) release_oldest();
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
         const int q = warp & 3;

@@ -558,7 +558,10 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
                        unsigned long long* counter = nullptr, const void* resid = nullptr,
                        int* r_idx = nullptr, float* r_w = nullptr, int r_E = 0, int r_Ep = 0,
                        const float* w_scale = nullptr, bool swap_ab = false,
-                       int* r_hist = nullptr) {
+                       int* r_hist = nullptr, const int32_t* a_gather = nullptr,
+                       int a_row_bytes = 0) {
+    // a_gather (bf16 kernel only): logical A row r (r < a_rows) is row a_gather[r] of A,
+    // loaded by the kernel's gather warps
     // w_scale != null: B holds int8 codes, one fp32 scale per B row (INT8 kernels); with
     // swap_ab the weight-streaming INT8 kernel for few rows per group runs
     if (a_rows <= 0 || G <= 0) return MOE_OK;
@@ -566,12 +569,16 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     swap_ab = swap_ab && w_scale != nullptr;
     if (swap_ab && !q8t_supports(EPI)) return MOE_ERR_UNSUPPORTED;
     CUtensorMap ta, tb;
-    if (!make_tmap_bf16(&ta, A, (uint64_t)a_rows, (uint64_t)K, swap_ab ? QT_NT : GM_BM))
-        return MOE_ERR_CUDA;
+    const bool gathered = a_gather && !w_scale;
     if (swap_ab ? !make_tmap_i8(&tb, B, (uint64_t)b_rows_total, (uint64_t)K, GM_BN / 2, QT_BK,
                                 CU_TENSOR_MAP_SWIZZLE_128B)
         : w_scale ? !make_tmap_i8(&tb, B, (uint64_t)b_rows_total, (uint64_t)K, GM_BN / 2)
                   : !make_tmap_bf16(&tb, B, (uint64_t)b_rows_total, (uint64_t)K, GM_BN / 2))
+        return MOE_ERR_CUDA;
+    // gathered A is read with cp.async, not through a tensor map (a_rows counts the
+    // logical, permuted rows)
+    if (gathered) ta = tb;
+    else if (!make_tmap_bf16(&ta, A, (uint64_t)a_rows, (uint64_t)K, swap_ab ? QT_NT : GM_BM))
         return MOE_ERR_CUDA;
     GemmParams p{};
     p.G = G;
@@ -604,6 +611,11 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     p.w_scale = w_scale;
     p.r_hist = r_hist;
     p.r_hist_chunk = kDispTok;
+    if (gathered) {
+        p.a_gather = a_gather;
+        p.a_src = static_cast<const uint8_t*>(A);
+        p.a_row_bytes = a_row_bytes;
+    }
     const int smem = gm_smem_bytes(G);
     static std::once_flag attr_once[64];
     static cudaError_t attr_err[64];
@@ -649,7 +661,8 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
                             ta, tb, p));
     } else {
         MOE_LAUNCH(name ? name : gemm_name<EPI>(), s,
-                   launch_k(grouped_gemm_kernel<EPI>, grid, GM_THREADS, smem, s, ta, tb, p));
+                   launch_k(grouped_gemm_kernel<EPI>, grid,
+                            GM_THREADS + (p.a_gather ? GM_GATHER_THREADS : 0), smem, s, ta, tb, p));
     }
     if (split) {
         const long long work = a_rows * (long long)(N / 4);
@@ -730,7 +743,10 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
                     const float* topk_w, const int32_t* perm_token, const int32_t* perm_slot,
                     float* y, int32_t* mtile, bool mtile_ready, int32_t* shared_tab,
                     __nv_bfloat16* h, __nv_bfloat16* hs, float* partial,
-                    unsigned long long* counters, cudaStream_t s, void* fused_out = nullptr) {
+                    unsigned long long* counters, cudaStream_t s, void* fused_out = nullptr,
+                    bool gather_a = false) {
+    // gather_a: x_perm is not materialised; the routed up projection reads row p of its A
+    // from x[perm_token[p]] (bf16 weights only)
     // fused_out (top-1, no shared expert, unsplit down projection): the down projection
     // writes the layer output [T, d] directly (combine fused); y is not written
     // counters: kNumCounters tile counters; [kCntUp], [kCntDown] are already zero when
@@ -770,16 +786,21 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
     const float* rs1 = q8 ? R.s1 : nullptr;
     const float* rs2 = q8 ? R.s2 : nullptr;
     const bool swap_r = q8t_routed(c), swap_s = q8t_shared(c);
+    const bool ga = gather_a && !q8;
+    const void* a_up = ga ? x : x_perm;
+    const int32_t* a_idx = ga ? perm_token : nullptr;
     if (c.kind == MOE_EXPERT_SWIGLU)
-        MOE_TRY(launch_gemm<EPI_SWIGLU_BF16>(x_perm, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
+        MOE_TRY(launch_gemm<EPI_SWIGLU_BF16>(a_up, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
                                              offsets, mtile, h, F, R.b1, nullptr, nullptr, nullptr,
                                              k, s, nullptr, fp.up, partial, counters + kCntUp,
-                                             nullptr, nullptr, nullptr, 0, 0, rs1, swap_r));
+                                             nullptr, nullptr, nullptr, 0, 0, rs1, swap_r, nullptr,
+                                             a_idx, d * 2));
     else
-        MOE_TRY(launch_gemm<EPI_GELU_BF16>(x_perm, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
+        MOE_TRY(launch_gemm<EPI_GELU_BF16>(a_up, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
                                            offsets, mtile, h, F, R.b1, nullptr, nullptr, nullptr, k,
                                            s, nullptr, fp.up, partial, counters + kCntUp, nullptr,
-                                           nullptr, nullptr, 0, 0, rs1, swap_r));
+                                           nullptr, nullptr, 0, 0, rs1, swap_r, nullptr, a_idx,
+                                           d * 2));
     if (fused_out)
         MOE_TRY(launch_gemm<EPI_COMBINE1_BF16>(h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets,
                                                mtile, fused_out, d, R.b2, topk_w, perm_token,
@@ -974,6 +995,10 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate
     int32_t* perm_slot = at<int32_t>(ws, L.perm_slot);
     int32_t* slot_dest = at<int32_t>(ws, L.slot_dest);
     void* x_perm = at<void>(ws, L.x_perm);
+    // bf16 experts with k >= 4: the up projection gathers its rows of x itself (no x_perm
+    // copy, which is k times the size of x). With fewer slots per token the copy is cheaper
+    // than the slower A loads of the gathering kernel (16-byte cp.async instead of TMA).
+    const bool gather_a = is_bf16_kind(c) && c.w_dtype != MOE_I8 && c.top_k >= 4;
     float* y = at<float>(ws, L.y);
     int32_t* mtile = at<int32_t>(ws, L.mtile);
     // Top-1 layers without a shared expert write the output from the down projection.
@@ -987,7 +1012,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate
                        at<int32_t>(ws, L.cand), stream,
                        hist_by_router ? at<int32_t>(ws, L.blockcnt) : nullptr));
     MOE_TRY(dispatch_impl(c, idx, x, ld, at<int32_t>(ws, L.counts), offsets, perm_token, perm_slot,
-                          slot_dest, x_perm, at<int32_t>(ws, L.blockcnt),
+                          slot_dest, gather_a ? nullptr : x_perm, at<int32_t>(ws, L.blockcnt),
                           at<int32_t>(ws, L.blockoff), mtile,
                           at<unsigned long long>(ws, L.counters), stream, at<int32_t>(ws, L.cand),
                           at<int32_t>(ws, L.prop), at<int32_t>(ws, L.cnt0),
@@ -998,7 +1023,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate
     MOE_TRY(ffn_impl(c, x_perm, offsets, *routed, shared, x, w, perm_token, perm_slot, y, mtile,
                      true, at<int32_t>(ws, L.shared_tab), at<__nv_bfloat16>(ws, L.h),
                      at<__nv_bfloat16>(ws, L.hs), at<float>(ws, L.partial),
-                     at<unsigned long long>(ws, L.counters), stream, fuse1 ? out : nullptr));
+                     at<unsigned long long>(ws, L.counters), stream, fuse1 ? out : nullptr,
+                     gather_a));
     if (fuse1) return MOE_OK;   // dropped tokens were written by the dispatch
     return combine_impl(c, x, y, slot_dest, w, out, stream);
 }
