@@ -590,7 +590,9 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
         uint32_t ph = 0;
         int q = 0;
         uint32_t qph = 0;
-        int pend[GM_GATHER_DEPTH + 1];
+        int pend[GM_GATHER_DEPTH + 1];   // stages issued but not yet arrived, oldest first
+#pragma unroll
+        for (int i = 0; i <= GM_GATHER_DEPTH; ++i) pend[i] = 0;
         int npend = 0;
         auto release_oldest = [&]() {   // the oldest pending stage has landed: FULL
             fence_proxy_async_smem();
