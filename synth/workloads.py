@@ -243,6 +243,10 @@ WORKLOADS = {
     "decode64_i8": Workload("decode64_i8", T=64, d=7168, E=256, k=8, F=2048, kind="swiglu",
                             act="bf16", gate_dist="uniform", int8=True,
                             note="decode, 64 tokens, INT8 expert weights"),
+    # decode8_i8's expert shapes with 32 experts: small enough for multi-pass profiler captures
+    "decode8_i8_e32": Workload("decode8_i8_e32", T=8, d=7168, E=32, k=8, F=2048, kind="swiglu",
+                               act="bf16", gate_dist="uniform", int8=True,
+                               note="decode, 8 tokens, INT8 weights, 32 experts (for profiling)"),
     "decode1": Workload("decode1", T=1, d=7168, E=256, k=8, F=2048, kind="swiglu", act="bf16",
                         gate_dist="uniform", note="decode, 1 token"),
     "decode8": Workload("decode8", T=8, d=7168, E=256, k=8, F=2048, kind="swiglu", act="bf16",
