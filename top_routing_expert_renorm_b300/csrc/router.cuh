@@ -224,21 +224,45 @@ __global__ void __launch_bounds__(256) topk_renorm_kernel(const float* __restric
     const int lane = threadIdx.x & 31;
     const long long t0 = (long long)blockIdx.x * kTopkTok;
     const int nt = (int)min((long long)kTopkTok, (long long)T - t0);
-    for (int i = threadIdx.x; i < nt * E; i += blockDim.x) {
-        const int tt = i / E, e = i - tt * E;
-        const float* L = parts + (t0 + tt) * row_stride + e;
-        float s = L[0];
-        for (int p = 1; p < n_parts; p += 8) {
-            float v[8];
+    // Each thread forms kTopkSums logits at a time and issues all their part loads before
+    // the first add, so that one memory round trip serves several sums.
+    constexpr int kTopkSums = 4;
+    const int n = nt * E;
+    for (int i0 = threadIdx.x; i0 < n; i0 += kTopkSums * blockDim.x) {
+        const float* L[kTopkSums];
+        float s[kTopkSums];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) v[q] = (p + q < n_parts) ? L[(p + q) * part_stride] : 0.0f;
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (p + q < n_parts) s += v[q];
+        for (int u = 0; u < kTopkSums; ++u) {
+            const int i = i0 + u * blockDim.x;
+            const int tt = i / E, e = i - tt * E;
+            L[u] = parts + (t0 + tt) * row_stride + e;
+            s[u] = (i < n) ? L[u][0] : 0.0f;
         }
-        if (bias) s += bias[e];
-        sL[i] = s;
-        if (logits) logits[(t0 + tt) * E + e] = s;
+        for (int p = 1; p < n_parts; p += 8) {
+            float v[kTopkSums][8];
+#pragma unroll
+            for (int u = 0; u < kTopkSums; ++u)
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    v[u][q] = (i0 + u * (int)blockDim.x < n && p + q < n_parts)
+                                  ? L[u][(p + q) * part_stride]
+                                  : 0.0f;
+#pragma unroll
+            for (int u = 0; u < kTopkSums; ++u)
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (p + q < n_parts) s[u] += v[u][q];
+        }
+#pragma unroll
+        for (int u = 0; u < kTopkSums; ++u) {
+            const int i = i0 + u * blockDim.x;
+            if (i >= n) break;
+            const int tt = i / E, e = i - tt * E;
+            float sv = s[u];
+            if (bias) sv += bias[e];
+            sL[i] = sv;
+            if (logits) logits[(t0 + tt) * E + e] = sv;
+        }
     }
     __syncthreads();
     const int wt = threadIdx.x >> 5;
