@@ -730,11 +730,17 @@ moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const
                        launch_k(router_splitk_kernel<64>, grid, 256, 0, s, xb, Wg, parts, T, d, E));
         }
     }
-    MOE_LAUNCH("topk_renorm", s,
-               launch_k(topk_renorm_kernel, (T + kTopkTok - 1) / kTopkTok, 256,
-                        kTopkTok * E * sizeof(float), s, parts, rp.n_parts, rp.part_stride,
-                        rp.row_stride, bias, logits, T, E, k, c.n_group, c.topk_group, idx, w,
-                        cand));
+    const int tk_blocks = (T + kTopkTok - 1) / kTopkTok;
+    const size_t tk_smem = kTopkTok * E * sizeof(float);
+#define MOE_TOPK(VPL)                                                                           \
+    MOE_LAUNCH("topk_renorm", s,                                                                \
+               launch_k(topk_renorm_kernel<VPL>, tk_blocks, 256, tk_smem, s, parts, rp.n_parts, \
+                        rp.part_stride, rp.row_stride, bias, logits, T, E, k, c.n_group,        \
+                        c.topk_group, idx, w, cand))
+    if (E <= 64) MOE_TOPK(2);
+    else if (E <= 256) MOE_TOPK(8);
+    else MOE_TOPK(32);
+#undef MOE_TOPK
     return MOE_OK;
 }
 

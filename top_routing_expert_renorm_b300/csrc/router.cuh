@@ -210,7 +210,9 @@ __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
 // the same candidate set, -1 where the set has fewer experts.
 constexpr int kTopkTok = 8;
 
-__global__ void __launch_bounds__(256) topk_renorm_kernel(const float* __restrict__ parts,
+// VPL: logits per lane of the selecting warp, ceil(E / 32) rounded up to 2, 8 or 32.
+template <int VPL>
+__global__ void __launch_bounds__(256, 3) topk_renorm_kernel(const float* __restrict__ parts,
                                                           int n_parts, long long part_stride,
                                                           long long row_stride,
                                                           const float* __restrict__ bias,
@@ -269,10 +271,10 @@ __global__ void __launch_bounds__(256) topk_renorm_kernel(const float* __restric
     if (wt >= nt) return;
     const long long t = t0 + wt;
     const float* Ls = sL + wt * E;
-    float v[32];
+    float v[VPL];
     uint32_t avail = 0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < VPL; ++i) {
         const int e = lane + 32 * i;
         v[i] = 0.0f;
         if (e < E) {
@@ -307,23 +309,33 @@ __global__ void __launch_bounds__(256) topk_renorm_kernel(const float* __restric
             if (bg == lane) gavail = 0;
         }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < VPL; ++i) {
             const int e = lane + 32 * i;
             if (e < E && !((chosen >> (e / gsize)) & 1u)) avail &= ~(1u << i);
         }
     }
-    // best remaining candidate (logit descending, id ascending) over the warp; it leaves
-    // the candidate set. be = -1 when the set is empty.
-    auto pick = [&](float& bv, int& be) {
-        bv = 0.0f;
-        be = -1;
+    // Each lane keeps its own best remaining candidate (lb, le); a round takes the warp's
+    // best of those (logit descending, id ascending), which leaves the candidate set, and
+    // only the lane that owned it rescans its (E / 32) values. be = -1 when the set is empty.
+    const int nv = (E + 31) / 32;   // values per lane (warp-uniform)
+    float lb = 0.0f;
+    int le = -1;
+    auto local_best = [&]() {
+        lb = 0.0f;
+        le = -1;
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if ((avail >> i) & 1u)
-                if (better(v[i], lane + 32 * i, bv, be)) {
-                    bv = v[i];
-                    be = lane + 32 * i;
-                }
+        for (int i = 0; i < VPL; ++i) {
+            if (i >= nv) break;
+            if (((avail >> i) & 1u) && better(v[i], lane + 32 * i, lb, le)) {
+                lb = v[i];
+                le = lane + 32 * i;
+            }
+        }
+    };
+    local_best();
+    auto pick = [&](float& bv, int& be) {
+        bv = lb;
+        be = le;
 #pragma unroll
         for (int off = 16; off; off >>= 1) {
             const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
@@ -333,7 +345,10 @@ __global__ void __launch_bounds__(256) topk_renorm_kernel(const float* __restric
                 be = oe;
             }
         }
-        if (be >= 0 && (be & 31) == lane) avail &= ~(1u << (be >> 5));
+        if (be >= 0 && (be & 31) == lane) {
+            avail &= ~(1u << (be >> 5));
+            local_best();
+        }
     };
     float my_v = 0.0f, l0 = 0.0f;
     int my_e = 0;
