@@ -96,6 +96,11 @@ SMALL = {
                            overflow="shared"),
     "ovf_shared_hot_k1": W("os2", T=200, d=64, E=8, k=1, F=64, kind="gelu", act="bf16",
                            cf=0.5, gate_bias="hot", has_shared=True, overflow="shared"),
+    # combinations: INT8 experts with re-routing / with overflow to the shared expert
+    "i8t_reroute_k4": W("c1", T=48, d=256, E=16, k=4, F=128, kind="swiglu", act="bf16",
+                        cf=0.5, gate_bias="zipf", int8=True, overflow="reroute"),
+    "i8_ovf_shared": W("c2", T=300, d=128, E=8, k=2, F=128, kind="gelu", act="bf16", cf=0.5,
+                       has_shared=True, gate_bias="hot", int8=True, overflow="shared"),
     # K = 64: one half-filled 128-code K block (zero codes and activations past the end)
     "i8t_k64": W("q8t5", T=10, d=64, E=4, k=2, F=64, kind="swiglu", act="bf16",
                  expert_bias=True, has_shared=True, int8=True),
