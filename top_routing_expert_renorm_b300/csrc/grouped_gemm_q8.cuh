@@ -245,14 +245,11 @@ __global__ void __launch_bounds__(GM_Q8_THREADS, 1)
             const int kb1 = min(kblocks, kb0 + p.kb_per_split);
             bool ok = true;
             for (int kb = kb0; kb < kb1; ++kb) {
-                int w_ok = 1;
-                if (lane == 0)
-                    w_ok = (!*s_abort && mbar_wait(bar(QFULL + qs), qph) &&
-                            mbar_wait(bar(CEMPTY + cs), cph ^ 1))
-                               ? 1
-                               : 0;
-                w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-                if (!w_ok) {
+                // every lane waits: each one reads TMA-written codes and overwrites a stage
+                // the tensor core has finished reading
+                const bool w_ok = !*s_abort && mbar_wait(bar(QFULL + qs), qph) &&
+                                  mbar_wait(bar(CEMPTY + cs), cph ^ 1);
+                if (!__all_sync(0xffffffffu, w_ok)) {
                     if (lane == 0) *s_abort = 1;
                     ok = false;
                     break;
