@@ -96,6 +96,12 @@ SMALL = {
                            overflow="shared"),
     "ovf_shared_hot_k1": W("os2", T=200, d=64, E=8, k=1, F=64, kind="gelu", act="bf16",
                            cf=0.5, gate_bias="hot", has_shared=True, overflow="shared"),
+    # fp32 Linear experts (fp32 router path) with the overflow variants
+    "linear_reroute": W("lr", T=96, d=16, E=5, k=2, F=16, kind="linear", act="f32", cf=0.5,
+                        expert_bias=True, overflow="reroute"),
+    "linear_ovf_shared": W("lo", T=96, d=16, E=5, k=2, F=16, kind="linear", act="f32", cf=0.5,
+                           has_shared=True, add_residual=True, expert_bias=True,
+                           overflow="shared"),
     # combinations: INT8 experts with re-routing / with overflow to the shared expert
     "i8t_reroute_k4": W("c1", T=48, d=256, E=16, k=4, F=128, kind="swiglu", act="bf16",
                         cf=0.5, gate_bias="zipf", int8=True, overflow="reroute"),
