@@ -126,12 +126,27 @@ __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ x,
                 if (va) load4<OT>(x + t * d + ca, a);
                 if (vb) load4<OT>(x + t * d + cb, b);
             }
-            for (int j = 0; j < k; ++j) {
-                const int r = __shfl_sync(0xffffffffu, mydest, j);
-                if (r < 0) continue;
-                const float* yr = y + (long long)r * d;
-                if (va) add4(a, *reinterpret_cast<const float4*>(yr + ca));
-                if (vb) add4(b, *reinterpret_cast<const float4*>(yr + cb));
+            // Slots in groups of four: the group's row loads are all issued before its adds,
+            // which then run in slot order (a dropped slot adds nothing).
+            for (int j0 = 0; j0 < k; j0 += 4) {
+                int r[4];
+                float4 ya[4], yb[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    r[u] = (j0 + u < k) ? __shfl_sync(0xffffffffu, mydest, j0 + u) : -1;
+                    ya[u] = yb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (r[u] >= 0) {
+                        const float* yr = y + (long long)r[u] * d;
+                        if (va) ya[u] = *reinterpret_cast<const float4*>(yr + ca);
+                        if (vb) yb[u] = *reinterpret_cast<const float4*>(yr + cb);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (r[u] < 0) continue;
+                    if (va) add4(a, ya[u]);
+                    if (vb) add4(b, yb[u]);
+                }
             }
             if (y_shared) {
                 const float* ys = y_shared + t * d;
