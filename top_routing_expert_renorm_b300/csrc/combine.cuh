@@ -91,8 +91,10 @@ __device__ __forceinline__ void fma4(float4& a, float s, const float4& v) {
     a.w = fmaf(s, v.w, a.w);
 }
 
+constexpr int kCombineGroup = 8;
+
 template <typename OT>
-__global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ x,
+__global__ void __launch_bounds__(256, 2) combine_kernel(const OT* __restrict__ x,
                                                       const float* __restrict__ y,
                                                       const int* __restrict__ slot_dest,
                                                       const float* __restrict__ y_shared,
@@ -126,13 +128,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ x,
                 if (va) load4<OT>(x + t * d + ca, a);
                 if (vb) load4<OT>(x + t * d + cb, b);
             }
-            // Slots in groups of four: the group's row loads are all issued before its adds,
-            // which then run in slot order (a dropped slot adds nothing).
-            for (int j0 = 0; j0 < k; j0 += 4) {
-                int r[4];
-                float4 ya[4], yb[4];
+            // Slots in groups of kCombineGroup: the group's row loads are all issued before
+            // its adds, which then run in slot order (a dropped slot adds nothing).
+            for (int j0 = 0; j0 < k; j0 += kCombineGroup) {
+                int r[kCombineGroup];
+                float4 ya[kCombineGroup], yb[kCombineGroup];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < kCombineGroup; ++u) {
                     r[u] = (j0 + u < k) ? __shfl_sync(0xffffffffu, mydest, j0 + u) : -1;
                     ya[u] = yb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (r[u] >= 0) {
@@ -142,7 +144,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const OT* __restrict__ x,
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < kCombineGroup; ++u) {
                     if (r[u] < 0) continue;
                     if (va) add4(a, ya[u]);
                     if (vb) add4(b, yb[u]);
