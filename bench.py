@@ -282,6 +282,17 @@ def default_sample(wl):
 # ---------------------------------------------------------------------------------
 # reference arm: the oracle timed as the reference implementation
 # ---------------------------------------------------------------------------------
+def workload_config(wl, world):
+    """The workload part of `config`, the same on both arms."""
+    return {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "top_k": wl.k, "F": wl.F,
+            "kind": wl.kind, "capacity_factor": wl.cf, "shared_expert": wl.has_shared,
+            "residual": wl.add_residual,
+            "expert_groups": [wl.n_group, wl.topk_group] if wl.n_group else None,
+            "expert_weights": "int8 codes + fp32 row scales" if wl.int8 else "bf16",
+            "overflow": wl.overflow,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def run_reference(args, wl):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -302,8 +313,7 @@ def run_reference(args, wl):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * total_s / max(1, len(vals)), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "top_k": wl.k,
-                   "F": wl.F, "kind": wl.kind, "capacity_factor": wl.cf},
+        "config": workload_config(wl, int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": descs},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -510,13 +520,7 @@ def run_ours(args, wl):
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.bf16 else "f32",
         "data": "synthetic (seeded counter-based generator; random-init weights)",
-        "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "top_k": wl.k,
-                   "F": wl.F, "kind": wl.kind, "capacity_factor": wl.cf,
-                   "shared_expert": wl.has_shared, "residual": wl.add_residual,
-                   "expert_groups": [wl.n_group, wl.topk_group] if wl.n_group else None,
-                   "expert_weights": "int8 codes + fp32 row scales" if wl.int8 else "bf16",
-                   "overflow": wl.overflow,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        "config": {**workload_config(wl, world),
                    "l2": f"flushed between steps ({args.flush_mib} MiB write)",
                    "kept_rows_P": P, "touched_experts": touched},
         "roofline": roof,
