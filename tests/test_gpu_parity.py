@@ -57,6 +57,11 @@ SMALL = {
                              cf=1.0, add_residual=True),
     "k2_hist_by_router": W("hbr2", T=2100, d=128, E=16, k=2, F=128, kind="swiglu",
                            act="bf16", cf=1.0, gate_bias="zipf"),
+    # the tensor-core router with its K split in two (few M tiles, d >= 2048)
+    "router_ksplit_k2": W("rks1", T=300, d=2048, E=16, k=2, F=128, kind="gelu", act="bf16",
+                          cf=1.0, gate_bias="zipf"),
+    "router_ksplit_top1": W("rks2", T=600, d=2048, E=8, k=1, F=128, kind="swiglu",
+                            act="bf16", cf=1.25, add_residual=True, expert_bias=True),
     # weight-only INT8 experts: codes widened in shared memory, scales in the epilogue
     "i8_gelu_bias_k2": W("q8g", T=333, d=192, E=6, k=2, F=256, kind="gelu", act="bf16",
                          expert_bias=True, int8=True),

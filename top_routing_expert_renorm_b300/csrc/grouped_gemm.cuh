@@ -70,8 +70,11 @@ struct GemmParams {
     int* r_idx;                   // EPI_ROUTER_TOPK: top-k ids [T, top_k]
     float* r_w;                   //                  renormalised weights [T, top_k]
     int r_E, r_Ep;                //                  experts, padded experts per term (32 | 64)
+    long long r_rows;             //                  T (rows of r_part per part)
     int* r_hist;                  //                  nullable [T / r_hist_chunk][r_E]: selected
     int r_hist_chunk;             //                  experts per chunk of tokens (zeroed before)
+    float* r_part;                //                  k_splits > 1: partial logits [S][T][r_Ep]
+    int* r_tile_cnt;              //                  and arrivals per M tile (zeroed before)
     // split-K: every output tile is computed as k_splits units over consecutive ranges of
     // kb_per_split K blocks; with partial != null each unit stores its raw fp32 sums at
     // partial + split * part_stride + row * ld_part + column (columns as in B's rows, so
@@ -152,7 +155,9 @@ __device__ __forceinline__ void gm_epilogue_partial(const GemmParams& p, uint32_
 
 template <int EPI>
 __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t tb, int g, int nb,
-                                                 bool row_ok, long long grow) {
+                                                 bool row_ok, long long grow, int mb = 0,
+                                                 int ks = 0, volatile int* s_flag = nullptr) {
+    // mb, ks, s_flag: EPI_ROUTER_TOPK with K split (see there)
     const float* brow = p.bias ? p.bias + (long long)g * p.b_rows_per_group : nullptr;
     const float* srow = p.w_scale ? p.w_scale + (long long)g * p.b_rows_per_group : nullptr;
     if constexpr (EPI == EPI_SWIGLU_BF16) {
@@ -243,6 +248,38 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) L[c * 32 + i] = 0.0f;
+            }
+        }
+        if (p.k_splits > 1) {
+            // K split in two parts (few M tiles): each part stores its partial logits; the
+            // CTA whose part arrives second at the M tile adds the other part (a commutative
+            // fp32 add, so the result does not depend on which one that is) and selects.
+            // The four epilogue warps meet at named barrier 1.
+            float* mine = p.r_part + ((long long)ks * p.r_rows + grow) * Ep;
+            if (row_ok) {
+#pragma unroll
+                for (int e = 0; e < MAXE; e += 4)
+                    if (e < Ep)
+                        *reinterpret_cast<float4*>(mine + e) = make_float4(L[e], L[e + 1], L[e + 2], L[e + 3]);
+            }
+            __threadfence();
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (threadIdx.x == 64) *s_flag = atomicAdd(p.r_tile_cnt + mb, 1);
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (*s_flag != p.k_splits - 1) return;   // another part finishes this tile
+            __threadfence();
+            if (row_ok) {
+                const float* other = p.r_part + ((long long)(1 - ks) * p.r_rows + grow) * Ep;
+#pragma unroll
+                for (int e = 0; e < MAXE; e += 4) {
+                    if (e < Ep) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4*>(other + e));
+                        L[e] += v.x;
+                        L[e + 1] += v.y;
+                        L[e + 2] += v.z;
+                        L[e + 3] += v.w;
+                    }
+                }
             }
         }
         if (row_ok) {
@@ -412,6 +449,7 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
     // unit-id ring full[16..23] / empty[24..31]
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 32);
     volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 33);
+    volatile int* s_flag = reinterpret_cast<volatile int*>(bars + 34);   // router K split
     volatile long long* s_unit = reinterpret_cast<volatile long long*>(bars + 40);   // [GM_TQ]
     int* s_ro = reinterpret_cast<int*>(bars + GM_HDR_BYTES / 8);
     int* s_mt = s_ro + (p.G + 1);
@@ -711,7 +749,7 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
             const long long grow = (long long)s_ro[g] + r_tile;
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * GM_BN);
             if (p.partial) gm_epilogue_partial<EPI>(p, tb, nb, ks, row_ok, grow);
-            else gm_epilogue_tile<EPI>(p, tb, g, nb, row_ok, grow);
+            else gm_epilogue_tile<EPI>(p, tb, g, nb, row_ok, grow, mb, ks, s_flag);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(TEMPTY + acc));

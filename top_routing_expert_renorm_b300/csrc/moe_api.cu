@@ -237,6 +237,8 @@ struct RouterPlan {
     int n_parts;
     long long part_stride, row_stride;
     size_t bg_bytes, d_bytes, scratch_bytes;
+    int ksplit = 1;           // path 2 with the fused top-k: K split of the router GEMM
+    long long mtiles = 0;     // its M tiles
 };
 
 size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
@@ -269,10 +271,17 @@ RouterPlan router_plan(const moe_config& c) {
         r.part_stride = r.Ep;
         r.row_stride = 3ll * r.Ep;
         r.bg_bytes = al256(3 * (size_t)r.Ep * d * 2);
-        // partial logits only when the three terms do not fit one accumulator (E > 64);
-        // otherwise the GEMM epilogue selects the top k itself
-        r.d_bytes = router_fused_topk(c, r.Ep) ? 0 : al256(T * 3 * (size_t)r.Ep * 4);
-        r.scratch_bytes = r.bg_bytes + r.d_bytes + 256;
+        // partial logits when the three terms do not fit one accumulator (E > 64); otherwise
+        // the GEMM epilogue selects the top k itself, with K split in two when there are
+        // too few M tiles to fill half the SMs and K is long enough for the split to pay
+        // (d >= 2048; two partial logit sets, per-tile counters)
+        const bool fused = router_fused_topk(c, r.Ep);
+        r.mtiles = ((long long)c.T + 127) / 128;
+        r.ksplit = (fused && 2 * r.mtiles <= num_sms() && c.d / GM_BK >= 32) ? 2 : 1;
+        r.d_bytes = fused ? (r.ksplit > 1 ? al256(2 * T * (size_t)r.Ep * 4) : 0)
+                          : al256(T * 3 * (size_t)r.Ep * 4);
+        r.scratch_bytes = r.bg_bytes + r.d_bytes + 256 +
+                          (r.ksplit > 1 ? al256((size_t)r.mtiles * 4) : 0);
     } else {
         r.path = 3;
         r.n_parts = (c.d + RS_K - 1) / RS_K;
@@ -559,7 +568,8 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
                        int* r_idx = nullptr, float* r_w = nullptr, int r_E = 0, int r_Ep = 0,
                        const float* w_scale = nullptr, bool swap_ab = false,
                        int* r_hist = nullptr, const int32_t* a_gather = nullptr,
-                       int a_row_bytes = 0) {
+                       int a_row_bytes = 0, float* r_part = nullptr, int* r_tile_cnt = nullptr) {
+    // r_part, r_tile_cnt (EPI_ROUTER_TOPK with sp.S == 2): the epilogue's split-K exchange
     // a_gather (bf16 kernel only): logical A row r (r < a_rows) is row a_gather[r] of A,
     // loaded by the kernel's gather warps
     // w_scale != null: B holds int8 codes, one fp32 scale per B row (INT8 kernels); with
@@ -611,6 +621,16 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     p.w_scale = w_scale;
     p.r_hist = r_hist;
     p.r_hist_chunk = kDispTok;
+    if constexpr (EPI == EPI_ROUTER_TOPK) {
+        if (sp.S > 1) {   // the epilogue adds the two K parts itself (no partial buffer pass)
+            if (sp.S != 2 || !r_part || !r_tile_cnt) return MOE_ERR_UNSUPPORTED;
+            p.k_splits = sp.S;
+            p.kb_per_split = sp.kbs;
+            p.r_part = r_part;
+            p.r_tile_cnt = r_tile_cnt;
+            p.r_rows = a_rows;
+        }
+    }
     if (gathered) {
         p.a_gather = a_gather;
         p.a_src = static_cast<const uint8_t*>(A);
@@ -700,18 +720,26 @@ moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const
         parts = reinterpret_cast<float*>(static_cast<char*>(scratch) + rp.bg_bytes);
         int32_t* tables =
             reinterpret_cast<int32_t*>(static_cast<char*>(scratch) + rp.bg_bytes + rp.d_bytes);
+        int32_t* tile_cnt = rp.ksplit > 1
+                                ? reinterpret_cast<int32_t*>(static_cast<char*>(scratch) +
+                                                             rp.bg_bytes + rp.d_bytes + 256)
+                                : nullptr;
         const dim3 grid((d + 31) / 32, rp.Ep / 32);
         MOE_LAUNCH("gate_split", s,
                    launch_k(gate_split_kernel, grid, 256, 0, s,
                        Wg, d, E, rp.Ep, Bg, T, tables,
                        reinterpret_cast<unsigned long long*>(tables + 4), hist,
-                       hist ? (int)(((T + kDispTok - 1) / kDispTok) * (long long)E) : 0));
+                       hist ? (int)(((T + kDispTok - 1) / kDispTok) * (long long)E) : 0, tile_cnt,
+                       (int)rp.mtiles));
         if (router_fused_topk(c, rp.Ep)) {   // the three terms fit one accumulator: fused top-k
+            SplitPlan sp;
+            sp.S = rp.ksplit;
+            sp.kbs = (d / GM_BK + sp.S - 1) / sp.S;
             MOE_TRY(launch_gemm<EPI_ROUTER_TOPK>(
                 x, T, d, Bg, 3ll * rp.Ep, 3 * rp.Ep, 1, 3 * rp.Ep, tables, tables + 2, logits, E,
-                bias, nullptr, nullptr, nullptr, k, s, nullptr, SplitPlan(), nullptr,
+                bias, nullptr, nullptr, nullptr, k, s, nullptr, sp, nullptr,
                 reinterpret_cast<unsigned long long*>(tables + 4), nullptr, idx, w, E, rp.Ep,
-                nullptr, false, hist));
+                nullptr, false, hist, nullptr, 0, parts, tile_cnt));
             return MOE_OK;
         }
         MOE_TRY(launch_gemm<EPI_F32>(x, T, d, Bg, 3ll * rp.Ep, 3 * rp.Ep, 1, 3 * rp.Ep, tables,
