@@ -275,24 +275,34 @@ constexpr int kOneCtaBatch = 16;
 constexpr int kOneCtaMaxAssign = 4096;
 constexpr int kOneCtaMaxE = 320;
 
+//
+// With blockcnt (the per-chunk histogram of dispatch_hist_kernel or of the router's
+// epilogue) the same kernel runs one CTA per chunk of kDispTok tokens instead: each CTA
+// takes its rank bases from the chunks before it and the totals from all of them, so the
+// scan needs no kernel of its own; CTA 0 writes load, counts, offsets and the M-tile table.
 __global__ void __launch_bounds__(1024) dispatch_one_cta_kernel(
     const int* __restrict__ idx, int T, int k, int E, int cap, int* __restrict__ load,
     int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ perm_token,
     int* __restrict__ perm_slot, int* __restrict__ slot_dest, int* __restrict__ mtile_offsets,
-    unsigned long long* __restrict__ counters, int n_counters, DroppedRows dr) {
+    unsigned long long* __restrict__ counters, int n_counters, DroppedRows dr,
+    const int* __restrict__ blockcnt, int nb) {
     pdl_entry();
     extern __shared__ int dsm[];
-    if (counters && (int)threadIdx.x < n_counters) counters[threadIdx.x] = 0ull;
+    const bool first = blockIdx.x == 0;
+    if (first && counters && (int)threadIdx.x < n_counters) counters[threadIdx.x] = 0ull;
     __shared__ int s_warp[32];
     int* wcnt = dsm;            // [32][E] running counters
     int* s_off = dsm + 32 * E;  // [E] offsets
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
-    const long long n = (long long)T * k;
+    const long long cbeg = blockcnt ? (long long)blockIdx.x * kDispTok * k : 0;
+    const long long cend =
+        blockcnt ? min((long long)(blockIdx.x + 1) * kDispTok, (long long)T) * k : (long long)T * k;
+    const long long n = cend - cbeg;
     const int seg = (int)(((n + 31) / 32 + 31) / 32 * 32);   // assignments per warp
     const int rounds = seg / 32;
-    const long long wbeg = (long long)wid * seg;
-    const long long wend = min(wbeg + seg, n);
+    const long long wbeg = cbeg + (long long)wid * seg;
+    const long long wend = min(wbeg + seg, cend);
     int* my = wcnt + wid * E;
     const unsigned lt_mask = (1u << lane) - 1u;
     // ids of rounds r0 .. r0+kOneCtaBatch-1 of this lane (-1 past the run or out of range)
@@ -325,31 +335,41 @@ __global__ void __launch_bounds__(1024) dispatch_one_cta_kernel(
         }
     }
     __syncthreads();
-    // load, capacity, offsets; warp counters become rank bases
+    // load, capacity, offsets; warp counters become rank bases (after the earlier chunks)
     const int e = threadIdx.x;
     int kept = 0;
     if (e < E) {
-        int run = 0;
+        int run = 0, all = 0;
+        if (blockcnt) {
+            for (int b = 0; b < nb; ++b) {
+                const int c = blockcnt[(long long)b * E + e];
+                if (b < (int)blockIdx.x) run += c;
+                all += c;
+            }
+        }
         for (int w = 0; w < 32; ++w) {
             const int c = wcnt[w * E + e];
             wcnt[w * E + e] = run;
             run += c;
         }
-        load[e] = run;
-        kept = min(run, cap);
-        counts[e] = kept;
+        if (!blockcnt) all = run;
+        kept = min(all, cap);
+        if (first) {
+            load[e] = all;
+            counts[e] = kept;
+        }
     }
     int total;
     const int off = block_excl_scan_1024(kept, s_warp, total);
     if (e < E) {
-        offsets[e] = off;
         s_off[e] = off;
+        if (first) offsets[e] = off;
     }
-    if (e == 0) offsets[E] = total;
+    if (first && e == 0) offsets[E] = total;
     const int tiles = (kept + kMTile - 1) / kMTile;
     int ttot;
     const int toff = block_excl_scan_1024(tiles, s_warp, ttot);
-    if (mtile_offsets) {
+    if (first && mtile_offsets) {
         if (e < E) mtile_offsets[e] = toff;
         if (e == 0) mtile_offsets[E] = ttot;
     }

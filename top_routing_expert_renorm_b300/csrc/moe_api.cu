@@ -482,19 +482,27 @@ moe_status dispatch_impl(const moe_config& c, const int32_t* idx, const void* x,
         MOE_LAUNCH("dispatch_one_cta", s,
                    launch_k(dispatch_one_cta_kernel, 1, 1024, 33 * E * sizeof(int), s, idx, T, k,
                             E, cap, load, counts, offsets, perm_token, perm_slot, slot_dest,
-                            mtile, counters, 2, dr));
+                            mtile, counters, 2, dr, nullptr, 0));
     } else {
-    if (!hist_ready)
-        MOE_LAUNCH("dispatch_hist", s,
-                   launch_k(dispatch_hist_kernel, nb, 256, E * sizeof(int), s, idx, T, k, E,
-                            blockcnt));
-    MOE_LAUNCH("dispatch_scan", s,
-               launch_k(dispatch_scan_kernel, 1, 1024, 0, s, blockcnt, nb, E, cap, blockoff, load, counts,
-                                                       offsets, mtile, counters, 2));
-    MOE_LAUNCH("dispatch_rank", s,
-               launch_k(dispatch_rank_kernel<kRankScatter>, nb, 256, rsm, s,
-                   idx, T, k, E, cap, blockoff, offsets, perm_token, perm_slot, slot_dest, nullptr,
-                   nullptr, dr));
+        if (!hist_ready)
+            MOE_LAUNCH("dispatch_hist", s,
+                       launch_k(dispatch_hist_kernel, nb, 256, E * sizeof(int), s, idx, T, k, E,
+                                blockcnt));
+        if (E <= kOneCtaMaxE) {
+            // one CTA per chunk: scan folded into the ranking kernel
+            MOE_LAUNCH("dispatch_rank", s,
+                       launch_k(dispatch_one_cta_kernel, nb, 1024, 33 * E * sizeof(int), s, idx, T,
+                                k, E, cap, load, counts, offsets, perm_token, perm_slot, slot_dest,
+                                mtile, counters, 2, dr, blockcnt, nb));
+        } else {
+            MOE_LAUNCH("dispatch_scan", s,
+                       launch_k(dispatch_scan_kernel, 1, 1024, 0, s, blockcnt, nb, E, cap, blockoff,
+                                load, counts, offsets, mtile, counters, 2));
+            MOE_LAUNCH("dispatch_rank", s,
+                       launch_k(dispatch_rank_kernel<kRankScatter>, nb, 256, rsm, s, idx, T, k, E,
+                                cap, blockoff, offsets, perm_token, perm_slot, slot_dest, nullptr,
+                                nullptr, dr));
+        }
     }
     if (x_perm) {
         const int es = c.act_dtype == MOE_BF16 ? 2 : 4;
