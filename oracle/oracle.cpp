@@ -444,6 +444,49 @@ void oracle_quantize_rows_i8(const uint16_t* w_bf16, long long rows, int cols, i
     }
 }
 
+// Weight-only INT4 experts [Quant]: the INT8 form with codes in [-7, 7] (the symmetric
+// range of a 4-bit two's complement code; -8 is never produced):
+//   s = max_k |w[n][k]| / 7, q = round-half-even(w / s) clamped to [-7, 7], in fp32.
+// Storage, two codes per byte along the row: byte j of a row holds column 2j in its low
+// nibble and column 2j+1 in its high nibble, each as the 4-bit two's complement of the code;
+// a row of `cols` codes (cols even) takes cols / 2 bytes.
+void oracle_quantize_rows_i4(const uint16_t* w_bf16, long long rows, int cols, uint8_t* packed,
+                             float* scale) {
+    for (long long r = 0; r < rows; ++r) {
+        float m = 0.0f;
+        for (int c = 0; c < cols; ++c) {
+            const float v = std::fabs((float)bf16_bits_to_double(w_bf16[r * cols + c]));
+            if (v > m) m = v;
+        }
+        const float sc = m / 7.0f;
+        scale[r] = sc;
+        for (int c = 0; c < cols; c += 2) {
+            int code[2] = {0, 0};
+            for (int u = 0; u < 2; ++u) {
+                if (sc > 0.0f) {
+                    const float v = (float)bf16_bits_to_double(w_bf16[r * cols + c + u]);
+                    float qv = std::nearbyint(v / sc);   // nearest, ties to even
+                    if (qv > 7.0f) qv = 7.0f;
+                    if (qv < -7.0f) qv = -7.0f;
+                    code[u] = (int)qv;
+                }
+            }
+            packed[r * (cols / 2) + c / 2] = (uint8_t)((code[0] & 15) | ((code[1] & 15) << 4));
+        }
+    }
+}
+
+// The codes of a packed INT4 matrix [rows, cols / 2] as int8 [rows, cols]: the nibble's
+// value v in 0..15 is the code v for v < 8 and v - 16 otherwise.
+void oracle_unpack_i4(const uint8_t* packed, long long rows, int cols, int8_t* q) {
+    for (long long r = 0; r < rows; ++r)
+        for (int c = 0; c < cols; ++c) {
+            const uint8_t b = packed[r * (cols / 2) + c / 2];
+            const int v = (c % 2 == 0) ? (b & 15) : (b >> 4);
+            q[r * cols + c] = (int8_t)(v < 8 ? v : v - 16);
+        }
+}
+
 // O8 with INT8 weights: as oracle_expert_row for GELU / SWIGLU, the weight of row n,
 // column c being s[n] * q[n][c]. h is rounded to bf16 (the activations are bf16).
 void oracle_expert_row_q8(int kind, const void* x_row, int x_dtype, const int8_t* q1,

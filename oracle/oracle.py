@@ -49,6 +49,10 @@ def lib():
         L.oracle_expert_row.argtypes = [i32, vp, i32, vp, vp, vp, vp, i32, i32, i32, vp]
         L.oracle_quantize_rows_i8.restype = None
         L.oracle_quantize_rows_i8.argtypes = [vp, ctypes.c_longlong, i32, vp, vp]
+        L.oracle_quantize_rows_i4.restype = None
+        L.oracle_quantize_rows_i4.argtypes = [vp, ctypes.c_longlong, i32, vp, vp]
+        L.oracle_unpack_i4.restype = None
+        L.oracle_unpack_i4.argtypes = [vp, ctypes.c_longlong, i32, vp]
         L.oracle_expert_row_q8.restype = None
         L.oracle_expert_row_q8.argtypes = [i32, vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, vp]
         L.oracle_combine_row.restype = None
@@ -267,6 +271,29 @@ def quantize_rows_i8(w_bf16):
     s = np.empty(w.shape[:-1], np.float32)
     lib().oracle_quantize_rows_i8(_p(w), rows, cols, _p(q), _p(s))
     return q, s
+
+
+def quantize_rows_i4(w_bf16):
+    """Per-row absmax INT4 codes, packed two per byte ([..., cols / 2] uint8: column 2j in
+    the low nibble of byte j, 2j+1 in the high one), and fp32 scales [rows]."""
+    w = np.ascontiguousarray(w_bf16, np.uint16)
+    cols = w.shape[-1]
+    assert cols % 2 == 0
+    rows = w.size // cols
+    packed = np.empty(w.shape[:-1] + (cols // 2,), np.uint8)
+    s = np.empty(w.shape[:-1], np.float32)
+    lib().oracle_quantize_rows_i4(_p(w), rows, cols, _p(packed), _p(s))
+    return packed, s
+
+
+def unpack_i4(packed):
+    """int8 codes [..., 2 * bytes] of a packed INT4 matrix."""
+    pk = np.ascontiguousarray(packed, np.uint8)
+    cols = 2 * pk.shape[-1]
+    rows = pk.size // pk.shape[-1]
+    q = np.empty(pk.shape[:-1] + (cols,), np.int8)
+    lib().oracle_unpack_i4(_p(pk), rows, cols, _p(q))
+    return q
 
 
 def expert_row_q8(kind, x_row, q1, s1, b1, q2, s2, b2, d, F):

@@ -576,6 +576,93 @@ def test_int8_expert_equals_bf16_expert_on_exactly_representable_weights(kind, F
 
 
 # --------------------------------------------------------------------------
+# weight-only INT4 experts (same page and section): s = max|w| / 7, q = rne(w / s) in
+# [-7, 7], two codes per byte (even column in the low nibble, 4-bit two's complement)
+# --------------------------------------------------------------------------
+
+def test_int4_packing_worked_example():
+    # max 7 -> s = 1; 3.5 and 2.5 are ties (to 4 and 2), -2.5 and -3.5 too (to -2 and -4)
+    w = _bf16_bits([[7.0, -7.0, 1.0, -2.0, 3.5, 2.5, 0.0, 6.0, -2.5, -3.5]])
+    packed, s = orc.quantize_rows_i4(w)
+    assert s[0] == 1.0
+    # codes 7,-7 | 1,-2 | 4,2 | 0,6 | -2,-4 as (low, high) nibbles
+    assert packed[0].tolist() == [0x97, 0xE1, 0x24, 0x60, 0xCE]
+    assert orc.unpack_i4(packed)[0].tolist() == [7, -7, 1, -2, 4, 2, 0, 6, -2, -4]
+
+
+def test_int4_unpack_covers_every_nibble():
+    # nibble v means v for v < 8 and v - 16 otherwise, low nibble first
+    packed = np.arange(256, dtype=np.uint8).reshape(1, 256)
+    q = orc.unpack_i4(packed)[0].astype(np.int64)
+    v = np.arange(256)
+    signed = lambda n: np.where(n < 8, n, n - 16)
+    assert np.array_equal(q[0::2], signed(v & 15))
+    assert np.array_equal(q[1::2], signed(v >> 4))
+
+
+def test_int4_quantize_on_the_grid_is_exact():
+    rng = np.random.default_rng(11)
+    m = rng.integers(-7, 8, size=(6, 40))
+    m[:, 5] = 7 * np.array([1, -1, 1, -1, 1, -1])
+    scales = 2.0 ** np.array([-9, -3, 0, 3, -14, -1])
+    w = _bf16_bits(m * scales[:, None])
+    packed, s = orc.quantize_rows_i4(w)
+    assert packed.shape == (6, 20)
+    assert np.array_equal(s, scales.astype(np.float32) * np.float32(1.0))
+    assert np.array_equal(orc.unpack_i4(packed).astype(np.int64), m)
+
+
+def test_int4_quantize_bound_max_and_zero_row():
+    rng = np.random.default_rng(12)
+    vals = rng.standard_normal((50, 64)).astype(np.float32) * rng.uniform(0.01, 10, (50, 1))
+    vals[9] = 0.0
+    w = _bf16_bits(vals)
+    wf = bf16_bits_to_f64(w)
+    packed, s = orc.quantize_rows_i4(w)
+    q = orc.unpack_i4(packed)
+    assert s[9] == 0.0 and not packed[9].any()
+    assert q.min() >= -7 and q.max() <= 7             # -8 is never produced
+    for r in range(50):
+        if r == 9:
+            continue
+        amax = np.abs(wf[r]).max()
+        assert s[r] == np.float32(np.float32(amax) / np.float32(7.0))
+        assert np.abs(q[r]).max() == 7
+        err = np.abs(wf[r] - s[r].astype(np.float64) * q[r])
+        # nearest code in [-7, 7], up to the fp32 rounding of w / s (|w / s| < 8)
+        assert (err <= s[r] * (0.5 + 2.0 ** -20)).all()
+
+
+@pytest.mark.parametrize("kind,F", [(orc.GELU, 48), (orc.SWIGLU, 32)])
+def test_int4_expert_equals_bf16_expert_on_exactly_representable_weights(kind, F):
+    # the INT4 expert is the INT8 expert on the unpacked codes; with power-of-two scales
+    # every s * q is a bf16 value and the result equals the bf16 expert's bit for bit
+    rng = np.random.default_rng(100 + kind + F)
+    d = 24
+    N1 = F if kind == orc.GELU else 2 * F
+    m1 = rng.integers(-7, 8, (N1, d))
+    m2 = rng.integers(-7, 8, (d, F))
+    m1[:, 0] = 7 * rng.choice([-1, 1], N1)     # every row reaches 7: the scale is s itself
+    m2[:, 0] = 7 * rng.choice([-1, 1], d)
+    s1 = (2.0 ** rng.integers(-9, -2, N1)).astype(np.float32)
+    s2 = (2.0 ** rng.integers(-9, -2, d)).astype(np.float32)
+    w1 = _bf16_bits(s1[:, None] * m1)
+    w2 = _bf16_bits(s2[:, None] * m2)
+    p1, t1 = orc.quantize_rows_i4(w1)
+    p2, t2 = orc.quantize_rows_i4(w2)
+    q1, q2 = orc.unpack_i4(p1), orc.unpack_i4(p2)
+    assert np.array_equal(t1[:, None].astype(np.float64) * q1, s1[:, None].astype(np.float64) * m1)
+    assert np.array_equal(t2[:, None].astype(np.float64) * q2, s2[:, None].astype(np.float64) * m2)
+    b1 = rng.standard_normal(N1).astype(np.float32)
+    b2 = rng.standard_normal(d).astype(np.float32)
+    for t in range(4):
+        x = _bf16_bits(rng.standard_normal(d))
+        a = orc.expert_row_q8(kind, x, q1, t1, b1, q2, t2, b2, d, F)
+        b = orc.expert_row(kind, x, w1, b1, w2, b2, d, F)
+        assert np.array_equal(a, b)
+
+
+# --------------------------------------------------------------------------
 # overflow variants: re-routing to the next-ranked expert, overflow weight to the
 # shared expert ("MoE 并行" 推理时的负载均衡 and Q4; adv12 Q2)
 # --------------------------------------------------------------------------
