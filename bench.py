@@ -127,10 +127,11 @@ def kernel_algorithmic_cost(wl, name, P, touched):
     es = 2 if wl.bf16 else 4
     T, d, F, E = wl.T, wl.d, wl.F, wl.E
     N1 = wl.N1
-    name = re.sub(r"_q8t?_", "_", name)     # INT8-weight kernels: same algorithm
-    we = 1 if wl.int8 else 2               # bytes per expert weight
-    sc1 = 4 * N1 if wl.int8 else 0         # per-row scales of one expert
-    sc2 = 4 * d if wl.int8 else 0
+    name = re.sub(r"_q[48]t?_", "_", name)  # INT8 / INT4-weight kernels: same algorithm
+    quant = wl.int8 or wl.int4
+    we = 1 if wl.int8 else (0.5 if wl.int4 else 2)   # bytes per expert weight
+    sc1 = 4 * N1 if quant else 0           # per-row scales of one expert
+    sc2 = 4 * d if quant else 0
     up = {"grouped_gemm_gelu", "grouped_gemm_swiglu"}
     if name in up:
         fl = 2.0 * P * d * N1
@@ -168,6 +169,8 @@ def kernel_algorithmic_cost(wl, name, P, touched):
 
 KERNEL_FILES = {
     "grouped_gemm_q8t": ["grouped_gemm_q8t.cuh", "grouped_gemm_q8.cuh", "grouped_gemm.cuh",
+                         "common.cuh"],
+    "grouped_gemm_q4t": ["grouped_gemm_q8t.cuh", "grouped_gemm_q8.cuh", "grouped_gemm.cuh",
                          "common.cuh"],
     "grouped_gemm_q8": ["grouped_gemm_q8.cuh", "grouped_gemm.cuh", "common.cuh"],
     "grouped_gemm": ["grouped_gemm.cuh", "common.cuh"],
@@ -249,6 +252,11 @@ def cpu_oracle_sample(wl, sample_tokens, seed=0):
             q1, s1 = orc.quantize_rows_i8(w1)
             q2, s2 = orc.quantize_rows_i8(w2)
             return lambda xr: orc.expert_row_q8(wl.kind_code, xr, q1, s1, b1, q2, s2, b2, wl.d, wl.F)
+        if wl.int4:
+            p1, s1 = orc.quantize_rows_i4(w1)
+            p2, s2 = orc.quantize_rows_i4(w2)
+            q1, q2 = orc.unpack_i4(p1), orc.unpack_i4(p2)
+            return lambda xr: orc.expert_row_q8(wl.kind_code, xr, q1, s1, b1, q2, s2, b2, wl.d, wl.F)
         return lambda xr: orc.expert_row(wl.kind_code, xr, w1, b1, w2, b2, wl.d, wl.F)
     Wc = {e: expert_fn(e) for e in need}
     shared = expert_fn(0, True) if wl.has_shared else None
@@ -288,7 +296,8 @@ def workload_config(wl, world):
             "kind": wl.kind, "capacity_factor": wl.cf, "shared_expert": wl.has_shared,
             "residual": wl.add_residual,
             "expert_groups": [wl.n_group, wl.topk_group] if wl.n_group else None,
-            "expert_weights": "int8 codes + fp32 row scales" if wl.int8 else "bf16",
+            "expert_weights": ("int8 codes + fp32 row scales" if wl.int8 else
+                               "int4 codes (2 per byte) + fp32 row scales" if wl.int4 else "bf16"),
             "overflow": wl.overflow,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
@@ -364,8 +373,8 @@ def run_ours(args, wl):
     cfg = moe.config_for(wl)
     layer = moe.MoELayer(cfg, inp["wg"], inp["gate_bias"], inp["w1"], inp["b1"], inp["w2"],
                          inp["b2"], inp["shared"])
-    if wl.int8:
-        # the layer holds the INT8 codes; the bf16 originals are no longer needed
+    if wl.int8 or wl.int4:
+        # the layer holds the INT8 / INT4 codes; the bf16 originals are no longer needed
         inp["w1"] = inp["w2"] = inp["shared"] = None
         torch.cuda.synchronize()
         torch.cuda.empty_cache()

@@ -59,7 +59,7 @@ typedef enum {
     MOE_ERR_DEVICE_INDEX = 7   /* a kernel saw an expert id outside [0,E) and skipped it */
 } moe_status;
 
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_I8 = 2 } moe_dtype;
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_I8 = 2, MOE_I4 = 3 } moe_dtype;
 
 /* Expert FFN forms.
  *  LINEAR : y = W1 x + b1; W1 [E][d][d] fp32 (the tutorial's nn.Linear(d, d) experts).
@@ -107,7 +107,9 @@ typedef struct {
                                   only): weight-only INT8 experts ["MoE 混合专家架构" 5.3 量化支持]:
                                   w1/w2 hold int8 codes q and s1/s2 one fp32 scale per weight
                                   row; the experts compute with s[n] * q[n][k] (see
-                                  moe_quantize_i8). Routed and shared experts alike. */
+                                  moe_quantize_i8). Routed and shared experts alike.
+                                  MOE_I4: the same with 4-bit codes in [-7, 7], two per byte
+                                  (w1 [E][N1][d/2], w2 [E][d][F/2] bytes; see moe_quantize_i4). */
     int32_t overflow;          /* moe_overflow; 0 = MOE_OVERFLOW_DROP */
 } moe_config;
 
@@ -119,8 +121,8 @@ typedef struct {
     const float* b1;
     const void* w2;
     const float* b2;
-    const float* s1;   /* w_dtype == MOE_I8: scales [E][N1] of the w1 rows, else ignored */
-    const float* s2;   /* w_dtype == MOE_I8: scales [E][d] of the w2 rows, else ignored */
+    const float* s1;   /* MOE_I8 / MOE_I4 weights: scales [E][N1] of the w1 rows, else ignored */
+    const float* s2;   /* MOE_I8 / MOE_I4 weights: scales [E][d] of the w2 rows, else ignored */
 } moe_expert_weights;
 
 /* Bytes of scratch needed by any entry point below for this configuration
@@ -259,6 +261,16 @@ moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_idx, 
  * and scale 0 / codes 0 for an all-zero row. q [rows, cols] int8 and scale [rows] fp32 are
  * caller-owned device buffers. Stacked expert weights [E][N][K] are E*N rows of K. */
 moe_status moe_quantize_i8(const void* w, int64_t rows, int32_t cols, int8_t* q, float* scale,
+                           cudaStream_t stream);
+
+/* Weight-only INT4 codes of bf16 weights [the same reading with 4-bit codes, used by MOE_I4
+ * experts]: for every row r of w [rows, cols] (bf16, cols a multiple of 32):
+ *   scale[r] = max_c |w[r][c]| / 7   (fp32)
+ *   code(r, c) = round-half-even(w[r][c] / scale[r]) clamped to [-7, 7]   (fp32 division)
+ * and scale 0 / codes 0 for an all-zero row. q [rows, cols / 2] bytes: byte j of row r holds
+ * code(r, 2j) in its low nibble and code(r, 2j+1) in its high nibble, each as a 4-bit two's
+ * complement. q and scale [rows] fp32 are caller-owned device buffers. */
+moe_status moe_quantize_i4(const void* w, int64_t rows, int32_t cols, uint8_t* q, float* scale,
                            cudaStream_t stream);
 
 /* Host-only load report [adv12 3.3 EPLB, 4.2 expert_imbalance, 4.3 eplb_rebalance]:

@@ -40,6 +40,7 @@ class Workload:
     gate_bias: str = "none"     # "none" | "zipf" | "hot" (+20 on expert 0: one expert takes all)
     expert_bias: bool = False
     int8: bool = False          # weight-only INT8 experts (codes + per-row scales)
+    int4: bool = False          # weight-only INT4 experts (packed codes + per-row scales)
     n_group: int = 0            # group-limited routing: expert groups (0 = plain top-k)
     topk_group: int = 0         # groups kept per token
     overflow: str = "drop"      # over-capacity slots: "drop" | "shared" | "reroute"
@@ -191,11 +192,13 @@ class Workload:
         return fl
 
     def bytes(self, touched_experts):
-        """Weights of touched experts + gate weights + x read + out written (INT8 experts:
-        one byte per weight plus a 4-byte scale per weight row)."""
+        """Weights of touched experts + gate weights + x read + out written (INT8 / INT4
+        experts: one / half a byte per weight plus a 4-byte scale per weight row)."""
         es = 2 if self.bf16 else 4
         if self.int8:
             per = (self.N1 * self.d + self.w2_per_expert) + 4 * (self.N1 + self.d)
+        elif self.int4:
+            per = (self.N1 * self.d + self.w2_per_expert) // 2 + 4 * (self.N1 + self.d)
         else:
             per = (self.N1 * self.d + self.w2_per_expert) * es
         b = touched_experts * per + self.d * self.E * 4 + 2 * self.T * self.d * es
@@ -247,6 +250,19 @@ WORKLOADS = {
     "decode8_i8_e32": Workload("decode8_i8_e32", T=8, d=7168, E=32, k=8, F=2048, kind="swiglu",
                                act="bf16", gate_dist="uniform", int8=True,
                                note="decode, 8 tokens, INT8 weights, 32 experts (for profiling)"),
+    # weight-only INT4 experts (packed codes + per-row scales) for the decode-sized layers
+    "decode1_i4": Workload("decode1_i4", T=1, d=7168, E=256, k=8, F=2048, kind="swiglu",
+                           act="bf16", gate_dist="uniform", int4=True,
+                           note="decode, 1 token, INT4 expert weights"),
+    "decode8_i4": Workload("decode8_i4", T=8, d=7168, E=256, k=8, F=2048, kind="swiglu",
+                           act="bf16", gate_dist="uniform", int4=True,
+                           note="decode, 8 tokens, INT4 expert weights"),
+    "decode64_i4": Workload("decode64_i4", T=64, d=7168, E=256, k=8, F=2048, kind="swiglu",
+                            act="bf16", gate_dist="uniform", int4=True,
+                            note="decode, 64 tokens, INT4 expert weights"),
+    "decode8_i4_e32": Workload("decode8_i4_e32", T=8, d=7168, E=32, k=8, F=2048, kind="swiglu",
+                               act="bf16", gate_dist="uniform", int4=True,
+                               note="decode, 8 tokens, INT4 weights, 32 experts (for profiling)"),
     "decode1": Workload("decode1", T=1, d=7168, E=256, k=8, F=2048, kind="swiglu", act="bf16",
                         gate_dist="uniform", note="decode, 1 token"),
     "decode8": Workload("decode8", T=8, d=7168, E=256, k=8, F=2048, kind="swiglu", act="bf16",

@@ -65,14 +65,15 @@ class GpuRun:
         self.x_perm = torch.empty(Pmax, d, dtype=inp["x"].dtype, device=self.dev)
         moe.dispatch(cfg, self.idx, inp["x"], self.load, self.counts, self.offsets,
                      self.perm_token, self.perm_slot, self.slot_dest, self.x_perm, ws)
-        if wl.int8:
-            # INT8 experts: codes and row scales from the library's quantiser
-            self.q = moe.quantize_weights(inp["w1"], inp["w2"])
+        if wl.int8 or wl.int4:
+            # INT8 / INT4 experts: codes and row scales from the library's quantiser
+            bits = 8 if wl.int8 else 4
+            self.q = moe.quantize_weights(inp["w1"], inp["w2"], bits=bits)
             routed = moe.weights(self.q[0], inp["b1"], self.q[2], inp["b2"], self.q[1], self.q[3])
             shared = None
             if inp["shared"] is not None:
                 sw1, sb1, sw2, sb2 = inp["shared"]
-                self.sq = moe.quantize_weights(sw1, sw2)
+                self.sq = moe.quantize_weights(sw1, sw2, bits=bits)
                 shared = moe.weights(self.sq[0], sb1, self.sq[2], sb2, self.sq[1], self.sq[3])
         else:
             routed = moe.weights(inp["w1"], inp["b1"], inp["w2"], inp["b2"])
@@ -151,23 +152,27 @@ def check_dispatch(r, idx_ref):
 
 
 def _expert_fn(wl, e, shared=False):
-    """Oracle expert of the workload: bf16 weights, or their INT8 codes for INT8 layers."""
+    """Oracle expert of the workload: bf16 weights, or their INT8 / INT4 codes for quantised
+    layers (INT4 codes unpacked from the oracle's own packing)."""
     w1, b1, w2, b2 = (wl.w1_host(e, shared), wl.b1_host(e, shared), wl.w2_host(e, shared),
                       wl.b2_host(e, shared))
-    if wl.int8:
-        q1, s1 = orc.quantize_rows_i8(w1)
-        q2, s2 = orc.quantize_rows_i8(w2)
+    if wl.int8 or wl.int4:
+        q1, s1 = (orc.quantize_rows_i8 if wl.int8 else orc.quantize_rows_i4)(w1)
+        q2, s2 = (orc.quantize_rows_i8 if wl.int8 else orc.quantize_rows_i4)(w2)
+        if wl.int4:
+            q1, q2 = orc.unpack_i4(q1), orc.unpack_i4(q2)
         return lambda xr: orc.expert_row_q8(wl.kind_code, xr, q1, s1, b1, q2, s2, b2, wl.d, wl.F)
     return lambda xr: orc.expert_row(wl.kind_code, xr, w1, b1, w2, b2, wl.d, wl.F)
 
 
 def check_quantized_weights(r, experts):
-    """The library's INT8 codes and scales equal the oracle's, bit for bit."""
+    """The library's INT8 / INT4 codes and scales equal the oracle's, bit for bit."""
     wl = r.wl
     q1, s1, q2, s2 = r.q
+    quant = orc.quantize_rows_i8 if wl.int8 else orc.quantize_rows_i4
     for e in experts:
-        oq1, os1 = orc.quantize_rows_i8(wl.w1_host(e))
-        oq2, os2 = orc.quantize_rows_i8(wl.w2_host(e))
+        oq1, os1 = quant(wl.w1_host(e))
+        oq2, os2 = quant(wl.w2_host(e))
         assert np.array_equal(to_np(q1[e]), oq1) and np.array_equal(to_np(s1[e]), os1)
         assert np.array_equal(to_np(q2[e]), oq2) and np.array_equal(to_np(s2[e]), os2)
 
@@ -233,7 +238,7 @@ def full_check(wl, sample=None, seed=0):
     pt = to_np(r.perm_token)[:P]
     chk = np.arange(0, P, max(1, P // 512))
     assert np.array_equal(xp[chk], x_all[pt[chk]])
-    if wl.int8:
+    if wl.int8 or wl.int4:
         used = sorted({int(e) for e in idx_ref[rows].ravel()})
         check_quantized_weights(r, used[:8])
     ref = oracle_rows(wl, x_rows, rows, route_idx, w_ref, sd, {})

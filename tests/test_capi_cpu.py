@@ -134,6 +134,28 @@ def test_int8_weights_need_scales(lib):
     assert lib.moe_quantize_i8(ok, 0, 64, ok, ok, None) == C.MOE_OK
 
 
+def test_int4_weights_need_scales(lib):
+    cfg = api.make_config(64, 128, 4, 2, 128, 0.0, "gelu", True, int4_weights=True)
+    assert cfg.w_dtype == C.MOE_I4 and api.workspace_size(cfg) > 0
+    lin = api.make_config(64, 8, 4, 2, 0, 0.0, "linear", False, int4_weights=True)
+    assert api.workspace_size(lin) == 0                     # INT4 is for GELU / SwiGLU experts
+    with pytest.raises(ValueError):
+        api.make_config(64, 128, 4, 2, 128, int8_weights=True, int4_weights=True)
+    ok = ctypes.c_void_p(1 << 20)
+    bad = ctypes.c_void_p((1 << 20) + 4)
+    r = ctypes.byref(cfg)
+    w = C.MoeExpertWeights(w1=ok, b1=None, w2=ok, b2=None, s1=None, s2=ok)
+    assert lib.moe_forward(r, ok, ok, None, ctypes.byref(w), None, ok, None, None, None, ok,
+                           1 << 40, None) == C.MOE_ERR_INVALID_ARG
+    # the quantiser's own argument checks (no launch): a row of 32 codes is 16 bytes
+    assert lib.moe_quantize_i4(ok, 4, 48, ok, ok, None) == C.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_i4(ok, 4, 16, ok, ok, None) == C.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_i4(ok, -1, 64, ok, ok, None) == C.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_i4(ok, 4, 64, ok, None, None) == C.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_i4(ok, 4, 64, bad, ok, None) == C.MOE_ERR_MISALIGNED
+    assert lib.moe_quantize_i4(ok, 0, 64, ok, ok, None) == C.MOE_OK
+
+
 def test_overflow_policies(lib):
     for ov in ("drop", "shared", "reroute"):
         cfg = api.make_config(64, 128, 8, 2, 128, 1.0, "swiglu", True, has_shared=True,

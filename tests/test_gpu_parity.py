@@ -115,6 +115,23 @@ SMALL = {
     # K = 64: one half-filled 128-code K block (zero codes and activations past the end)
     "i8t_k64": W("q8t5", T=10, d=64, E=4, k=2, F=64, kind="swiglu", act="bf16",
                  expert_bias=True, has_shared=True, int8=True),
+    # weight-only INT4 experts (weight-streaming kernel, one 256-code stage per two MMA K
+    # blocks): K tails inside a stage (d = 192, F = 320: a stage with one K block), ragged
+    # feature tiles, many rows per expert, split-K with a split ending inside a stage
+    "i4_swiglu_bias_shared": W("q4a", T=24, d=256, E=16, k=4, F=192, kind="swiglu",
+                               act="bf16", expert_bias=True, has_shared=True, int4=True),
+    "i4_gelu_two_tiles": W("q4b", T=64, d=192, E=4, k=2, F=320, kind="gelu", act="bf16",
+                           expert_bias=True, has_shared=True, int4=True),
+    "i4_top1_cap_res": W("q4c", T=1000, d=128, E=4, k=1, F=320, kind="gelu", act="bf16",
+                         cf=1.25, add_residual=True, int4=True),
+    "i4_split_swiglu_shared": W("q4d", T=3, d=2112, E=8, k=2, F=256, kind="swiglu",
+                                act="bf16", expert_bias=True, has_shared=True, int4=True),
+    "i4_hot_cap_res": W("q4e", T=40, d=128, E=8, k=1, F=128, kind="gelu", act="bf16",
+                        cf=0.5, gate_bias="hot", add_residual=True, int4=True),
+    "i4_k64": W("q4f", T=10, d=64, E=4, k=2, F=64, kind="swiglu", act="bf16",
+                expert_bias=True, has_shared=True, int4=True),
+    "i4_reroute_k4": W("q4g", T=48, d=256, E=16, k=4, F=128, kind="swiglu", act="bf16",
+                       cf=0.5, gate_bias="zipf", int4=True, overflow="reroute"),
 }
 
 
@@ -200,6 +217,7 @@ def test_forward_is_deterministic():
     ("deepseek_grouped", 4),
     ("decode1", None), ("decode8", 4), ("decode64", 4),
     ("decode1_i8", None), ("decode8_i8", 4), ("decode64_i8", 4), ("deepseek_reroute", 4),
+    ("decode1_i4", None), ("decode8_i4", 4), ("decode64_i4", 4),
 ])
 def test_full_size_sampled(name, sample):
     r, stats = full_check(get(name), sample=sample, seed=1)
@@ -335,11 +353,51 @@ def test_int8_layer_object_quantises_bf16_weights():
     assert torch.equal(layer(inp["x"]), r.out)
 
 
+def test_int4_quantiser_matches_oracle_bitwise():
+    import oracle as orc
+    g = torch.Generator(device="cpu").manual_seed(12)
+    w = (torch.randn(37, 192, generator=g) * torch.rand(37, 1, generator=g) * 4)
+    w[3] = 0.0                        # all-zero row: scale 0, codes 0
+    w[5, :] = -0.25                   # constant row: every code -7
+    w[6] = 0.0
+    w[6, 7] = 1e-30                   # one tiny value among zeros: code 7 (high nibble)
+    w = w.to(torch.bfloat16)
+    q = torch.empty(37, 96, dtype=torch.uint8, device="cuda")
+    s = torch.empty(37, dtype=torch.float32, device="cuda")
+    moe.quantize_i4(w.cuda(), q, s)
+    oq, os_ = orc.quantize_rows_i4(to_np(w))
+    assert np.array_equal(to_np(q), oq)
+    assert np.array_equal(to_np(s), os_)
+    assert (to_np(q)[5] == 0x99).all() and (to_np(q)[3] == 0).all() and to_np(s)[3] == 0
+    assert to_np(q)[6, 3] == 0x70
+
+
+def test_int4_layer_object_quantises_bf16_weights():
+    wl = SMALL["i4_swiglu_bias_shared"]
+    r = GpuRun(wl).run()
+    inp = r.inp
+    layer = moe.MoELayer(r.cfg, inp["wg"], inp["gate_bias"], inp["w1"], inp["b1"], inp["w2"],
+                         inp["b2"], inp["shared"])
+    assert torch.equal(layer(inp["x"]), r.out)
+
+
+def test_int4_split_k_ends_inside_a_code_stage():
+    # d = 2112: 8.25 code stages of 256; the up projections split K in two, the second
+    # split ending half-way through its last stage
+    moe.profile_begin()
+    GpuRun(SMALL["i4_split_swiglu_shared"]).run()
+    stats = moe.profile_end()
+    assert "splitk_reduce_swiglu" in stats, sorted(stats)
+
+
 @pytest.mark.parametrize("name,prefix", [("i8_split_swiglu_bias_shared", "grouped_gemm_q8t_"),
                                          ("i8t_gelu_two_tiles", "grouped_gemm_q8t_"),
-                                         ("i8_swiglu_zipf_shared", "grouped_gemm_q8_")])
+                                         ("i8_swiglu_zipf_shared", "grouped_gemm_q8_"),
+                                         ("i4_top1_cap_res", "grouped_gemm_q4t_"),
+                                         ("i4_swiglu_bias_shared", "grouped_gemm_q4t_")])
 def test_int8_uses_the_int8_kernels(name, prefix):
-    # few rows per expert: the weight-streaming kernel; otherwise the shared-memory one
+    # INT8 with few rows per expert: the weight-streaming kernel; otherwise the
+    # shared-memory one. INT4: always the weight-streaming kernel.
     moe.profile_begin()
     GpuRun(SMALL[name]).run()
     stats = moe.profile_end()

@@ -20,7 +20,7 @@ MOE_ERR_TIMEOUT = 6
 MOE_ERR_DEVICE_INDEX = 7
 
 # moe_dtype / moe_expert_kind
-MOE_F32, MOE_BF16, MOE_I8 = 0, 1, 2
+MOE_F32, MOE_BF16, MOE_I8, MOE_I4 = 0, 1, 2, 3
 MOE_EXPERT_LINEAR, MOE_EXPERT_GELU, MOE_EXPERT_SWIGLU = 0, 1, 2
 MOE_OVERFLOW_DROP, MOE_OVERFLOW_SHARED, MOE_OVERFLOW_REROUTE = 0, 1, 2
 
@@ -73,6 +73,7 @@ def load():
         "moe_grouped_gemm": (i32, [vp, i64, vp, i32, i32, i32, vp, vp, vp, vp]),
         "moe_load_report": (i32, [vp, i32, i32, vp, vp, vp]),
         "moe_quantize_i8": (i32, [vp, i64, i32, vp, vp, vp]),
+        "moe_quantize_i4": (i32, [vp, i64, i32, vp, vp, vp]),
         "moe_last_device_status": (i32, [vp]),
         "moe_status_string": (ctypes.c_char_p, [i32]),
         "moe_profile_begin": (i32, []),

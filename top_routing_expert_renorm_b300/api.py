@@ -45,15 +45,19 @@ OVERFLOW = {"drop": C.MOE_OVERFLOW_DROP, "shared": C.MOE_OVERFLOW_SHARED,
 
 def make_config(T, d, E, top_k, F=0, capacity_factor=0.0, kind="gelu", bf16=True,
                 has_shared=False, add_residual=False, n_group=0, topk_group=0, int8_weights=False,
-                overflow="drop"):
-    """overflow: "drop", "shared" (dropped weight to the shared expert) or "reroute"."""
+                overflow="drop", int4_weights=False):
+    """overflow: "drop", "shared" (dropped weight to the shared expert) or "reroute".
+    int8_weights / int4_weights: weight-only INT8 / INT4 experts (codes + row scales)."""
+    if int8_weights and int4_weights:
+        raise ValueError("int8_weights and int4_weights exclude each other")
     kinds = {"linear": C.MOE_EXPERT_LINEAR, "gelu": C.MOE_EXPERT_GELU,
              "swiglu": C.MOE_EXPERT_SWIGLU}
     return MoeConfig(T=T, d=d, E=E, top_k=top_k, F=F, capacity_factor=capacity_factor,
                      act_dtype=C.MOE_BF16 if bf16 else C.MOE_F32, kind=kinds[kind],
                      has_shared=int(bool(has_shared)), add_residual=int(bool(add_residual)),
                      n_group=n_group, topk_group=topk_group,
-                     w_dtype=C.MOE_I8 if int8_weights else 0, overflow=OVERFLOW[overflow])
+                     w_dtype=C.MOE_I8 if int8_weights else (C.MOE_I4 if int4_weights else 0),
+                     overflow=OVERFLOW[overflow])
 
 
 def config_for(workload, T=None):
@@ -62,26 +66,42 @@ def config_for(workload, T=None):
                        workload.F if workload.kind != "linear" else 0, workload.cf,
                        workload.kind, workload.bf16, workload.has_shared, workload.add_residual,
                        workload.n_group, workload.topk_group, workload.int8,
-                       workload.overflow)
+                       workload.overflow, workload.int4)
 
 
 def weights(w1, b1=None, w2=None, b2=None, s1=None, s2=None):
-    """Expert weights; for INT8 experts w1 / w2 are the int8 codes and s1 / s2 their
-    per-row fp32 scales (see quantize_i8)."""
+    """Expert weights; for INT8 / INT4 experts w1 / w2 are the codes and s1 / s2 their
+    per-row fp32 scales (see quantize_i8, quantize_i4)."""
     return MoeExpertWeights(w1=_ptr(w1), b1=_ptr(b1), w2=_ptr(w2), b2=_ptr(b2), s1=_ptr(s1),
                             s2=_ptr(s2))
 
 
-def quantize_weights(w1, w2, stream=None):
-    """INT8 codes and per-row scales of stacked bf16 expert weights: (q1, s1, q2, s2)."""
+def quantize_weights(w1, w2, stream=None, bits=8):
+    """INT8 (bits=8) or packed INT4 (bits=4) codes and per-row scales of stacked bf16 expert
+    weights: (q1, s1, q2, s2)."""
     import torch
     out = []
     for w in (w1, w2):
-        q = torch.empty(w.shape, dtype=torch.int8, device=w.device)
         s = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
-        quantize_i8(w, q, s, stream)
+        if bits == 8:
+            q = torch.empty(w.shape, dtype=torch.int8, device=w.device)
+            quantize_i8(w, q, s, stream)
+        elif bits == 4:
+            q = torch.empty(w.shape[:-1] + (w.shape[-1] // 2,), dtype=torch.uint8, device=w.device)
+            quantize_i4(w, q, s, stream)
+        else:
+            raise ValueError("bits must be 8 or 4")
         out += [q, s]
     return tuple(out)
+
+
+def quantize_i4(w, q, scale, stream=None):
+    """Per-row absmax INT4 codes of a bf16 tensor (rows = all but the last axis, a multiple
+    of 32 wide) into the uint8 tensor q (last axis halved: column 2j in the low nibble of
+    byte j) and the fp32 tensor scale (one value per row)."""
+    cols = w.shape[-1]
+    _check(C.load().moe_quantize_i4(_ptr(w), w.numel() // cols, cols, _ptr(q), _ptr(scale),
+                                    _stream(stream)), "moe_quantize_i4")
 
 
 def quantize_i8(w, q, scale, stream=None):

@@ -422,4 +422,37 @@ __global__ void __launch_bounds__(256) quantize_rows_i8_kernel(const __nv_bfloat
     }
 }
 
+// ---- per-row absmax INT4 quantisation of bf16 weights --------------------------------
+// One warp per row: s = max|w| / 7 (fp32), q = rne(w / s) clamped to [-7, 7]; s = 0 and
+// q = 0 for an all-zero row. Two codes per byte (column 2j in the low nibble of byte j,
+// 4-bit two's complement); cols is even, a row takes cols / 2 bytes.
+__global__ void __launch_bounds__(256) quantize_rows_i4_kernel(const __nv_bfloat16* __restrict__ w,
+                                                               long long rows, int cols,
+                                                               uint8_t* __restrict__ q,
+                                                               float* __restrict__ scale) {
+    pdl_entry();
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
+         r += warps) {
+        const __nv_bfloat16* wr = w + r * cols;
+        float m = 0.0f;
+        for (int c = lane; c < cols; c += 32) m = fmaxf(m, fabsf(__bfloat162float(wr[c])));
+#pragma unroll
+        for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        const float s = __fdiv_rn(m, 7.0f);
+        if (lane == 0) scale[r] = s;
+        uint8_t* qr = q + r * (cols / 2);
+        for (int j = lane; j < cols / 2; j += 32) {
+            int v[2] = {0, 0};
+            if (s > 0.0f) {
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+                    v[u] = max(-7, min(7, __float2int_rn(__fdiv_rn(__bfloat162float(wr[2 * j + u]), s))));
+            }
+            qr[j] = (uint8_t)((v[0] & 15) | ((v[1] & 15) << 4));
+        }
+    }
+}
+
 }  // namespace moe

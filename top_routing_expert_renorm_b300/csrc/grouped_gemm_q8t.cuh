@@ -1,6 +1,7 @@
-// Grouped GEMM with weight-only INT8 weights for groups of few rows (decode).
+// Grouped GEMM with weight-only INT8 or INT4 weights for groups of few rows (decode).
 //
-// "MoE 混合专家架构" 5.3 量化支持: INT8 expert weights, D[r][n] = s[n] * sum_k A[r][k] * q[n][k].
+// "MoE 混合专家架构" 5.3 量化支持: INT8 / INT4 expert weights,
+// D[r][n] = s[n] * sum_k A[r][k] * q[n][k].
 // With a handful of token rows per expert the layer is a stream of weight codes; widening
 // the codes in shared memory (grouped_gemm_q8_kernel) costs six bytes of shared-memory
 // traffic per code and caps the stream below the HBM rate. Here the roles of the operands
@@ -15,7 +16,10 @@
 // each weight row is read from HBM in 128-byte pieces. TMEM columns: accumulator a, half
 // h at a*64 + h*32; widened A stage c, half h at 128 + c*128 + h*64 (64 columns = 128 bf16
 // of K). A K tail of 64 reads zero codes and zero activations past the end of the rows.
-//   warp 0       unit scheduler + TMA of the int8 codes (two 128-row boxes of 128 bytes,
+// INT4 codes (BITS = 4) are packed two per byte along K (even k in the low nibble), so a
+// 128-byte box row holds 256 codes: each code stage then feeds two TMEM stages of 128
+// codes, and K splits start on a code stage (an even number of 128-code blocks).
+//   warp 0       unit scheduler + TMA of the codes (two 128-row boxes of 128 bytes,
 //                128-byte swizzle) into a QT_NQ-deep ring;
 //   warp 1       MMA issuer (A from TMEM, B from shared memory);
 //   warps 2-5    epilogue: lane = weight row (output feature), column = activation row;
@@ -43,6 +47,27 @@ static_assert(QT_A_COL + QT_NC * 2 * (QT_BK / 4) <= QT_TMEM_COLS, "TMEM columns 
 
 __host__ __device__ constexpr int gm_q8t_smem_bytes(int G) {
     return 1024 + QT_RING_BYTES + QT_HDR_BYTES + 2 * (G + 1) * 4;
+}
+
+// Four-bit codes -> bf16, exactly and without conversion instructions: nibble v (two's
+// complement code q) xor 8 is u = q + 8 in 0..15; the bf16 pattern 0x4300 | u is 128 + u
+// (bf16 keeps 7 fraction bits, enough for 4), and subtracting 136 leaves q. Word w holds
+// codes k..k+7 of a row (nibble i = code k+i); the mask pairs nibbles i and i+4 in the
+// two halves of a word, and a byte permute re-pairs them as (k+2j, k+2j+1).
+__device__ __forceinline__ void widen8_i4(uint32_t w, uint32_t (&o)[4]) {
+    constexpr uint32_t k136 = 0x43084308u;   // bf16 136.0 in both halves
+    uint32_t pr[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t b = ((w >> (4 * i)) & 0x000F000Fu) ^ k136;   // 128 + u of (k+i, k+i+4)
+        const __nv_bfloat162 v = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&b),
+                                         *reinterpret_cast<const __nv_bfloat162*>(&k136));
+        pr[i] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    o[0] = __byte_perm(pr[0], pr[1], 0x5410);   // (k, k+1)
+    o[1] = __byte_perm(pr[2], pr[3], 0x5410);   // (k+2, k+3)
+    o[2] = __byte_perm(pr[0], pr[1], 0x7632);   // (k+4, k+5)
+    o[3] = __byte_perm(pr[2], pr[3], 0x7632);   // (k+6, k+7)
 }
 
 // One half of a unit's accumulator (32 activation rows of weight row / feature f) ->
@@ -80,13 +105,15 @@ __device__ __forceinline__ void qt_store_half(const GemmParams& p, const float (
     }
 }
 
-template <int EPI>
+template <int EPI, int BITS>
 __global__ void __launch_bounds__(QT_THREADS, 1)
     grouped_gemm_q8t_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmQ, const GemmParams p) {
     static_assert(EPI == EPI_GELU_BF16 || EPI == EPI_SWIGLU_BF16 || EPI == EPI_SCALE_F32 ||
                       EPI == EPI_F32,
                   "epilogue not supported by the swapped INT8 kernel");
+    static_assert(BITS == 8 || BITS == 4, "codes are 8 or 4 bits wide");
+    constexpr int KPQ = 8 / BITS;   // 128-code K blocks per code stage
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -222,7 +249,8 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
                 const int n0 = (EPI == EPI_SWIGLU_BF16) ? nb * 128 : nb * GM_BN;
                 const int b0 = g * p.b_rows_per_group + n0;
                 const int b1 = b0 + p.up_offset;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                // code stage kb holds 128-code blocks KPQ*kb .. KPQ*kb + KPQ-1 (x = kb * 128 bytes)
+                for (int kb = kb0 / KPQ; kb < (kb1 + KPQ - 1) / KPQ; ++kb) {
                     if (*s_abort || !mbar_wait(bar(QEMPTY + stage), ph ^ 1)) {
                         *s_abort = 1;
                         ok = false;
@@ -283,7 +311,7 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
                 if (last_par[s] >= 0) mbar_wait(bar(BFULL + s), (uint32_t)last_par[s]);
         }
     } else if (warp >= 7) {
-        // ---------------- converters: int8 codes -> bf16 A operand in TMEM -----------------
+        // ---------------- converters: int8 / int4 codes -> bf16 A operand in TMEM ----------
         const int qd = warp & 3, h = (warp - 7) >> 2;
         const int r = h * 128 + qd * 32 + lane;          // weight row of the stage
         const int sw = r & 7;                            // 128-byte swizzle of that row
@@ -303,6 +331,21 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
                 widen4(w.w, v[8 * c + 6], v[8 * c + 7]);
             }
         };
+        // 64 four-bit codes (chunks c0, c0+1 of the row) -> 32 bf16x2 columns
+        auto widen_half4 = [&](const uint8_t* row, int c0, uint32_t (&v)[32]) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const uint4 w = *reinterpret_cast<const uint4*>(row + (((c0 + c) ^ sw) << 4));
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t o[4];
+                    widen8_i4(ws[j], o);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) v[16 * c + 4 * j + i] = o[i];
+                }
+            }
+        };
         bool ok = true;
         while (ok) {
             long long t;
@@ -312,7 +355,10 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
             const int kb0 = ks * p.kb_per_split;
             const int kb1 = min(kblocks, kb0 + p.kb_per_split);
             for (int kb = kb0; kb < kb1; ++kb) {
-                const bool w_ok = !*s_abort && mbar_wait(bar(QFULL + qs), qph) &&
+                // sub: the 128-code block of the code stage. The stage's first block waits
+                // for the codes; its last block (or the unit's last) releases them.
+                const int sub = (kb - kb0) % KPQ;
+                const bool w_ok = !*s_abort && (sub != 0 || mbar_wait(bar(QFULL + qs), qph)) &&
                                   mbar_wait(bar(CEMPTY + cs), cph ^ 1);
                 if (!__all_sync(0xffffffffu, w_ok)) {
                     if (lane == 0) *s_abort = 1;
@@ -322,17 +368,23 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
                 tc_fence_after();
                 const uint8_t* row = q_tiles + qs * QT_Q_BYTES + r * QT_BK;
                 uint32_t v0[32], v1[32];
-                widen_half(row, 0, v0);
-                widen_half(row, 4, v1);
+                if constexpr (BITS == 8) {
+                    widen_half(row, 0, v0);
+                    widen_half(row, 4, v1);
+                } else {
+                    widen_half4(row, 4 * sub, v0);
+                    widen_half4(row, 4 * sub + 2, v1);
+                }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(QEMPTY + qs));   // codes consumed
+                const bool q_done = sub == KPQ - 1 || kb == kb1 - 1;
+                if (q_done && lane == 0) mbar_arrive(bar(QEMPTY + qs));   // codes consumed
                 tmem_store_32cols(t_lane + cs * 128, v0);
                 tmem_store_32cols(t_lane + cs * 128 + 32, v1);
                 tmem_store_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(CFULL + cs));
-                if (++qs == QT_NQ) {
+                if (q_done && ++qs == QT_NQ) {
                     qs = 0;
                     qph ^= 1;
                 }

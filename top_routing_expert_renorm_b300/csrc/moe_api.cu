@@ -187,7 +187,7 @@ moe_status check_cfg(const moe_config* c) {
         return MOE_ERR_INVALID_ARG;
     if (c->act_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
     if (c->w_dtype != 0 && c->w_dtype != c->act_dtype) {
-        if (c->w_dtype != MOE_I8) return MOE_ERR_INVALID_ARG;
+        if (c->w_dtype != MOE_I8 && c->w_dtype != MOE_I4) return MOE_ERR_INVALID_ARG;
         if (c->kind != MOE_EXPERT_GELU && c->kind != MOE_EXPERT_SWIGLU) return MOE_ERR_UNSUPPORTED;
     }
     if (c->overflow < MOE_OVERFLOW_DROP || c->overflow > MOE_OVERFLOW_REROUTE) return MOE_ERR_INVALID_ARG;
@@ -332,13 +332,29 @@ SplitPlan split_plan(long long max_mtiles, int n_tiles, int K, int sms, int bk =
     return sp;
 }
 
+// Weight-only quantised experts: codes plus one fp32 scale per weight row.
+bool quant_w(const moe_config& c) { return c.w_dtype == MOE_I8 || c.w_dtype == MOE_I4; }
+int code_bits(const moe_config& c) { return c.w_dtype == MOE_I4 ? 4 : 8; }
+
 // INT8 experts with few rows per group run the weight-streaming kernel
 // (grouped_gemm_q8t_kernel: operands swapped, 32-row activation tiles): the routed
 // experts when they average at most 32 rows, the shared expert up to 64 tokens.
+// INT4 experts always run it.
 bool q8t_routed(const moe_config& c) {
-    return c.w_dtype == MOE_I8 && (long long)c.T * c.top_k <= 32ll * c.E;
+    return c.w_dtype == MOE_I4 || (c.w_dtype == MOE_I8 && (long long)c.T * c.top_k <= 32ll * c.E);
 }
-bool q8t_shared(const moe_config& c) { return c.w_dtype == MOE_I8 && c.T <= 64; }
+bool q8t_shared(const moe_config& c) {
+    return c.w_dtype == MOE_I4 || (c.w_dtype == MOE_I8 && c.T <= 64);
+}
+
+// Split plan of a weight-streaming launch, in 128-code K blocks. An INT4 code stage holds
+// two of them and a split must start on one, so INT4 plans are made over 256-code blocks.
+SplitPlan qt_split_plan(long long max_mtiles, int n_tiles, int K, int sms, int bits) {
+    const int per = 8 / bits;
+    SplitPlan sp = split_plan(max_mtiles, n_tiles, K, sms, QT_BK * per);
+    sp.kbs *= per;
+    return sp;
+}
 
 // Upper bound on the M tiles of the routed experts: sum_e ceil(n_e / m) over the
 // non-empty experts <= P / m + min(E, P), m = 128 rows (32 for the weight-streaming
@@ -362,9 +378,9 @@ FfnPlan ffn_plan(const moe_config& c) {
     const int dn_nt = (c.d + GM_BN - 1) / GM_BN;
     const long long N1 = c.kind == MOE_EXPERT_SWIGLU ? 2ll * c.F : c.F;
     const long long mt = routed_mtiles_bound(c);
-    const int rbk = q8t_routed(c) ? QT_BK : GM_BK;
-    f.up = split_plan(mt, up_nt, c.d, sms, rbk);
-    f.down = split_plan(mt, dn_nt, c.F, sms, rbk);
+    const int bits = code_bits(c);
+    f.up = q8t_routed(c) ? qt_split_plan(mt, up_nt, c.d, sms, bits) : split_plan(mt, up_nt, c.d, sms);
+    f.down = q8t_routed(c) ? qt_split_plan(mt, dn_nt, c.F, sms, bits) : split_plan(mt, dn_nt, c.F, sms);
     auto need = [&](const SplitPlan& sp, long long rows, long long cols) {
         if (sp.S > 1) f.partial_floats = std::max<size_t>(f.partial_floats, (size_t)(sp.S * rows * cols));
     };
@@ -373,9 +389,10 @@ FfnPlan ffn_plan(const moe_config& c) {
     if (c.has_shared) {
         const int sm = q8t_shared(c) ? QT_NT : kMTile;
         const long long smt = (c.T + sm - 1) / sm;
-        const int sbk = q8t_shared(c) ? QT_BK : GM_BK;
-        f.sh_up = split_plan(smt, up_nt, c.d, sms, sbk);
-        f.sh_down = split_plan(smt, dn_nt, c.F, sms, sbk);
+        f.sh_up = q8t_shared(c) ? qt_split_plan(smt, up_nt, c.d, sms, bits)
+                                : split_plan(smt, up_nt, c.d, sms);
+        f.sh_down = q8t_shared(c) ? qt_split_plan(smt, dn_nt, c.F, sms, bits)
+                                  : split_plan(smt, dn_nt, c.F, sms);
         need(f.sh_up, c.T, N1);
         need(f.sh_down, c.T, c.d);
     }
@@ -540,12 +557,13 @@ const char* gemm_q8_name() {
 }
 
 template <int EPI>
-const char* gemm_q8t_name() {
+const char* gemm_q8t_name(int bits) {
+    const bool q4 = bits == 4;
     switch (EPI) {
-        case EPI_F32: return "grouped_gemm_q8t_f32";
-        case EPI_GELU_BF16: return "grouped_gemm_q8t_gelu";
-        case EPI_SWIGLU_BF16: return "grouped_gemm_q8t_swiglu";
-        default: return "grouped_gemm_q8t_scale";
+        case EPI_F32: return q4 ? "grouped_gemm_q4t_f32" : "grouped_gemm_q8t_f32";
+        case EPI_GELU_BF16: return q4 ? "grouped_gemm_q4t_gelu" : "grouped_gemm_q8t_gelu";
+        case EPI_SWIGLU_BF16: return q4 ? "grouped_gemm_q4t_swiglu" : "grouped_gemm_q8t_swiglu";
+        default: return q4 ? "grouped_gemm_q4t_scale" : "grouped_gemm_q8t_scale";
     }
 }
 
@@ -576,19 +594,24 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
                        int* r_idx = nullptr, float* r_w = nullptr, int r_E = 0, int r_Ep = 0,
                        const float* w_scale = nullptr, bool swap_ab = false,
                        int* r_hist = nullptr, const int32_t* a_gather = nullptr,
-                       int a_row_bytes = 0, float* r_part = nullptr, int* r_tile_cnt = nullptr) {
+                       int a_row_bytes = 0, float* r_part = nullptr, int* r_tile_cnt = nullptr,
+                       int w_bits = 8) {
     // r_part, r_tile_cnt (EPI_ROUTER_TOPK with sp.S == 2): the epilogue's split-K exchange
     // a_gather (bf16 kernel only): logical A row r (r < a_rows) is row a_gather[r] of A,
     // loaded by the kernel's gather warps
-    // w_scale != null: B holds int8 codes, one fp32 scale per B row (INT8 kernels); with
-    // swap_ab the weight-streaming INT8 kernel for few rows per group runs
+    // w_scale != null: B holds w_bits-wide codes (8: int8; 4: two per byte, even k in the
+    // low nibble), one fp32 scale per B row (INT8 / INT4 kernels); with swap_ab the
+    // weight-streaming kernel for few rows per group runs (INT4: only that kernel)
     if (a_rows <= 0 || G <= 0) return MOE_OK;
     if (G > GM_MAX_GROUPS) return MOE_ERR_UNSUPPORTED;
     swap_ab = swap_ab && w_scale != nullptr;
     if (swap_ab && !q8t_supports(EPI)) return MOE_ERR_UNSUPPORTED;
+    if (w_scale && w_bits != 8 && (w_bits != 4 || !swap_ab)) return MOE_ERR_UNSUPPORTED;
+    if (w_bits == 4 && sp.S > 1 && sp.kbs % 2 != 0) return MOE_ERR_UNSUPPORTED;
     CUtensorMap ta, tb;
     const bool gathered = a_gather && !w_scale;
-    if (swap_ab ? !make_tmap_i8(&tb, B, (uint64_t)b_rows_total, (uint64_t)K, GM_BN / 2, QT_BK,
+    const uint64_t b_cols = (w_scale && w_bits == 4) ? (uint64_t)K / 2 : (uint64_t)K;   // bytes
+    if (swap_ab ? !make_tmap_i8(&tb, B, (uint64_t)b_rows_total, b_cols, GM_BN / 2, QT_BK,
                                 CU_TENSOR_MAP_SWIZZLE_128B)
         : w_scale ? !make_tmap_i8(&tb, B, (uint64_t)b_rows_total, (uint64_t)K, GM_BN / 2)
                   : !make_tmap_bf16(&tb, B, (uint64_t)b_rows_total, (uint64_t)K, GM_BN / 2))
@@ -659,19 +682,20 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     const int grid = num_sms();
     if (swap_ab) {
         if constexpr (q8t_supports(EPI)) {
-            static std::once_flag qt_once[64];
-            static cudaError_t qt_err[64];
+            static std::once_flag qt_once[2][64];
+            static cudaError_t qt_err[2][64];
+            const int b4 = w_bits == 4 ? 1 : 0;
+            auto kern = b4 ? grouped_gemm_q8t_kernel<EPI, 4> : grouped_gemm_q8t_kernel<EPI, 8>;
             if (dev >= 0 && dev < 64) {
-                std::call_once(qt_once[dev], [&] {
-                    qt_err[dev] = cudaFuncSetAttribute(grouped_gemm_q8t_kernel<EPI>,
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       gm_q8t_smem_bytes(GM_MAX_GROUPS));
+                std::call_once(qt_once[b4][dev], [&] {
+                    qt_err[b4][dev] = cudaFuncSetAttribute(kern,
+                                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                           gm_q8t_smem_bytes(GM_MAX_GROUPS));
                 });
-                if (qt_err[dev] != cudaSuccess) return MOE_ERR_CUDA;
+                if (qt_err[b4][dev] != cudaSuccess) return MOE_ERR_CUDA;
             }
-            MOE_LAUNCH(name ? name : gemm_q8t_name<EPI>(), s,
-                       launch_k(grouped_gemm_q8t_kernel<EPI>, grid, QT_THREADS, gm_q8t_smem_bytes(G),
-                                s, ta, tb, p));
+            MOE_LAUNCH(name ? name : gemm_q8t_name<EPI>(w_bits), s,
+                       launch_k(kern, grid, QT_THREADS, gm_q8t_smem_bytes(G), s, ta, tb, p));
         }
     } else if (w_scale) {
         static std::once_flag q8_once[64];
@@ -823,8 +847,9 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
         MOE_LAUNCH("mtile_table", s,
                    launch_k(mtile_table_kernel, 1, 1024, 0, s, offsets, E, mtile, counters + kCntUp, 2));
     const int64_t N1 = n1_of(c);
-    // INT8 weights: per-row scales select the INT8 kernel
-    const bool q8 = c.w_dtype == MOE_I8;
+    // INT8 / INT4 weights: per-row scales select the quantised-weight kernels
+    const bool q8 = quant_w(c);
+    const int wb = code_bits(c);
     const float* rs1 = q8 ? R.s1 : nullptr;
     const float* rs2 = q8 ? R.s2 : nullptr;
     const bool swap_r = q8t_routed(c), swap_s = q8t_shared(c);
@@ -836,13 +861,13 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
                                              offsets, mtile, h, F, R.b1, nullptr, nullptr, nullptr,
                                              k, s, nullptr, fp.up, partial, counters + kCntUp,
                                              nullptr, nullptr, nullptr, 0, 0, rs1, swap_r, nullptr,
-                                             a_idx, d * 2));
+                                             a_idx, d * 2, nullptr, nullptr, wb));
     else
         MOE_TRY(launch_gemm<EPI_GELU_BF16>(a_up, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
                                            offsets, mtile, h, F, R.b1, nullptr, nullptr, nullptr, k,
                                            s, nullptr, fp.up, partial, counters + kCntUp, nullptr,
                                            nullptr, nullptr, 0, 0, rs1, swap_r, nullptr, a_idx,
-                                           d * 2));
+                                           d * 2, nullptr, nullptr, wb));
     if (fused_out)
         MOE_TRY(launch_gemm<EPI_COMBINE1_BF16>(h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets,
                                                mtile, fused_out, d, R.b2, topk_w, perm_token,
@@ -853,7 +878,8 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
         MOE_TRY(launch_gemm<EPI_SCALE_F32>(h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets,
                                            mtile, y, d, R.b2, topk_w, perm_token, perm_slot, k, s,
                                            nullptr, fp.down, partial, counters + kCntDown, nullptr,
-                                           nullptr, nullptr, 0, 0, rs2, swap_r));
+                                           nullptr, nullptr, 0, 0, rs2, swap_r, nullptr,
+                                           nullptr, 0, nullptr, nullptr, wb));
     if (c.has_shared) {
         MOE_LAUNCH("single_group_table", s,
                    launch_k(single_group_table_kernel, 1, 32, 0, s, T, shared_tab, shared_tab + 2,
@@ -863,17 +889,20 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
                                                  shared_tab + 2, hs, F, S->b1, nullptr, nullptr,
                                                  nullptr, k, s, nullptr, fp.sh_up, partial,
                                                  counters + kCntSharedUp, nullptr, nullptr,
-                                                 nullptr, 0, 0, q8 ? S->s1 : nullptr, swap_s));
+                                                 nullptr, 0, 0, q8 ? S->s1 : nullptr, swap_s,
+                                           nullptr, nullptr, 0, nullptr, nullptr, wb));
         else
             MOE_TRY(launch_gemm<EPI_GELU_BF16>(x, T, d, S->w1, N1, (int)N1, 1, F, shared_tab,
                                                shared_tab + 2, hs, F, S->b1, nullptr, nullptr,
                                                nullptr, k, s, nullptr, fp.sh_up, partial,
                                                counters + kCntSharedUp, nullptr, nullptr, nullptr,
-                                               0, 0, q8 ? S->s1 : nullptr, swap_s));
+                                               0, 0, q8 ? S->s1 : nullptr, swap_s,
+                                           nullptr, nullptr, 0, nullptr, nullptr, wb));
         MOE_TRY(launch_gemm<EPI_F32>(hs, T, F, S->w2, d, d, 1, d, shared_tab, shared_tab + 2,
                                      y_shared, d, S->b2, nullptr, nullptr, nullptr, k, s, nullptr,
                                      fp.sh_down, partial, counters + kCntSharedDown, nullptr,
-                                     nullptr, nullptr, 0, 0, q8 ? S->s2 : nullptr, swap_s));
+                                     nullptr, nullptr, 0, 0, q8 ? S->s2 : nullptr, swap_s,
+                                           nullptr, nullptr, 0, nullptr, nullptr, wb));
     }
     return MOE_OK;
 }
@@ -908,7 +937,7 @@ moe_status combine_impl(const moe_config& c, const void* x, const float* y,
 moe_status check_weights(const moe_config& c, const moe_expert_weights* W) {
     if (!W || !W->w1) return MOE_ERR_INVALID_ARG;
     if (c.kind != MOE_EXPERT_LINEAR && !W->w2) return MOE_ERR_INVALID_ARG;
-    if (c.w_dtype == MOE_I8 && (!W->s1 || !W->s2)) return MOE_ERR_INVALID_ARG;
+    if (quant_w(c) && (!W->s1 || !W->s2)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(W->w1) || !aligned16(W->w2) || !aligned16(W->b1) || !aligned16(W->b2) ||
         !aligned16(W->s1) || !aligned16(W->s2))
         return MOE_ERR_MISALIGNED;
@@ -1040,7 +1069,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate
     // bf16 experts with k >= 4: the up projection gathers its rows of x itself (no x_perm
     // copy, which is k times the size of x). With fewer slots per token the copy is cheaper
     // than the slower A loads of the gathering kernel (16-byte cp.async instead of TMA).
-    const bool gather_a = is_bf16_kind(c) && c.w_dtype != MOE_I8 && c.top_k >= 4;
+    const bool gather_a = is_bf16_kind(c) && !quant_w(c) && c.top_k >= 4;
     float* y = at<float>(ws, L.y);
     int32_t* mtile = at<int32_t>(ws, L.mtile);
     // Top-1 layers without a shared expert write the output from the down projection.
@@ -1110,6 +1139,19 @@ moe_status moe_quantize_i8(const void* w, int64_t rows, int32_t cols, int8_t* q,
         1, std::min<long long>((rows + 7) / 8, (long long)num_sms() * 16));
     MOE_LAUNCH("quantize_i8", stream,
                launch_k(quantize_rows_i8_kernel, blocks, 256, 0, stream,
+                        static_cast<const __nv_bfloat16*>(w), (long long)rows, (int)cols, q, scale));
+    return MOE_OK;
+}
+
+moe_status moe_quantize_i4(const void* w, int64_t rows, int32_t cols, uint8_t* q, float* scale,
+                           cudaStream_t stream) {
+    if (!w || !q || !scale || rows < 0 || cols < 32 || cols % 32 != 0) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(q) || !aligned16(scale)) return MOE_ERR_MISALIGNED;
+    if (rows == 0) return MOE_OK;
+    const int blocks = (int)std::max<long long>(
+        1, std::min<long long>((rows + 7) / 8, (long long)num_sms() * 16));
+    MOE_LAUNCH("quantize_i4", stream,
+               launch_k(quantize_rows_i4_kernel, blocks, 256, 0, stream,
                         static_cast<const __nv_bfloat16*>(w), (long long)rows, (int)cols, q, scale));
     return MOE_OK;
 }

@@ -10,18 +10,20 @@ class MoELayer:
     """One MoE layer. Tensors (all on one CUDA device, contiguous):
     W_gate [d, E] fp32, gate_bias [E] fp32 or None, w1 [E, N1, d], b1 [E, N1] or None,
     w2 [E, d, F] (not for LINEAR), b2 [E, d] or None, shared = (w1, b1, w2, b2[, s1, s2]) or
-    None; with INT8 experts w1 / w2 hold int8 codes and s1 [E, N1] / s2 [E, d] their scales.
+    None; with INT8 experts w1 / w2 hold int8 codes and s1 [E, N1] / s2 [E, d] their scales,
+    with INT4 experts w1 [E, N1, d/2] / w2 [E, d, F/2] the packed codes (uint8).
     The workspace is sized for up to `max_tokens` tokens per call."""
 
     def __init__(self, cfg, W_gate, gate_bias, w1, b1=None, w2=None, b2=None, shared=None,
                  s1=None, s2=None):
         import torch
         self.cfg = cfg
-        if cfg.w_dtype == api.C.MOE_I8 and w1.dtype == torch.bfloat16:
-            # bf16 weights for an INT8 layer: quantise them once (codes + per-row scales)
-            w1, s1, w2, s2 = api.quantize_weights(w1, w2)
+        bits = {api.C.MOE_I8: 8, api.C.MOE_I4: 4}.get(cfg.w_dtype)
+        if bits and w1.dtype == torch.bfloat16:
+            # bf16 weights for an INT8 / INT4 layer: quantise them once (codes + row scales)
+            w1, s1, w2, s2 = api.quantize_weights(w1, w2, bits=bits)
             if shared is not None:
-                sw1, ss1, sw2, ss2 = api.quantize_weights(shared[0], shared[2])
+                sw1, ss1, sw2, ss2 = api.quantize_weights(shared[0], shared[2], bits=bits)
                 shared = (sw1, shared[1], sw2, shared[3], ss1, ss2)
         self._keep = [W_gate, gate_bias, w1, b1, w2, b2, shared, s1, s2]
         self.W_gate, self.gate_bias = W_gate, gate_bias
