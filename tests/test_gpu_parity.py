@@ -395,7 +395,7 @@ def test_int4_split_k_ends_inside_a_code_stage():
                                          ("i8_swiglu_zipf_shared", "grouped_gemm_q8_"),
                                          ("i4_top1_cap_res", "grouped_gemm_q4t_"),
                                          ("i4_swiglu_bias_shared", "grouped_gemm_q4t_")])
-def test_int8_uses_the_int8_kernels(name, prefix):
+def test_quantised_layers_use_their_kernels(name, prefix):
     # INT8 with few rows per expert: the weight-streaming kernel; otherwise the
     # shared-memory one. INT4: always the weight-streaming kernel.
     moe.profile_begin()
