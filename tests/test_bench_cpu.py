@@ -1,0 +1,73 @@
+"""The benchmark's cost accounting (CPU only): the algorithmic FLOPs and bytes behind every
+roofline fraction, checked against totals worked out by hand from the layer's shapes.
+
+Per forward: FLOPs = 2*T*d*E (gate GEMM) + 2*P*m*d*F (kept rows through the experts; m = 2
+for GELU, 3 for SwiGLU) + the shared expert on all T tokens; bytes = weights of the experts
+that received a kept row + W_gate (fp32) + x read + out written."""
+
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from synth import get  # noqa: E402
+
+
+@pytest.mark.parametrize("name,P,touched,flops,nbytes", [
+    # T=8192, d=1024, E=64, k=1, GELU F=4096: 1.07e9 router + 1.374e11 experts;
+    # 64 * 2 * 4096 * 1024 * 2 B of weights + 256 KiB W_gate + 2 * 16 MiB of x / out
+    ("switch", 8192, 64, 1.385e11, 1.108e9),
+    # T=4096, d=4096, E=8, k=2, SwiGLU F=14336, no capacity: P = T * k
+    ("mixtral", 8192, 8, 2.887e12, 2.886e9),
+    # T=8192, d=7168, E=256 (+1 shared), k=8, SwiGLU F=2048, all experts touched
+    ("deepseek", 65536, 256, 6.524e12, 2.288e10),
+])
+def test_layer_totals(name, P, touched, flops, nbytes):
+    wl = get(name)
+    assert wl.flops(P) == pytest.approx(flops, rel=1e-3)
+    assert wl.bytes(touched) == pytest.approx(nbytes, rel=1e-3)
+
+
+@pytest.mark.parametrize("touched,nbytes", [(8, 0.712e9), (57.4, 5.07e9), (222.4, 19.6e9)])
+def test_decode_bytes_at_expected_touched_experts(touched, nbytes):
+    # decode, T in {1, 8, 64}: expected distinct experts 8, 57.4 and 222.4 of 256
+    assert get("decode8").bytes(touched) == pytest.approx(nbytes, rel=3e-3)
+
+
+def test_quantised_weight_bytes():
+    bf, i8, i4 = get("decode8"), get("decode8_i8"), get("decode8_i4")
+    n_w = bf.N1 * bf.d + bf.d * bf.F               # weights of one expert
+    scales = 4 * (bf.N1 + bf.d)                    # one fp32 scale per weight row
+    assert bf.bytes(1) - bf.bytes(0) == 2 * n_w
+    assert i8.bytes(1) - i8.bytes(0) == n_w + scales
+    assert i4.bytes(1) - i4.bytes(0) == n_w // 2 + scales
+    assert i4.bytes(0) == i8.bytes(0) == bf.bytes(0)   # W_gate, x, out do not change
+
+
+@pytest.mark.parametrize("name", ["switch", "mixtral", "deepseek", "decode64"])
+def test_kernel_costs_add_up_to_the_layer_flops(name):
+    wl = get(name)
+    P, touched = wl.T * wl.k, min(wl.E, wl.T * wl.k)
+    up = "grouped_gemm_gelu" if wl.kind == "gelu" else "grouped_gemm_swiglu"
+    down = "grouped_gemm_combine1" if (wl.k == 1 and not wl.has_shared) else "grouped_gemm_scale"
+    fl = sum(bench.kernel_algorithmic_cost(wl, n, P, touched)[0]
+             for n in ("router_gemm_topk", up, down))
+    if wl.has_shared:
+        fl += bench.kernel_algorithmic_cost(wl, "grouped_gemm_f32", P, touched)[0]
+    assert fl == pytest.approx(wl.flops(P), rel=1e-12)
+
+
+@pytest.mark.parametrize("quant,bytes_per_weight", [("q8t", 1.0), ("q4t", 0.5)])
+def test_quantised_kernels_count_their_code_bytes(quant, bytes_per_weight):
+    bf = get("decode64")
+    wq = get("decode64_i8" if quant == "q8t" else "decode64_i4")
+    P, touched = 512, 222
+    for kind, rows in (("swiglu", bf.N1 * bf.d), ("scale", bf.d * bf.F)):
+        fl_b, by_b = bench.kernel_algorithmic_cost(bf, f"grouped_gemm_{kind}", P, touched)
+        fl_q, by_q = bench.kernel_algorithmic_cost(wq, f"grouped_gemm_{quant}_{kind}", P, touched)
+        scales = 4 * (bf.N1 if kind == "swiglu" else bf.d)
+        assert fl_q == fl_b
+        assert by_q == pytest.approx(by_b - touched * rows * (2 - bytes_per_weight) + touched * scales)
