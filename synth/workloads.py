@@ -263,6 +263,14 @@ WORKLOADS = {
     "decode8_i4_e32": Workload("decode8_i4_e32", T=8, d=7168, E=32, k=8, F=2048, kind="swiglu",
                                act="bf16", gate_dist="uniform", int4=True,
                                note="decode, 8 tokens, INT4 weights, 32 experts (for profiling)"),
+    # the Switch-style layer with quantised experts: INT8 runs the shared-memory widening
+    # kernel (many rows per expert), INT4 the weight-streaming one
+    "switch_i8": Workload("switch_i8", T=8192, d=1024, E=64, k=1, F=4096, kind="gelu",
+                          act="bf16", cf=1.25, add_residual=True, int8=True,
+                          note="Switch-style top-1 GELU layer with INT8 expert weights"),
+    "switch_i4": Workload("switch_i4", T=8192, d=1024, E=64, k=1, F=4096, kind="gelu",
+                          act="bf16", cf=1.25, add_residual=True, int4=True,
+                          note="Switch-style top-1 GELU layer with INT4 expert weights"),
     "decode1": Workload("decode1", T=1, d=7168, E=256, k=8, F=2048, kind="swiglu", act="bf16",
                         gate_dist="uniform", note="decode, 1 token"),
     "decode8": Workload("decode8", T=8, d=7168, E=256, k=8, F=2048, kind="swiglu", act="bf16",

@@ -218,6 +218,7 @@ def test_forward_is_deterministic():
     ("decode1", None), ("decode8", 4), ("decode64", 4),
     ("decode1_i8", None), ("decode8_i8", 4), ("decode64_i8", 4), ("deepseek_reroute", 4),
     ("decode1_i4", None), ("decode8_i4", 4), ("decode64_i4", 4),
+    ("switch_i8", 32), ("switch_i4", 32),
 ])
 def test_full_size_sampled(name, sample):
     r, stats = full_check(get(name), sample=sample, seed=1)
