@@ -271,6 +271,10 @@ WORKLOADS = {
     "switch_i4": Workload("switch_i4", T=8192, d=1024, E=64, k=1, F=4096, kind="gelu",
                           act="bf16", cf=1.25, add_residual=True, int4=True,
                           note="Switch-style top-1 GELU layer with INT4 expert weights"),
+    # decode8's expert shapes in bf16 with 32 experts: small enough for multi-pass profiler captures
+    "decode8_e32": Workload("decode8_e32", T=8, d=7168, E=32, k=8, F=2048, kind="swiglu",
+                            act="bf16", gate_dist="uniform",
+                            note="decode, 8 tokens, bf16 weights, 32 experts (for profiling)"),
     "decode1": Workload("decode1", T=1, d=7168, E=256, k=8, F=2048, kind="swiglu", act="bf16",
                         gate_dist="uniform", note="decode, 1 token"),
     "decode8": Workload("decode8", T=8, d=7168, E=256, k=8, F=2048, kind="swiglu", act="bf16",
