@@ -34,9 +34,9 @@
 namespace moe {
 
 constexpr int QT_NT = 32;                           // activation rows per tile (MMA N)
-constexpr int QT_BK = 128;                          // codes per K block
+constexpr int QT_BK = 128;                          // codes per K block (MMA and TMEM stage)
 constexpr int QT_NQ = 5, QT_NB = 4, QT_NC = 3;
-constexpr int QT_Q_BYTES = GM_BN * QT_BK;           // 256 weight rows x 128 codes = 32 KB
+constexpr int QT_Q_BYTES = GM_BN * QT_BK;           // 256 weight rows x 128 bytes = 32 KB
 constexpr int QT_B_BYTES = QT_NT * QT_BK * 2;       // 32 rows x 128 bf16 = 8 KB (two boxes)
 constexpr int QT_RING_BYTES = QT_NQ * QT_Q_BYTES + QT_NB * QT_B_BYTES;
 constexpr int QT_HDR_BYTES = 1024;
@@ -117,8 +117,8 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    uint8_t* q_tiles = smem;                                   // NQ x 16 KB int8 codes
-    uint8_t* b_tiles = smem + QT_NQ * QT_Q_BYTES;              // NB x 4 KB bf16 activations
+    uint8_t* q_tiles = smem;                                   // NQ x 32 KB of codes
+    uint8_t* b_tiles = smem + QT_NQ * QT_Q_BYTES;              // NB x 8 KB bf16 activations
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + QT_RING_BYTES);
     const int QFULL = 0, QEMPTY = QT_NQ, BFULL = 2 * QT_NQ, BEMPTY = BFULL + QT_NB,
               CFULL = BEMPTY + QT_NB, CEMPTY = CFULL + QT_NC, TFULL = CEMPTY + QT_NC,
