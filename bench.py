@@ -4,10 +4,12 @@
 One step = one whole forward of the layer (route -> dispatch -> expert FFNs ->
 combine) over one batch of T synthetic tokens, through the C ABI. Inputs are
 seeded synthetic tensors with the workload's shapes and distributions (no
-dataset or trained weights are involved). Default workload: the Switch-style
-top-1 layer (T=8192, d=1024, E=64, GELU d->4096->d, capacity factor 1.25).
+dataset or trained weights are involved). Default workload: the DeepSeek-V3-shaped
+layer (T=8192, d=7168, 256 routed + 1 shared SwiGLU experts with F=2048, top-8,
+capacity factor 1.0), the largest configuration that fits one GPU. The same run
+then reports every other named configuration (device-timed) under "configs".
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--no-configs]
   python bench.py --impl reference ...   # the CPU oracle, timed as the reference arm
 
 Prints exactly one JSON line on stdout (rank 0). With N > 1 (torchrun) every rank
@@ -19,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import re
 import statistics
 import subprocess
@@ -32,24 +35,34 @@ sys.path.insert(0, ROOT)
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 METRIC = "MoE-layer fwd tokens/s on 1 B300; % of bf16 tensor / HBM roofline"
+DEFAULT_WORKLOAD = "deepseek"
+# every other configuration, reported from the same process (device-timed)
+SWEEP = ["tiny", "switch", "mixtral", "deepseek_cf125", "deepseek_grouped", "deepseek_reroute",
+         "decode1", "decode8", "decode64", "decode1_i8", "decode8_i8", "decode64_i8",
+         "decode1_i4", "decode8_i4", "decode64_i4", "switch_i8", "switch_i4"]
 
 
 def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="switch")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--flush-mib", type=int, default=256,
                     help="L2 flush buffer written between timed steps (L2 is 126 MB)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration sweep after the headline workload")
+    ap.add_argument("--configs", default=",".join(SWEEP),
+                    help="comma-separated workloads of the sweep")
+    ap.add_argument("--sweep-steps", type=int, default=10)
+    return ap.parse_args(argv)
 
 
 def load_peaks():
@@ -59,6 +72,20 @@ def load_peaks():
         return p, "measured"
     except Exception:
         return FALLBACK_PEAKS, "fallback"
+
+
+def host_cpu():
+    """CPU model and logical core count of the machine running the oracle."""
+    model = platform.processor() or "unknown"
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return model, os.cpu_count()
 
 
 # ---------------------------------------------------------------------------------
@@ -119,34 +146,74 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------------
-# algorithmic cost per kernel (for the roofline object)
+# algorithmic cost per kernel
 # ---------------------------------------------------------------------------------
-def kernel_algorithmic_cost(wl, name, P, touched):
-    """(flops, bytes) per STEP for all launches of kernel `name`, from the
-    algorithm's sizes (not from measured traffic)."""
+def _weight_bytes(wl):
+    """(bytes of one expert's W1 incl. row scales, bytes of its W2 incl. row scales)."""
+    es = 2 if wl.bf16 else 4
+    if wl.int8 or wl.int4:
+        per = 1 if wl.int8 else 0.5
+        return wl.N1 * wl.d * per + 4 * wl.N1, wl.w2_per_expert * per + 4 * wl.d
+    return wl.N1 * wl.d * es, wl.w2_per_expert * es
+
+
+def _base_name(name):
+    return re.sub(r"_q[48]t?_", "_", name)   # INT8 / INT4-weight kernels: same algorithm
+
+
+def kernel_roofline_cost(wl, name, P, touched):
+    """(flops, bytes) per STEP of all launches of kernel `name`, counted the way the
+    layer's roofline counts them: the FLOPs of the contraction the kernel performs, and
+    the layer-level bytes it owns -- the weights of the experts with kept rows that it
+    streams, W_gate, x read once, the layer output written once. Implementation buffers
+    (permuted rows, hidden activations, expert outputs) are not counted."""
     es = 2 if wl.bf16 else 4
     T, d, F, E = wl.T, wl.d, wl.F, wl.E
-    N1 = wl.N1
-    name = re.sub(r"_q[48]t?_", "_", name)  # INT8 / INT4-weight kernels: same algorithm
-    quant = wl.int8 or wl.int4
-    we = 1 if wl.int8 else (0.5 if wl.int4 else 2)   # bytes per expert weight
-    sc1 = 4 * N1 if quant else 0           # per-row scales of one expert
-    sc2 = 4 * d if quant else 0
-    up = {"grouped_gemm_gelu", "grouped_gemm_swiglu"}
-    if name in up:
-        fl = 2.0 * P * d * N1
-        by = touched * (N1 * d * we + sc1) + P * d * 2 + P * F * 2
+    w1b, w2b = _weight_bytes(wl)
+    name = _base_name(name)
+    if name in ("grouped_gemm_gelu", "grouped_gemm_swiglu"):
+        fl = 2.0 * P * d * wl.N1 + (2.0 * T * d * wl.N1 if wl.has_shared else 0.0)
+        return fl, touched * w1b + (w1b if wl.has_shared else 0) + T * d * es
+    if name == "grouped_gemm_scale":
+        return 2.0 * P * F * d, touched * w2b
+    if name == "grouped_gemm_combine1":
+        return 2.0 * P * F * d, touched * w2b + T * d * es
+    if name == "grouped_gemm_f32":            # shared expert down projection
+        return 2.0 * T * F * d, w2b
+    if name == "grouped_gemm_shared_combine":  # shared expert down projection + combine
+        return 2.0 * T * F * d, w2b + T * d * es
+    if name.startswith("router") or name == "router_splitk":
+        return 2.0 * T * d * E, T * d * es + d * E * 4
+    if name.startswith("combine"):
+        return 0.0, T * d * es
+    if name == "linear_expert":
+        return 2.0 * P * d * d, touched * d * d * 4 + T * d * es
+    return 0.0, 0.0
+
+
+def kernel_algorithmic_cost(wl, name, P, touched):
+    """(flops, bytes) per STEP for all launches of kernel `name`, counting every
+    buffer the kernel's algorithm must read or write (including implementation
+    buffers: hidden activations, expert outputs); a finer figure than the roofline
+    cost, kept to explain measured traffic."""
+    es = 2 if wl.bf16 else 4
+    T, d, F, E = wl.T, wl.d, wl.F, wl.E
+    w1b, w2b = _weight_bytes(wl)
+    name = _base_name(name)
+    if name in ("grouped_gemm_gelu", "grouped_gemm_swiglu"):
+        fl = 2.0 * P * d * wl.N1
+        by = touched * w1b + P * d * 2 + P * F * 2
         if wl.has_shared:
-            fl += 2.0 * T * d * N1
-            by += N1 * d * we + sc1 + T * d * 2 + T * F * 2
+            fl += 2.0 * T * d * wl.N1
+            by += w1b + T * d * 2 + T * F * 2
         return fl, by
     if name == "grouped_gemm_scale":
-        return 2.0 * P * F * d, touched * (d * F * we + sc2) + P * F * 2 + P * d * 4
+        return 2.0 * P * F * d, touched * w2b + P * F * 2 + P * d * 4
     if name == "grouped_gemm_combine1":   # top-1 down projection writing the layer output
-        return 2.0 * P * F * d, (touched * (d * F * we + sc2) + P * F * 2 + P * d * es
+        return 2.0 * P * F * d, (touched * w2b + P * F * 2 + P * d * es
                                  + (P * d * es if wl.add_residual else 0))
     if name == "grouped_gemm_f32":        # shared expert down projection
-        return 2.0 * T * F * d, d * F * we + sc2 + T * F * 2 + T * d * 4
+        return 2.0 * T * F * d, w2b + T * F * 2 + T * d * 4
     if name.startswith("router_logits") or name == "router_splitk":
         return 2.0 * T * d * E, T * d * es + d * E * 4 + T * E * 4
     if name == "router_gemm_tc":          # algorithmic: the fp32 gate GEMM it computes
@@ -219,32 +286,87 @@ def recorded_traffic(kernel, workload):
         return None
 
 
+def roofline_of(wl, name, launches, ms, steps, P, touched, peaks, peak_src):
+    """The roofline object of kernel `name` from its per-step algorithmic cost and its
+    measured CUDA-event time (ms summed over `steps` steps)."""
+    fl, by = kernel_roofline_cost(wl, name, P, touched)
+    t_step_s = ms / steps / 1000.0
+    hbm = float(peaks["hbm_gbs"])
+    tflops = float(peaks["bf16_tflops"])
+    if fl / (tflops * 1e12) > by / (hbm * 1e9):
+        roof = {"bound": "tensor", "achieved": fl / t_step_s / 1e12, "peak": tflops,
+                "unit": "TFLOP/s"}
+        sus = float(peaks.get("bf16_tflops_sustained", tflops))
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        roof["frac_of_sustained"] = roof["achieved"] / sus
+    else:
+        roof = {"bound": "hbm", "achieved": by / t_step_s / 1e9, "peak": hbm, "unit": "GB/s"}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = recorded_traffic(name, wl.name)
+    roof["kernel"] = name
+    roof["launches_per_step"] = launches / steps
+    roof["ms_per_step"] = ms / steps
+    roof["peak_source"] = (f"{peak_src} ("
+                           f"{'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'}"
+                           f"; {'bf16 burst' if roof['bound'] == 'tensor' else 'copy bandwidth'})")
+    roof["algorithmic_bytes_per_step"] = by
+    roof["algorithmic_flops_per_step"] = fl
+    fi, bi = kernel_algorithmic_cost(wl, name, P, touched)
+    roof["impl_bytes_per_step"] = bi
+    return roof
+
+
+def layer_roofline(wl, P, touched, step_ms, peaks):
+    """Roofline time of the whole layer (slower of its FLOPs at the tensor peak and its
+    bytes at the copy bandwidth) over the measured step time."""
+    fl, by = wl.flops(P), wl.bytes(touched)
+    t_fl = fl / (float(peaks["bf16_tflops"]) * 1e12)
+    t_by = by / (float(peaks["hbm_gbs"]) * 1e9)
+    return {"frac": max(t_fl, t_by) / (step_ms / 1000.0), "bound": "tensor" if t_fl > t_by else "hbm",
+            "roofline_ms": 1000.0 * max(t_fl, t_by), "flops": fl, "bytes": by}
+
+
 # ---------------------------------------------------------------------------------
 # CPU baseline (the oracle, as it stands, single-threaded)
 # ---------------------------------------------------------------------------------
-def cpu_oracle_sample(wl, sample_tokens, seed=0):
-    """Time the oracle on a bounded sample: full routing + dispatch over all T tokens,
-    expert FFNs + combine for `sample_tokens` seeded tokens. Returns
-    (tokens_per_s, seconds_total, description)."""
+def cpu_oracle_sample(wl, route_budget_s, ffn_budget_s, seed=0):
+    """Time the oracle on a bounded sample of the workload: gate logits + top-k +
+    dispatch for seeded tokens until `route_budget_s` is spent (all T tokens if they fit;
+    the dispatch then ranks that sample's assignments at the layer's capacity), and the
+    expert FFNs + combine of further seeded tokens until `ffn_budget_s` is spent (at least
+    one). Expert weights are regenerated outside the timed parts. Returns
+    (tokens_per_s, seconds_timed, description)."""
     import numpy as np
     import oracle as orc
     rng = np.random.default_rng(seed)
-    S = min(sample_tokens, wl.T)
-    rows = np.sort(rng.choice(wl.T, size=S, replace=False))
-    x = wl.x_host()
+    order = rng.permutation(wl.T)
     Wg, gb = wl.wg_host(), wl.gate_bias_host()
-    t0 = time.perf_counter()
-    L = orc.gate_logits(x, Wg, gb)
-    idx, w = orc.topk_renorm(L, wl.k, wl.n_group, wl.topk_group)
     cap = orc.capacity(np.float32(wl.cf), wl.T, wl.k, wl.E)
+    # ---- routing + dispatch on a token sample (chunks until the budget is spent) ----
+    chunk = max(1, min(wl.T, 512, int(3e7 / (wl.d * wl.E))))   # first chunk: well under 1 s
+    S_r, t_route, Ls = 0, 0.0, []
+    while S_r < wl.T and (S_r == 0 or t_route < route_budget_s):
+        rows = np.sort(order[S_r:S_r + chunk])
+        xr = wl.x_host(rows)
+        t0 = time.perf_counter()
+        L = orc.gate_logits(xr, Wg, gb)
+        t_route += time.perf_counter() - t0
+        Ls.append(L)
+        S_r += len(rows)
+        if t_route > 0 and S_r < wl.T and S_r == len(rows):   # size later chunks to the rate
+            chunk = max(1, int(S_r * 0.25 * route_budget_s / t_route))
+    L = np.concatenate(Ls)
+    t0 = time.perf_counter()
+    idx, w = orc.topk_renorm(L, wl.k, wl.n_group, wl.topk_group)
     if wl.overflow == "reroute":
         cand = orc.rank_candidates(L, wl.k, wl.k, wl.n_group, wl.topk_group)
-        counts, offsets, pt, ps, sd, idx = orc.dispatch_reroute(idx, cand, wl.E, cap)
+        counts, offsets, pt, ps, sd, idx2 = orc.dispatch_reroute(idx, cand, wl.E, cap)
     else:
         counts, offsets, pt, ps, sd = orc.dispatch(idx, wl.E, cap)
-    t_route = time.perf_counter() - t0
-    need = sorted({int(idx[t, j]) for t in rows for j in range(wl.k) if sd[t, j] >= 0})
+        idx2 = idx
+    t_route += time.perf_counter() - t0
 
+    # ---- expert FFNs + combine, one token at a time until the budget is spent ----
     def expert_fn(e, shared=False):
         w1, b1, w2, b2 = (wl.w1_host(e, shared), wl.b1_host(e, shared), wl.w2_host(e, shared),
                           wl.b2_host(e, shared))
@@ -258,40 +380,45 @@ def cpu_oracle_sample(wl, sample_tokens, seed=0):
             q1, q2 = orc.unpack_i4(p1), orc.unpack_i4(p2)
             return lambda xr: orc.expert_row_q8(wl.kind_code, xr, q1, s1, b1, q2, s2, b2, wl.d, wl.F)
         return lambda xr: orc.expert_row(wl.kind_code, xr, w1, b1, w2, b2, wl.d, wl.F)
-    Wc = {e: expert_fn(e) for e in need}
+
     shared = expert_fn(0, True) if wl.has_shared else None
-    t0 = time.perf_counter()
-    for t in rows:
-        xr = np.ascontiguousarray(x[t])
+    cache = {}
+    S_f, t_ffn = 0, 0.0
+    while S_f < S_r and (S_f == 0 or t_ffn < ffn_budget_s):
+        i = S_f
+        t = int(order[i])
+        xr = np.ascontiguousarray(wl.x_host([t])[0])
+        kept = (sd[i] >= 0).astype(np.int32)
+        need = [int(idx2[i, j]) for j in range(wl.k) if kept[j]]
+        if len(cache) > 16:
+            cache.clear()
+        for e in need:
+            if e not in cache:
+                cache[e] = expert_fn(e)
+        t0 = time.perf_counter()
         ys = np.zeros((wl.k, wl.d))
-        kept = (sd[t] >= 0).astype(np.int32)
         for j in range(wl.k):
             if kept[j]:
-                ys[j] = Wc[int(idx[t, j])](xr)
+                ys[j] = cache[int(idx2[i, j])](xr)
         ysh = shared(xr) if shared else None
-        orc.combine_row(xr, wl.add_residual, w[t], kept, ys, ysh,
+        orc.combine_row(xr, wl.add_residual, w[i], kept, ys, ysh,
                         orc.BF16 if wl.bf16 else orc.F32,
                         overflow_to_shared=wl.overflow == "shared")
-    t_ffn = time.perf_counter() - t0
-    per_token = t_route / wl.T + t_ffn / S
-    desc = (f"routing+dispatch of all {wl.T} tokens ({t_route:.2f} s) + expert FFN and "
-            f"combine of {S} seeded tokens ({t_ffn:.2f} s); tokens/s = 1/(t_route/T + t_ffn/S)")
+        t_ffn += time.perf_counter() - t0
+        S_f += 1
+    per_token = t_route / S_r + t_ffn / S_f
+    part = f"all {wl.T}" if S_r == wl.T else f"a seeded sample of {S_r} of the {wl.T}"
+    desc = (f"gate logits + top-k + dispatch of {part} tokens ({t_route:.2f} s; the dispatch at the "
+            f"layer's capacity {cap}) + expert FFNs and combine of {S_f} of those tokens "
+            f"({t_ffn:.2f} s); tokens/s = 1/(t_route/{S_r} + t_ffn/{S_f}); single-threaded")
     return 1.0 / per_token, t_route + t_ffn, desc
-
-
-def default_sample(wl):
-    """Sample size giving roughly 2-5 s of single-core oracle work per run."""
-    m = {"linear": 1, "gelu": 2, "swiglu": 3}[wl.kind]
-    per_row = 2.0 * m * wl.d * (wl.F if wl.kind != "linear" else wl.d) * (
-        wl.k + (1 if wl.has_shared else 0))
-    return int(max(1, min(wl.T, 3e9 / per_row)))
 
 
 # ---------------------------------------------------------------------------------
 # reference arm: the oracle timed as the reference implementation
 # ---------------------------------------------------------------------------------
-def workload_config(wl, world):
-    """The workload part of `config`, the same on both arms."""
+def workload_config(wl, world, flush_mib):
+    """`config` of the line: the workload only, identical on both arms."""
     return {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "top_k": wl.k, "F": wl.F,
             "kind": wl.kind, "capacity_factor": wl.cf, "shared_expert": wl.has_shared,
             "residual": wl.add_residual,
@@ -299,6 +426,7 @@ def workload_config(wl, world):
             "expert_weights": ("int8 codes + fp32 row scales" if wl.int8 else
                                "int4 codes (2 per byte) + fp32 row scales" if wl.int4 else "bf16"),
             "overflow": wl.overflow,
+            "l2": f"flushed between timed steps ({flush_mib} MiB write)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
@@ -306,25 +434,25 @@ def run_reference(args, wl):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    S = max(1, default_sample(wl) // 2)
     vals = []
     descs = None
     for i in range(args.warmup + args.steps):
-        v, secs, desc = cpu_oracle_sample(wl, S, seed=i)
+        v, secs, desc = cpu_oracle_sample(wl, 1.0, 1.0, seed=i)
         if i >= args.warmup:
             vals.append((v, secs))
             descs = desc
     total_tokens = sum(v * s for v, s in vals)   # token-equivalents processed
     total_s = sum(s for _, s in vals)
     value = total_tokens / total_s
+    model, ncpu = host_cpu()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * total_s / max(1, len(vals)), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(wl, int(os.environ.get("WORLD_SIZE", "1"))),
+        "config": workload_config(wl, int(os.environ.get("WORLD_SIZE", "1")), args.flush_mib),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": descs},
+                         "sample": descs, "host_cpu": model, "host_nproc": ncpu},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -352,13 +480,133 @@ def job_tokens_per_s(T, steps, world, total_ms):
     return T * steps * world / (total_ms / 1000.0)
 
 
+def build_layer(wl, dev):
+    """Device inputs and the MoELayer of workload `wl` (bf16 originals of quantised
+    experts are released once the layer holds their codes)."""
+    import torch
+    import top_routing_expert_renorm_b300 as moe
+    inp = wl.device_inputs(dev)
+    cfg = moe.config_for(wl)
+    layer = moe.MoELayer(cfg, inp["wg"], inp["gate_bias"], inp["w1"], inp["b1"], inp["w2"],
+                         inp["b2"], inp["shared"])
+    if wl.int8 or wl.int4:
+        inp["w1"] = inp["w2"] = inp["shared"] = None
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return inp, cfg, layer
+
+
+def measure(wl, layer, x, steps, warmup, flush, world, dev, clocks=None, barrier=None):
+    """Device-timed forwards: `warmup` untimed, then `steps` timed (CUDA events on the
+    launch stream around each step, L2 flushed before each), then the same steps again
+    with an event pair around every launch for the per-kernel breakdown."""
+    import numpy as np
+    import torch
+    import top_routing_expert_renorm_b300 as moe
+    stream = torch.cuda.current_stream()
+    out = torch.empty_like(x)
+    load = torch.empty(wl.E, dtype=torch.int32, device=dev)
+
+    def step():
+        layer(x, out=out, load=load)
+
+    for _ in range(max(warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    st = moe.last_device_status()
+    if st != 0:
+        raise RuntimeError(f"{wl.name}: device status after warm-up: {moe.status_string(st)}")
+    ld = load.cpu().numpy()
+    cap = moe.capacity(layer.cfg)
+    P = int(np.minimum(ld, cap).sum())
+    touched = int((np.minimum(ld, cap) > 0).sum())
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    n_launch0 = moe.kernel_launch_count()
+    for i in range(steps):
+        flush.zero_()                      # L2 flush between timed steps (not timed)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    n_launch = moe.kernel_launch_count() - n_launch0
+    # Per-kernel durations: the same steps again with an event pair around every launch
+    # (events between launches serialise kernels that may otherwise overlap their
+    # neighbours' start and end, so this pass is not the timed one).
+    moe.profile_begin()
+    for i in range(steps):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    kstats = moe.profile_end()
+    if barrier:
+        barrier()
+    clk = clocks.stop() if clocks else None
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    st = moe.last_device_status()
+    if st != 0:
+        raise RuntimeError(f"{wl.name}: device status after timing: {moe.status_string(st)}")
+    return dict(total_ms=total_ms, step_ms=step_ms, kstats=kstats, P=P, touched=touched,
+                n_launch=n_launch, clocks=clk, out=out)
+
+
+def dominant(kstats, wl):
+    """The kernel with the most time per step among those with a roofline cost."""
+    ranked = sorted(kstats.items(), key=lambda kv: -kv[1][1])
+    for name, (launches, ms) in ranked:
+        fl, by = kernel_roofline_cost(wl, name, 1, 1)
+        if fl > 0 or by > 0:
+            return name, launches, ms
+    name, (launches, ms) = ranked[0]
+    return name, launches, ms
+
+
+def sweep(args, dev, flush, peaks, peak_src):
+    """Every configuration of the sweep, device-timed in this process."""
+    import torch
+    from synth import get
+    res = {}
+    for name in [n for n in args.configs.split(",") if n and n != args.workload]:
+        try:
+            wl = get(name)
+            inp, cfg, layer = build_layer(wl, dev)
+            m = measure(wl, layer, inp["x"], args.sweep_steps, 3, flush, 1, dev)
+            K = args.sweep_steps
+            dname, dl, dms = dominant(m["kstats"], wl)
+            roof = roofline_of(wl, dname, dl, dms, K, m["P"], m["touched"], peaks, peak_src)
+            lay = layer_roofline(wl, m["P"], m["touched"], m["total_ms"] / K, peaks)
+            res[name] = {
+                "tokens_per_s": job_tokens_per_s(wl.T, K, 1, m["total_ms"]),
+                "ms_per_step": m["total_ms"] / K,
+                "layer_roofline_frac": lay["frac"], "layer_bound": lay["bound"],
+                "kept_rows_P": m["P"], "touched_experts": m["touched"],
+                "dominant_kernel": dname, "dominant_bound": roof["bound"],
+                "dominant_achieved": roof["achieved"], "dominant_unit": roof["unit"],
+                "dominant_frac": roof["frac"],
+                "launches_per_step": m["n_launch"] / K,
+                "kernels_ms_per_step": {k: v[1] / K for k, v in
+                                        sorted(m["kstats"].items(), key=lambda kv: -kv[1][1])},
+            }
+            del inp, layer, m
+        except Exception as e:   # a failed configuration must not hide the headline line
+            res[name] = {"error": f"{type(e).__name__}: {e}"}
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, wl):
     import torch
     import torch.distributed as dist
-    import numpy as np
     import __graft_entry__
     __graft_entry__.build()
-    import top_routing_expert_renorm_b300 as moe
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -368,98 +616,22 @@ def run_ours(args, wl):
         dist.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.current_stream()
-
-    inp = wl.device_inputs(dev)
-    cfg = moe.config_for(wl)
-    layer = moe.MoELayer(cfg, inp["wg"], inp["gate_bias"], inp["w1"], inp["b1"], inp["w2"],
-                         inp["b2"], inp["shared"])
-    if wl.int8 or wl.int4:
-        # the layer holds the INT8 / INT4 codes; the bf16 originals are no longer needed
-        inp["w1"] = inp["w2"] = inp["shared"] = None
-        torch.cuda.synchronize()
-        torch.cuda.empty_cache()
-    x = inp["x"]
-    out = torch.empty_like(x)
-    load = torch.empty(wl.E, dtype=torch.int32, device=dev)
     flush = torch.empty(args.flush_mib * 2 ** 20 // 4, dtype=torch.float32, device=dev)
-
-    def step():
-        layer(x, out=out, load=load)
-
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize()
-    st = moe.last_device_status()
-    if st != 0:
-        raise RuntimeError(f"device status after warm-up: {moe.status_string(st)}")
-    ld = load.cpu().numpy()
-    cap = moe.capacity(cfg)
-    P = int(np.minimum(ld, cap).sum())
-    touched = int((np.minimum(ld, cap) > 0).sum())
-
-    # ---- timed region ----
-    K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
-    clocks = ClockSampler(torch.cuda.current_device())
-    clocks.start()
-    time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    n_launch0 = moe.kernel_launch_count()
-    for i in range(K):
-        flush.zero_()                      # L2 flush between timed steps (not timed)
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    n_launch = moe.kernel_launch_count() - n_launch0
-    # Per-kernel durations: the same K steps again with an event pair around every
-    # launch (events between launches serialise kernels that may otherwise overlap
-    # their neighbours' start and end, so this pass is not the timed one).
-    moe.profile_begin()
-    for i in range(K):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    kstats = moe.profile_end()
-    if world > 1:
-        dist.barrier()
-    clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = max_over_ranks(sum(step_ms), world, dev)
-    st = moe.last_device_status()
-    if st != 0:
-        raise RuntimeError(f"device status after timing: {moe.status_string(st)}")
-    value = job_tokens_per_s(wl.T, K, world, total_ms)
-
-    # ---- roofline of the dominant kernel ----
     peaks, peak_src = load_peaks()
-    dom = max(kstats.items(), key=lambda kv: kv[1][1])
-    dname, (dlaunch, dms) = dom
-    fl, by = kernel_algorithmic_cost(wl, dname, P, touched)
-    t_step_s = dms / K / 1000.0
-    hbm = float(peaks["hbm_gbs"])
-    tflops = float(peaks["bf16_tflops"])
-    if fl / (tflops * 1e12) > by / (hbm * 1e9):
-        roof = {"bound": "tensor", "achieved": fl / t_step_s / 1e12, "peak": tflops,
-                "unit": "TFLOP/s"}
-    else:
-        roof = {"bound": "hbm", "achieved": by / t_step_s / 1e9, "peak": hbm, "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    tr = recorded_traffic(dname, wl.name)
-    roof["traffic"] = tr
-    roof["kernel"] = dname
-    roof["launches_per_step"] = dlaunch / K
-    roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
-    roof["algorithmic_bytes_per_step"] = by
-    roof["algorithmic_flops_per_step"] = fl
-    # whole-layer roofline (slower of FLOPs at tensor peak and bytes at HBM peak)
-    lay_fl = wl.flops(P)
-    lay_by = wl.bytes(touched)
-    layer_roof_s = max(lay_fl / (tflops * 1e12), lay_by / (hbm * 1e9))
-    layer_frac = layer_roof_s / (total_ms / K / 1000.0)
+
+    inp, cfg, layer = build_layer(wl, dev)
+    x = inp["x"]
+    K = args.steps
+    m = measure(wl, layer, x, K, args.warmup, flush, world, dev,
+                clocks=ClockSampler(torch.cuda.current_device()),
+                barrier=(dist.barrier if world > 1 else None))
+    total_ms, kstats, P, touched = m["total_ms"], m["kstats"], m["P"], m["touched"]
+    value = job_tokens_per_s(wl.T, K, world, total_ms)
+    dname, dlaunch, dms = dominant(kstats, wl)
+    roof = roofline_of(wl, dname, dlaunch, dms, K, P, touched, peaks, peak_src)
+    lay = layer_roofline(wl, P, touched, total_ms / K, peaks)
+    out = m["out"]
+    n_launch, clk = m["n_launch"], m["clocks"]
 
     # ---- end to end through the public API with host buffers ----
     # Every step copies its input x from pinned host memory and its output back to pinned
@@ -512,12 +684,21 @@ def run_ours(args, wl):
                "h2d_bytes_per_step": nb, "d2h_bytes_per_step": out.numel() * out.element_size(),
                "overlap": "uploads/downloads on their own streams, double-buffered",
                "launch": "MoELayer.capture CUDA graph per buffer pair, replayed every step"}
+        del graphs, xd, od, xh, oh
+    del inp, layer, x, out, m
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+    configs = None
+    if rank == 0 and world == 1 and not args.no_configs:
+        configs = sweep(args, dev, flush, peaks, peak_src)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, secs, desc = cpu_oracle_sample(wl, default_sample(wl))
+        v, secs, desc = cpu_oracle_sample(wl, 4.0, 8.0)
+        model, ncpu = host_cpu()
         cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": desc, "seconds": secs}
+               "sample": desc, "seconds": secs, "host_cpu": model, "host_nproc": ncpu}
 
     if world > 1:
         dist.barrier()
@@ -529,17 +710,18 @@ def run_ours(args, wl):
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.bf16 else "f32",
         "data": "synthetic (seeded counter-based generator; random-init weights)",
-        "config": {**workload_config(wl, world),
-                   "l2": f"flushed between steps ({args.flush_mib} MiB write)",
-                   "kept_rows_P": P, "touched_experts": touched},
+        "config": workload_config(wl, world, args.flush_mib),
+        "run": {"kept_rows_P": P, "touched_experts": touched},
         "roofline": roof,
-        "layer_roofline_frac": layer_frac,
+        "layer_roofline_frac": lay["frac"],
+        "layer_roofline": lay,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": n_launch,
         "clocks": clk,
         "kernels_ms_per_step": {k: v[1] / K for k, v in sorted(kstats.items(),
                                                                 key=lambda kv: -kv[1][1])},
+        "configs": configs,
     }
     print(json.dumps(line), flush=True)
     return 0

@@ -36,7 +36,10 @@ class Workload:
     cf: float = 0.0         # capacity factor; <= 0: no limit
     add_residual: bool = False
     has_shared: bool = False
-    gate_dist: str = "normal"   # "normal" | "uniform"
+    gate_dist: str = "normal"   # "normal" | "uniform" | "zero" (every logit equal) |
+                                # "grid" (integers -1, 0, 1: logits tie exactly and often)
+    x_dist: str = "normal"      # "normal" | "grid" (integers -1, 0, 1 in the first 16 features,
+                                # 0 elsewhere: few distinct logits)
     gate_bias: str = "none"     # "none" | "zipf" | "hot" (+20 on expert 0: one expert takes all)
     expert_bias: bool = False
     int8: bool = False          # weight-only INT8 experts (codes + per-row scales)
@@ -80,8 +83,24 @@ class Workload:
         return normal_K(1.0 / math.sqrt(self.F if self.kind != "linear" else self.d))
 
     # ---- host tensors (numpy; bf16 as uint16 bit patterns) ------------------
+    def _grid(self, tid, n):
+        """n integers in {-1, 0, 1}: uniform values on (-1.5, 1.5) rounded to the nearest
+        integer (exact in fp32 and bf16)."""
+        u = host_fill(self.seed, tid, 0, n, UNIFORM, uniform_K(1.5), False)
+        return np.clip(np.rint(u), -1.0, 1.0).astype(np.float32)
+
+    def _x_grid(self):
+        g = self._grid(TID_X, self.T * self.d).reshape(self.T, self.d)
+        g[:, 16:] = 0.0
+        if self.bf16:   # integers are exact in bf16: the upper half of the fp32 pattern
+            return (g.view(np.uint32) >> 16).astype(np.uint16)
+        return g
+
     def x_host(self, rows=None):
         """All of x [T, d], or the listed rows only."""
+        if self.x_dist == "grid":
+            g = self._x_grid()
+            return g if rows is None else g[np.asarray(rows, dtype=np.int64)]
         if rows is None:
             return host_fill(self.seed, TID_X, 0, self.T * self.d, NORMAL, normal_K(1.0),
                              self.bf16).reshape(self.T, self.d)
@@ -91,6 +110,10 @@ class Workload:
                                                    np.uint16 if self.bf16 else np.float32)
 
     def wg_host(self):
+        if self.gate_dist == "zero":
+            return np.zeros((self.d, self.E), np.float32)
+        if self.gate_dist == "grid":
+            return self._grid(TID_WG, self.d * self.E).reshape(self.d, self.E)
         dist, K = self._wg_dist_K()
         return host_fill(self.seed, TID_WG, 0, self.d * self.E, dist, K, False).reshape(self.d, self.E)
 
@@ -153,9 +176,17 @@ class Workload:
         import torch
         adt = torch.bfloat16 if self.bf16 else torch.float32
         emp = lambda *s, dt=adt: torch.empty(*s, dtype=dt, device=device)  # noqa: E731
-        x = dev_fill(emp(self.T, self.d), self.seed, TID_X, 0, NORMAL, normal_K(1.0))
-        dist, K = self._wg_dist_K()
-        wg = dev_fill(emp(self.d, self.E, dt=torch.float32), self.seed, TID_WG, 0, dist, K)
+        if self.x_dist == "grid":   # small tie-test layers: made on the host, uploaded
+            xh = self._x_grid()
+            x = torch.from_numpy(xh.view(np.int16) if self.bf16 else xh).to(device)
+            x = x.view(torch.bfloat16) if self.bf16 else x
+        else:
+            x = dev_fill(emp(self.T, self.d), self.seed, TID_X, 0, NORMAL, normal_K(1.0))
+        if self.gate_dist in ("zero", "grid"):
+            wg = torch.from_numpy(self.wg_host()).to(device)
+        else:
+            dist, K = self._wg_dist_K()
+            wg = dev_fill(emp(self.d, self.E, dt=torch.float32), self.seed, TID_WG, 0, dist, K)
         gb = self.gate_bias_host()
         gb = None if gb is None else torch.from_numpy(gb).to(device)
         w1 = dev_fill(emp(self.E, self.N1, self.d), self.seed, TID_W1, 0, NORMAL, self._w1_K())

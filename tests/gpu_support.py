@@ -177,26 +177,41 @@ def check_quantized_weights(r, experts):
         assert np.array_equal(to_np(q2[e]), oq2) and np.array_equal(to_np(s2[e]), os2)
 
 
-def oracle_rows(wl, x_host_rows, rows, idx_ref, w_ref, sd, cache):
+def expert_outputs(wl, requests, x_all):
+    """Oracle expert outputs for requests {expert id or "shared": tokens}, one expert's
+    weights in memory at a time. Returns {(expert, token): y[d] float64}."""
+    out = {}
+    for e in sorted(requests, key=str):
+        fn = _expert_fn(wl, 0, True) if e == "shared" else _expert_fn(wl, e)
+        for t in sorted(requests[e]):
+            out[(e, t)] = fn(np.ascontiguousarray(x_all[t]))
+        del fn
+    return out
+
+
+def oracle_rows(wl, x_all, rows, idx_ref, w_ref, sd, ys=None):
     """Oracle outputs for the given tokens, with routing fed from the GPU logits; idx_ref
-    names the expert that processes each kept slot."""
+    names the expert that processes each kept slot. ys: expert outputs computed already."""
+    req = {}
+    for t in rows:
+        for j in range(wl.k):
+            if sd[t, j] >= 0:
+                req.setdefault(int(idx_ref[t, j]), set()).add(int(t))
+        if wl.has_shared:
+            req.setdefault("shared", set()).add(int(t))
+    ys = dict(ys or {})
+    missing = {e: {t for t in ts if (e, t) not in ys} for e, ts in req.items()}
+    ys.update(expert_outputs(wl, {e: ts for e, ts in missing.items() if ts}, x_all))
     out = []
-    for t_i, t in enumerate(rows):
-        xr = np.ascontiguousarray(x_host_rows[t_i])
-        ys = np.zeros((wl.k, wl.d))
+    for t in rows:
+        xr = np.ascontiguousarray(x_all[t])
+        yk = np.zeros((wl.k, wl.d))
         kept = (sd[t] >= 0).astype(np.int32)
         for j in range(wl.k):
             if kept[j]:
-                e = int(idx_ref[t, j])
-                if e not in cache:
-                    cache[e] = _expert_fn(wl, e)
-                ys[j] = cache[e](xr)
-        ysh = None
-        if wl.has_shared:
-            if "shared" not in cache:
-                cache["shared"] = _expert_fn(wl, 0, True)
-            ysh = cache["shared"](xr)
-        out.append(orc.combine_row(xr, wl.add_residual, w_ref[t], kept, ys, ysh,
+                yk[j] = ys[(int(idx_ref[t, j]), int(t))]
+        ysh = ys[("shared", int(t))] if wl.has_shared else None
+        out.append(orc.combine_row(xr, wl.add_residual, w_ref[t], kept, yk, ysh,
                                    orc.BF16 if wl.bf16 else orc.F32,
                                    overflow_to_shared=wl.overflow == "shared"))
     return np.stack(out)
@@ -216,23 +231,103 @@ def check_outputs(wl, got, ref):
     return float(err.max() / mx), 0.0
 
 
-def full_check(wl, sample=None, seed=0):
+def targeted_tokens(r, idx_ref, route_idx, sd, n_total, seed):
+    """Tokens where a tiled kernel is most likely to break, plus seeded random ones up to
+    n_total: the tokens at rows 0, 127, 128, 255, 256 and the last row of a few experts'
+    row blocks (first and last touched expert, the most loaded one, a middle one, and the
+    first and last with more than one 128-row M tile), rows 0, 127, 128 and T-1 of the
+    shared expert, capacity-dropped tokens and re-routed tokens. Also returns the
+    targeted positions p of the permuted rows."""
+    wl = r.wl
+    offsets = to_np(r.offsets).astype(np.int64)
+    pt = to_np(r.perm_token)
+    counts = np.diff(offsets)
+    touched = np.nonzero(counts)[0]
+    picks = {int(touched[0]), int(touched[-1]), int(touched[np.argmax(counts[touched])]),
+             int(touched[len(touched) // 2])}
+    big = touched[counts[touched] > 128]
+    if len(big):
+        picks.update({int(big[0]), int(big[-1])})
+    positions = []
+    for e in sorted(picks):
+        n = int(counts[e])
+        for q in sorted({0, 127, 128, 255, 256, n - 1}):
+            if 0 <= q < n:
+                positions.append(int(offsets[e]) + q)
+    tokens = {int(pt[p]) for p in positions}
+    if wl.has_shared:
+        tokens.update(t for t in (0, 127, 128, wl.T - 1) if 0 <= t < wl.T)
+    rng = np.random.default_rng(seed)
+    dropped = np.nonzero((sd < 0).any(axis=1))[0]
+    if len(dropped):
+        tokens.update(int(t) for t in rng.choice(dropped, size=min(2, len(dropped)), replace=False))
+    full = np.nonzero((sd < 0).all(axis=1))[0]
+    if len(full):
+        tokens.add(int(full[0]))
+    moved = np.nonzero(((route_idx != idx_ref) & (sd >= 0)).any(axis=1))[0]
+    if len(moved):
+        tokens.update(int(t) for t in rng.choice(moved, size=min(2, len(moved)), replace=False))
+    rest = np.setdiff1d(np.arange(wl.T), np.fromiter(tokens, np.int64, len(tokens)))
+    need = max(0, n_total - len(tokens))
+    if need and len(rest):
+        tokens.update(int(t) for t in rng.choice(rest, size=min(need, len(rest)), replace=False))
+    return np.array(sorted(tokens), dtype=np.int64), np.array(positions, dtype=np.int64)
+
+
+def check_expert_rows(r, positions, route_idx, w_ref, x_all, rows):
+    """Rows of the staged expert output y (fp32, routing weight applied) at the given
+    permuted positions, against the oracle expert times the slot's weight; and the shared
+    expert's rows of the checked tokens. Returns the expert outputs it computed, plus those
+    of every slot of `rows` (for the token-level check)."""
+    wl = r.wl
+    pt, ps = to_np(r.perm_token), to_np(r.perm_slot)
+    sd = to_np(r.slot_dest)
+    y = r.y.cpu().numpy()
+    req = {}
+    for p in positions:
+        t, j = int(pt[p]), int(ps[p])
+        req.setdefault(int(route_idx[t, j]), set()).add(t)
+    for t in rows:
+        for j in range(wl.k):
+            if sd[t, j] >= 0:
+                req.setdefault(int(route_idx[t, j]), set()).add(int(t))
+    shared_rows = sorted({int(t) for t in rows})
+    if wl.has_shared:
+        req["shared"] = set(shared_rows)
+    ys = expert_outputs(wl, req, x_all)
+    got, ref = [], []
+    for p in positions:
+        t, j = int(pt[p]), int(ps[p])
+        ref.append(ys[(int(route_idx[t, j]), t)] * float(w_ref[t, j]))
+        got.append(y[p])
+    if wl.has_shared:
+        Pmax = wl.T * wl.k
+        for t in shared_rows:
+            ref.append(ys[("shared", t)])
+            got.append(y[Pmax + t])
+    check_outputs(wl, np.stack(got), np.stack(ref))
+    return ys
+
+
+def full_check(wl, sample=None, seed=0, targeted=False):
     """Run the CUDA path on `wl` and check it against the oracle.
-    sample=None: every token; otherwise that many seeded tokens (routing and
-    dispatch are still checked in full)."""
+    sample=None: every token; otherwise that many tokens (routing and dispatch are still
+    checked in full): seeded random ones, or with targeted=True the tile-boundary,
+    dropped and re-routed tokens of targeted_tokens() topped up with random ones, plus the
+    staged expert-output rows at the targeted positions."""
     r = GpuRun(wl).run()
+    x_all = wl.x_host()
+    idx_ref, w_ref = check_routing(r)
+    cap, sd, P, route_idx = check_dispatch(r, idx_ref)
+    positions = np.empty(0, np.int64)
     if sample is None or sample >= wl.T:
         rows = np.arange(wl.T)
-        x_rows = wl.x_host()
-        x_all = x_rows
+    elif targeted:
+        rows, positions = targeted_tokens(r, idx_ref, route_idx, sd, sample, seed)
     else:
         rng = np.random.default_rng(seed)
         rows = np.sort(rng.choice(wl.T, size=sample, replace=False))
-        x_all = wl.x_host()
-        x_rows = x_all[rows]
     check_logits(wl, x_all, rows, to_np(r.logits)[rows])
-    idx_ref, w_ref = check_routing(r)
-    cap, sd, P, route_idx = check_dispatch(r, idx_ref)
     # gathered rows are exact copies
     xp = to_np(r.x_perm)[:P]
     pt = to_np(r.perm_token)[:P]
@@ -241,7 +336,11 @@ def full_check(wl, sample=None, seed=0):
     if wl.int8 or wl.int4:
         used = sorted({int(e) for e in idx_ref[rows].ravel()})
         check_quantized_weights(r, used[:8])
-    ref = oracle_rows(wl, x_rows, rows, route_idx, w_ref, sd, {})
+    ys = None
+    if len(positions) and wl.kind != "linear":
+        ys = check_expert_rows(r, positions, route_idx, w_ref, x_all, rows)
+    ref = oracle_rows(wl, x_all, rows, route_idx, w_ref, sd, ys)
     stats = check_outputs(wl, to_np(r.out)[rows], ref)
     check_outputs(wl, to_np(r.out_stages)[rows], ref)
+    r.checked_rows = rows
     return r, stats

@@ -71,3 +71,58 @@ def test_quantised_kernels_count_their_code_bytes(quant, bytes_per_weight):
         scales = 4 * (bf.N1 if kind == "swiglu" else bf.d)
         assert fl_q == fl_b
         assert by_q == pytest.approx(by_b - touched * rows * (2 - bytes_per_weight) + touched * scales)
+
+
+def test_roofline_bytes_follow_the_layer_terms():
+    # Switch-style top-1 GELU layer: the up projection owns W1 of the 64 touched experts
+    # (64 * 4096 * 1024 * 2 B = 536.9 MB) and the read of x (8192 * 1024 * 2 B = 16.8 MB);
+    # hidden activations are an implementation buffer and are not counted
+    wl = get("switch")
+    fl, by = bench.kernel_roofline_cost(wl, "grouped_gemm_gelu", 8184, 64)
+    assert by == 64 * 4096 * 1024 * 2 + 8192 * 1024 * 2
+    assert fl == 2.0 * 8184 * 1024 * 4096
+    # the fused top-1 down projection also writes the layer output once
+    _, by_d = bench.kernel_roofline_cost(wl, "grouped_gemm_combine1", 8184, 64)
+    assert by_d == 64 * 1024 * 4096 * 2 + 8192 * 1024 * 2
+
+
+@pytest.mark.parametrize("name", ["switch", "deepseek", "mixtral", "decode64_i4"])
+def test_roofline_terms_of_the_kernels_add_up_to_the_layer(name):
+    # weights + W_gate + x + out over router, up, down (and combine) = the layer's bytes,
+    # except that the router and the up projection each must read x once
+    wl = get(name)
+    P, touched = wl.T * wl.k, min(wl.E, wl.T * wl.k)
+    up = "grouped_gemm_gelu" if wl.kind == "gelu" else "grouped_gemm_swiglu"
+    fused = wl.k == 1 and not wl.has_shared
+    names = ["router_gemm_topk", up, "grouped_gemm_combine1" if fused else "grouped_gemm_scale"]
+    if wl.has_shared:
+        names.append("grouped_gemm_f32")
+    if not fused:
+        names.append("combine_bf16")
+    by = sum(bench.kernel_roofline_cost(wl, n, P, touched)[1] for n in names)
+    fl = sum(bench.kernel_roofline_cost(wl, n, P, touched)[0] for n in names)
+    es = 2 if wl.bf16 else 4
+    assert by - wl.T * wl.d * es == pytest.approx(wl.bytes(touched), rel=1e-12)
+    assert fl == pytest.approx(wl.flops(P), rel=1e-12)
+
+
+def test_both_arms_report_the_same_config():
+    wl = get("deepseek")
+    a = bench.workload_config(wl, 1, 256)
+    b = bench.workload_config(wl, 1, 256)
+    assert a == b and a["workload"] == "deepseek" and "l2" in a
+    for k in ("kept_rows_P", "touched_experts"):     # run-derived values stay out of config
+        assert k not in a
+
+
+def test_default_workload_is_the_largest_single_gpu_layer():
+    args = bench.parse([])
+    assert args.workload == "deepseek"
+    assert get(args.workload).flops(get(args.workload).T * get(args.workload).k) == max(
+        get(n).flops(get(n).T * get(n).k) for n in bench.SWEEP + ["deepseek"])
+
+
+def test_cpu_oracle_sample_is_bounded_and_positive():
+    v, secs, desc = bench.cpu_oracle_sample(get("tiny"), 0.5, 0.5)
+    assert v > 0 and secs < 5
+    assert "all 64 tokens" in desc

@@ -213,17 +213,80 @@ def test_forward_is_deterministic():
 
 
 @pytest.mark.parametrize("name,sample", [
-    ("switch", 32), ("mixtral", 8), ("deepseek", 4), ("deepseek_cf125", 4),
-    ("deepseek_grouped", 4),
-    ("decode1", None), ("decode8", 4), ("decode64", 4),
-    ("decode1_i8", None), ("decode8_i8", 4), ("decode64_i8", 4), ("deepseek_reroute", 4),
-    ("decode1_i4", None), ("decode8_i4", 4), ("decode64_i4", 4),
-    ("switch_i8", 32), ("switch_i4", 32),
+    ("switch", 48), ("mixtral", 32), ("deepseek", 32), ("deepseek_cf125", 32),
+    ("deepseek_grouped", 32), ("deepseek_reroute", 32),
+    ("decode1", None), ("decode8", None), ("decode64", 16),
+    ("decode1_i8", None), ("decode8_i8", None), ("decode64_i8", 16),
+    ("decode1_i4", None), ("decode8_i4", None), ("decode64_i4", 16),
+    ("switch_i8", 48), ("switch_i4", 48),
 ])
 def test_full_size_sampled(name, sample):
-    r, stats = full_check(get(name), sample=sample, seed=1)
+    # routing and dispatch in full; outputs of the tokens at the row-block and M-tile
+    # boundaries of several experts, dropped and re-routed tokens, topped up with random
+    # ones; the staged expert-output rows at those boundaries
+    r, stats = full_check(get(name), sample=sample, seed=1, targeted=True)
+    if sample is not None:
+        assert len(r.checked_rows) >= sample
     del r
     torch.cuda.empty_cache()
+
+
+# Exact ties among logits, on every selection path: the lower expert id wins, ties of
+# group scores go to the lower group, and re-routing candidates follow the same order.
+TIES = {
+    # W_gate = 0: every logit equal, so the ids are 0..k-1 and every weight is 1/k
+    "zero_f32_cuda_core": W("z1", T=96, d=16, E=8, k=3, F=16, kind="linear", act="f32",
+                            gate_dist="zero", expert_bias=True),
+    "zero_splitk": W("z2", T=40, d=256, E=64, k=6, F=64, kind="gelu", act="bf16",
+                     gate_dist="zero"),
+    "zero_tc_fused": W("z3", T=300, d=128, E=32, k=4, F=64, kind="gelu", act="bf16",
+                       gate_dist="zero"),
+    "zero_tc_fused_ksplit": W("z4", T=300, d=2048, E=16, k=2, F=64, kind="gelu", act="bf16",
+                              gate_dist="zero"),
+    "zero_tc_topk_kernel": W("z5", T=300, d=128, E=128, k=8, F=64, kind="gelu", act="bf16",
+                             gate_dist="zero"),
+    "zero_grouped": W("z6", T=300, d=128, E=64, k=4, F=64, kind="gelu", act="bf16",
+                      gate_dist="zero", n_group=8, topk_group=2),
+    # integer x and W_gate: integer logits with many exact ties, inside the top k and at
+    # its boundary
+    "grid_f32_cuda_core": W("g1", T=96, d=16, E=8, k=3, F=16, kind="linear", act="f32",
+                            gate_dist="grid", x_dist="grid", expert_bias=True),
+    "grid_splitk": W("g2", T=40, d=256, E=64, k=6, F=64, kind="gelu", act="bf16",
+                     gate_dist="grid", x_dist="grid"),
+    "grid_tc_fused": W("g3", T=300, d=128, E=32, k=4, F=64, kind="gelu", act="bf16",
+                       gate_dist="grid", x_dist="grid"),
+    "grid_tc_fused_ksplit": W("g4", T=300, d=2048, E=16, k=2, F=64, kind="gelu", act="bf16",
+                              gate_dist="grid", x_dist="grid"),
+    "grid_tc_topk_kernel": W("g5", T=300, d=128, E=128, k=8, F=64, kind="gelu", act="bf16",
+                             gate_dist="grid", x_dist="grid"),
+    "grid_grouped_tc": W("g6", T=300, d=128, E=64, k=4, F=64, kind="gelu", act="bf16",
+                         gate_dist="grid", x_dist="grid", n_group=8, topk_group=2),
+    "grid_grouped_splitk": W("g7", T=40, d=256, E=64, k=6, F=64, kind="gelu", act="bf16",
+                             gate_dist="grid", x_dist="grid", n_group=16, topk_group=3),
+    "grid_reroute_tc": W("g8", T=300, d=128, E=16, k=2, F=64, kind="gelu", act="bf16",
+                         gate_dist="grid", x_dist="grid", cf=0.5, overflow="reroute"),
+    "grid_reroute_grouped_splitk": W("g9", T=40, d=256, E=64, k=6, F=64, kind="gelu",
+                                     act="bf16", gate_dist="grid", x_dist="grid", n_group=16,
+                                     topk_group=3, cf=1.0, overflow="reroute"),
+}
+
+
+@pytest.mark.parametrize("name", list(TIES))
+def test_tied_logits_select_the_lower_expert_id(name):
+    wl = TIES[name]
+    r, _ = full_check(wl)          # ids, dispatch bit-exact; every token's output
+    L = to_np(r.logits)
+    assert np.array_equal(L, np.rint(L)), "integer inputs must give exact integer logits"
+    if wl.gate_dist == "zero":
+        assert (to_np(r.idx) == np.arange(wl.k)).all()
+        assert np.abs(to_np(r.w) - np.float32(1.0 / wl.k)).max() <= 2e-6
+        return
+    # the ties were really there: the k-th and (k+1)-th largest logits are equal in many
+    # rows, and so are two logits inside the top k
+    srt = -np.sort(-L, axis=1)
+    assert (srt[:, wl.k - 1] == srt[:, wl.k]).mean() >= 0.1
+    if wl.k > 1:
+        assert (srt[:, :wl.k - 1] == srt[:, 1:wl.k]).any(axis=1).mean() >= 0.1
 
 
 def test_layer_object_matches_forward():
