@@ -132,6 +132,15 @@ SMALL = {
                 expert_bias=True, has_shared=True, int4=True),
     "i4_reroute_k4": W("q4g", T=48, d=256, E=16, k=4, F=128, kind="swiglu", act="bf16",
                        cf=0.5, gate_bias="zipf", int4=True, overflow="reroute"),
+    # 256-row tiles (>= ~200 rows per expert; k >= 4 then reads x_perm instead of gathering
+    # in the GEMM), a shared expert, ragged M (300 rows = 256 + 44) and N tiles; three M
+    # tiles with an 88-row last one; a long-K down projection (F >= 4096) with 256-row tiles
+    "wide_k4_shared": W("gw4", T=600, d=192, E=8, k=4, F=192, kind="swiglu",
+                               act="bf16", cf=1.0, has_shared=True),
+    "wide_gelu_bias_k2": W("wg2", T=1200, d=128, E=4, k=2, F=320, kind="gelu", act="bf16",
+                           expert_bias=True),
+    "wide_long_k_down": W("wld", T=520, d=128, E=2, k=1, F=4096, kind="swiglu", act="bf16",
+                          has_shared=True, expert_bias=True),
 }
 
 
@@ -470,10 +479,11 @@ def test_quantised_layers_use_their_kernels(name, prefix):
 
 
 @pytest.mark.parametrize("name,gathers", [("swiglu_k8_cap_shared", True), ("max_E_max_k", True),
-                                          ("gelu_bias_k2", False)])
+                                          ("gelu_bias_k2", False), ("wide_k4_shared", False)])
 def test_forward_gathers_rows_in_the_gemm_for_many_slots(name, gathers):
-    # k >= 4: moe_forward's up projection reads rows of x through perm_token itself (no
-    # row-gather kernel); the staged path still materialises x_perm. Both match the oracle
+    # k >= 4 with 128-row tiles: moe_forward's up projection reads rows of x through
+    # perm_token itself (no row-gather kernel); the staged path still materialises x_perm,
+    # and so does the forward with 256-row tiles. Both match the oracle
     # (full_check in test_small_parity) and each other.
     wl = SMALL[name]
     moe.profile_begin()

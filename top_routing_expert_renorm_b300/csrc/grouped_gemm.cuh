@@ -8,9 +8,14 @@
 // applied to the tokens routed to it, silu on the W1 slice) run as one launch over
 // all experts instead of a loop.
 //
-// Tiling: 128 rows x 256 accumulator columns x 64 K per stage, 4-stage TMA ring
-// (48 KB per stage, 128-byte swizzle), two 256-column fp32 accumulators in TMEM so
+// Tiling (MT = 1): 128 rows x 256 accumulator columns x 64 K per stage, 4-stage TMA
+// ring (48 KB per stage, 128-byte swizzle), two 256-column fp32 accumulators in TMEM so
 // the epilogue of one tile overlaps the MMAs of the next.
+// Wide tiles (MT = 2, groups of >= ~200 rows): 256 rows x 256 columns per tile, two M = 128
+// MMAs per K step sharing the B tile, 3-stage ring of 64 KB stages, the two 128-row
+// halves filling all 512 TMEM columns (one accumulator set). Per FLOP a tile then moves
+// a third fewer operand bytes from L2 and the ring covers 1.5x the load latency, at the
+// cost of an epilogue that no longer overlaps the next tile's MMAs.
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer (+ TMEM
 // allocation), warps 2-5 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
 // Tiles are ordered expert-major, then N block, then M block, so the CTAs working
@@ -95,6 +100,9 @@ constexpr int GM_BM = 128, GM_BN = 256, GM_BK = 64, GM_STAGES = 4;
 constexpr int GM_A_BYTES = GM_BM * GM_BK * 2;     // 16 KB
 constexpr int GM_B_BYTES = GM_BN * GM_BK * 2;     // 32 KB
 constexpr int GM_STAGE_BYTES = GM_A_BYTES + GM_B_BYTES;
+// per M-tile height MT (128-row halves per tile): ring depth and stage size
+__host__ __device__ constexpr int gm_stages(int MT) { return MT == 1 ? GM_STAGES : 3; }
+__host__ __device__ constexpr int gm_stage_bytes(int MT) { return MT * GM_A_BYTES + GM_B_BYTES; }
 constexpr int GM_THREADS = 192;
 constexpr int GM_GATHER_THREADS = 128;    // extra warps 6..9 that gather A rows
 constexpr int GM_TMEM_COLS = 512;
@@ -102,8 +110,30 @@ constexpr int GM_MAX_GROUPS = 1025;
 constexpr int GM_TQ = 8;            // depth of the ring of scheduled unit ids
 constexpr int GM_HDR_BYTES = 512;   // barriers, TMEM address, abort flag, unit-id ring
 
-__host__ __device__ constexpr int gm_smem_bytes(int G) {
-    return 1024 + GM_STAGES * GM_STAGE_BYTES + GM_HDR_BYTES + 2 * (G + 1) * 4;
+__host__ __device__ constexpr int gm_smem_bytes(int G, int MT = 1) {
+    return 1024 + gm_stages(MT) * gm_stage_bytes(MT) + GM_HDR_BYTES + 2 * (G + 1) * 4;
+}
+
+// s_mt[0..G] = exclusive scan over the groups of ceil(rows_g / bm), from the row offsets
+// s_ro[0..G] (both in shared memory); one warp, lanes take contiguous runs of groups.
+__device__ __forceinline__ void gm_tile_table_warp(const int* s_ro, int* s_mt, int G, int bm,
+                                                   int lane) {
+    const int per = (G + 31) / 32;
+    const int g0 = min(G, lane * per), g1 = min(G, g0 + per);
+    int sum = 0;
+    for (int g = g0; g < g1; ++g) sum += (s_ro[g + 1] - s_ro[g] + bm - 1) / bm;
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    int run = incl - sum;
+    for (int g = g0; g < g1; ++g) {
+        s_mt[g] = run;
+        run += (s_ro[g + 1] - s_ro[g] + bm - 1) / bm;
+    }
+    if (lane == 31) s_mt[G] = incl;
 }
 
 // Work unit t -> (group g, M block mb, N block nb, K split ks). Units of one group are
@@ -167,8 +197,7 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
         for (int c = 0; c < 4; ++c) {
             float gv[32], uv[32];
             __syncwarp();
-            tmem_load_32cols(tb + c * 32, gv);
-            tmem_load_32cols(tb + 128 + c * 32, uv);
+            tmem_load_2x32cols(tb + c * 32, tb + 128 + c * 32, gv, uv);
             const int col = n0 + c * 32;
             if (row_ok && col < p.N) {
                 if (srow) {
@@ -188,7 +217,7 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
                         u0 += brow[p.up_offset + col + 2 * i];
                         u1 += brow[p.up_offset + col + 2 * i + 1];
                     }
-                    packed[i] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
+                    packed[i] = pack_bf16x2(silu_fast(g0) * u0, silu_fast(g1) * u1);
                 }
                 uint4* dst = reinterpret_cast<uint4*>(orow + col);
 #pragma unroll
@@ -390,31 +419,35 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
         }
         float* orow = reinterpret_cast<float*>(p.out) + grow * p.ld_out;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-            float v[32];
+        for (int c2 = 0; c2 < 8; c2 += 2) {   // two 32-column chunks per TMEM wait
+            float vv[2][32];
             __syncwarp();
-            tmem_load_32cols(tb + c * 32, v);
-            const int col = n0 + c * 32;
-            if (row_ok && col < p.N) {
-                if (srow) {
+            tmem_load_2x32cols(tb + c2 * 32, tb + (c2 + 1) * 32, vv[0], vv[1]);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] *= srow[col + i];
-                }
-                float4* dst = reinterpret_cast<float4*>(orow + col);
+            for (int h = 0; h < 2; ++h) {
+                float (&v)[32] = vv[h];
+                const int col = n0 + (c2 + h) * 32;
+                if (row_ok && col < p.N) {
+                    if (srow) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float4 o;
-                    o.x = v[4 * i + 0] + (brow ? brow[col + 4 * i + 0] : 0.0f);
-                    o.y = v[4 * i + 1] + (brow ? brow[col + 4 * i + 1] : 0.0f);
-                    o.z = v[4 * i + 2] + (brow ? brow[col + 4 * i + 2] : 0.0f);
-                    o.w = v[4 * i + 3] + (brow ? brow[col + 4 * i + 3] : 0.0f);
-                    if constexpr (EPI == EPI_SCALE_F32) {
-                        o.x *= scale;
-                        o.y *= scale;
-                        o.z *= scale;
-                        o.w *= scale;
+                        for (int i = 0; i < 32; ++i) v[i] *= srow[col + i];
                     }
-                    dst[i] = o;
+                    float4* dst = reinterpret_cast<float4*>(orow + col);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float4 o;
+                        o.x = v[4 * i + 0] + (brow ? brow[col + 4 * i + 0] : 0.0f);
+                        o.y = v[4 * i + 1] + (brow ? brow[col + 4 * i + 1] : 0.0f);
+                        o.z = v[4 * i + 2] + (brow ? brow[col + 4 * i + 2] : 0.0f);
+                        o.w = v[4 * i + 3] + (brow ? brow[col + 4 * i + 3] : 0.0f);
+                        if constexpr (EPI == EPI_SCALE_F32) {
+                            o.x *= scale;
+                            o.y *= scale;
+                            o.z *= scale;
+                            o.w *= scale;
+                        }
+                        dst[i] = o;
+                    }
                 }
             }
         }
@@ -436,15 +469,22 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 constexpr int GM_GATHER_DEPTH = 2;   // stages a gather thread keeps in flight before arriving
 
-template <int EPI>
+template <int EPI, int MT = 1>
 __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+    static_assert(MT == 1 || MT == 2, "tiles are 128 or 256 rows");
+    static_assert(MT == 1 || EPI != EPI_ROUTER_TOPK, "the router runs 128-row tiles");
+    constexpr int STAGES = gm_stages(MT);
+    constexpr int STAGE_BYTES = gm_stage_bytes(MT);
+    constexpr int A_BYTES = MT * GM_A_BYTES;
+    constexpr int BM = MT * GM_BM;
+    constexpr int NACC = MT == 1 ? 2 : 1;   // accumulator sets in TMEM (256 x 128 lanes each)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     uint8_t* tiles = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GM_STAGES * GM_STAGE_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
     // barrier slots: full[0..3], empty[4..7], tfull[8..9], tempty[10..11], drain[12],
     // unit-id ring full[16..23] / empty[24..31]
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 32);
@@ -461,7 +501,7 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
 
     const bool gather = p.a_gather != nullptr;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < GM_STAGES; ++s) {
+        for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar(FULL + s), gather ? 5 : 1);   // + the four gather warps
             mbar_init(bar(EMPTY + s), 1);
         }
@@ -488,7 +528,11 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
     pdl_entry();
     for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
         s_ro[i] = p.row_offsets[i];
-        s_mt[i] = p.mtile_offsets[i];
+        if (MT == 1) s_mt[i] = p.mtile_offsets[i];
+    }
+    if (MT > 1) {   // tiles of BM rows: the table is formed here from the row offsets
+        __syncthreads();
+        if (warp == 2) gm_tile_table_warp(s_ro, s_mt, p.G, BM, lane);
     }
     tc_fence_before();
     __syncthreads();
@@ -502,9 +546,9 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
             // ---------------- TMA producer ----------------
             int stage = 0;
             uint32_t ph = 0;
-            int last_par[GM_STAGES];
+            int last_par[STAGES];
 #pragma unroll
-            for (int s = 0; s < GM_STAGES; ++s) last_par[s] = -1;
+            for (int s = 0; s < STAGES; ++s) last_par[s] = -1;
             bool ok = true;
             int q = 0;
             uint32_t qph = 0;
@@ -530,7 +574,7 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
                 gm_decode(t, p.G, p.n_tiles, p.k_splits, s_mt, g, mb, nb, ks);
                 const int kb0 = ks * p.kb_per_split;
                 const int kb1 = min(kblocks, kb0 + p.kb_per_split);
-                const int a_row = s_ro[g] + mb * GM_BM;
+                const int a_row = s_ro[g] + mb * BM;
                 const int n0 = (EPI == EPI_SWIGLU_BF16) ? nb * 128 : nb * GM_BN;
                 const int b0 = g * p.b_rows_per_group + n0;
                 const int b1 = b0 + p.up_offset;
@@ -540,14 +584,19 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    const uint32_t sa = smem_addr(tiles + stage * GM_STAGE_BYTES);
-                    mbar_arrive_expect_tx(bar(FULL + stage), gather ? GM_B_BYTES : GM_STAGE_BYTES);
-                    if (!gather) tma_load_2d(sa, &tmA, bar(FULL + stage), kb * GM_BK, a_row);
-                    tma_load_2d(sa + GM_A_BYTES, &tmB, bar(FULL + stage), kb * GM_BK, b0);
-                    tma_load_2d(sa + GM_A_BYTES + GM_B_BYTES / 2, &tmB, bar(FULL + stage),
+                    const uint32_t sa = smem_addr(tiles + stage * STAGE_BYTES);
+                    mbar_arrive_expect_tx(bar(FULL + stage), gather ? GM_B_BYTES : STAGE_BYTES);
+                    if (!gather) {
+#pragma unroll
+                        for (int h = 0; h < MT; ++h)
+                            tma_load_2d(sa + h * GM_A_BYTES, &tmA, bar(FULL + stage), kb * GM_BK,
+                                        a_row + h * GM_BM);
+                    }
+                    tma_load_2d(sa + A_BYTES, &tmB, bar(FULL + stage), kb * GM_BK, b0);
+                    tma_load_2d(sa + A_BYTES + GM_B_BYTES / 2, &tmB, bar(FULL + stage),
                                 kb * GM_BK, b1);
                     last_par[stage] = (int)ph;
-                    if (++stage == GM_STAGES) {
+                    if (++stage == STAGES) {
                         stage = 0;
                         ph ^= 1;
                     }
@@ -555,7 +604,7 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
                 t = next;
             }
             // Every copy this thread started must have landed before the CTA exits.
-            for (int s = 0; s < GM_STAGES; ++s)
+            for (int s = 0; s < STAGES; ++s)
                 if (last_par[s] >= 0) mbar_wait(bar(FULL + s), (uint32_t)last_par[s]);
         }
     } else if (warp == 1) {
@@ -578,6 +627,8 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
                     qph ^= 1;
                 }
                 if (t < 0) break;
+                // MT = 1: accumulator set acc (columns acc*256), freed as a whole.
+                // MT = 2: halves h (columns h*256) freed one after the other (TEMPTY + h).
                 if (*s_abort || !mbar_wait(bar(TEMPTY + acc), aph ^ 1)) {
                     *s_abort = 1;
                     break;
@@ -588,29 +639,82 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
                 const int kb0 = (int)within * p.kb_per_split;
                 const int kb1 = min(kblocks, kb0 + p.kb_per_split);
                 bool ok = true;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                int kb_start = kb0;
+                if constexpr (MT == 2) {
+                    // While the epilogue still drains half 1 of the previous tile, run half
+                    // 0's MMAs over the first J stages of this one; then half 1's over the
+                    // same stages, releasing them. Each half still accumulates in K order.
+                    const int J = min(STAGES, kb1 - kb0);
+                    int st = stage;
+                    uint32_t sph = ph;
+                    for (int j = 0; j < J && ok; ++j) {
+                        if (!mbar_wait(bar(FULL + st), sph)) {
+                            *s_abort = 1;
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sa = smem_addr(tiles + st * STAGE_BYTES);
+#pragma unroll
+                        for (int kk = 0; kk < GM_BK / 16; ++kk)
+                            umma_bf16(dt, sw128_kmajor_desc(sa + kk * 32),
+                                      sw128_kmajor_desc(sa + A_BYTES + kk * 32), idesc,
+                                      (j != 0 || kk != 0) ? 1u : 0u);
+                        if (++st == STAGES) {
+                            st = 0;
+                            sph ^= 1;
+                        }
+                    }
+                    if (!ok) break;
+                    if (*s_abort || !mbar_wait(bar(TEMPTY + 1), aph ^ 1)) {
+                        *s_abort = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int j = 0; j < J; ++j) {
+                        const uint32_t sa = smem_addr(tiles + stage * STAGE_BYTES);
+#pragma unroll
+                        for (int kk = 0; kk < GM_BK / 16; ++kk)
+                            umma_bf16(dt + GM_BN, sw128_kmajor_desc(sa + GM_A_BYTES + kk * 32),
+                                      sw128_kmajor_desc(sa + A_BYTES + kk * 32), idesc,
+                                      (j != 0 || kk != 0) ? 1u : 0u);
+                        umma_commit(bar(EMPTY + stage));
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            ph ^= 1;
+                        }
+                    }
+                    kb_start = kb0 + J;
+                }
+                for (int kb = kb_start; kb < kb1; ++kb) {
                     if (!mbar_wait(bar(FULL + stage), ph)) {
                         *s_abort = 1;
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_addr(tiles + stage * GM_STAGE_BYTES);
-                    const uint32_t sb = sa + GM_A_BYTES;
+                    const uint32_t sa = smem_addr(tiles + stage * STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < GM_BK / 16; ++kk)
-                        umma_bf16(dt, sw128_kmajor_desc(sa + kk * 32), sw128_kmajor_desc(sb + kk * 32),
-                                  idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+#pragma unroll
+                        for (int h = 0; h < MT; ++h)
+                            umma_bf16(dt + (uint32_t)(h * GM_BN),
+                                      sw128_kmajor_desc(sa + h * GM_A_BYTES + kk * 32),
+                                      sw128_kmajor_desc(sb + kk * 32), idesc,
+                                      (kb != kb0 || kk != 0) ? 1u : 0u);
                     umma_commit(bar(EMPTY + stage));
-                    if (++stage == GM_STAGES) {
+                    if (++stage == STAGES) {
                         stage = 0;
                         ph ^= 1;
                     }
                 }
                 if (!ok) break;
                 umma_commit(bar(TFULL + acc));
-                acc ^= 1;
-                if (acc == 0) aph ^= 1;
+                if (++acc == NACC) {
+                    acc = 0;
+                    aph ^= 1;
+                }
             }
             // All MMAs issued by this thread must be complete before TMEM is freed.
             umma_commit(bar(DRAIN));
@@ -618,10 +722,11 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
         }
     } else if (warp >= 6) {
         // ---------------- A rows gathered with cp.async (warps 6..9) ----------------
-        // Thread a copies 16-byte chunk (a & 7) of rows (a >> 3) + 16 i, i = 0..7, of each
-        // K block into the 128-byte-swizzled A tile. A stage's copies are waited for (and
-        // made visible to the tensor core) GM_GATHER_DEPTH stages later, then the warp
+        // Thread a copies 16-byte chunk (a & 7) of rows (a >> 3) + 16 i, i = 0..8*MT-1, of
+        // each K block into the 128-byte-swizzled A tile. A stage's copies are waited for
+        // (and made visible to the tensor core) GM_GATHER_DEPTH stages later, then the warp
         // arrives on the stage's FULL barrier.
+        constexpr int RPT = 8 * MT;   // rows per thread
         const int a = threadIdx.x - GM_THREADS;
         const int chunk = a & 7, r0 = a >> 3;
         int stage = 0;
@@ -665,11 +770,11 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
             const int kb0 = ks * p.kb_per_split;
             const int kb1 = min(kblocks, kb0 + p.kb_per_split);
             const int rows_g = s_ro[g + 1] - s_ro[g];
-            const uint8_t* src[8];
-            uint32_t nbytes[8];
+            const uint8_t* src[RPT];
+            uint32_t nbytes[RPT];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = mb * GM_BM + r0 + 16 * i;
+            for (int i = 0; i < RPT; ++i) {
+                const int r = mb * BM + r0 + 16 * i;
                 const bool valid = r < rows_g;
                 const long long tok = valid ? (long long)p.a_gather[s_ro[g] + r] : 0;
                 src[i] = p.a_src + tok * p.a_row_bytes + chunk * 16;
@@ -682,10 +787,10 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
                     ok = false;
                     break;
                 }
-                const uint32_t sa = smem_addr(tiles + stage * GM_STAGE_BYTES);
+                const uint32_t sa = smem_addr(tiles + stage * STAGE_BYTES);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int r = r0 + 16 * i;
+                for (int i = 0; i < RPT; ++i) {
+                    const int r = r0 + 16 * i;   // row of the BM-row tile (halves are contiguous)
                     cp_async_16(sa + r * 128 + ((chunk ^ (r & 7)) << 4), src[i] + kb * GM_BK * 2,
                                 nbytes[i]);
                 }
@@ -695,7 +800,7 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
                     cp_async_wait<GM_GATHER_DEPTH>();
                     release_oldest();
                 }
-                if (++stage == GM_STAGES) {
+                if (++stage == STAGES) {
                     stage = 0;
                     ph ^= 1;
                 }
@@ -742,19 +847,30 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
                 break;
             }
             tc_fence_after();
-            const int r_in = q * 32 + lane;
             const int rows_g = s_ro[g + 1] - s_ro[g];
-            const int r_tile = mb * GM_BM + r_in;   // row within the group
-            const bool row_ok = r_tile < rows_g;
-            const long long grow = (long long)s_ro[g] + r_tile;
-            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * GM_BN);
-            if (p.partial) gm_epilogue_partial<EPI>(p, tb, nb, ks, row_ok, grow);
-            else gm_epilogue_tile<EPI>(p, tb, g, nb, row_ok, grow, mb, ks, s_flag);
+#pragma unroll 1
+            for (int h = 0; h < MT; ++h) {
+                const int r_in = h * GM_BM + q * 32 + lane;
+                const int r_tile = mb * BM + r_in;   // row within the group
+                const bool row_ok = r_tile < rows_g;
+                const long long grow = (long long)s_ro[g] + r_tile;
+                const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                    (uint32_t)((acc + h) * GM_BN);
+                if (p.partial) gm_epilogue_partial<EPI>(p, tb, nb, ks, row_ok, grow);
+                else gm_epilogue_tile<EPI>(p, tb, g, nb, row_ok, grow, mb, ks, s_flag);
+                if (MT == 2 && h == 0) {   // half 0 is free for the next tile's MMAs
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(TEMPTY + 0));
+                }
+            }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(TEMPTY + acc));
-            acc ^= 1;
-            if (acc == 0) aph ^= 1;
+            if (lane == 0) mbar_arrive(bar(TEMPTY + (MT == 2 ? 1 : acc)));
+            if (++acc == NACC) {
+                acc = 0;
+                aph ^= 1;
+            }
         }
     }
 
@@ -827,7 +943,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmParams p,
         if constexpr (EPI == EPI_SWIGLU_BF16 || EPI == EPI_GELU_BF16) {
             float h0, h1, h2, h3;
             if constexpr (EPI == EPI_SWIGLU_BF16) {
-                h0 = silu(a.x) * u.x; h1 = silu(a.y) * u.y; h2 = silu(a.z) * u.z; h3 = silu(a.w) * u.w;
+                h0 = silu_fast(a.x) * u.x; h1 = silu_fast(a.y) * u.y; h2 = silu_fast(a.z) * u.z;
+                h3 = silu_fast(a.w) * u.w;
             } else {
                 h0 = gelu_erf(a.x); h1 = gelu_erf(a.y); h2 = gelu_erf(a.z); h3 = gelu_erf(a.w);
             }

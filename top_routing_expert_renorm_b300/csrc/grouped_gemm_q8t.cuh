@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
                         for (int j = 0; j < QT_NT; ++j)
                             if (j < nvalid)
                                 O[(long long)j * p.ld_out] =
-                                    __float2bfloat16_rn(silu(a0[j] * sg + bg) * (a1[j] * su + bu));
+                                    __float2bfloat16_rn(silu_fast(a0[j] * sg + bg) * (a1[j] * su + bu));
                     }
                 }
             } else {

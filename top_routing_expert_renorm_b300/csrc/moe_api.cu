@@ -347,6 +347,34 @@ bool q8t_shared(const moe_config& c) {
     return c.w_dtype == MOE_I4 || (c.w_dtype == MOE_I8 && c.T <= 64);
 }
 
+// Tile heights of the bf16 expert GEMMs. 256-row tiles (two M = 128 MMAs sharing each B
+// tile, one accumulator set) move a third fewer operand bytes per FLOP and their 3-stage
+// ring covers 1.5x the load latency of the 128-row tiles' 4-stage ring, but their epilogue
+// no longer overlaps the next tile's MMAs. Measured (per-role wait counters): they win for
+// groups of >= ~200 rows when K is long enough for the mainloop to dwarf the epilogue --
+// the up projections (K = d) and down projections with K = F >= 4096; for the DeepSeek-V3
+// down projection (K = 2048, fp32 row stores) they lose. With 256-row tiles the A rows are
+// read from a materialised x_perm by TMA: the cp.async row gather cannot keep enough of
+// the 3-stage ring in flight.
+constexpr double kWideTileMinRows = 192.0;
+constexpr int kWideDownMinK = 4096;
+
+struct ExpertTiles {
+    int up = 1, down = 1, sh_up = 1, sh_down = 1;
+};
+
+ExpertTiles expert_tiles(const moe_config& c) {
+    ExpertTiles t;
+    if (c.kind == MOE_EXPERT_LINEAR || c.w_dtype == MOE_I8 || c.w_dtype == MOE_I4) return t;
+    const double routed_rows = (double)c.T * c.top_k / c.E;
+    const bool r = routed_rows >= kWideTileMinRows, sh = (double)c.T >= kWideTileMinRows;
+    t.up = r ? 2 : 1;
+    t.down = (r && c.F >= kWideDownMinK) ? 2 : 1;
+    t.sh_up = sh ? 2 : 1;
+    t.sh_down = (sh && c.F >= kWideDownMinK) ? 2 : 1;
+    return t;
+}
+
 // Split plan of a weight-streaming launch, in 128-code K blocks. An INT4 code stage holds
 // two of them and a split must start on one, so INT4 plans are made over 256-code blocks.
 SplitPlan qt_split_plan(long long max_mtiles, int n_tiles, int K, int sms, int bits) {
@@ -595,7 +623,8 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
                        const float* w_scale = nullptr, bool swap_ab = false,
                        int* r_hist = nullptr, const int32_t* a_gather = nullptr,
                        int a_row_bytes = 0, float* r_part = nullptr, int* r_tile_cnt = nullptr,
-                       int w_bits = 8) {
+                       int w_bits = 8, int mt = 1) {
+    // mt: 128-row halves per tile of the bf16 kernel (2: 256-row tiles, unsplit launches)
     // r_part, r_tile_cnt (EPI_ROUTER_TOPK with sp.S == 2): the epilogue's split-K exchange
     // a_gather (bf16 kernel only): logical A row r (r < a_rows) is row a_gather[r] of A,
     // loaded by the kernel's gather warps
@@ -711,6 +740,25 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
         MOE_LAUNCH(name ? name : gemm_q8_name<EPI>(), s,
                    launch_k(grouped_gemm_q8_kernel<EPI>, grid, GM_Q8_THREADS, gm_q8_smem_bytes(G), s,
                             ta, tb, p));
+    } else if (mt == 2 && !split) {
+        if constexpr (EPI != EPI_ROUTER_TOPK) {
+            static std::once_flag wide_once[64];
+            static cudaError_t wide_err[64];
+            if (dev >= 0 && dev < 64) {
+                std::call_once(wide_once[dev], [&] {
+                    wide_err[dev] = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, 2>,
+                                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                         gm_smem_bytes(GM_MAX_GROUPS, 2));
+                });
+                if (wide_err[dev] != cudaSuccess) return MOE_ERR_CUDA;
+            }
+            MOE_LAUNCH(name ? name : gemm_name<EPI>(), s,
+                       launch_k(grouped_gemm_kernel<EPI, 2>, grid,
+                                GM_THREADS + (p.a_gather ? GM_GATHER_THREADS : 0),
+                                gm_smem_bytes(G, 2), s, ta, tb, p));
+        } else {
+            return MOE_ERR_UNSUPPORTED;
+        }
     } else {
         MOE_LAUNCH(name ? name : gemm_name<EPI>(), s,
                    launch_k(grouped_gemm_kernel<EPI>, grid,
@@ -856,18 +904,19 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
     const bool ga = gather_a && !q8;
     const void* a_up = ga ? x : x_perm;
     const int32_t* a_idx = ga ? perm_token : nullptr;
+    const ExpertTiles et = expert_tiles(c);
     if (c.kind == MOE_EXPERT_SWIGLU)
         MOE_TRY(launch_gemm<EPI_SWIGLU_BF16>(a_up, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
                                              offsets, mtile, h, F, R.b1, nullptr, nullptr, nullptr,
                                              k, s, nullptr, fp.up, partial, counters + kCntUp,
                                              nullptr, nullptr, nullptr, 0, 0, rs1, swap_r, nullptr,
-                                             a_idx, d * 2, nullptr, nullptr, wb));
+                                             a_idx, d * 2, nullptr, nullptr, wb, ga ? 1 : et.up));
     else
         MOE_TRY(launch_gemm<EPI_GELU_BF16>(a_up, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
                                            offsets, mtile, h, F, R.b1, nullptr, nullptr, nullptr, k,
                                            s, nullptr, fp.up, partial, counters + kCntUp, nullptr,
                                            nullptr, nullptr, 0, 0, rs1, swap_r, nullptr, a_idx,
-                                           d * 2, nullptr, nullptr, wb));
+                                           d * 2, nullptr, nullptr, wb, ga ? 1 : et.up));
     if (fused_out)
         MOE_TRY(launch_gemm<EPI_COMBINE1_BF16>(h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets,
                                                mtile, fused_out, d, R.b2, topk_w, perm_token,
@@ -879,7 +928,7 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
                                            mtile, y, d, R.b2, topk_w, perm_token, perm_slot, k, s,
                                            nullptr, fp.down, partial, counters + kCntDown, nullptr,
                                            nullptr, nullptr, 0, 0, rs2, swap_r, nullptr,
-                                           nullptr, 0, nullptr, nullptr, wb));
+                                           nullptr, 0, nullptr, nullptr, wb, et.down));
     if (c.has_shared) {
         MOE_LAUNCH("single_group_table", s,
                    launch_k(single_group_table_kernel, 1, 32, 0, s, T, shared_tab, shared_tab + 2,
@@ -890,19 +939,19 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
                                                  nullptr, k, s, nullptr, fp.sh_up, partial,
                                                  counters + kCntSharedUp, nullptr, nullptr,
                                                  nullptr, 0, 0, q8 ? S->s1 : nullptr, swap_s,
-                                           nullptr, nullptr, 0, nullptr, nullptr, wb));
+                                           nullptr, nullptr, 0, nullptr, nullptr, wb, et.sh_up));
         else
             MOE_TRY(launch_gemm<EPI_GELU_BF16>(x, T, d, S->w1, N1, (int)N1, 1, F, shared_tab,
                                                shared_tab + 2, hs, F, S->b1, nullptr, nullptr,
                                                nullptr, k, s, nullptr, fp.sh_up, partial,
                                                counters + kCntSharedUp, nullptr, nullptr, nullptr,
                                                0, 0, q8 ? S->s1 : nullptr, swap_s,
-                                           nullptr, nullptr, 0, nullptr, nullptr, wb));
+                                           nullptr, nullptr, 0, nullptr, nullptr, wb, et.sh_up));
         MOE_TRY(launch_gemm<EPI_F32>(hs, T, F, S->w2, d, d, 1, d, shared_tab, shared_tab + 2,
                                      y_shared, d, S->b2, nullptr, nullptr, nullptr, k, s, nullptr,
                                      fp.sh_down, partial, counters + kCntSharedDown, nullptr,
                                      nullptr, nullptr, 0, 0, q8 ? S->s2 : nullptr, swap_s,
-                                           nullptr, nullptr, 0, nullptr, nullptr, wb));
+                                           nullptr, nullptr, 0, nullptr, nullptr, wb, et.sh_down));
     }
     return MOE_OK;
 }
@@ -1066,10 +1115,12 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate
     int32_t* perm_slot = at<int32_t>(ws, L.perm_slot);
     int32_t* slot_dest = at<int32_t>(ws, L.slot_dest);
     void* x_perm = at<void>(ws, L.x_perm);
-    // bf16 experts with k >= 4: the up projection gathers its rows of x itself (no x_perm
-    // copy, which is k times the size of x). With fewer slots per token the copy is cheaper
-    // than the slower A loads of the gathering kernel (16-byte cp.async instead of TMA).
-    const bool gather_a = is_bf16_kind(c) && !quant_w(c) && c.top_k >= 4;
+    // bf16 experts with k >= 4 and 128-row tiles: the up projection gathers its rows of x
+    // itself (no x_perm copy, which is k times the size of x). With fewer slots per token
+    // the copy is cheaper than the slower A loads of the gathering kernel (16-byte cp.async
+    // instead of TMA), and 256-row tiles read a materialised x_perm (see expert_tiles).
+    const bool gather_a =
+        is_bf16_kind(c) && !quant_w(c) && c.top_k >= 4 && expert_tiles(c).up == 1;
     float* y = at<float>(ws, L.y);
     int32_t* mtile = at<int32_t>(ws, L.mtile);
     // Top-1 layers without a shared expert write the output from the down projection.
