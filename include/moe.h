@@ -205,10 +205,10 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32
  *            + (has_shared ? a_t * y[T*k + t] : 0)
  * summed in fp32 in that order and rounded once to act_dtype; a_t = 1, or with
  * MOE_OVERFLOW_SHARED a_t = 1 + sum of topk_w[t, j] over the dropped slots (fp32, slot order).
- *   x [T, d] (read iff add_residual), y as written by moe_expert_ffn, slot_dest [T, k],
- *   topk_w [T, k] (read iff MOE_OVERFLOW_SHARED, else nullable), out [T, d] act_dtype output. */
+ *   x [T, d] (read iff add_residual), y as written by moe_expert_ffn, topk_w [T, k] (read
+ *   iff MOE_OVERFLOW_SHARED, else nullable), slot_dest [T, k], out [T, d] act_dtype output. */
 moe_status moe_combine(const moe_config* cfg, const void* x, const float* y,
-                       const int32_t* slot_dest, const float* topk_w, void* out,
+                       const float* topk_w, const int32_t* slot_dest, void* out,
                        cudaStream_t stream);
 
 /* The whole layer: route -> dispatch -> expert FFNs -> combine, stream-ordered, no
@@ -245,7 +245,9 @@ moe_status moe_grouped_gemm(const void* A, int64_t a_rows, const void* B, int32_
  * allows T <= 32768 tokens; with E = 256, T <= 131072). It calls no cudaMalloc, cudaFree or
  * other allocating routine. Its first call on a device looks up the array's
  * device address (cudaGetSymbolAddress, with that device current), so make that
- * first call before any stream capture. All calls share the one array: calls that
+ * first call before any stream capture. That address is kept for the rest of the
+ * process: resetting the device (cudaDeviceReset) after the first call is not
+ * supported, since the array then lives at a new address. All calls share the one array: calls that
  * overlap on the GPU (different streams, or different host threads) race on it and
  * must be ordered by the caller. MOE_OVERFLOW_REROUTE needs the workspace moe_route
  * wrote and is rejected here with MOE_ERR_UNSUPPORTED. */

@@ -172,7 +172,8 @@ def test_overflow_policies(lib):
     # the shared-overflow combine needs the routing weights
     sh = api.make_config(64, 128, 8, 2, 128, 1.0, "swiglu", True, has_shared=True,
                          overflow="shared")
-    assert lib.moe_combine(ctypes.byref(sh), ok, ok, ok, None, ok, None) == C.MOE_ERR_INVALID_ARG
+    # (cfg, x, y, topk_w, slot_dest, out, stream)
+    assert lib.moe_combine(ctypes.byref(sh), ok, ok, None, ok, ok, None) == C.MOE_ERR_INVALID_ARG
 
 
 def test_unsupported_dtype_kind_pairs(lib):
@@ -193,7 +194,7 @@ def test_misaligned_and_missing_pointers(lib):
     assert lib.moe_route(r, bad, ok, None, ok, ok, ok, ok, None) == C.MOE_ERR_MISALIGNED
     assert lib.moe_route(r, None, ok, None, ok, ok, ok, ok, None) == C.MOE_ERR_INVALID_ARG
     assert lib.moe_route(r, ok, ok, None, None, ok, ok, None, None) == C.MOE_ERR_WORKSPACE
-    assert lib.moe_combine(r, ok, ok, ok, None, bad, None) == C.MOE_ERR_MISALIGNED
+    assert lib.moe_combine(r, ok, ok, None, ok, bad, None) == C.MOE_ERR_MISALIGNED
     w = C.MoeExpertWeights(w1=ok, b1=None, w2=None, b2=None)   # GELU needs w2
     assert lib.moe_forward(r, ok, ok, None, ctypes.byref(w), None, ok, None, None, None, ok,
                            1 << 40, None) == C.MOE_ERR_INVALID_ARG

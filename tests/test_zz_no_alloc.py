@@ -94,3 +94,34 @@ def test_noalloc_dispatch_rejects_problems_beyond_its_array():
     st = fn(ctypes.byref(cfg), p, None, p, p, p, p, p, p, None, None)
     assert st == C.MOE_ERR_WORKSPACE
     assert moe.kernel_launch_count() == n0       # rejected before any launch
+
+
+@pytest.mark.parametrize("T,accepted", [(32768, True), (32769, False)])
+def test_noalloc_dispatch_limit_is_exact(T, accepted):
+    # E = 1024: ceil(T/256) * E fits the array for T = 32768 (128 chunks) and not for one
+    # token more (129 chunks)
+    E = 1024
+    cfg = moe.make_config(T=T, d=64, E=E, top_k=1, F=64, kind="gelu")
+    g = torch.Generator(device="cpu").manual_seed(T)
+    idx = torch.randint(0, E, (T, 1), dtype=torch.int32, generator=g).cuda()
+    wl = Workload("na_lim", T=T, d=64, E=E, k=1, F=64, kind="gelu", act="bf16")
+    got = _buffers(wl)
+    if not accepted:
+        with pytest.raises(moe.MoeError) as e:
+            moe.dispatch_noalloc(cfg, idx, None, got["load"], got["counts"], got["offsets"],
+                                 got["perm_token"], got["perm_slot"], got["slot_dest"], None)
+        assert e.value.status == C.MOE_ERR_WORKSPACE
+        return
+    ws = torch.empty(moe.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    ref = _buffers(wl)
+    moe.dispatch(cfg, idx, None, ref["load"], ref["counts"], ref["offsets"], ref["perm_token"],
+                 ref["perm_slot"], ref["slot_dest"], None, ws)
+    moe.dispatch_noalloc(cfg, idx, None, got["load"], got["counts"], got["offsets"],
+                         got["perm_token"], got["perm_slot"], got["slot_dest"], None)
+    assert moe.last_device_status() == 0
+    P = int(ref["offsets"][-1].item())
+    assert P == T
+    for key in ("load", "counts", "offsets", "slot_dest"):
+        assert torch.equal(got[key], ref[key]), key
+    for key in ("perm_token", "perm_slot"):
+        assert torch.equal(got[key][:P], ref[key][:P]), key

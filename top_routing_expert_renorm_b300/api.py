@@ -149,8 +149,8 @@ def expert_ffn(cfg, x_perm, offsets, routed, shared, x, topk_w, perm_token, perm
 
 def combine(cfg, x, y, slot_dest, out, topk_w=None, stream=None):
     """topk_w is read when the layer sends overflow weight to the shared expert."""
-    _check(C.load().moe_combine(ctypes.byref(cfg), _ptr(x), _ptr(y), _ptr(slot_dest),
-                                _ptr(topk_w), _ptr(out), _stream(stream)), "moe_combine")
+    _check(C.load().moe_combine(ctypes.byref(cfg), _ptr(x), _ptr(y), _ptr(topk_w),
+                                _ptr(slot_dest), _ptr(out), _stream(stream)), "moe_combine")
 
 
 def forward(cfg, x, W_gate, gate_bias, routed, shared, out, ws, topk_idx=None, topk_w=None,

@@ -46,23 +46,52 @@ __device__ __forceinline__ void write_dropped_rows(const DroppedRows& dr, unsign
 constexpr int kDispWarps = 8;
 constexpr int kMTile = 128;      // rows per tensor-core M tile
 
+// ---- warp-private counts of a run of expert ids (no atomics) --------------------------
+// The warp's lanes read 32 ids at a time; lanes holding the same id form one
+// __match_any_sync group, whose lowest lane adds the group's size to the warp's own
+// counter row `my` [E] in shared memory. Only one lane of a warp writes a counter at a
+// time, so no update can be lost and the result does not depend on any ordering.
+// Ids outside [0, E) are skipped (and reported when `report`; re-routing proposals use
+// -1 for "none" and are counted with report = false).
+__device__ __forceinline__ void warp_count_ids(const int* __restrict__ idx, long long wbeg,
+                                               long long wend, int E, int* my, bool report) {
+    const int lane = threadIdx.x & 31;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (long long base = wbeg; base < wend; base += 32) {
+        const long long i = base + lane;
+        int e = (i < wend) ? idx[i] : -1;
+        if (i < wend && (e < 0 || e >= E)) {
+            if (report) raise_error(DEVERR_INDEX);
+            e = -1;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && (peers & lt_mask) == 0) my[e] += __popc(peers);
+        __syncwarp();
+    }
+}
+
 // ---- histogram: blockcnt[b][e] = assignments of chunk b routed to e ------------------
+// Warp w counts a contiguous run of the chunk's assignments into its own row of
+// shared memory (warp_count_ids); the rows are then summed per expert. No atomics.
 __global__ void __launch_bounds__(256) dispatch_hist_kernel(const int* __restrict__ idx, int T,
                                                             int k, int E,
                                                             int* __restrict__ blockcnt) {
     pdl_entry();
-    extern __shared__ int cnt[];
-    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+    extern __shared__ int wcnt[];   // [kDispWarps][E]
+    const int wid = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < kDispWarps * E; i += blockDim.x) wcnt[i] = 0;
     __syncthreads();
     const long long beg = (long long)blockIdx.x * kDispTok * k;
     const long long end = min((long long)(blockIdx.x + 1) * kDispTok, (long long)T) * k;
-    for (long long i = beg + threadIdx.x; i < end; i += blockDim.x) {
-        const int e = idx[i];
-        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);   // shared-memory count, order-free
-        else raise_error(DEVERR_INDEX);
-    }
+    const long long seg = ((end - beg + kDispWarps - 1) / kDispWarps + 31) / 32 * 32;
+    const long long wbeg = beg + wid * seg;
+    warp_count_ids(idx, wbeg, min(wbeg + seg, end), E, wcnt + wid * E, true);
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) blockcnt[(long long)blockIdx.x * E + e] = cnt[e];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int c = 0;
+        for (int w = 0; w < kDispWarps; ++w) c += wcnt[w * E + e];
+        blockcnt[(long long)blockIdx.x * E + e] = c;
+    }
 }
 
 // ---- block-wide exclusive scan of one int per thread (blockDim.x == 1024) -------------
@@ -235,9 +264,10 @@ __global__ void __launch_bounds__(256) reroute_propose_kernel(const int* __restr
                                                               int k, int E, int* __restrict__ prop,
                                                               int* __restrict__ blockcnt) {
     pdl_entry();
-    extern __shared__ int cnt[];
-    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
-    __syncthreads();
+    extern __shared__ int wcnt[];   // [kDispWarps][E]
+    const int wid = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < kDispWarps * E; i += blockDim.x) wcnt[i] = 0;
+    // pass 1: one thread per token hands its dropped slots their proposals
     const int t_end = min((blockIdx.x + 1) * kDispTok, T);
     for (int t = blockIdx.x * kDispTok + threadIdx.x; t < t_end; t += blockDim.x) {
         int m = 0;
@@ -251,13 +281,23 @@ __global__ void __launch_bounds__(256) reroute_propose_kernel(const int* __restr
                     raise_error(DEVERR_INDEX);
                     e = -1;
                 }
-                if (e >= 0) atomicAdd(&cnt[e], 1);   // shared-memory count, order-free
             }
             prop[i] = e < 0 ? -1 : e;
         }
     }
+    __syncthreads();   // the chunk's proposals are written (and visible to this CTA)
+    // pass 2: warp-private counts of the chunk's proposals, summed per expert
+    const long long beg = (long long)blockIdx.x * kDispTok * k;
+    const long long end = (long long)t_end * k;
+    const long long seg = ((end - beg + kDispWarps - 1) / kDispWarps + 31) / 32 * 32;
+    const long long wbeg = beg + wid * seg;
+    warp_count_ids(prop, wbeg, min(wbeg + seg, end), E, wcnt + wid * E, false);
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) blockcnt[(long long)blockIdx.x * E + e] = cnt[e];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int c = 0;
+        for (int w = 0; w < kDispWarps; ++w) c += wcnt[w * E + e];
+        blockcnt[(long long)blockIdx.x * E + e] = c;
+    }
 }
 
 // ---- the whole dispatch in one CTA of 1024 threads -------------------------------------
@@ -285,7 +325,10 @@ __global__ void __launch_bounds__(1024) dispatch_one_cta_kernel(
     int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ perm_token,
     int* __restrict__ perm_slot, int* __restrict__ slot_dest, int* __restrict__ mtile_offsets,
     unsigned long long* __restrict__ counters, int n_counters, DroppedRows dr,
-    const int* __restrict__ blockcnt, int nb) {
+    const int* __restrict__ blockcnt, int nb, int hist_sub) {
+    // hist_sub: rows of blockcnt per chunk (1: per-chunk counts of dispatch_hist_kernel;
+    // kDispTok / 32: per-warp counts of 32 tokens each from the router's top-k epilogue),
+    // summed here
     pdl_entry();
     extern __shared__ int dsm[];
     const bool first = blockIdx.x == 0;
@@ -341,9 +384,11 @@ __global__ void __launch_bounds__(1024) dispatch_one_cta_kernel(
     if (e < E) {
         int run = 0, all = 0;
         if (blockcnt) {
-            for (int b = 0; b < nb; ++b) {
+            const int sub_tok = kDispTok / hist_sub;   // tokens per row
+            const int rows = (int)(((long long)T + sub_tok - 1) / sub_tok);
+            for (int b = 0; b < rows; ++b) {
                 const int c = blockcnt[(long long)b * E + e];
-                if (b < (int)blockIdx.x) run += c;
+                if (b < (int)blockIdx.x * hist_sub) run += c;
                 all += c;
             }
         }

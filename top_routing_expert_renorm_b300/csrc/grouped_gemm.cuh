@@ -76,8 +76,8 @@ struct GemmParams {
     float* r_w;                   //                  renormalised weights [T, top_k]
     int r_E, r_Ep;                //                  experts, padded experts per term (32 | 64)
     long long r_rows;             //                  T (rows of r_part per part)
-    int* r_hist;                  //                  nullable [T / r_hist_chunk][r_E]: selected
-    int r_hist_chunk;             //                  experts per chunk of tokens (zeroed before)
+    int* r_hist;                  //                  nullable [ceil(T / 32)][r_E]: selected
+                                  //                  experts per 32 tokens (one epilogue warp)
     float* r_part;                //                  k_splits > 1: partial logits [S][T][r_Ep]
     int* r_tile_cnt;              //                  and arrivals per M tile (zeroed before)
     // split-K: every output tile is computed as k_splits units over consecutive ranges of
@@ -110,8 +110,10 @@ constexpr int GM_MAX_GROUPS = 1025;
 constexpr int GM_TQ = 8;            // depth of the ring of scheduled unit ids
 constexpr int GM_HDR_BYTES = 512;   // barriers, TMEM address, abort flag, unit-id ring
 
+constexpr int GM_RHIST_BYTES = 4 * 64 * 4;   // router top-k: 64 counters per epilogue warp
 __host__ __device__ constexpr int gm_smem_bytes(int G, int MT = 1) {
-    return 1024 + gm_stages(MT) * gm_stage_bytes(MT) + GM_HDR_BYTES + 2 * (G + 1) * 4;
+    return 1024 + gm_stages(MT) * gm_stage_bytes(MT) + GM_HDR_BYTES + 2 * (G + 1) * 4 +
+           GM_RHIST_BYTES;
 }
 
 // s_mt[0..G] = exclusive scan over the groups of ceil(rows_g / bm), from the row offsets
@@ -186,8 +188,10 @@ __device__ __forceinline__ void gm_epilogue_partial(const GemmParams& p, uint32_
 template <int EPI>
 __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t tb, int g, int nb,
                                                  bool row_ok, long long grow, int mb = 0,
-                                                 int ks = 0, volatile int* s_flag = nullptr) {
-    // mb, ks, s_flag: EPI_ROUTER_TOPK with K split (see there)
+                                                 int ks = 0, volatile int* s_flag = nullptr,
+                                                 int* s_rh = nullptr) {
+    // mb, ks, s_flag: EPI_ROUTER_TOPK with K split (see there); s_rh: that epilogue
+    // warp's 64 histogram counters in shared memory
     const float* brow = p.bias ? p.bias + (long long)g * p.b_rows_per_group : nullptr;
     const float* srow = p.w_scale ? p.w_scale + (long long)g * p.b_rows_per_group : nullptr;
     if constexpr (EPI == EPI_SWIGLU_BF16) {
@@ -311,6 +315,7 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
                 }
             }
         }
+        int ids[32];
         if (row_ok) {
             if (p.bias) {
 #pragma unroll
@@ -325,7 +330,6 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
             }
             uint64_t taken = 0;
             float vals[32];
-            int ids[32];
             for (int j = 0; j < k; ++j) {
                 float bv = 0.0f;
                 int be = -1;
@@ -349,10 +353,31 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
                 p.r_idx[grow * k + j] = ids[j];
                 p.r_w[grow * k + j] = ex[j] / ssum;
             }
-            // the dispatch's per-chunk expert histogram (order-free counts)
-            if (p.r_hist)
-                for (int j = 0; j < k; ++j)
-                    atomicAdd(p.r_hist + (grow / p.r_hist_chunk) * E + ids[j], 1);
+        }
+        // The dispatch's expert histogram, one row per warp (32 consecutive tokens): the
+        // lanes holding the same id in slot j form a __match_any_sync group whose lowest
+        // lane adds the group's size to the warp's counters in shared memory (no atomics),
+        // then the warp stores its row. Every row of a token block that holds a token is
+        // written, so the rows need no zeroing.
+        if (p.r_hist) {
+            const int lane = threadIdx.x & 31;
+            const unsigned lt_mask = (1u << lane) - 1u;
+            s_rh[lane] = 0;
+            s_rh[lane + 32] = 0;
+            __syncwarp();
+            for (int j = 0; j < k; ++j) {
+                const int e = row_ok ? ids[j] : -1;
+                const unsigned peers = __match_any_sync(0xffffffffu, e);
+                if (e >= 0 && (peers & lt_mask) == 0) s_rh[e] += __popc(peers);
+                __syncwarp();
+            }
+            const long long r32 = (grow - lane) >> 5;   // the warp's 32-token row
+            if (grow - lane < p.r_rows) {
+                int* hrow = p.r_hist + r32 * E;
+                if (lane < E) hrow[lane] = s_rh[lane];
+                if (lane + 32 < E) hrow[lane + 32] = s_rh[lane + 32];
+            }
+            __syncwarp();
         }
     } else if constexpr (EPI == EPI_COMBINE1_BF16) {
         // Same fp32 operations, in the same order, as the scale epilogue followed by the
@@ -493,6 +518,7 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
     volatile long long* s_unit = reinterpret_cast<volatile long long*>(bars + 40);   // [GM_TQ]
     int* s_ro = reinterpret_cast<int*>(bars + GM_HDR_BYTES / 8);
     int* s_mt = s_ro + (p.G + 1);
+    int* s_rh = s_mt + (p.G + 1);   // [4][64] router histogram counters
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto bar = [&](int i) { return smem_addr(bars + i); };
@@ -857,7 +883,8 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
                 const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) +
                                     (uint32_t)((acc + h) * GM_BN);
                 if (p.partial) gm_epilogue_partial<EPI>(p, tb, nb, ks, row_ok, grow);
-                else gm_epilogue_tile<EPI>(p, tb, g, nb, row_ok, grow, mb, ks, s_flag);
+                else gm_epilogue_tile<EPI>(p, tb, g, nb, row_ok, grow, mb, ks, s_flag,
+                                           s_rh + (warp & 3) * 64);
                 if (MT == 2 && h == 0) {   // half 0 is free for the next tile's MMAs
                     tc_fence_before();
                     __syncwarp();

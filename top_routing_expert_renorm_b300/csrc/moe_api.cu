@@ -455,7 +455,7 @@ WsLayout ws_layout(const moe_config& c) {
     L.load = take(E * 4);
     L.counts = take(E * 4);
     L.offsets = take((E + 1) * 4);
-    L.blockcnt = take(nb * E * 4);
+    L.blockcnt = take(std::max(nb, (T + 31) / 32) * E * 4);   // per chunk, or per 32 tokens
     L.blockoff = take(nb * E * 4);
     const bool rr = c.overflow == MOE_OVERFLOW_REROUTE;
     L.cand = take(rr ? Pmax * 4 : 0);
@@ -491,7 +491,8 @@ moe_status dispatch_impl(const moe_config& c, const int32_t* idx, const void* x,
                          const int32_t* cand = nullptr, int32_t* prop = nullptr,
                          int32_t* cnt0 = nullptr, DroppedRows dr = DroppedRows{},
                          bool hist_ready = false) {
-    // hist_ready: blockcnt already holds the per-chunk histogram (filled by the router)
+    // hist_ready: blockcnt already holds the expert histogram, one row per 32 tokens
+    // (filled by the router's top-k epilogue)
     // counters (nullable): the routed up/down GEMM tile counters, zeroed here
     // cand, prop, cnt0: re-routing candidates (from the router) and scratch
     // dr: top-1 layers with the combine fused into the down projection write the output
@@ -505,7 +506,7 @@ moe_status dispatch_impl(const moe_config& c, const int32_t* idx, const void* x,
         // round 0 (ranks only), proposals of the dropped slots, room and offsets, then
         // ranks of the proposals and the scatter of every slot
         MOE_LAUNCH("dispatch_hist", s,
-                   launch_k(dispatch_hist_kernel, nb, 256, E * sizeof(int), s, idx, T, k, E,
+                   launch_k(dispatch_hist_kernel, nb, 256, kDispWarps * E * sizeof(int), s, idx, T, k, E,
                             blockcnt));
         MOE_LAUNCH("dispatch_scan", s,
                    launch_k(dispatch_scan_kernel, 1, 1024, 0, s, blockcnt, nb, E, cap, blockoff,
@@ -515,7 +516,7 @@ moe_status dispatch_impl(const moe_config& c, const int32_t* idx, const void* x,
                             blockoff, offsets, perm_token, perm_slot, slot_dest, nullptr, nullptr,
                             DroppedRows{}));
         MOE_LAUNCH("reroute_propose", s,
-                   launch_k(reroute_propose_kernel, nb, 256, E * sizeof(int), s, slot_dest, cand,
+                   launch_k(reroute_propose_kernel, nb, 256, kDispWarps * E * sizeof(int), s, slot_dest, cand,
                             T, k, E, prop, blockcnt));
         MOE_LAUNCH("reroute_scan", s,
                    launch_k(reroute_scan_kernel, 1, 1024, 0, s, blockcnt, nb, E, cap, blockoff,
@@ -527,18 +528,19 @@ moe_status dispatch_impl(const moe_config& c, const int32_t* idx, const void* x,
         MOE_LAUNCH("dispatch_one_cta", s,
                    launch_k(dispatch_one_cta_kernel, 1, 1024, 33 * E * sizeof(int), s, idx, T, k,
                             E, cap, load, counts, offsets, perm_token, perm_slot, slot_dest,
-                            mtile, counters, 2, dr, nullptr, 0));
+                            mtile, counters, 2, dr, nullptr, 0, 1));
     } else {
         if (!hist_ready)
             MOE_LAUNCH("dispatch_hist", s,
-                       launch_k(dispatch_hist_kernel, nb, 256, E * sizeof(int), s, idx, T, k, E,
+                       launch_k(dispatch_hist_kernel, nb, 256, kDispWarps * E * sizeof(int), s, idx, T, k, E,
                                 blockcnt));
         if (E <= kOneCtaMaxE) {
             // one CTA per chunk: scan folded into the ranking kernel
             MOE_LAUNCH("dispatch_rank", s,
                        launch_k(dispatch_one_cta_kernel, nb, 1024, 33 * E * sizeof(int), s, idx, T,
                                 k, E, cap, load, counts, offsets, perm_token, perm_slot, slot_dest,
-                                mtile, counters, 2, dr, blockcnt, nb));
+                                mtile, counters, 2, dr, blockcnt, nb,
+                                hist_ready ? kDispTok / 32 : 1));
         } else {
             MOE_LAUNCH("dispatch_scan", s,
                        launch_k(dispatch_scan_kernel, 1, 1024, 0, s, blockcnt, nb, E, cap, blockoff,
@@ -680,15 +682,14 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     p.r_Ep = r_Ep;
     p.w_scale = w_scale;
     p.r_hist = r_hist;
-    p.r_hist_chunk = kDispTok;
     if constexpr (EPI == EPI_ROUTER_TOPK) {
+        p.r_rows = a_rows;
         if (sp.S > 1) {   // the epilogue adds the two K parts itself (no partial buffer pass)
             if (sp.S != 2 || !r_part || !r_tile_cnt) return MOE_ERR_UNSUPPORTED;
             p.k_splits = sp.S;
             p.kb_per_split = sp.kbs;
             p.r_part = r_part;
             p.r_tile_cnt = r_tile_cnt;
-            p.r_rows = a_rows;
         }
     }
     if (gathered) {
@@ -784,8 +785,8 @@ moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const
                       float* logits, int32_t* idx, float* w, void* scratch, int32_t* cand,
                       cudaStream_t s, int32_t* hist = nullptr) {
     // cand: the re-routing candidates [T, k] (written iff overflow == REROUTE)
-    // hist: the dispatch's per-chunk histogram [ceil(T / kDispTok)][E], filled by the fused
-    //       top-k epilogue when non-null (the caller checks router_fills_hist)
+    // hist: the dispatch's expert histogram, one row per 32 tokens [ceil(T / 32)][E], written
+    //       by the fused top-k epilogue when non-null (the caller checks that it is fused)
     if (c.overflow != MOE_OVERFLOW_REROUTE) cand = nullptr;
     const int T = c.T, E = c.E, d = c.d, k = c.top_k;
     const RouterPlan rp = router_plan(c);
@@ -808,8 +809,7 @@ moe_status route_impl(const moe_config& c, const void* x, const float* Wg, const
         MOE_LAUNCH("gate_split", s,
                    launch_k(gate_split_kernel, grid, 256, 0, s,
                        Wg, d, E, rp.Ep, Bg, T, tables,
-                       reinterpret_cast<unsigned long long*>(tables + 4), hist,
-                       hist ? (int)(((T + kDispTok - 1) / kDispTok) * (long long)E) : 0, tile_cnt,
+                       reinterpret_cast<unsigned long long*>(tables + 4), tile_cnt,
                        (int)rp.mtiles));
         if (router_fused_topk(c, rp.Ep)) {   // the three terms fit one accumulator: fused top-k
             SplitPlan sp;
@@ -1078,7 +1078,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32
 }
 
 moe_status moe_combine(const moe_config* cfg, const void* x, const float* y,
-                       const int32_t* slot_dest, const float* topk_w, void* out,
+                       const float* topk_w, const int32_t* slot_dest, void* out,
                        cudaStream_t stream) {
     MOE_TRY(check_cfg(cfg));
     const moe_config& c = *cfg;

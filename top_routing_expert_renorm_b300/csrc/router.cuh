@@ -92,15 +92,12 @@ __global__ void __launch_bounds__(256) gate_split_kernel(const float* __restrict
                                                          __nv_bfloat16* __restrict__ Bg, int T,
                                                          int* __restrict__ tables,
                                                          unsigned long long* __restrict__ counter,
-                                                         int* __restrict__ hist, int hist_n,
                                                          int* __restrict__ tile_cnt, int n_tile_cnt) {
-    // hist (nullable): the dispatch histogram the router GEMM's epilogue fills; tile_cnt
-    // (nullable): the arrival counters of its K-split M tiles; both zeroed here
+    // tile_cnt (nullable): the arrival counters of the router GEMM's K-split M tiles,
+    // zeroed here
     pdl_entry();
     const int nthreads = gridDim.x * gridDim.y * blockDim.x;
     const int tid = (blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
-    if (hist)
-        for (int i = tid; i < hist_n; i += nthreads) hist[i] = 0;
     if (tile_cnt)
         for (int i = tid; i < n_tile_cnt; i += nthreads) tile_cnt[i] = 0;
     __shared__ float tile[32][33];
