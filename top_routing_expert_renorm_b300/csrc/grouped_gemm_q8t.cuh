@@ -21,7 +21,10 @@
 // codes, and K splits start on a code stage (an even number of 128-code blocks).
 //   warp 0       unit scheduler + TMA of the codes (two 128-row boxes of 128 bytes,
 //                128-byte swizzle) into a QT_NQ-deep ring;
-//   warp 1       MMA issuer (A from TMEM, B from shared memory);
+//   warps 1, 15  MMA issuers (A from TMEM, B from shared memory), warp 1 for the weight
+//                rows of half 0 and warp 15 for half 1: each tcgen05.mma with A in TMEM
+//                holds its issuing thread far longer than the tensor pipe needs for it,
+//                so two issuers keep twice the MMAs in flight;
 //   warps 2-5    epilogue: lane = weight row (output feature), column = activation row;
 //   warp 6       TMA of the bf16 activation rows into a QT_NB-deep ring;
 //   warps 7-14   converters: warp 7 + 4h + i widens rows 32q .. 32q+31 (q = warp % 4, the
@@ -40,7 +43,7 @@ constexpr int QT_Q_BYTES = GM_BN * QT_BK;           // 256 weight rows x 128 byt
 constexpr int QT_B_BYTES = QT_NT * QT_BK * 2;       // 32 rows x 128 bf16 = 8 KB (two boxes)
 constexpr int QT_RING_BYTES = QT_NQ * QT_Q_BYTES + QT_NB * QT_B_BYTES;
 constexpr int QT_HDR_BYTES = 1024;
-constexpr int QT_THREADS = 480;
+constexpr int QT_THREADS = 512;
 constexpr int QT_TMEM_COLS = 512;
 constexpr int QT_ACC_COL = 0, QT_A_COL = 128;
 static_assert(QT_A_COL + QT_NC * 2 * (QT_BK / 4) <= QT_TMEM_COLS, "TMEM columns overflow");
@@ -141,20 +144,20 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
         }
         for (int s = 0; s < QT_NB; ++s) {
             mbar_init(bar(BFULL + s), 1);
-            mbar_init(bar(BEMPTY + s), 1);    // MMA commit
+            mbar_init(bar(BEMPTY + s), 2);    // the two MMA issuers' commits
         }
         for (int s = 0; s < QT_NC; ++s) {
             mbar_init(bar(CFULL + s), 8);     // the eight converter warps
-            mbar_init(bar(CEMPTY + s), 1);    // MMA commit
+            mbar_init(bar(CEMPTY + s), 2);    // the two MMA issuers' commits
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(bar(TFULL + a), 1);
+            mbar_init(bar(TFULL + a), 2);
             mbar_init(bar(TEMPTY + a), 4);
         }
-        mbar_init(bar(DRAIN), 1);
+        mbar_init(bar(DRAIN), 2);
         for (int i = 0; i < GM_TQ; ++i) {
             mbar_init(bar(UFULL + i), 1);
-            mbar_init(bar(UEMPTY + i), 14);  // MMA, B producer, 4 epilogue, 8 converter warps
+            mbar_init(bar(UEMPTY + i), 15);  // 2 MMA, B producer, 4 epilogue, 8 converter warps
         }
         *s_abort = 0;
         mbar_fence_init();
@@ -310,7 +313,7 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
             for (int s = 0; s < QT_NB; ++s)
                 if (last_par[s] >= 0) mbar_wait(bar(BFULL + s), (uint32_t)last_par[s]);
         }
-    } else if (warp >= 7) {
+    } else if (warp >= 7 && warp < 15) {
         // ---------------- converters: int8 / int4 codes -> bf16 A operand in TMEM ----------
         const int qd = warp & 3, h = (warp - 7) >> 2;
         const int r = h * 128 + qd * 32 + lane;          // weight row of the stage
@@ -371,15 +374,21 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
                 if constexpr (BITS == 8) {
                     widen_half(row, 0, v0);
                     widen_half(row, 4, v1);
+                    tmem_store_32cols(t_lane + cs * 128, v0);
+                    tmem_store_32cols(t_lane + cs * 128 + 32, v1);
                 } else {
+                    // 4-bit codes: the first 64 codes' TMEM store is in flight while the
+                    // next 64 are widened (both register sets stay untouched until the wait);
+                    // measured faster for INT4 and slower for INT8, whose loads of the second
+                    // half then no longer overlap the first half's widening
                     widen_half4(row, 4 * sub, v0);
+                    tmem_store_32cols(t_lane + cs * 128, v0);
                     widen_half4(row, 4 * sub + 2, v1);
+                    tmem_store_32cols(t_lane + cs * 128 + 32, v1);
                 }
                 __syncwarp();
                 const bool q_done = sub == KPQ - 1 || kb == kb1 - 1;
                 if (q_done && lane == 0) mbar_arrive(bar(QEMPTY + qs));   // codes consumed
-                tmem_store_32cols(t_lane + cs * 128, v0);
-                tmem_store_32cols(t_lane + cs * 128 + 32, v1);
                 tmem_store_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -394,9 +403,10 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 15) {
         if (lane == 0) {
-            // ---------------- MMA issuer ----------------
+            // ---------------- MMA issuers: warp 1 half 0, warp 15 half 1 ----------------
+            const int hh = warp == 1 ? 0 : 1;
             constexpr uint32_t idesc = idesc_bf16_f32(128, QT_NT);
             int bs = 0, cs = 0, acc = 0;
             uint32_t bph = 0, cph = 0, aph = 0;
@@ -421,17 +431,14 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t sb = smem_addr(b_tiles + bs * QT_B_BYTES);
+                    const uint32_t dt = tmem_base + QT_ACC_COL + acc * 64 + hh * 32;
+                    const uint32_t at = tmem_base + QT_A_COL + cs * 128 + hh * 64;
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const uint32_t dt = tmem_base + QT_ACC_COL + acc * 64 + hh * 32;
-                        const uint32_t at = tmem_base + QT_A_COL + cs * 128 + hh * 64;
-#pragma unroll
-                        for (int kk = 0; kk < QT_BK / 16; ++kk)   // B: two 64-wide K boxes
-                            umma_bf16_tmem_a(dt, at + kk * 8,
-                                             sw128_kmajor_desc(sb + (kk >> 2) * (QT_B_BYTES / 2) +
-                                                               (kk & 3) * 32),
-                                             idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < QT_BK / 16; ++kk)   // B: two 64-wide K boxes
+                        umma_bf16_tmem_a(dt, at + kk * 8,
+                                         sw128_kmajor_desc(sb + (kk >> 2) * (QT_B_BYTES / 2) +
+                                                           (kk & 3) * 32),
+                                         idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
                     umma_commit(bar(CEMPTY + cs));
                     umma_commit(bar(BEMPTY + bs));
                     if (++bs == QT_NB) {
