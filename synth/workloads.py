@@ -267,6 +267,12 @@ WORKLOADS = {
     "deepseek_e32": Workload("deepseek_e32", T=1024, d=7168, E=32, k=8, F=2048, kind="swiglu",
                              act="bf16", cf=1.0, has_shared=True,
                              note="DeepSeek-V3 expert shapes, 32 experts (for profiling)"),
+    # the DeepSeek-V3-shaped layer's routing, dispatch, gather and combine (T, d, E, k, the
+    # shared expert) with F = 64 (0.7 GB of expert weights): memory-bound kernels at full
+    # size within a few GB for multi-pass profiler captures
+    "deepseek_memprof": Workload("deepseek_memprof", T=8192, d=7168, E=256, k=8, F=64,
+                                 kind="swiglu", act="bf16", cf=1.0, has_shared=True,
+                                 note="DeepSeek-V3 routing/dispatch/combine shapes, F = 64 (for profiling)"),
     # weight-only INT8 experts (codes + per-row scales) for the decode-sized layers
     "decode1_i8": Workload("decode1_i8", T=1, d=7168, E=256, k=8, F=2048, kind="swiglu",
                            act="bf16", gate_dist="uniform", int8=True,

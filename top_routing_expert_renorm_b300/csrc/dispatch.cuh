@@ -378,18 +378,49 @@ __global__ void __launch_bounds__(1024) dispatch_one_cta_kernel(
         }
     }
     __syncthreads();
+    // Histogram rows of all chunks (chunked mode): thread (g, e) of G = 1024 / E groups sums
+    // rows g, g + G, ... of expert e, both over all rows and over the rows of the chunks
+    // before this one; the G partial sums are then added in group order.
+    __shared__ int s_hsum[2][1024];
+    if (blockcnt) {
+        const int G = (int)blockDim.x / E;
+        const int g = threadIdx.x / E, ee = threadIdx.x - g * E;
+        if (g < G) {
+            const int sub_tok = kDispTok / hist_sub;   // tokens per row
+            const int rows = (int)(((long long)T + sub_tok - 1) / sub_tok);
+            const int before = (int)blockIdx.x * hist_sub;
+            int run_p = 0, all_p = 0;
+            int b = g;
+            for (; b + 3 * G < rows; b += 4 * G) {   // four loads in flight
+                int c[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) c[u] = blockcnt[(long long)(b + u * G) * E + ee];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    all_p += c[u];
+                    if (b + u * G < before) run_p += c[u];
+                }
+            }
+            for (; b < rows; b += G) {
+                const int c = blockcnt[(long long)b * E + ee];
+                all_p += c;
+                if (b < before) run_p += c;
+            }
+            s_hsum[0][threadIdx.x] = run_p;
+            s_hsum[1][threadIdx.x] = all_p;
+        }
+    }
+    __syncthreads();
     // load, capacity, offsets; warp counters become rank bases (after the earlier chunks)
     const int e = threadIdx.x;
     int kept = 0;
     if (e < E) {
         int run = 0, all = 0;
         if (blockcnt) {
-            const int sub_tok = kDispTok / hist_sub;   // tokens per row
-            const int rows = (int)(((long long)T + sub_tok - 1) / sub_tok);
-            for (int b = 0; b < rows; ++b) {
-                const int c = blockcnt[(long long)b * E + e];
-                if (b < (int)blockIdx.x * hist_sub) run += c;
-                all += c;
+            const int G = (int)blockDim.x / E;
+            for (int g = 0; g < G; ++g) {
+                run += s_hsum[0][g * E + e];
+                all += s_hsum[1][g * E + e];
             }
         }
         for (int w = 0; w < 32; ++w) {
@@ -448,6 +479,41 @@ __global__ void __launch_bounds__(1024) dispatch_one_cta_kernel(
             if (dr.out)
                 write_dropped_rows(dr, __ballot_sync(0xffffffffu, dropped),
                                    wbeg + (long long)(r0 + j) * 32, lane);
+        }
+    }
+}
+
+// ---- the same copy organised by token (k >= 2): one warp per token reads its row of x once
+// and writes it to each of its kept slots' rows (slot_dest[t*k + j] >= 0), so x is read
+// once instead of k times. 16-byte vectors, four per lane in flight; row_bytes is a
+// multiple of 16.
+__global__ void __launch_bounds__(256) gather_rows_by_token_kernel(
+    const uint8_t* __restrict__ x, const int* __restrict__ slot_dest, int T, int k,
+    uint8_t* __restrict__ x_perm, int row_bytes) {
+    pdl_entry();
+    const int lane = threadIdx.x & 31;
+    const int nvec = row_bytes / 16;
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
+        const int mydest = lane < k ? slot_dest[(long long)t * k + lane] : -1;
+        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * row_bytes);
+        for (int c0 = 0; c0 < nvec; c0 += 128) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = c0 + u * 32 + lane;
+                if (c < nvec) v[u] = __ldg(src + c);
+            }
+            for (int j = 0; j < k; ++j) {
+                const int pos = __shfl_sync(0xffffffffu, mydest, j);
+                if (pos < 0) continue;
+                uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)pos * row_bytes);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = c0 + u * 32 + lane;
+                    if (c < nvec) dst[c] = v[u];
+                }
+            }
         }
     }
 }

@@ -554,11 +554,19 @@ moe_status dispatch_impl(const moe_config& c, const int32_t* idx, const void* x,
     if (x_perm) {
         const int es = c.act_dtype == MOE_BF16 ? 2 : 4;
         const long long Pmax = (long long)T * k;
-        const int blocks = (int)std::min<long long>((Pmax + 7) / 8, (long long)num_sms() * 16);
-        MOE_LAUNCH("gather_rows", s,
-                   launch_k(gather_rows_kernel, std::max(blocks, 1), 256, 0, s,
-                       static_cast<const uint8_t*>(x), perm_token, offsets + E,
-                       static_cast<uint8_t*>(x_perm), c.d * es));
+        if (k >= 2) {   // by token: every row of x read once
+            const int blocks = (int)std::min<long long>((T + 7) / 8, (long long)num_sms() * 16);
+            MOE_LAUNCH("gather_rows", s,
+                       launch_k(gather_rows_by_token_kernel, std::max(blocks, 1), 256, 0, s,
+                                static_cast<const uint8_t*>(x), slot_dest, T, k,
+                                static_cast<uint8_t*>(x_perm), c.d * es));
+        } else {
+            const int blocks = (int)std::min<long long>((Pmax + 7) / 8, (long long)num_sms() * 16);
+            MOE_LAUNCH("gather_rows", s,
+                       launch_k(gather_rows_kernel, std::max(blocks, 1), 256, 0, s,
+                           static_cast<const uint8_t*>(x), perm_token, offsets + E,
+                           static_cast<uint8_t*>(x_perm), c.d * es));
+        }
     }
     return MOE_OK;
 }
