@@ -7,7 +7,7 @@ import torch
 
 import top_routing_expert_renorm_b300 as moe
 from synth import Workload, get, host_fill, dev_fill, normal_K, uniform_K, NORMAL, UNIFORM
-from gpu_support import GpuRun, full_check, to_np, as_f64
+from gpu_support import GpuRun, full_check, to_np, as_f64, check_outputs
 
 pytestmark = pytest.mark.gpu
 
@@ -491,6 +491,24 @@ def test_forward_gathers_rows_in_the_gemm_for_many_slots(name, gathers):
     stats = moe.profile_end()
     assert stats["gather_rows"][0] == (1 if gathers else 2)    # staged path (+ forward)
     assert np.array_equal(to_np(r.out), to_np(r.out_stages))
+
+
+@pytest.mark.parametrize("name,merged", [("swiglu_zipf_shared", True), ("swiglu_k8_cap_shared", True),
+                                         ("wide_k4_shared", True), ("split_swiglu_bias_shared", False),
+                                         ("i8_swiglu_zipf_shared", False)])
+def test_forward_runs_the_shared_expert_as_an_extra_group(name, merged):
+    # bf16 layers with a shared expert and unsplit up projections: moe_forward runs the
+    # shared expert as one more group of the routed up projection (one launch, one tail),
+    # the staged entry points as a launch of its own; both match the oracle
+    # (test_small_parity) and each other within the parity criteria.
+    wl = SMALL[name]
+    moe.profile_begin()
+    r = GpuRun(wl).run()
+    stats = moe.profile_end()
+    up = [n for n in stats if n.startswith("grouped_gemm_") and n.endswith(("swiglu", "gelu"))]
+    assert sum(stats[n][0] for n in up) == (3 if merged else 4)
+    assert stats.get("append_group", (0, 0))[0] == (1 if merged else 0)
+    check_outputs(wl, to_np(r.out), as_f64(to_np(r.out_stages)))
 
 
 def test_split_k_is_used_for_few_tokens():

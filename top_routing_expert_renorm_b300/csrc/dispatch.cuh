@@ -595,6 +595,18 @@ __global__ void __launch_bounds__(1024) mtile_table_kernel(const int* __restrict
     write_tile_tables(rows, g, G, s_warp, mtile_offsets);
 }
 
+// Row and M-tile offsets of one more group of `rows` rows after the E groups of a
+// dispatch (the shared expert as group E of the routed up projection): offsets[E + 1] and
+// mtile_offsets[E + 1].
+__global__ void append_group_kernel(int* __restrict__ offsets, int* __restrict__ mtile_offsets,
+                                    int E, int rows) {
+    pdl_entry();
+    if (threadIdx.x == 0) {
+        offsets[E + 1] = offsets[E] + rows;
+        if (mtile_offsets) mtile_offsets[E + 1] = mtile_offsets[E] + (rows + kMTile - 1) / kMTile;
+    }
+}
+
 // Row and M-tile tables of a single group of `rows` rows (the shared expert).
 __global__ void single_group_table_kernel(int rows, int* __restrict__ row_offsets,
                                           int* __restrict__ mtile_offsets,

@@ -94,6 +94,16 @@ struct GemmParams {
     // it fetched-and-incremented from this counter (zeroed by the kernel that writes
     // the launch's tables). Null: static round-robin over the units.
     unsigned long long* tile_counter;
+    // An extra group (the shared expert) in the same launch: group xg1 - 1 (0 = none) reads
+    // its A rows from the second A map (rows from 0; gathered: row r of the group is row r of
+    // a_src) and its weights from the second B map (rows from 0), with bias xg_bias [N1]; its
+    // output rows follow the others' in the row numbering of row_offsets.
+    int xg1;
+    const float* xg_bias;
+    // 1: the output row of group-row r is r (out already points at the group's first row)
+    // instead of row_offsets[g] + r (single-group launches whose rows sit at a device-side
+    // offset of A)
+    int out_local;
 };
 
 constexpr int GM_BM = 128, GM_BN = 256, GM_BK = 64, GM_STAGES = 4;
@@ -193,6 +203,7 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
     // mb, ks, s_flag: EPI_ROUTER_TOPK with K split (see there); s_rh: that epilogue
     // warp's 64 histogram counters in shared memory
     const float* brow = p.bias ? p.bias + (long long)g * p.b_rows_per_group : nullptr;
+    if (g == p.xg1 - 1) brow = p.xg_bias;   // the extra group (bf16 weights: no row scales)
     const float* srow = p.w_scale ? p.w_scale + (long long)g * p.b_rows_per_group : nullptr;
     if constexpr (EPI == EPI_SWIGLU_BF16) {
         const int n0 = nb * 128;
@@ -497,7 +508,11 @@ constexpr int GM_GATHER_DEPTH = 2;   // stages a gather thread keeps in flight b
 template <int EPI, int MT = 1>
 __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmA2,
+                        const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
+    // tmA2 / tmB2: A rows and weights of the extra group p.xg1 - 1 (copies of tmA / tmB
+    // when the launch has none)
     static_assert(MT == 1 || MT == 2, "tiles are 128 or 256 rows");
     static_assert(MT == 1 || EPI != EPI_ROUTER_TOPK, "the router runs 128-row tiles");
     constexpr int STAGES = gm_stages(MT);
@@ -544,6 +559,10 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
         mbar_fence_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (p.xg1) {
+            tma_prefetch_desc(&tmA2);
+            tma_prefetch_desc(&tmB2);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(s_tmem), GM_TMEM_COLS);
@@ -600,9 +619,12 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
                 gm_decode(t, p.G, p.n_tiles, p.k_splits, s_mt, g, mb, nb, ks);
                 const int kb0 = ks * p.kb_per_split;
                 const int kb1 = min(kblocks, kb0 + p.kb_per_split);
-                const int a_row = s_ro[g] + mb * BM;
+                const bool xg = g == p.xg1 - 1;   // the extra group: its own A and B maps
+                const CUtensorMap* mA = xg ? &tmA2 : &tmA;
+                const CUtensorMap* mB = xg ? &tmB2 : &tmB;
+                const int a_row = (xg ? 0 : s_ro[g]) + mb * BM;
                 const int n0 = (EPI == EPI_SWIGLU_BF16) ? nb * 128 : nb * GM_BN;
-                const int b0 = g * p.b_rows_per_group + n0;
+                const int b0 = (xg ? 0 : g * p.b_rows_per_group) + n0;
                 const int b1 = b0 + p.up_offset;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (*s_abort || !mbar_wait(bar(EMPTY + stage), ph ^ 1)) {
@@ -615,12 +637,12 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
                     if (!gather) {
 #pragma unroll
                         for (int h = 0; h < MT; ++h)
-                            tma_load_2d(sa + h * GM_A_BYTES, &tmA, bar(FULL + stage), kb * GM_BK,
+                            tma_load_2d(sa + h * GM_A_BYTES, mA, bar(FULL + stage), kb * GM_BK,
                                         a_row + h * GM_BM);
                     }
-                    tma_load_2d(sa + A_BYTES, &tmB, bar(FULL + stage), kb * GM_BK, b0);
-                    tma_load_2d(sa + A_BYTES + GM_B_BYTES / 2, &tmB, bar(FULL + stage),
-                                kb * GM_BK, b1);
+                    tma_load_2d(sa + A_BYTES, mB, bar(FULL + stage), kb * GM_BK, b0);
+                    tma_load_2d(sa + A_BYTES + GM_B_BYTES / 2, mB, bar(FULL + stage), kb * GM_BK,
+                                b1);
                     last_par[stage] = (int)ph;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -799,10 +821,11 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
             const uint8_t* src[RPT];
             uint32_t nbytes[RPT];
 #pragma unroll
+            const bool xg = g == p.xg1 - 1;   // the extra group reads row r of a_src
             for (int i = 0; i < RPT; ++i) {
                 const int r = mb * BM + r0 + 16 * i;
                 const bool valid = r < rows_g;
-                const long long tok = valid ? (long long)p.a_gather[s_ro[g] + r] : 0;
+                const long long tok = valid ? (xg ? (long long)r : (long long)p.a_gather[s_ro[g] + r]) : 0;
                 src[i] = p.a_src + tok * p.a_row_bytes + chunk * 16;
                 nbytes[i] = valid ? 16u : 0u;
             }
@@ -879,7 +902,7 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
                 const int r_in = h * GM_BM + q * 32 + lane;
                 const int r_tile = mb * BM + r_in;   // row within the group
                 const bool row_ok = r_tile < rows_g;
-                const long long grow = (long long)s_ro[g] + r_tile;
+                const long long grow = p.out_local ? (long long)r_tile : (long long)s_ro[g] + r_tile;
                 const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) +
                                     (uint32_t)((acc + h) * GM_BN);
                 if (p.partial) gm_epilogue_partial<EPI>(p, tb, nb, ks, row_ok, grow);

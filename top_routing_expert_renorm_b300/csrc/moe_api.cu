@@ -454,7 +454,7 @@ WsLayout ws_layout(const moe_config& c) {
     L.w = take(Pmax * 4);
     L.load = take(E * 4);
     L.counts = take(E * 4);
-    L.offsets = take((E + 1) * 4);
+    L.offsets = take((E + 2) * 4);   // + the shared expert's end (moe_forward)
     L.blockcnt = take(std::max(nb, (T + 31) / 32) * E * 4);   // per chunk, or per 32 tokens
     L.blockoff = take(nb * E * 4);
     const bool rr = c.overflow == MOE_OVERFLOW_REROUTE;
@@ -465,10 +465,12 @@ WsLayout ws_layout(const moe_config& c) {
     L.perm_slot = take(Pmax * 4);
     L.slot_dest = take(Pmax * 4);
     L.x_perm = take(Pmax * d * es);
-    L.mtile = take((E + 1) * 4);
+    L.mtile = take((E + 2) * 4);
     L.shared_tab = take(4 * 4);
     L.counters = take(kNumCounters * 8);
-    L.h = take(is_bf16_kind(c) ? Pmax * F * 2 : 0);
+    // H rows: routed [0, P) and, when moe_forward runs the shared expert as an extra group of
+    // the routed up projection, the shared expert's rows [P, P + T)
+    L.h = take(is_bf16_kind(c) ? (Pmax + (c.has_shared ? T : 0)) * F * 2 : 0);
     L.hs = take(is_bf16_kind(c) && c.has_shared ? T * F * 2 : 0);
     L.y = take((Pmax + (c.has_shared ? T : 0)) * d * 4);
     L.partial = take(ffn_plan(c).partial_floats * 4);
@@ -633,8 +635,13 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
                        const float* w_scale = nullptr, bool swap_ab = false,
                        int* r_hist = nullptr, const int32_t* a_gather = nullptr,
                        int a_row_bytes = 0, float* r_part = nullptr, int* r_tile_cnt = nullptr,
-                       int w_bits = 8, int mt = 1) {
+                       int w_bits = 8, int mt = 1, const void* A2 = nullptr, int64_t a2_rows = 0,
+                       const void* B2 = nullptr, int64_t b2_rows = 0, const float* bias2 = nullptr,
+                       int xg = -1, bool out_local = false) {
     // mt: 128-row halves per tile of the bf16 kernel (2: 256-row tiles, unsplit launches)
+    // xg >= 0 (bf16 kernel, unsplit): group xg reads A rows 0.. of A2 [a2_rows, K] (gathered
+    // A: rows 0.. of A itself) and weights B2 [b2_rows, K], with bias bias2
+    // out_local: output row r of the (single) group is row r of out
     // r_part, r_tile_cnt (EPI_ROUTER_TOPK with sp.S == 2): the epilogue's split-K exchange
     // a_gather (bf16 kernel only): logical A row r (r < a_rows) is row a_gather[r] of A,
     // loaded by the kernel's gather warps
@@ -647,8 +654,9 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     if (swap_ab && !q8t_supports(EPI)) return MOE_ERR_UNSUPPORTED;
     if (w_scale && w_bits != 8 && (w_bits != 4 || !swap_ab)) return MOE_ERR_UNSUPPORTED;
     if (w_bits == 4 && sp.S > 1 && sp.kbs % 2 != 0) return MOE_ERR_UNSUPPORTED;
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, ta2, tb2;
     const bool gathered = a_gather && !w_scale;
+    if (xg >= 0 && (w_scale || sp.S > 1 || !B2)) return MOE_ERR_UNSUPPORTED;
     const uint64_t b_cols = (w_scale && w_bits == 4) ? (uint64_t)K / 2 : (uint64_t)K;   // bytes
     if (swap_ab ? !make_tmap_i8(&tb, B, (uint64_t)b_rows_total, b_cols, GM_BN / 2, QT_BK,
                                 CU_TENSOR_MAP_SWIZZLE_128B)
@@ -660,6 +668,13 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     if (gathered) ta = tb;
     else if (!make_tmap_bf16(&ta, A, (uint64_t)a_rows, (uint64_t)K, swap_ab ? QT_NT : GM_BM))
         return MOE_ERR_CUDA;
+    ta2 = ta;
+    tb2 = tb;
+    if (xg >= 0) {
+        if (!make_tmap_bf16(&tb2, B2, (uint64_t)b2_rows, (uint64_t)K, GM_BN / 2)) return MOE_ERR_CUDA;
+        if (!gathered && !make_tmap_bf16(&ta2, A2, (uint64_t)a2_rows, (uint64_t)K, GM_BM))
+            return MOE_ERR_CUDA;
+    }
     GemmParams p{};
     p.G = G;
     p.N = N;
@@ -683,6 +698,9 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     p.ld_part = (EPI == EPI_SWIGLU_BF16) ? 2ll * N : N;
     p.part_stride = (long long)a_rows * p.ld_part;
     p.tile_counter = counter;
+    p.xg1 = xg + 1;
+    p.xg_bias = bias2;
+    p.out_local = out_local ? 1 : 0;
     p.resid = static_cast<const __nv_bfloat16*>(resid);
     p.r_idx = r_idx;
     p.r_w = r_w;
@@ -764,14 +782,15 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
             MOE_LAUNCH(name ? name : gemm_name<EPI>(), s,
                        launch_k(grouped_gemm_kernel<EPI, 2>, grid,
                                 GM_THREADS + (p.a_gather ? GM_GATHER_THREADS : 0),
-                                gm_smem_bytes(G, 2), s, ta, tb, p));
+                                gm_smem_bytes(G, 2), s, ta, tb, ta2, tb2, p));
         } else {
             return MOE_ERR_UNSUPPORTED;
         }
     } else {
         MOE_LAUNCH(name ? name : gemm_name<EPI>(), s,
                    launch_k(grouped_gemm_kernel<EPI>, grid,
-                            GM_THREADS + (p.a_gather ? GM_GATHER_THREADS : 0), smem, s, ta, tb, p));
+                            GM_THREADS + (p.a_gather ? GM_GATHER_THREADS : 0), smem, s, ta, tb, ta2,
+                            tb2, p));
     }
     if (split) {
         const long long work = a_rows * (long long)(N / 4);
@@ -866,7 +885,11 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
                     float* y, int32_t* mtile, bool mtile_ready, int32_t* shared_tab,
                     __nv_bfloat16* h, __nv_bfloat16* hs, float* partial,
                     unsigned long long* counters, cudaStream_t s, void* fused_out = nullptr,
-                    bool gather_a = false) {
+                    bool gather_a = false, bool merge_shared = false) {
+    // merge_shared (moe_forward; bf16 weights, a shared expert, unsplit up projections,
+    // offsets and mtile with E + 2 entries): the shared expert runs as group E of the
+    // routed up projection (its H rows follow the routed ones), and its down projection
+    // reads those rows through offsets[E .. E+1]
     // gather_a: x_perm is not materialised; the routed up projection reads row p of its A
     // from x[perm_token[p]] (bf16 weights only)
     // fused_out (top-1, no shared expert, unsplit down projection): the down projection
@@ -913,6 +936,41 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
     const void* a_up = ga ? x : x_perm;
     const int32_t* a_idx = ga ? perm_token : nullptr;
     const ExpertTiles et = expert_tiles(c);
+    if (merge_shared) {
+        if (!(c.has_shared && !q8 && fp.up.S == 1 && fp.sh_up.S == 1 && fp.sh_down.S == 1))
+            return MOE_ERR_UNSUPPORTED;
+        MOE_LAUNCH("append_group", s, launch_k(append_group_kernel, 1, 32, 0, s,
+                                                const_cast<int32_t*>(offsets), mtile, E, T));
+        const int mt = ga ? 1 : et.up;
+        const char* nm = c.kind == MOE_EXPERT_SWIGLU ? "grouped_gemm_swiglu" : "grouped_gemm_gelu";
+        if (c.kind == MOE_EXPERT_SWIGLU)
+            MOE_TRY(launch_gemm<EPI_SWIGLU_BF16>(
+                a_up, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E + 1, F, offsets, mtile, h, F, R.b1,
+                nullptr, nullptr, nullptr, k, s, nm, SplitPlan(), nullptr, counters + kCntUp,
+                nullptr, nullptr, nullptr, 0, 0, nullptr, false, nullptr, a_idx, d * 2, nullptr,
+                nullptr, wb, mt, x, T, S->w1, N1, S->b1, E));
+        else
+            MOE_TRY(launch_gemm<EPI_GELU_BF16>(
+                a_up, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E + 1, F, offsets, mtile, h, F, R.b1,
+                nullptr, nullptr, nullptr, k, s, nm, SplitPlan(), nullptr, counters + kCntUp,
+                nullptr, nullptr, nullptr, 0, 0, nullptr, false, nullptr, a_idx, d * 2, nullptr,
+                nullptr, wb, mt, x, T, S->w1, N1, S->b1, E));
+        MOE_TRY(launch_gemm<EPI_SCALE_F32>(h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets,
+                                           mtile, y, d, R.b2, topk_w, perm_token, perm_slot, k, s,
+                                           nullptr, fp.down, partial, counters + kCntDown, nullptr,
+                                           nullptr, nullptr, 0, 0, nullptr, false, nullptr,
+                                           nullptr, 0, nullptr, nullptr, wb, et.down));
+        MOE_LAUNCH("single_group_table", s,
+                   launch_k(single_group_table_kernel, 1, 32, 0, s, T, shared_tab, shared_tab + 2,
+                            counters + kCntSharedUp, 2));
+        // rows [P, P + T) of H (offsets[E .. E+1]), written to the shared rows of y
+        return launch_gemm<EPI_F32>(h, Pmax + T, F, S->w2, d, d, 1, d, offsets + E, shared_tab + 2,
+                                    y_shared, d, S->b2, nullptr, nullptr, nullptr, k, s, nullptr,
+                                    SplitPlan(), nullptr, counters + kCntSharedDown, nullptr,
+                                    nullptr, nullptr, 0, 0, nullptr, false, nullptr, nullptr, 0,
+                                    nullptr, nullptr, wb, et.sh_down, nullptr, 0, nullptr, 0,
+                                    nullptr, -1, true);
+    }
     if (c.kind == MOE_EXPERT_SWIGLU)
         MOE_TRY(launch_gemm<EPI_SWIGLU_BF16>(a_up, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
                                              offsets, mtile, h, F, R.b1, nullptr, nullptr, nullptr,
@@ -1150,11 +1208,15 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate
                                               static_cast<uint8_t*>(out), c.d * 2, c.add_residual}
                                 : DroppedRows{},
                           hist_by_router));
+    // The shared expert as group E of the routed up projection (one launch, one tail).
+    const FfnPlan fpl = ffn_plan(c);
+    const bool merge_shared = c.has_shared && is_bf16_kind(c) && !quant_w(c) && fpl.up.S == 1 &&
+                              fpl.sh_up.S == 1 && fpl.sh_down.S == 1;
     MOE_TRY(ffn_impl(c, x_perm, offsets, *routed, shared, x, w, perm_token, perm_slot, y, mtile,
                      true, at<int32_t>(ws, L.shared_tab), at<__nv_bfloat16>(ws, L.h),
                      at<__nv_bfloat16>(ws, L.hs), at<float>(ws, L.partial),
                      at<unsigned long long>(ws, L.counters), stream, fuse1 ? out : nullptr,
-                     gather_a));
+                     gather_a, merge_shared));
     if (fuse1) return MOE_OK;   // dropped tokens were written by the dispatch
     return combine_impl(c, x, y, slot_dest, w, out, stream);
 }
