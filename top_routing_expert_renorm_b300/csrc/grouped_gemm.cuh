@@ -820,8 +820,8 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
             const int rows_g = s_ro[g + 1] - s_ro[g];
             const uint8_t* src[RPT];
             uint32_t nbytes[RPT];
-#pragma unroll
             const bool xg = g == p.xg1 - 1;   // the extra group reads row r of a_src
+#pragma unroll
             for (int i = 0; i < RPT; ++i) {
                 const int r = mb * BM + r0 + 16 * i;
                 const bool valid = r < rows_g;

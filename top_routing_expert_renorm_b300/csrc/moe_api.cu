@@ -225,6 +225,46 @@ int32_t capacity_of(const moe_config& c) {
 // ---------------------------------------------------------------------------------
 // workspace layout (256-byte aligned regions, identical for every entry point)
 // ---------------------------------------------------------------------------------
+// ---------------------------------------------------------------------------------
+// split-K plan of one grouped-GEMM launch
+// ---------------------------------------------------------------------------------
+// When an upper bound on the launch's output tiles cannot fill the SMs twice, every
+// tile is cut along K into S units (at least 4 K blocks each) so that the units
+// spread over whole waves of SMs; S maximises the fraction of SM slots in use
+// (a larger S must win by 2 %). The plan depends only on the configuration, so the
+// workspace can hold its partial sums.
+struct SplitPlan {
+    int S = 1;
+    int kbs = 0;   // K blocks per split
+};
+
+SplitPlan split_plan(long long max_mtiles, int n_tiles, int K, int sms, int bk = GM_BK) {
+    // bk: K elements per block of the kernel that runs (GM_BK, or QT_BK for the
+    // weight-streaming INT8 kernel)
+    SplitPlan sp;
+    const int KB = (K + bk - 1) / bk;
+    sp.kbs = KB;
+    const long long tiles = max_mtiles * n_tiles;
+    if (tiles <= 0 || tiles >= 2ll * sms) return sp;
+    auto eff = [&](long long units) {
+        const long long waves = (units + sms - 1) / sms;
+        return (double)units / (double)(waves * sms);
+    };
+    double best = eff(tiles);
+    for (int S = 2; S <= 16; ++S) {
+        const int kbs = (KB + S - 1) / S;
+        if (kbs < 4) break;
+        const int Se = (KB + kbs - 1) / kbs;
+        const double e = eff(tiles * Se);
+        if (e > best + 0.02) {
+            best = e;
+            sp.S = Se;
+            sp.kbs = kbs;
+        }
+    }
+    return sp;
+}
+
 // Router scratch: raw partial logits (and, on the tensor-core path, the split gate
 // weights and the one-group tables). Paths: fp32 activations -> CUDA-core GEMM;
 // bf16 activations with T >= kRouterTensorMinT -> exact 3-way bf16 split on the tensor
@@ -290,46 +330,6 @@ RouterPlan router_plan(const moe_config& c) {
         r.scratch_bytes = al256((size_t)r.n_parts * T * E * 4);
     }
     return r;
-}
-
-// ---------------------------------------------------------------------------------
-// split-K plan of one grouped-GEMM launch
-// ---------------------------------------------------------------------------------
-// When an upper bound on the launch's output tiles cannot fill the SMs twice, every
-// tile is cut along K into S units (at least 4 K blocks each) so that the units
-// spread over whole waves of SMs; S maximises the fraction of SM slots in use
-// (a larger S must win by 2 %). The plan depends only on the configuration, so the
-// workspace can hold its partial sums.
-struct SplitPlan {
-    int S = 1;
-    int kbs = 0;   // K blocks per split
-};
-
-SplitPlan split_plan(long long max_mtiles, int n_tiles, int K, int sms, int bk = GM_BK) {
-    // bk: K elements per block of the kernel that runs (GM_BK, or QT_BK for the
-    // weight-streaming INT8 kernel)
-    SplitPlan sp;
-    const int KB = (K + bk - 1) / bk;
-    sp.kbs = KB;
-    const long long tiles = max_mtiles * n_tiles;
-    if (tiles <= 0 || tiles >= 2ll * sms) return sp;
-    auto eff = [&](long long units) {
-        const long long waves = (units + sms - 1) / sms;
-        return (double)units / (double)(waves * sms);
-    };
-    double best = eff(tiles);
-    for (int S = 2; S <= 16; ++S) {
-        const int kbs = (KB + S - 1) / S;
-        if (kbs < 4) break;
-        const int Se = (KB + kbs - 1) / kbs;
-        const double e = eff(tiles * Se);
-        if (e > best + 0.02) {
-            best = e;
-            sp.S = Se;
-            sp.kbs = kbs;
-        }
-    }
-    return sp;
 }
 
 // Weight-only quantised experts: codes plus one fp32 scale per weight row.
