@@ -162,19 +162,23 @@ def test_device_generator_matches_host():
             assert np.array_equal(to_np(t), h)
 
 
-@pytest.mark.parametrize("M,row_splits,N,K", [
-    (300, [0, 100, 100, 300], 256, 128),      # an empty group
-    (1000, [0, 129, 400, 401, 1000, 1000], 320, 192),   # ragged N tile
-    (129, [0, 129], 64, 64),
-    (64, [0, 1, 64], 512, 1024),
+@pytest.mark.parametrize("M,row_splits,N,K,off", [
+    (300, [0, 100, 100, 300], 256, 128, 0),      # an empty group
+    (1000, [0, 129, 400, 401, 1000, 1000], 320, 192, 0),   # ragged N tile
+    (129, [0, 129], 64, 64, 0),
+    (64, [0, 1, 64], 512, 1024, 0),
+    # output 16 bytes past a 32-byte boundary: the epilogue's 16-byte stores
+    (300, [0, 100, 100, 300], 256, 128, 4),
 ])
-def test_grouped_gemm_building_block(M, row_splits, N, K):
+def test_grouped_gemm_building_block(M, row_splits, N, K, off):
     G = len(row_splits) - 1
     g = torch.Generator(device="cpu").manual_seed(M + N + K)
     A = torch.randn(M, K, generator=g).to(torch.bfloat16)
     B = (torch.randn(G, N, K, generator=g) / K ** 0.5).to(torch.bfloat16)
     ro = torch.tensor(row_splits, dtype=torch.int32)
-    D = torch.full((M, N), float("nan"), device="cuda")
+    buf = torch.full((M * N + off,), float("nan"), device="cuda")
+    D = buf[off:].view(M, N)
+    assert D.data_ptr() % 32 == (16 if off == 4 else 0)
     ws = torch.empty(moe.grouped_gemm_ws_size(G), dtype=torch.uint8, device="cuda")
     moe.grouped_gemm(A.cuda(), B.cuda(), ro.cuda(), D, ws)
     assert moe.last_device_status() == 0

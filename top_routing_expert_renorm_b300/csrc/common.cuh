@@ -279,6 +279,15 @@ __device__ __forceinline__ float gelu_erf(float a) {
 // the denominator overflows to +inf and the result is -0.
 __device__ __forceinline__ float silu_fast(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
+// One 32-byte global store of eight floats (a whole L2 sector); p must be 32-byte
+// aligned. A warp writing rows of fp32 tiles (one row per lane) makes half as many
+// partial-sector requests as with 16-byte stores.
+__device__ __forceinline__ void st_global_v8(float* p, const float4& a, const float4& b) {
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(a.x),
+                 "f"(a.y), "f"(a.z), "f"(a.w), "f"(b.x), "f"(b.y), "f"(b.z), "f"(b.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);

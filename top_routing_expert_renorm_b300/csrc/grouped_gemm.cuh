@@ -174,6 +174,8 @@ template <int EPI>
 __device__ __forceinline__ void gm_epilogue_partial(const GemmParams& p, uint32_t tb, int nb, int ks,
                                                     bool row_ok, long long grow) {
     float* prow = p.partial + (long long)ks * p.part_stride + grow * p.ld_part;
+    const bool v8 = ((reinterpret_cast<uintptr_t>(p.partial) |
+                      (uintptr_t)((p.part_stride | p.ld_part) * 4)) & 31) == 0;
     constexpr int chunks = GM_BN / 32;
 #pragma unroll 1
     for (int c = 0; c < chunks; ++c) {
@@ -187,10 +189,18 @@ __device__ __forceinline__ void gm_epilogue_partial(const GemmParams& p, uint32_
             col = nb * GM_BN + c * 32;
         const int lim = (EPI == EPI_SWIGLU_BF16) ? ((c < chunks / 2) ? p.N : 2 * p.N) : p.N;
         if (row_ok && col < lim) {
-            float4* dst = reinterpret_cast<float4*>(prow + col);
+            if (v8) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                for (int i = 0; i < 4; ++i)
+                    st_global_v8(prow + col + 8 * i,
+                                 make_float4(v[8 * i], v[8 * i + 1], v[8 * i + 2], v[8 * i + 3]),
+                                 make_float4(v[8 * i + 4], v[8 * i + 5], v[8 * i + 6], v[8 * i + 7]));
+            } else {
+                float4* dst = reinterpret_cast<float4*>(prow + col);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            }
         }
     }
 }
@@ -454,6 +464,9 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
                 scale = p.topk_w[(long long)p.perm_token[grow] * p.top_k + p.perm_slot[grow]];
         }
         float* orow = reinterpret_cast<float*>(p.out) + grow * p.ld_out;
+        // 32-byte stores when every row starts on a 32-byte boundary (the caller's buffers
+        // need only 16-byte alignment)
+        const bool v8 = ((reinterpret_cast<uintptr_t>(p.out) | (uintptr_t)(p.ld_out * 4)) & 31) == 0;
 #pragma unroll 1
         for (int c2 = 0; c2 < 8; c2 += 2) {   // two 32-column chunks per TMEM wait
             float vv[2][32];
@@ -468,21 +481,27 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] *= srow[col + i];
                     }
-                    float4* dst = reinterpret_cast<float4*>(orow + col);
+                    float4 o[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        float4 o;
-                        o.x = v[4 * i + 0] + (brow ? brow[col + 4 * i + 0] : 0.0f);
-                        o.y = v[4 * i + 1] + (brow ? brow[col + 4 * i + 1] : 0.0f);
-                        o.z = v[4 * i + 2] + (brow ? brow[col + 4 * i + 2] : 0.0f);
-                        o.w = v[4 * i + 3] + (brow ? brow[col + 4 * i + 3] : 0.0f);
+                        o[i].x = v[4 * i + 0] + (brow ? brow[col + 4 * i + 0] : 0.0f);
+                        o[i].y = v[4 * i + 1] + (brow ? brow[col + 4 * i + 1] : 0.0f);
+                        o[i].z = v[4 * i + 2] + (brow ? brow[col + 4 * i + 2] : 0.0f);
+                        o[i].w = v[4 * i + 3] + (brow ? brow[col + 4 * i + 3] : 0.0f);
                         if constexpr (EPI == EPI_SCALE_F32) {
-                            o.x *= scale;
-                            o.y *= scale;
-                            o.z *= scale;
-                            o.w *= scale;
+                            o[i].x *= scale;
+                            o[i].y *= scale;
+                            o[i].z *= scale;
+                            o[i].w *= scale;
                         }
-                        dst[i] = o;
+                    }
+                    if (v8) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) st_global_v8(orow + col + 8 * i, o[2 * i], o[2 * i + 1]);
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(orow + col);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) dst[i] = o[i];
                     }
                 }
             }
