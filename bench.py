@@ -174,7 +174,7 @@ def kernel_roofline_cost(wl, name, P, touched):
     if name in ("grouped_gemm_gelu", "grouped_gemm_swiglu"):
         fl = 2.0 * P * d * wl.N1 + (2.0 * T * d * wl.N1 if wl.has_shared else 0.0)
         return fl, touched * w1b + (w1b if wl.has_shared else 0) + T * d * es
-    if name == "grouped_gemm_scale":
+    if name in ("grouped_gemm_scale", "grouped_gemm_scale_h16"):
         return 2.0 * P * F * d, touched * w2b
     if name == "grouped_gemm_combine1":
         return 2.0 * P * F * d, touched * w2b + T * d * es
@@ -209,6 +209,8 @@ def kernel_algorithmic_cost(wl, name, P, touched):
         return fl, by
     if name == "grouped_gemm_scale":
         return 2.0 * P * F * d, touched * w2b + P * F * 2 + P * d * 4
+    if name == "grouped_gemm_scale_h16":   # expert-output rows as fp16 + a byte per 32 values
+        return 2.0 * P * F * d, touched * w2b + P * F * 2 + P * d * 2 + P * d // 32
     if name == "grouped_gemm_combine1":   # top-1 down projection writing the layer output
         return 2.0 * P * F * d, (touched * w2b + P * F * 2 + P * d * es
                                  + (P * d * es if wl.add_residual else 0))
@@ -225,8 +227,9 @@ def kernel_algorithmic_cost(wl, name, P, touched):
     if name == "topk_renorm":
         return 0.0, T * E * 4 + T * wl.k * 8
     if name.startswith("combine"):
-        rows = P + (T if wl.has_shared else 0)
-        return 0.0, rows * d * 4 + T * d * es * (2 if wl.add_residual else 1) + T * wl.k * 4
+        shared = T * d * 4 if wl.has_shared else 0
+        routed = P * d * 2 + P * d // 32 if name == "combine_h16" else P * d * 4
+        return 0.0, routed + shared + T * d * es * (2 if wl.add_residual else 1) + T * wl.k * 4
     if name == "gather_rows":
         return 0.0, 2.0 * P * d * es + P * 4
     if name == "linear_expert":

@@ -111,6 +111,13 @@ typedef struct {
                                   MOE_I4: the same with 4-bit codes in [-7, 7], two per byte
                                   (w1 [E][N1][d/2], w2 [E][d][F/2] bytes; see moe_quantize_i4). */
     int32_t overflow;          /* moe_overflow; 0 = MOE_OVERFLOW_DROP */
+    int32_t y_fp32;            /* Expert-output rows inside moe_forward (routed experts with
+                                  bf16 weights, top_k >= 4 and an unsplit down projection;
+                                  other layers always keep fp32 rows): 0 = fp16 with one
+                                  power-of-two scale per 32 columns of a row (half the bytes
+                                  of fp32; every element keeps fp16's 11-bit significand and
+                                  no finite value overflows), 1 = fp32, as moe_expert_ffn
+                                  always writes them. */
 } moe_config;
 
 /* One set of stacked expert weights (nn.Linear [out, in] layout, K contiguous).

@@ -45,7 +45,10 @@ class GpuRun:
         self.inp = wl.device_inputs(device)
         self.cfg = moe.config_for(wl)
 
-    def run(self):
+    def run(self, fp32_y=False):
+        """fp32_y: also run moe_forward with fp32 expert-output rows (out_f32y), the
+        format of the staged path (moe_forward's default rows are fp16 with a
+        power-of-two scale per 32 columns)."""
         wl, inp, cfg = self.wl, self.inp, self.cfg
         T, E, k, d = wl.T, wl.E, wl.k, wl.d
         i32 = dict(dtype=torch.int32, device=self.dev)
@@ -91,6 +94,12 @@ class GpuRun:
         self.load_f = torch.empty(E, **i32)
         moe.forward(cfg, inp["x"], inp["wg"], inp["gate_bias"], routed, shared, self.out, ws2,
                     topk_idx=self.idx_f, topk_w=self.w_f, load=self.load_f)
+        if fp32_y:
+            cfg32 = moe.config_for(wl)
+            cfg32.y_fp32 = 1
+            self.out_f32y = torch.empty_like(inp["x"])
+            moe.forward(cfg32, inp["x"], inp["wg"], inp["gate_bias"], routed, shared,
+                        self.out_f32y, torch.empty_like(ws))
         st = moe.last_device_status()
         assert st == 0, f"device status {moe.status_string(st)}"
         torch.cuda.synchronize()

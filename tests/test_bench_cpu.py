@@ -106,6 +106,19 @@ def test_roofline_terms_of_the_kernels_add_up_to_the_layer(name):
     assert fl == pytest.approx(wl.flops(P), rel=1e-12)
 
 
+def test_compact_expert_rows_cost_the_same_roofline_and_fewer_bytes():
+    # the down projection and combine that keep expert-output rows as fp16 with one scale
+    # byte per 32 values own the same layer-level terms; their algorithmic traffic drops by
+    # P * d * (4 - 2 - 1/32) bytes each
+    wl = get("deepseek")
+    P, touched = wl.T * wl.k, wl.E
+    for a, b in (("grouped_gemm_scale", "grouped_gemm_scale_h16"), ("combine_bf16", "combine_h16")):
+        assert bench.kernel_roofline_cost(wl, a, P, touched) == bench.kernel_roofline_cost(wl, b, P, touched)
+        fa, ba = bench.kernel_algorithmic_cost(wl, a, P, touched)
+        fb, bb = bench.kernel_algorithmic_cost(wl, b, P, touched)
+        assert fa == fb and ba - bb == P * wl.d * 2 - P * wl.d // 32
+
+
 def test_both_arms_report_the_same_config():
     wl = get("deepseek")
     a = bench.workload_config(wl, 1, 256)

@@ -32,7 +32,7 @@ class MoeConfig(ctypes.Structure):
                 ("kind", ctypes.c_int32), ("has_shared", ctypes.c_int32),
                 ("add_residual", ctypes.c_int32), ("n_group", ctypes.c_int32),
                 ("topk_group", ctypes.c_int32), ("w_dtype", ctypes.c_int32),
-                ("overflow", ctypes.c_int32)]
+                ("overflow", ctypes.c_int32), ("y_fp32", ctypes.c_int32)]
 
 
 class MoeExpertWeights(ctypes.Structure):

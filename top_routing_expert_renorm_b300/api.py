@@ -45,9 +45,11 @@ OVERFLOW = {"drop": C.MOE_OVERFLOW_DROP, "shared": C.MOE_OVERFLOW_SHARED,
 
 def make_config(T, d, E, top_k, F=0, capacity_factor=0.0, kind="gelu", bf16=True,
                 has_shared=False, add_residual=False, n_group=0, topk_group=0, int8_weights=False,
-                overflow="drop", int4_weights=False):
+                overflow="drop", int4_weights=False, y_fp32=False):
     """overflow: "drop", "shared" (dropped weight to the shared expert) or "reroute".
-    int8_weights / int4_weights: weight-only INT8 / INT4 experts (codes + row scales)."""
+    int8_weights / int4_weights: weight-only INT8 / INT4 experts (codes + row scales).
+    y_fp32: forward() keeps fp32 expert-output rows instead of fp16 with a power-of-two
+    scale per 32 columns."""
     if int8_weights and int4_weights:
         raise ValueError("int8_weights and int4_weights exclude each other")
     kinds = {"linear": C.MOE_EXPERT_LINEAR, "gelu": C.MOE_EXPERT_GELU,
@@ -57,7 +59,7 @@ def make_config(T, d, E, top_k, F=0, capacity_factor=0.0, kind="gelu", bf16=True
                      has_shared=int(bool(has_shared)), add_residual=int(bool(add_residual)),
                      n_group=n_group, topk_group=topk_group,
                      w_dtype=C.MOE_I8 if int8_weights else (C.MOE_I4 if int4_weights else 0),
-                     overflow=OVERFLOW[overflow])
+                     overflow=OVERFLOW[overflow], y_fp32=int(bool(y_fp32)))
 
 
 def config_for(workload, T=None):

@@ -44,7 +44,11 @@ enum EpiKind : int {
     // router with E <= 64: accumulator columns [p*Ep, p*Ep + E) are the three bf16-split
     // terms of x * W_gate; the epilogue forms the logits, selects the top k and writes the
     // renormalised weights (the top-k kernel is not launched)
-    EPI_ROUTER_TOPK = 5
+    EPI_ROUTER_TOPK = 5,
+    // EPI_SCALE_F32's values stored compactly: each 32-column chunk of a row as fp16
+    // v * 2^-e, e chosen from the chunk's largest finite magnitude so that it lands in
+    // [2^14, 2^15), and e as one signed byte in out_exp [rows][ld_exp]
+    EPI_SCALE_H16 = 6
 };
 
 struct GemmParams {
@@ -104,6 +108,11 @@ struct GemmParams {
     // instead of row_offsets[g] + r (single-group launches whose rows sit at a device-side
     // offset of A)
     int out_local;
+    // 1 (fp32 epilogues): whole 32-row warp slices of a tile are written through the
+    // output tensor map (staged in shared memory, one bulk tensor store per 32 x 32 box)
+    int tma_out;
+    int8_t* out_exp;   // EPI_SCALE_H16: the chunk exponents, ld_exp bytes per row
+    int ld_exp;
 };
 
 constexpr int GM_BM = 128, GM_BN = 256, GM_BK = 64, GM_STAGES = 4;
@@ -121,9 +130,16 @@ constexpr int GM_TQ = 8;            // depth of the ring of scheduled unit ids
 constexpr int GM_HDR_BYTES = 512;   // barriers, TMEM address, abort flag, unit-id ring
 
 constexpr int GM_RHIST_BYTES = 4 * 64 * 4;   // router top-k: 64 counters per epilogue warp
-__host__ __device__ constexpr int gm_smem_bytes(int G, int MT = 1) {
-    return 1024 + gm_stages(MT) * gm_stage_bytes(MT) + GM_HDR_BYTES + 2 * (G + 1) * 4 +
-           GM_RHIST_BYTES;
+// fp32 epilogues: one staging box (32 rows x 32 fp32, 128-byte swizzle) per epilogue warp;
+// EPI_SCALE_H16: 32 rows x 64 fp16 in the same 4 KB
+__host__ __device__ constexpr bool gm_stages_out(int epi) {
+    return epi == EPI_F32 || epi == EPI_SCALE_F32 || epi == EPI_SCALE_H16;
+}
+constexpr int GM_OUT_BOX = 32;
+constexpr int GM_OUT_STAGE_BYTES = 4 * GM_OUT_BOX * GM_OUT_BOX * 4;
+__host__ __device__ constexpr int gm_smem_bytes(int G, int MT = 1, int epi = -1) {
+    return 1024 + gm_stages(MT) * gm_stage_bytes(MT) + (gm_stages_out(epi) ? GM_OUT_STAGE_BYTES : 0) +
+           GM_HDR_BYTES + 2 * (G + 1) * 4 + GM_RHIST_BYTES;
 }
 
 // s_mt[0..G] = exclusive scan over the groups of ceil(rows_g / bm), from the row offsets
@@ -209,9 +225,13 @@ template <int EPI>
 __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t tb, int g, int nb,
                                                  bool row_ok, long long grow, int mb = 0,
                                                  int ks = 0, volatile int* s_flag = nullptr,
-                                                 int* s_rh = nullptr) {
+                                                 int* s_rh = nullptr, const CUtensorMap* tm_out = nullptr,
+                                                 uint32_t out_stage = 0, bool tma = false) {
     // mb, ks, s_flag: EPI_ROUTER_TOPK with K split (see there); s_rh: that epilogue
     // warp's 64 histogram counters in shared memory
+    // tma (fp32 epilogues, warp-uniform: the warp's 32 rows are consecutive output rows,
+    // all in the group): each 32-column box is staged at out_stage (4 KB, 1024-byte
+    // aligned, the 128-byte swizzle of tm_out) and written by one bulk tensor store
     const float* brow = p.bias ? p.bias + (long long)g * p.b_rows_per_group : nullptr;
     if (g == p.xg1 - 1) brow = p.xg_bias;   // the extra group (bf16 weights: no row scales)
     const float* srow = p.w_scale ? p.w_scale + (long long)g * p.b_rows_per_group : nullptr;
@@ -456,8 +476,89 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
                                         packed[4 * i + 3]);
             }
         }
+    } else if constexpr (EPI == EPI_SCALE_H16) {
+        const int n0 = nb * GM_BN;
+        const int lane = threadIdx.x & 31;
+        float scale = 1.0f;
+        if (row_ok) scale = p.topk_w[(long long)p.perm_token[grow] * p.top_k + p.perm_slot[grow]];
+        __half* orow = reinterpret_cast<__half*>(p.out) + grow * p.ld_out;
+        int8_t* erow = p.out_exp + grow * p.ld_exp;
+        const bool v8 = ((reinterpret_cast<uintptr_t>(p.out) | (uintptr_t)(p.ld_out * 2)) & 31) == 0;
+        // the tile row's 8 exponents leave as one 8-byte store when all 8 chunks are in N
+        const bool whole = n0 + GM_BN <= p.N;
+        uint32_t ex_lo = 0, ex_hi = 0;
+#pragma unroll 1
+        for (int c2 = 0; c2 < 8; c2 += 2) {   // two 32-column chunks per TMEM wait
+            float vv[2][32];
+            __syncwarp();
+            tmem_load_2x32cols(tb + c2 * 32, tb + (c2 + 1) * 32, vv[0], vv[1]);
+            uint32_t hp[2][16];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float (&v)[32] = vv[h];
+                const int col = n0 + (c2 + h) * 32;
+                // the fp32 operations of EPI_SCALE_F32, in its order
+                float m = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    if (srow) v[i] *= srow[col + i];
+                    v[i] = (v[i] + (brow ? brow[col + i] : 0.0f)) * scale;
+                    const float a = fabsf(v[i]);
+                    m = (a <= 3.40282347e38f) ? fmaxf(m, a) : m;   // finite values only
+                }
+                // 2^ex <= m < 2^(ex+1) for normal m; the chunk is stored as v * 2^-e, e = ex - 14
+                const int ex = (int)((__float_as_uint(m) >> 23) & 0xffu) - 127;
+                const int e = min(126, max(-126, ex - 14));
+                const float inv = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const __half2 hh = __floats2half2_rn(v[2 * i] * inv, v[2 * i + 1] * inv);
+                    hp[h][i] = *reinterpret_cast<const uint32_t*>(&hh);
+                }
+                const int cc = c2 + h;
+                const uint32_t eb = (uint32_t)(e & 0xff) << (8 * (cc & 3));
+                if (cc < 4) ex_lo |= eb;
+                else ex_hi |= eb;
+                if (!tma && row_ok && col < p.N) {
+                    if (v8) {
+                        st_global_v8_b32(orow + col, hp[h]);
+                        st_global_v8_b32(orow + col + 16, hp[h] + 8);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(orow + col);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(hp[h][4 * i], hp[h][4 * i + 1], hp[h][4 * i + 2],
+                                                hp[h][4 * i + 3]);
+                    }
+                }
+                if (!whole && row_ok && col < p.N) erow[col / 32] = (int8_t)e;
+            }
+            const int col2 = n0 + c2 * 32;
+            if (tma && col2 < p.N) {
+                // 64 columns (128 bytes) of the warp's 32 rows: one box
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+                const uint32_t rb = out_stage + lane * 128;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t* w = hp[i >> 2] + 4 * (i & 3);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rb + ((i ^ (lane & 7)) << 4)),
+                                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                                 : "memory");
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(tm_out, out_stage, col2, (int)grow);
+                    bulk_commit();
+                }
+            }
+        }
+        if (whole && row_ok)
+            *reinterpret_cast<uint2*>(erow + n0 / 32) = make_uint2(ex_lo, ex_hi);
     } else {
         const int n0 = nb * GM_BN;
+        const int lane = threadIdx.x & 31;
         float scale = 1.0f;
         if constexpr (EPI == EPI_SCALE_F32) {
             if (row_ok)
@@ -476,7 +577,7 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
             for (int h = 0; h < 2; ++h) {
                 float (&v)[32] = vv[h];
                 const int col = n0 + (c2 + h) * 32;
-                if (row_ok && col < p.N) {
+                if ((row_ok || tma) && col < p.N) {
                     if (srow) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] *= srow[col + i];
@@ -495,7 +596,20 @@ __device__ __forceinline__ void gm_epilogue_tile(const GemmParams& p, uint32_t t
                             o[i].w *= scale;
                         }
                     }
-                    if (v8) {
+                    if (tma) {
+                        // the previous box has left the staging buffer
+                        if (lane == 0) bulk_wait_read_all();
+                        __syncwarp();
+                        const uint32_t rb = out_stage + lane * 128;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) st_shared_v4(rb + ((i ^ (lane & 7)) << 4), o[i]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(tm_out, out_stage, col, (int)grow);
+                            bulk_commit();
+                        }
+                    } else if (v8) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) st_global_v8(orow + col + 8 * i, o[2 * i], o[2 * i + 1]);
                     } else {
@@ -529,9 +643,11 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmA2,
-                        const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tmB2,
+                        const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
     // tmA2 / tmB2: A rows and weights of the extra group p.xg1 - 1 (copies of tmA / tmB
-    // when the launch has none)
+    // when the launch has none); tmD: the fp32 output [rows, N] in 32 x 32 boxes (used
+    // when p.tma_out)
     static_assert(MT == 1 || MT == 2, "tiles are 128 or 256 rows");
     static_assert(MT == 1 || EPI != EPI_ROUTER_TOPK, "the router runs 128-row tiles");
     constexpr int STAGES = gm_stages(MT);
@@ -543,7 +659,10 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     uint8_t* tiles = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    // fp32 epilogues: the four epilogue warps' output staging boxes follow the ring
+    uint8_t* out_stage = smem + STAGES * STAGE_BYTES;
+    constexpr int OUT_BYTES = gm_stages_out(EPI) ? GM_OUT_STAGE_BYTES : 0;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + OUT_BYTES);
     // barrier slots: full[0..3], empty[4..7], tfull[8..9], tempty[10..11], drain[12],
     // unit-id ring full[16..23] / empty[24..31]
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 32);
@@ -582,6 +701,7 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
             tma_prefetch_desc(&tmA2);
             tma_prefetch_desc(&tmB2);
         }
+        if (gm_stages_out(EPI) && p.tma_out) tma_prefetch_desc(&tmD);
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(s_tmem), GM_TMEM_COLS);
@@ -924,9 +1044,14 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
                 const long long grow = p.out_local ? (long long)r_tile : (long long)s_ro[g] + r_tile;
                 const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) +
                                     (uint32_t)((acc + h) * GM_BN);
-                if (p.partial) gm_epilogue_partial<EPI>(p, tb, nb, ks, row_ok, grow);
-                else gm_epilogue_tile<EPI>(p, tb, g, nb, row_ok, grow, mb, ks, s_flag,
-                                           s_rh + (warp & 3) * 64);
+                if (p.partial) {
+                    gm_epilogue_partial<EPI>(p, tb, nb, ks, row_ok, grow);
+                } else {
+                    const bool tma = gm_stages_out(EPI) && p.tma_out && __all_sync(0xffffffffu, row_ok);
+                    gm_epilogue_tile<EPI>(p, tb, g, nb, row_ok, grow, mb, ks, s_flag,
+                                          s_rh + (warp & 3) * 64, &tmD,
+                                          smem_addr(out_stage + q * (GM_OUT_STAGE_BYTES / 4)), tma);
+                }
                 if (MT == 2 && h == 0) {   // half 0 is free for the next tile's MMAs
                     tc_fence_before();
                     __syncwarp();
@@ -941,6 +1066,8 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
                 aph ^= 1;
             }
         }
+        // the warp's bulk stores are written before the kernel ends
+        if (gm_stages_out(EPI) && lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();

@@ -163,6 +163,28 @@ bool make_tmap_i8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D output [rows, cols] of fp32 (or fp16) with a row stride of ld elements, written in
+// boxes of 128 bytes x 32 rows with the 128-byte swizzle (the grouped GEMM's fp32 and
+// compact epilogues).
+bool make_tmap_out(CUtensorMap* m, void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                   bool fp16) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const uint64_t es = fp16 ? 2 : 4;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {ld * es};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / es), GM_OUT_BOX};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base,
+              dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Bytes per row of the chunk exponents of compact expert-output rows of d values: one per
+// 32 columns, rounded up to 16 so that a row's exponents start 16-byte aligned.
+int compact_exp_ld(long long d) { return (int)(((d / 32) + 15) & ~15ll); }
+
 // ---------------------------------------------------------------------------------
 // validation
 // ---------------------------------------------------------------------------------
@@ -581,6 +603,7 @@ const char* gemm_name() {
         case EPI_SWIGLU_BF16: return "grouped_gemm_swiglu";
         case EPI_COMBINE1_BF16: return "grouped_gemm_combine1";
         case EPI_ROUTER_TOPK: return "router_gemm_topk";
+        case EPI_SCALE_H16: return "grouped_gemm_scale_h16";
         default: return "grouped_gemm_scale";
     }
 }
@@ -637,8 +660,12 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
                        int a_row_bytes = 0, float* r_part = nullptr, int* r_tile_cnt = nullptr,
                        int w_bits = 8, int mt = 1, const void* A2 = nullptr, int64_t a2_rows = 0,
                        const void* B2 = nullptr, int64_t b2_rows = 0, const float* bias2 = nullptr,
-                       int xg = -1, bool out_local = false) {
+                       int xg = -1, bool out_local = false, int64_t out_rows = -1,
+                       int8_t* out_exp = nullptr) {
     // mt: 128-row halves per tile of the bf16 kernel (2: 256-row tiles, unsplit launches)
+    // out_rows: rows of out (default a_rows: output rows are numbered like A's)
+    // out_exp (EPI_SCALE_H16, bf16 kernel, unsplit): the chunk exponents of out's rows,
+    // compact_exp_ld(ld_out) bytes per row
     // xg >= 0 (bf16 kernel, unsplit): group xg reads A rows 0.. of A2 [a2_rows, K] (gathered
     // A: rows 0.. of A itself) and weights B2 [b2_rows, K], with bias bias2
     // out_local: output row r of the (single) group is row r of out
@@ -650,6 +677,8 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     // weight-streaming kernel for few rows per group runs (INT4: only that kernel)
     if (a_rows <= 0 || G <= 0) return MOE_OK;
     if (G > GM_MAX_GROUPS) return MOE_ERR_UNSUPPORTED;
+    if (EPI == EPI_SCALE_H16 && (w_scale || (sp.S > 1 && partial) || !out_exp || ld_out % 32 != 0))
+        return MOE_ERR_UNSUPPORTED;
     swap_ab = swap_ab && w_scale != nullptr;
     if (swap_ab && !q8t_supports(EPI)) return MOE_ERR_UNSUPPORTED;
     if (w_scale && w_bits != 8 && (w_bits != 4 || !swap_ab)) return MOE_ERR_UNSUPPORTED;
@@ -701,6 +730,19 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     p.xg1 = xg + 1;
     p.xg_bias = bias2;
     p.out_local = out_local ? 1 : 0;
+    p.out_exp = out_exp;
+    p.ld_exp = compact_exp_ld(ld_out);
+    // fp32 (and compact fp16) outputs of the bf16 kernel leave through a tensor map when
+    // its strides allow
+    CUtensorMap td = ta;
+    // (128-row tiles only: with 256-row tiles the epilogue frees TMEM for the next tile's
+    // MMAs, and the staging buffer's reuse waits slowed it down)
+    const long long out_es = EPI == EPI_SCALE_H16 ? 2 : 4;
+    if (gm_stages_out(EPI) && mt == 1 && !split && !w_scale && (ld_out * out_es) % 16 == 0 &&
+        aligned16(out) && N > 0 &&
+        make_tmap_out(&td, out, (uint64_t)(out_rows >= 0 ? out_rows : a_rows), (uint64_t)N,
+                      (uint64_t)ld_out, EPI == EPI_SCALE_H16))
+        p.tma_out = 1;
     p.resid = static_cast<const __nv_bfloat16*>(resid);
     p.r_idx = r_idx;
     p.r_w = r_w;
@@ -723,7 +765,7 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
         p.a_src = static_cast<const uint8_t*>(A);
         p.a_row_bytes = a_row_bytes;
     }
-    const int smem = gm_smem_bytes(G);
+    const int smem = gm_smem_bytes(G, 1, EPI);
     static std::once_flag attr_once[64];
     static cudaError_t attr_err[64];
     const int dev = current_device();
@@ -731,7 +773,7 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
         std::call_once(attr_once[dev], [&] {
             attr_err[dev] = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 gm_smem_bytes(GM_MAX_GROUPS));
+                                                 gm_smem_bytes(GM_MAX_GROUPS, 1, EPI));
         });
         if (attr_err[dev] != cudaSuccess) return MOE_ERR_CUDA;
     }
@@ -754,19 +796,23 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
                        launch_k(kern, grid, QT_THREADS, gm_q8t_smem_bytes(G), s, ta, tb, p));
         }
     } else if (w_scale) {
-        static std::once_flag q8_once[64];
-        static cudaError_t q8_err[64];
-        if (dev >= 0 && dev < 64) {
-            std::call_once(q8_once[dev], [&] {
-                q8_err[dev] = cudaFuncSetAttribute(grouped_gemm_q8_kernel<EPI>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   gm_q8_smem_bytes(GM_MAX_GROUPS));
-            });
-            if (q8_err[dev] != cudaSuccess) return MOE_ERR_CUDA;
+        if constexpr (EPI == EPI_SCALE_H16) {
+            return MOE_ERR_UNSUPPORTED;   // (rejected above; no INT8 instance of it)
+        } else {
+            static std::once_flag q8_once[64];
+            static cudaError_t q8_err[64];
+            if (dev >= 0 && dev < 64) {
+                std::call_once(q8_once[dev], [&] {
+                    q8_err[dev] = cudaFuncSetAttribute(grouped_gemm_q8_kernel<EPI>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       gm_q8_smem_bytes(GM_MAX_GROUPS));
+                });
+                if (q8_err[dev] != cudaSuccess) return MOE_ERR_CUDA;
+            }
+            MOE_LAUNCH(name ? name : gemm_q8_name<EPI>(), s,
+                       launch_k(grouped_gemm_q8_kernel<EPI>, grid, GM_Q8_THREADS,
+                                gm_q8_smem_bytes(G), s, ta, tb, p));
         }
-        MOE_LAUNCH(name ? name : gemm_q8_name<EPI>(), s,
-                   launch_k(grouped_gemm_q8_kernel<EPI>, grid, GM_Q8_THREADS, gm_q8_smem_bytes(G), s,
-                            ta, tb, p));
     } else if (mt == 2 && !split) {
         if constexpr (EPI != EPI_ROUTER_TOPK) {
             static std::once_flag wide_once[64];
@@ -775,14 +821,14 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
                 std::call_once(wide_once[dev], [&] {
                     wide_err[dev] = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, 2>,
                                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                         gm_smem_bytes(GM_MAX_GROUPS, 2));
+                                                         gm_smem_bytes(GM_MAX_GROUPS, 2, EPI));
                 });
                 if (wide_err[dev] != cudaSuccess) return MOE_ERR_CUDA;
             }
             MOE_LAUNCH(name ? name : gemm_name<EPI>(), s,
                        launch_k(grouped_gemm_kernel<EPI, 2>, grid,
                                 GM_THREADS + (p.a_gather ? GM_GATHER_THREADS : 0),
-                                gm_smem_bytes(G, 2), s, ta, tb, ta2, tb2, p));
+                                gm_smem_bytes(G, 2, EPI), s, ta, tb, ta2, tb2, td, p));
         } else {
             return MOE_ERR_UNSUPPORTED;
         }
@@ -790,14 +836,16 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
         MOE_LAUNCH(name ? name : gemm_name<EPI>(), s,
                    launch_k(grouped_gemm_kernel<EPI>, grid,
                             GM_THREADS + (p.a_gather ? GM_GATHER_THREADS : 0), smem, s, ta, tb, ta2,
-                            tb2, p));
+                            tb2, td, p));
     }
-    if (split) {
-        const long long work = a_rows * (long long)(N / 4);
-        const int blocks = (int)std::max<long long>(
-            1, std::min<long long>((work + 255) / 256, (long long)num_sms() * 8));
-        MOE_LAUNCH(reduce_name<EPI>(), s,
-                   launch_k(splitk_reduce_kernel<EPI>, blocks, 256, 0, s, p, row_offsets + G));
+    if constexpr (EPI != EPI_SCALE_H16) {   // (compact rows come from unsplit launches only)
+        if (split) {
+            const long long work = a_rows * (long long)(N / 4);
+            const int blocks = (int)std::max<long long>(
+                1, std::min<long long>((work + 255) / 256, (long long)num_sms() * 8));
+            MOE_LAUNCH(reduce_name<EPI>(), s,
+                       launch_k(splitk_reduce_kernel<EPI>, blocks, 256, 0, s, p, row_offsets + G));
+        }
     }
     return MOE_OK;
 }
@@ -885,7 +933,10 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
                     float* y, int32_t* mtile, bool mtile_ready, int32_t* shared_tab,
                     __nv_bfloat16* h, __nv_bfloat16* hs, float* partial,
                     unsigned long long* counters, cudaStream_t s, void* fused_out = nullptr,
-                    bool gather_a = false, bool merge_shared = false) {
+                    bool gather_a = false, bool merge_shared = false, int8_t* y_exp = nullptr) {
+    // y_exp (moe_forward; bf16 weights, unsplit routed down projection): the routed rows
+    // of y are written compactly (EPI_SCALE_H16: fp16 values at y, chunk exponents at
+    // y_exp); the shared expert's rows stay fp32
     // merge_shared (moe_forward; bf16 weights, a shared expert, unsplit up projections,
     // offsets and mtile with E + 2 entries): the shared expert runs as group E of the
     // routed up projection (its H rows follow the routed ones), and its down projection
@@ -936,6 +987,20 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
     const void* a_up = ga ? x : x_perm;
     const int32_t* a_idx = ga ? perm_token : nullptr;
     const ExpertTiles et = expert_tiles(c);
+    auto down_routed = [&](const float* row_scale, bool swap) -> moe_status {
+        if (y_exp)
+            return launch_gemm<EPI_SCALE_H16>(
+                h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets, mtile, y, d, R.b2, topk_w,
+                perm_token, perm_slot, k, s, nullptr, SplitPlan(), nullptr, counters + kCntDown,
+                nullptr, nullptr, nullptr, 0, 0, nullptr, false, nullptr, nullptr, 0, nullptr,
+                nullptr, wb, et.down, nullptr, 0, nullptr, 0, nullptr, -1, false, -1, y_exp);
+        return launch_gemm<EPI_SCALE_F32>(h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets,
+                                          mtile, y, d, R.b2, topk_w, perm_token, perm_slot, k, s,
+                                          nullptr, fp.down, partial, counters + kCntDown, nullptr,
+                                          nullptr, nullptr, 0, 0, row_scale, swap, nullptr,
+                                          nullptr, 0, nullptr, nullptr, wb, et.down);
+    };
+    if (y_exp && (q8 || fp.down.S > 1 || fused_out)) return MOE_ERR_UNSUPPORTED;
     if (merge_shared) {
         if (!(c.has_shared && !q8 && fp.up.S == 1 && fp.sh_up.S == 1 && fp.sh_down.S == 1))
             return MOE_ERR_UNSUPPORTED;
@@ -955,11 +1020,7 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
                 nullptr, nullptr, nullptr, k, s, nm, SplitPlan(), nullptr, counters + kCntUp,
                 nullptr, nullptr, nullptr, 0, 0, nullptr, false, nullptr, a_idx, d * 2, nullptr,
                 nullptr, wb, mt, x, T, S->w1, N1, S->b1, E));
-        MOE_TRY(launch_gemm<EPI_SCALE_F32>(h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets,
-                                           mtile, y, d, R.b2, topk_w, perm_token, perm_slot, k, s,
-                                           nullptr, fp.down, partial, counters + kCntDown, nullptr,
-                                           nullptr, nullptr, 0, 0, nullptr, false, nullptr,
-                                           nullptr, 0, nullptr, nullptr, wb, et.down));
+        MOE_TRY(down_routed(nullptr, false));
         MOE_LAUNCH("single_group_table", s,
                    launch_k(single_group_table_kernel, 1, 32, 0, s, T, shared_tab, shared_tab + 2,
                             counters + kCntSharedUp, 2));
@@ -969,7 +1030,7 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
                                     SplitPlan(), nullptr, counters + kCntSharedDown, nullptr,
                                     nullptr, nullptr, 0, 0, nullptr, false, nullptr, nullptr, 0,
                                     nullptr, nullptr, wb, et.sh_down, nullptr, 0, nullptr, 0,
-                                    nullptr, -1, true);
+                                    nullptr, -1, true, T);
     }
     if (c.kind == MOE_EXPERT_SWIGLU)
         MOE_TRY(launch_gemm<EPI_SWIGLU_BF16>(a_up, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
@@ -990,11 +1051,7 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
                                                counters + kCntDown, c.add_residual ? x : nullptr,
                                                nullptr, nullptr, 0, 0, rs2));
     else
-        MOE_TRY(launch_gemm<EPI_SCALE_F32>(h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets,
-                                           mtile, y, d, R.b2, topk_w, perm_token, perm_slot, k, s,
-                                           nullptr, fp.down, partial, counters + kCntDown, nullptr,
-                                           nullptr, nullptr, 0, 0, rs2, swap_r, nullptr,
-                                           nullptr, 0, nullptr, nullptr, wb, et.down));
+        MOE_TRY(down_routed(rs2, swap_r));
     if (c.has_shared) {
         MOE_LAUNCH("single_group_table", s,
                    launch_k(single_group_table_kernel, 1, 32, 0, s, T, shared_tab, shared_tab + 2,
@@ -1023,8 +1080,10 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
 }
 
 moe_status combine_impl(const moe_config& c, const void* x, const float* y,
-                        const int32_t* slot_dest, const float* topk_w, void* out, cudaStream_t s) {
+                        const int32_t* slot_dest, const float* topk_w, void* out, cudaStream_t s,
+                        const int8_t* y_exp = nullptr) {
     // topk_w: read iff overflow == SHARED (the dropped slots' weights join the shared expert)
+    // y_exp (bf16 layers): the routed rows of y are compact (see ffn_impl)
     const float* ovf_w = (c.overflow == MOE_OVERFLOW_SHARED && c.has_shared) ? topk_w : nullptr;
     const int T = c.T, d = c.d, k = c.top_k;
     const long long Pmax = (long long)T * k;
@@ -1036,12 +1095,35 @@ moe_status combine_impl(const moe_config& c, const void* x, const float* y,
     const long long work = (long long)T * ((chunks + cpt - 1) / cpt);
     const int blocks = (int)std::max<long long>(1, std::min<long long>((work + 7) / 8,
                                                                        (long long)num_sms() * 8));
+    if (y_exp && c.act_dtype == MOE_F32) return MOE_ERR_UNSUPPORTED;
     if (c.act_dtype == MOE_F32)
         MOE_LAUNCH("combine_f32", s,
                    launch_k(combine_kernel<float>, blocks, 256, 0, s,
                        static_cast<const float*>(x), y, slot_dest, ysh, ovf_w,
                        static_cast<float*>(out), T, d, k, c.add_residual, cpt));
-    else
+    else if (y_exp) {
+        // one block of CH16_WARPS warps per SM, tasks of 512-column chunks (see
+        // combine_h16_kernel): whole tokens unless that leaves fewer than ~4096 tasks
+        const int ch16 = (d + CH16_COLS - 1) / CH16_COLS;
+        const int cpt16 = (int)std::max<long long>(
+            1, std::min<long long>(ch16, (long long)ch16 * T / 4096));
+        static std::once_flag c16_once[64];
+        static cudaError_t c16_err[64];
+        const int dev = current_device();
+        if (dev >= 0 && dev < 64) {
+            std::call_once(c16_once[dev], [&] {
+                c16_err[dev] = cudaFuncSetAttribute(combine_h16_kernel,
+                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    ch16_smem_bytes());
+            });
+            if (c16_err[dev] != cudaSuccess) return MOE_ERR_CUDA;
+        }
+        MOE_LAUNCH("combine_h16", s,
+                   launch_k(combine_h16_kernel, num_sms(), CH16_WARPS * 32, ch16_smem_bytes(), s,
+                       static_cast<const __nv_bfloat16*>(x), reinterpret_cast<const __half*>(y),
+                       y_exp, compact_exp_ld(d), slot_dest, ysh, ovf_w,
+                       static_cast<__nv_bfloat16*>(out), T, d, k, c.add_residual, cpt16));
+    } else
         MOE_LAUNCH("combine_bf16", s,
                    launch_k(combine_kernel<__nv_bfloat16>, blocks, 256, 0, s,
                        static_cast<const __nv_bfloat16*>(x), y, slot_dest, ysh, ovf_w,
@@ -1212,16 +1294,25 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate
     const FfnPlan fpl = ffn_plan(c);
     const bool merge_shared = c.has_shared && is_bf16_kind(c) && !quant_w(c) && fpl.up.S == 1 &&
                               fpl.sh_up.S == 1 && fpl.sh_down.S == 1;
+    // Compact routed rows of y (fp16 + a power-of-two scale per 32 columns, inside the fp32
+    // region: values in its first Pmax * d * 2 bytes, then Pmax rows of compact_exp_ld(d)
+    // exponent bytes; the shared rows keep their fp32 place after the routed ones).
+    // k >= 4 only: with fewer slots per token the compact combine's copy pipeline holds
+    // too few rows per step to beat the fp32 combine (Mixtral-shaped top-2 layer: 0.061 ms
+    // against 0.045 ms), and the bytes saved are small.
+    const bool compact_y = !c.y_fp32 && is_bf16_kind(c) && !quant_w(c) && !fuse1 &&
+                           fpl.down.S == 1 && c.top_k >= 4;
+    int8_t* y_exp = compact_y ? reinterpret_cast<int8_t*>(y) + (long long)c.T * c.top_k * c.d * 2
+                              : nullptr;
     MOE_TRY(ffn_impl(c, x_perm, offsets, *routed, shared, x, w, perm_token, perm_slot, y, mtile,
                      true, at<int32_t>(ws, L.shared_tab), at<__nv_bfloat16>(ws, L.h),
                      at<__nv_bfloat16>(ws, L.hs), at<float>(ws, L.partial),
                      at<unsigned long long>(ws, L.counters), stream, fuse1 ? out : nullptr,
-                     gather_a, merge_shared));
+                     gather_a, merge_shared, y_exp));
     if (fuse1) return MOE_OK;   // dropped tokens were written by the dispatch
-    return combine_impl(c, x, y, slot_dest, w, out, stream);
+    return combine_impl(c, x, y, slot_dest, w, out, stream, y_exp);
 }
 
-// M-tile table ((G+1) int32), then the tile counter (8-byte aligned).
 // M-tile table ((G+1) int32), then the tile counter (8-byte aligned).
 size_t gg_counter_offset(int32_t G) { return ((size_t)(G + 1) * 4 + 7) & ~size_t(7); }
 
