@@ -101,6 +101,14 @@ SMALL = {
                            overflow="shared"),
     "ovf_shared_hot_k1": W("os2", T=200, d=64, E=8, k=1, F=64, kind="gelu", act="bf16",
                            cf=0.5, gate_bias="hot", has_shared=True, overflow="shared"),
+    # capacity 256 with at least 192 rows per expert: the down projection runs as CTA pairs
+    # sharing each weight tile; Zipf-skewed routing leaves some experts one tile (the
+    # pair's second CTA computes nothing)
+    "pair_down_cap256": W("pd2", T=512, d=256, E=4, k=2, F=128, kind="swiglu", act="bf16",
+                          cf=1.0, gate_bias="zipf"),
+    # the same with k = 4 (compact rows) and a shared expert whose two tiles also pair up
+    "pair_down_k4_shared": W("pd4", T=256, d=192, E=4, k=4, F=128, kind="gelu", act="bf16",
+                             cf=1.0, has_shared=True, expert_bias=True),
     # k = 4: compact expert-output rows with the shared expert's overflow weight, a
     # residual and a width that is not a multiple of 512 (a ragged 512-column chunk)
     "ovf_shared_k4_res": W("os3", T=300, d=320, E=8, k=4, F=128, kind="swiglu", act="bf16",

@@ -113,6 +113,12 @@ struct GemmParams {
     int tma_out;
     int8_t* out_exp;   // EPI_SCALE_H16: the chunk exponents, ld_exp bytes per row
     int ld_exp;
+    // 1 (128-row tiles, unsplit, no gathered A, no extra group; launched as clusters of
+    // two CTAs): a unit is a pair of consecutive M tiles of one group and N block; CTA
+    // rank r of the cluster computes tile 2 * pair + r, each CTA loads one 128-row half of
+    // the B tile and multicasts it to both, and a stage is refilled only after both CTAs'
+    // MMAs have read it. Units are assigned to clusters round-robin.
+    int pair;
 };
 
 constexpr int GM_BM = 128, GM_BN = 256, GM_BK = 64, GM_STAGES = 4;
@@ -138,8 +144,9 @@ __host__ __device__ constexpr bool gm_stages_out(int epi) {
 constexpr int GM_OUT_BOX = 32;
 constexpr int GM_OUT_STAGE_BYTES = 4 * GM_OUT_BOX * GM_OUT_BOX * 4;
 __host__ __device__ constexpr int gm_smem_bytes(int G, int MT = 1, int epi = -1) {
+    // ring, output staging, header, row / M-tile / tile-pair tables, router counters
     return 1024 + gm_stages(MT) * gm_stage_bytes(MT) + (gm_stages_out(epi) ? GM_OUT_STAGE_BYTES : 0) +
-           GM_HDR_BYTES + 2 * (G + 1) * 4 + GM_RHIST_BYTES;
+           GM_HDR_BYTES + 3 * (G + 1) * 4 + GM_RHIST_BYTES;
 }
 
 // s_mt[0..G] = exclusive scan over the groups of ceil(rows_g / bm), from the row offsets
@@ -162,6 +169,27 @@ __device__ __forceinline__ void gm_tile_table_warp(const int* s_ro, int* s_mt, i
         run += (s_ro[g + 1] - s_ro[g] + bm - 1) / bm;
     }
     if (lane == 31) s_mt[G] = incl;
+}
+
+// s_mp[0..G] = exclusive scan over the groups of ceil(tiles_g / 2) (tile pairs), from the
+// M-tile offsets s_mt[0..G]; one warp.
+__device__ __forceinline__ void gm_pair_table_warp(const int* s_mt, int* s_mp, int G, int lane) {
+    const int per = (G + 31) / 32;
+    const int g0 = min(G, lane * per), g1 = min(G, g0 + per);
+    int sum = 0;
+    for (int g = g0; g < g1; ++g) sum += (s_mt[g + 1] - s_mt[g] + 1) / 2;
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    int run = incl - sum;
+    for (int g = g0; g < g1; ++g) {
+        s_mp[g] = run;
+        run += (s_mt[g + 1] - s_mt[g] + 1) / 2;
+    }
+    if (lane == 31) s_mp[G] = incl;
 }
 
 // Work unit t -> (group g, M block mb, N block nb, K split ks). Units of one group are
@@ -672,6 +700,9 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
     int* s_ro = reinterpret_cast<int*>(bars + GM_HDR_BYTES / 8);
     int* s_mt = s_ro + (p.G + 1);
     int* s_rh = s_mt + (p.G + 1);   // [4][64] router histogram counters
+    int* s_mp = s_rh + 4 * 64;      // [G + 1] tile-pair offsets (pair mode)
+    const bool pair = MT == 1 && p.pair;
+    const uint32_t crank = pair ? cluster_ctarank() : 0u;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto bar = [&](int i) { return smem_addr(bars + i); };
@@ -682,7 +713,7 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar(FULL + s), gather ? 5 : 1);   // + the four gather warps
-            mbar_init(bar(EMPTY + s), 1);
+            mbar_init(bar(EMPTY + s), pair ? 2 : 1);   // pair: both CTAs' MMAs
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar(TFULL + a), 1);
@@ -707,6 +738,8 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
         tmem_alloc(smem_addr(s_tmem), GM_TMEM_COLS);
         tmem_relinquish();
     }
+    // pair: both CTAs' barriers are initialised before either multicasts into the other
+    if (pair) cluster_sync_all();
     // Everything above is local set-up that may overlap the end of the preceding kernel;
     // the tables and operands may be its outputs.
     pdl_entry();
@@ -718,11 +751,25 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
         __syncthreads();
         if (warp == 2) gm_tile_table_warp(s_ro, s_mt, p.G, BM, lane);
     }
+    if (pair) {
+        __syncthreads();
+        if (warp == 2) gm_pair_table_warp(s_mt, s_mp, p.G, lane);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
-    const long long total = (long long)s_mt[p.G] * p.n_tiles * p.k_splits;
+    const long long total = pair ? (long long)s_mp[p.G] * p.n_tiles
+                                 : (long long)s_mt[p.G] * p.n_tiles * p.k_splits;
+    // unit t -> group, M tile, N block, K split (pair: tile 2 * pair index + this CTA's rank)
+    auto decode = [&](long long t, int& g, int& mb, int& nb, int& ks) {
+        if (pair) {
+            gm_decode(t, p.G, p.n_tiles, 1, s_mp, g, mb, nb, ks);
+            mb = 2 * mb + (int)crank;
+        } else {
+            gm_decode(t, p.G, p.n_tiles, p.k_splits, s_mt, g, mb, nb, ks);
+        }
+    };
     const int kblocks = p.K / GM_BK;
 
     if (warp == 0) {
@@ -736,7 +783,7 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
             bool ok = true;
             int q = 0;
             uint32_t qph = 0;
-            long long t = blockIdx.x;
+            long long t = pair ? (long long)cluster_id_x() : (long long)blockIdx.x;
             while (true) {
                 // publish the next unit id (-1: no more work) to the MMA and epilogue warps
                 if (*s_abort || !mbar_wait(bar(QEMPTY + q), qph ^ 1)) {
@@ -752,10 +799,11 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
                 }
                 if (pub < 0) break;
                 const long long next =
-                    p.tile_counter ? (long long)gridDim.x + (long long)atomicAdd(p.tile_counter, 1ull)
-                                   : t + gridDim.x;
+                    pair ? t + (long long)cluster_count_x()
+                    : p.tile_counter ? (long long)gridDim.x + (long long)atomicAdd(p.tile_counter, 1ull)
+                                     : t + gridDim.x;
                 int g, mb, nb, ks;
-                gm_decode(t, p.G, p.n_tiles, p.k_splits, s_mt, g, mb, nb, ks);
+                decode(t, g, mb, nb, ks);
                 const int kb0 = ks * p.kb_per_split;
                 const int kb1 = min(kblocks, kb0 + p.kb_per_split);
                 const bool xg = g == p.xg1 - 1;   // the extra group: its own A and B maps
@@ -779,9 +827,14 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
                             tma_load_2d(sa + h * GM_A_BYTES, mA, bar(FULL + stage), kb * GM_BK,
                                         a_row + h * GM_BM);
                     }
-                    tma_load_2d(sa + A_BYTES, mB, bar(FULL + stage), kb * GM_BK, b0);
-                    tma_load_2d(sa + A_BYTES + GM_B_BYTES / 2, mB, bar(FULL + stage), kb * GM_BK,
-                                b1);
+                    if (pair) {   // this CTA's half of B, into both CTAs' stage
+                        tma_load_2d_mc(sa + A_BYTES + crank * (GM_B_BYTES / 2), mB, bar(FULL + stage),
+                                       kb * GM_BK, crank ? b1 : b0, (uint16_t)3);
+                    } else {
+                        tma_load_2d(sa + A_BYTES, mB, bar(FULL + stage), kb * GM_BK, b0);
+                        tma_load_2d(sa + A_BYTES + GM_B_BYTES / 2, mB, bar(FULL + stage),
+                                    kb * GM_BK, b1);
+                    }
                     last_par[stage] = (int)ph;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -890,7 +943,9 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
                                       sw128_kmajor_desc(sa + h * GM_A_BYTES + kk * 32),
                                       sw128_kmajor_desc(sb + kk * 32), idesc,
                                       (kb != kb0 || kk != 0) ? 1u : 0u);
-                    umma_commit(bar(EMPTY + stage));
+                    // pair: the stage is free once both CTAs' MMAs have read it
+                    if (pair) umma_commit_mc(bar(EMPTY + stage), (uint16_t)3);
+                    else umma_commit(bar(EMPTY + stage));
                     if (++stage == STAGES) {
                         stage = 0;
                         ph ^= 1;
@@ -953,7 +1008,7 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
             t = __shfl_sync(0xffffffffu, t, 0);
             if (!got || t < 0) break;
             int g, mb, nb, ks;
-            gm_decode(t, p.G, p.n_tiles, p.k_splits, s_mt, g, mb, nb, ks);
+            decode(t, g, mb, nb, ks);
             const int kb0 = ks * p.kb_per_split;
             const int kb1 = min(kblocks, kb0 + p.kb_per_split);
             const int rows_g = s_ro[g + 1] - s_ro[g];
@@ -1026,7 +1081,7 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
             }
             if (t < 0) break;
             int g, mb, nb, ks;
-            gm_decode(t, p.G, p.n_tiles, p.k_splits, s_mt, g, mb, nb, ks);
+            decode(t, g, mb, nb, ks);
             int ok = 1;
             if (lane == 0) ok = (!*s_abort && mbar_wait(bar(TFULL + acc), aph)) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -1077,6 +1132,9 @@ __global__ void __launch_bounds__(GM_THREADS + GM_GATHER_THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, GM_TMEM_COLS);
     }
+    // pair: neither CTA leaves while the other may still multicast into it or arrive on
+    // its barriers
+    if (pair) cluster_sync_all();
 }
 
 // ---- split-K reduction + epilogue ---------------------------------------------------

@@ -81,6 +81,27 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...);
 }
 
+// The same launch as clusters of cluster_x CTAs along x (grid.x a multiple of it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, int cluster_x, Args&&... args) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = block;
+    lc.dynamicSmemBytes = smem;
+    lc.stream = stream;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = (unsigned)cluster_x;
+    at[1].val.clusterDim.y = 1;
+    at[1].val.clusterDim.z = 1;
+    lc.attrs = at;
+    lc.numAttrs = 2;
+    return cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...);
+}
+
 // EXPR is a launch_k(...) call.
 #define MOE_LAUNCH(NAME, STREAM, ...)                                   \
     do {                                                                \
@@ -644,6 +665,38 @@ const char* reduce_name() {
     }
 }
 
+// CTAs of a paired 128-row grouped GEMM launch: twice the number of two-CTA clusters that can
+// be resident at once (at most one CTA per SM; the pair schedule is round-robin, so every
+// cluster should be resident from the start), or 0 when that cannot be determined.
+template <int EPI>
+int gm_pair_grid(int sms) {
+    static std::once_flag once[64];
+    static int grid[64];
+    const int dev = current_device();
+    if (dev < 0 || dev >= 64) return 0;
+    std::call_once(once[dev], [&] {
+        grid[dev] = 0;
+        if (cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 gm_smem_bytes(GM_MAX_GROUPS, 1, EPI)) != cudaSuccess)
+            return;
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3((unsigned)(sms & ~1));
+        lc.blockDim = dim3(GM_THREADS);
+        lc.dynamicSmemBytes = gm_smem_bytes(GM_MAX_GROUPS, 1, EPI);
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        lc.attrs = at;
+        lc.numAttrs = 1;
+        int nc = 0;
+        if (cudaOccupancyMaxActiveClusters(&nc, grouped_gemm_kernel<EPI>, &lc) == cudaSuccess)
+            grid[dev] = 2 * std::min(nc, sms / 2);
+    });
+    return grid[dev];
+}
+
 // One grouped-GEMM launch (plus, when sp.S > 1, the split-K reduction that applies the
 // epilogue). `partial` must hold sp.S * a_rows * (SwiGLU ? 2N : N) floats when split.
 template <int EPI>
@@ -661,11 +714,13 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
                        int w_bits = 8, int mt = 1, const void* A2 = nullptr, int64_t a2_rows = 0,
                        const void* B2 = nullptr, int64_t b2_rows = 0, const float* bias2 = nullptr,
                        int xg = -1, bool out_local = false, int64_t out_rows = -1,
-                       int8_t* out_exp = nullptr) {
+                       int8_t* out_exp = nullptr, bool pair_ok = false) {
     // mt: 128-row halves per tile of the bf16 kernel (2: 256-row tiles, unsplit launches)
     // out_rows: rows of out (default a_rows: output rows are numbered like A's)
     // out_exp (EPI_SCALE_H16, bf16 kernel, unsplit): the chunk exponents of out's rows,
     // compact_exp_ld(ld_out) bytes per row
+    // pair_ok: run 128-row tiles in CTA pairs sharing each B tile (GemmParams::pair) when
+    // the launch allows it (unsplit, TMA-loaded A, no extra group, bf16 weights)
     // xg >= 0 (bf16 kernel, unsplit): group xg reads A rows 0.. of A2 [a2_rows, K] (gathered
     // A: rows 0.. of A itself) and weights B2 [b2_rows, K], with bias bias2
     // out_local: output row r of the (single) group is row r of out
@@ -732,6 +787,11 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     p.out_local = out_local ? 1 : 0;
     p.out_exp = out_exp;
     p.ld_exp = compact_exp_ld(ld_out);
+    bool pair = pair_ok && mt == 1 && !split && !gathered && xg < 0 && !w_scale &&
+                EPI != EPI_ROUTER_TOPK;
+    const int pair_grid = pair ? gm_pair_grid<EPI>(num_sms()) : 0;
+    if (pair_grid < 2) pair = false;
+    p.pair = pair ? 1 : 0;
     // fp32 (and compact fp16) outputs of the bf16 kernel leave through a tensor map when
     // its strides allow
     CUtensorMap td = ta;
@@ -832,6 +892,10 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
         } else {
             return MOE_ERR_UNSUPPORTED;
         }
+    } else if (pair) {
+        MOE_LAUNCH(name ? name : gemm_name<EPI>(), s,
+                   launch_k_cluster(grouped_gemm_kernel<EPI>, pair_grid, GM_THREADS, smem, s, 2, ta,
+                                    tb, ta2, tb2, td, p));
     } else {
         MOE_LAUNCH(name ? name : gemm_name<EPI>(), s,
                    launch_k(grouped_gemm_kernel<EPI>, grid,
@@ -987,18 +1051,31 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
     const void* a_up = ga ? x : x_perm;
     const int32_t* a_idx = ga ? perm_token : nullptr;
     const ExpertTiles et = expert_tiles(c);
+    // 128-row down projections run as CTA pairs sharing each B tile (GemmParams::pair)
+    // when their groups' tile counts are mostly even: a group with an odd count leaves one
+    // CTA of its last pair idle (DeepSeek-V3 shape at capacity 320, where many experts have
+    // three tiles: 7.63 -> 7.9 ms; at capacity 256: 6.27 -> 6.13 ms). Even enough: at most
+    // two tiles per expert (capacity <= 256 rows, two tiles expected), or six or more.
+    const double rows_e = (double)T * k / E;
+    const int32_t cap = capacity_of(c);
+    const bool pair_down = et.down == 1 && rows_e >= kWideTileMinRows &&
+                           ((cap > 0 && cap <= 2 * kMTile) || rows_e >= 6.0 * kMTile);
+    const int sh_tiles = (T + kMTile - 1) / kMTile;
+    const bool pair_sh = et.sh_down == 1 && sh_tiles >= 2 && (sh_tiles % 2 == 0 || sh_tiles >= 6);
     auto down_routed = [&](const float* row_scale, bool swap) -> moe_status {
         if (y_exp)
             return launch_gemm<EPI_SCALE_H16>(
                 h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets, mtile, y, d, R.b2, topk_w,
                 perm_token, perm_slot, k, s, nullptr, SplitPlan(), nullptr, counters + kCntDown,
                 nullptr, nullptr, nullptr, 0, 0, nullptr, false, nullptr, nullptr, 0, nullptr,
-                nullptr, wb, et.down, nullptr, 0, nullptr, 0, nullptr, -1, false, -1, y_exp);
+                nullptr, wb, et.down, nullptr, 0, nullptr, 0, nullptr, -1, false, -1, y_exp,
+                pair_down);
         return launch_gemm<EPI_SCALE_F32>(h, Pmax, F, R.w2, (int64_t)E * d, d, E, d, offsets,
                                           mtile, y, d, R.b2, topk_w, perm_token, perm_slot, k, s,
                                           nullptr, fp.down, partial, counters + kCntDown, nullptr,
                                           nullptr, nullptr, 0, 0, row_scale, swap, nullptr,
-                                          nullptr, 0, nullptr, nullptr, wb, et.down);
+                                          nullptr, 0, nullptr, nullptr, wb, et.down, nullptr, 0,
+                                          nullptr, 0, nullptr, -1, false, -1, nullptr, pair_down);
     };
     if (y_exp && (q8 || fp.down.S > 1 || fused_out)) return MOE_ERR_UNSUPPORTED;
     if (merge_shared) {
@@ -1030,7 +1107,7 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
                                     SplitPlan(), nullptr, counters + kCntSharedDown, nullptr,
                                     nullptr, nullptr, 0, 0, nullptr, false, nullptr, nullptr, 0,
                                     nullptr, nullptr, wb, et.sh_down, nullptr, 0, nullptr, 0,
-                                    nullptr, -1, true, T);
+                                    nullptr, -1, true, T, nullptr, pair_sh);
     }
     if (c.kind == MOE_EXPERT_SWIGLU)
         MOE_TRY(launch_gemm<EPI_SWIGLU_BF16>(a_up, Pmax, d, R.w1, (int64_t)E * N1, (int)N1, E, F,
@@ -1074,7 +1151,8 @@ moe_status ffn_impl(const moe_config& c, const void* x_perm, const int32_t* offs
                                      y_shared, d, S->b2, nullptr, nullptr, nullptr, k, s, nullptr,
                                      fp.sh_down, partial, counters + kCntSharedDown, nullptr,
                                      nullptr, nullptr, 0, 0, q8 ? S->s2 : nullptr, swap_s,
-                                           nullptr, nullptr, 0, nullptr, nullptr, wb, et.sh_down));
+                                     nullptr, nullptr, 0, nullptr, nullptr, wb, et.sh_down, nullptr,
+                                     0, nullptr, 0, nullptr, -1, false, -1, nullptr, pair_sh));
     }
     return MOE_OK;
 }
