@@ -420,6 +420,24 @@ def cpu_oracle_sample(wl, route_budget_s, ffn_budget_s, seed=0):
 # ---------------------------------------------------------------------------------
 # reference arm: the oracle timed as the reference implementation
 # ---------------------------------------------------------------------------------
+L2_BYTES = 126 * 10 ** 6
+
+
+def streams_past_l2(wl):
+    """True when one forward streams at least four times the L2 (126 MB) through it -- the
+    expert weights of the experts that can hold rows, W_gate, x and out -- so that the
+    weights a step reads are not left in L2 by the step before it; the timed steps then
+    run back to back. Otherwise a buffer larger than L2 is written between steps."""
+    return wl.bytes(min(wl.E, wl.T * wl.k)) >= 4 * L2_BYTES
+
+
+def l2_policy(wl, flush_mib):
+    if streams_past_l2(wl):
+        return (f"not flushed: each forward streams {wl.bytes(min(wl.E, wl.T * wl.k)) / 1e9:.2f} GB, "
+                "over 4x the 126 MB L2")
+    return f"flushed between timed steps ({flush_mib} MiB write)"
+
+
 def workload_config(wl, world, flush_mib):
     """`config` of the line: the workload only, identical on both arms."""
     return {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "top_k": wl.k, "F": wl.F,
@@ -429,7 +447,7 @@ def workload_config(wl, world, flush_mib):
             "expert_weights": ("int8 codes + fp32 row scales" if wl.int8 else
                                "int4 codes (2 per byte) + fp32 row scales" if wl.int4 else "bf16"),
             "overflow": wl.overflow,
-            "l2": f"flushed between timed steps ({flush_mib} MiB write)",
+            "l2": l2_policy(wl, flush_mib),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
@@ -501,14 +519,17 @@ def build_layer(wl, dev):
 
 def measure(wl, layer, x, steps, warmup, flush, world, dev, clocks=None, barrier=None):
     """Device-timed forwards: `warmup` untimed, then `steps` timed (CUDA events on the
-    launch stream around each step, L2 flushed before each), then the same steps again
-    with an event pair around every launch for the per-kernel breakdown."""
+    launch stream around each step; L2 flushed before each unless a forward streams
+    several times the L2, see streams_past_l2), then the same steps again with an event
+    pair around every launch for the per-kernel breakdown."""
     import numpy as np
     import torch
     import top_routing_expert_renorm_b300 as moe
     stream = torch.cuda.current_stream()
     out = torch.empty_like(x)
     load = torch.empty(wl.E, dtype=torch.int32, device=dev)
+
+    do_flush = not streams_past_l2(wl)
 
     def step():
         layer(x, out=out, load=load)
@@ -533,7 +554,8 @@ def measure(wl, layer, x, steps, warmup, flush, world, dev, clocks=None, barrier
     torch.cuda.synchronize()
     n_launch0 = moe.kernel_launch_count()
     for i in range(steps):
-        flush.zero_()                      # L2 flush between timed steps (not timed)
+        if do_flush:
+            flush.zero_()                  # L2 flush between timed steps (not timed)
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -544,7 +566,8 @@ def measure(wl, layer, x, steps, warmup, flush, world, dev, clocks=None, barrier
     # neighbours' start and end, so this pass is not the timed one).
     moe.profile_begin()
     for i in range(steps):
-        flush.zero_()
+        if do_flush:
+            flush.zero_()
         step()
     torch.cuda.synchronize()
     kstats = moe.profile_end()

@@ -119,6 +119,20 @@ def test_compact_expert_rows_cost_the_same_roofline_and_fewer_bytes():
         assert fa == fb and ba - bb == P * wl.d * 2 - P * wl.d // 32
 
 
+def test_l2_is_flushed_unless_a_forward_streams_several_times_the_l2():
+    # the tiny layer and the small quantised decode layers fit (or nearly fit) in the
+    # 126 MB L2: a buffer larger than L2 is written between their timed steps; layers
+    # streaming over 4x the L2 per forward run back to back, and config says which
+    assert not bench.streams_past_l2(get("tiny"))
+    assert "flushed" in bench.workload_config(get("tiny"), 1, 256)["l2"]
+    assert not bench.streams_past_l2(get("decode1_i4"))
+    for n in ("deepseek", "switch", "mixtral", "decode1", "decode64"):
+        wl = get(n)
+        assert bench.streams_past_l2(wl)
+        assert wl.bytes(min(wl.E, wl.T * wl.k)) >= 4 * 126e6
+        assert bench.workload_config(wl, 1, 256)["l2"].startswith("not flushed")
+
+
 def test_both_arms_report_the_same_config():
     wl = get("deepseek")
     a = bench.workload_config(wl, 1, 256)
