@@ -35,7 +35,7 @@ def as_f64(a):
     return bf16_to_f64(a) if a.dtype == np.uint16 else a.astype(np.float64)
 
 
-class GpuRun:
+class DeviceRun:
     """Inputs of a workload on the device and on the host, and the CUDA path's
     stage outputs (route, dispatch, expert FFN, combine) plus moe_forward."""
 
@@ -324,7 +324,7 @@ def full_check(wl, sample=None, seed=0, targeted=False):
     checked in full): seeded random ones, or with targeted=True the tile-boundary,
     dropped and re-routed tokens of targeted_tokens() topped up with random ones, plus the
     staged expert-output rows at the targeted positions."""
-    r = GpuRun(wl).run()
+    r = DeviceRun(wl).run()
     x_all = wl.x_host()
     idx_ref, w_ref = check_routing(r)
     cap, sd, P, route_idx = check_dispatch(r, idx_ref)

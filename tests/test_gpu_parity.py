@@ -7,7 +7,7 @@ import torch
 
 import top_routing_expert_renorm_b300 as moe
 from synth import Workload, get, host_fill, dev_fill, normal_K, uniform_K, NORMAL, UNIFORM
-from gpu_support import GpuRun, full_check, to_np, as_f64, check_outputs
+from gpu_support import DeviceRun, full_check, to_np, as_f64, check_outputs
 
 pytestmark = pytest.mark.gpu
 
@@ -213,7 +213,7 @@ def test_small_parity(name):
 
 def test_dropped_tokens_leave_as_x_bit_exact():
     wl = SMALL["hot_expert_cap"]
-    r = GpuRun(wl).run()
+    r = DeviceRun(wl).run()
     sd = to_np(r.slot_dest)
     dropped = (sd < 0).all(axis=1)
     assert dropped.sum() > 0
@@ -226,14 +226,14 @@ def test_dropped_tokens_leave_as_x_bit_exact():
 def test_top1_fused_combine_matches_staged_path_bitwise(name):
     # moe_forward fuses the combine into the down projection for top-1 layers without a
     # shared expert; the staged entry points do not. The fp32 operations are the same.
-    r = GpuRun(SMALL[name]).run()
+    r = DeviceRun(SMALL[name]).run()
     assert np.array_equal(to_np(r.out), to_np(r.out_stages))
 
 
 def test_forward_is_deterministic():
     wl = SMALL["swiglu_k8_cap_shared"]
-    a = GpuRun(wl).run(fp32_y=True)
-    b = GpuRun(wl).run(fp32_y=True)
+    a = DeviceRun(wl).run(fp32_y=True)
+    b = DeviceRun(wl).run(fp32_y=True)
     assert np.array_equal(to_np(a.out), to_np(b.out))
     assert np.array_equal(to_np(a.out_f32y), to_np(b.out_f32y))
     # with fp32 expert-output rows the forward performs the staged path's operations
@@ -252,7 +252,7 @@ def test_compact_expert_rows_are_used_and_stay_within_the_criteria(name, compact
     # differ from each other by a few fp16 ulps of the summed rows
     wl = SMALL[name]
     moe.profile_begin()
-    r = GpuRun(wl).run(fp32_y=True)
+    r = DeviceRun(wl).run(fp32_y=True)
     stats = moe.profile_end()
     n = 1 if compact else 0
     assert stats.get("grouped_gemm_scale_h16", (0, 0))[0] == n
@@ -340,7 +340,7 @@ def test_tied_logits_select_the_lower_expert_id(name):
 
 def test_layer_object_matches_forward():
     wl = SMALL["gelu_bias_k2"]
-    r = GpuRun(wl).run()
+    r = DeviceRun(wl).run()
     inp = r.inp
     layer = moe.MoELayer(r.cfg, inp["wg"], inp["gate_bias"], inp["w1"], inp["b1"], inp["w2"],
                          inp["b2"])
@@ -354,7 +354,7 @@ def test_layer_object_matches_forward():
 @pytest.mark.parametrize("name", ["swiglu_k8_cap_shared", "gelu_cap_res", "split_swiglu_bias_shared"])
 def test_captured_graph_matches_direct_forward(name):
     wl = SMALL[name]
-    r = GpuRun(wl).run()
+    r = DeviceRun(wl).run()
     inp = r.inp
     layer = moe.MoELayer(r.cfg, inp["wg"], inp["gate_bias"], inp["w1"], inp["b1"], inp["w2"],
                          inp["b2"], inp["shared"])
@@ -428,8 +428,8 @@ def test_out_of_range_expert_id_single_cta_dispatch():
 @pytest.mark.parametrize("name", ["reroute_top1_hot_res", "reroute_k2_zipf"])
 def test_reroute_keeps_more_rows_than_dropping(name):
     wl = SMALL[name]
-    r = GpuRun(wl).run()
-    plain = GpuRun(wl.with_(overflow="drop")).run()
+    r = DeviceRun(wl).run()
+    plain = DeviceRun(wl.with_(overflow="drop")).run()
     kept_rr = int((to_np(r.slot_dest) >= 0).sum())
     kept = int((to_np(plain.slot_dest) >= 0).sum())
     assert kept_rr > kept
@@ -459,7 +459,7 @@ def test_int8_quantiser_matches_oracle_bitwise():
 
 def test_int8_layer_object_quantises_bf16_weights():
     wl = SMALL["i8_swiglu_zipf_shared"]
-    r = GpuRun(wl).run()
+    r = DeviceRun(wl).run()
     inp = r.inp
     layer = moe.MoELayer(r.cfg, inp["wg"], inp["gate_bias"], inp["w1"], inp["b1"], inp["w2"],
                          inp["b2"], inp["shared"])
@@ -487,7 +487,7 @@ def test_int4_quantiser_matches_oracle_bitwise():
 
 def test_int4_layer_object_quantises_bf16_weights():
     wl = SMALL["i4_swiglu_bias_shared"]
-    r = GpuRun(wl).run()
+    r = DeviceRun(wl).run()
     inp = r.inp
     layer = moe.MoELayer(r.cfg, inp["wg"], inp["gate_bias"], inp["w1"], inp["b1"], inp["w2"],
                          inp["b2"], inp["shared"])
@@ -498,7 +498,7 @@ def test_int4_split_k_ends_inside_a_code_stage():
     # d = 2112: 8.25 code stages of 256; the up projections split K in two, the second
     # split ending half-way through its last stage
     moe.profile_begin()
-    GpuRun(SMALL["i4_split_swiglu_shared"]).run()
+    DeviceRun(SMALL["i4_split_swiglu_shared"]).run()
     stats = moe.profile_end()
     assert "splitk_reduce_swiglu" in stats, sorted(stats)
 
@@ -512,7 +512,7 @@ def test_quantised_layers_use_their_kernels(name, prefix):
     # INT8 with few rows per expert: the weight-streaming kernel; otherwise the
     # shared-memory one. INT4: always the weight-streaming kernel.
     moe.profile_begin()
-    GpuRun(SMALL[name]).run()
+    DeviceRun(SMALL[name]).run()
     stats = moe.profile_end()
     gemms = [n for n in stats if n.startswith("grouped_gemm_")]
     assert gemms and all(n.startswith(prefix) for n in gemms), gemms
@@ -527,7 +527,7 @@ def test_forward_gathers_rows_in_the_gemm_for_many_slots(name, gathers):
     # (full_check in test_small_parity) and each other.
     wl = SMALL[name]
     moe.profile_begin()
-    r = GpuRun(wl).run(fp32_y=True)
+    r = DeviceRun(wl).run(fp32_y=True)
     stats = moe.profile_end()
     assert stats["gather_rows"][0] == (1 if gathers else 3)    # staged path (+ 2 forwards)
     assert np.array_equal(to_np(r.out_f32y), to_np(r.out_stages))
@@ -543,7 +543,7 @@ def test_forward_runs_the_shared_expert_as_an_extra_group(name, merged):
     # (test_small_parity) and each other within the parity criteria.
     wl = SMALL[name]
     moe.profile_begin()
-    r = GpuRun(wl).run()
+    r = DeviceRun(wl).run()
     stats = moe.profile_end()
     up = [n for n in stats if n.startswith("grouped_gemm_") and n.endswith(("swiglu", "gelu"))]
     assert sum(stats[n][0] for n in up) == (3 if merged else 4)
@@ -554,7 +554,7 @@ def test_forward_runs_the_shared_expert_as_an_extra_group(name, merged):
 def test_split_k_is_used_for_few_tokens():
     wl = SMALL["split_swiglu_bias_shared"]
     moe.profile_begin()
-    GpuRun(wl).run()
+    DeviceRun(wl).run()
     stats = moe.profile_end()
     assert "splitk_reduce_swiglu" in stats and "splitk_reduce_scale" in stats
     assert "splitk_reduce_f32" in stats
@@ -564,7 +564,7 @@ def test_profile_and_launch_count():
     wl = SMALL["swiglu_bias"]
     n0 = moe.kernel_launch_count()
     moe.profile_begin()
-    GpuRun(wl).run()
+    DeviceRun(wl).run()
     stats = moe.profile_end()
     assert moe.kernel_launch_count() > n0
     assert "grouped_gemm_swiglu" in stats and "grouped_gemm_scale" in stats
