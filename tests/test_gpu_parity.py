@@ -351,8 +351,10 @@ def test_layer_object_matches_forward():
     assert out2.shape == (50, wl.d)
 
 
-@pytest.mark.parametrize("name", ["swiglu_k8_cap_shared", "gelu_cap_res", "split_swiglu_bias_shared"])
+@pytest.mark.parametrize("name", ["swiglu_k8_cap_shared", "gelu_cap_res", "split_swiglu_bias_shared",
+                                  "pair_down_k4_shared"])
 def test_captured_graph_matches_direct_forward(name):
+    # (pair_down_k4_shared: cluster launches of CTA pairs and compact expert rows in a graph)
     wl = SMALL[name]
     r = DeviceRun(wl).run()
     inp = r.inp
