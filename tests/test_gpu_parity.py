@@ -109,6 +109,10 @@ SMALL = {
     # the same with k = 4 (compact rows) and a shared expert whose two tiles also pair up
     "pair_down_k4_shared": W("pd4", T=256, d=192, E=4, k=4, F=128, kind="gelu", act="bf16",
                              cf=1.0, has_shared=True, expert_bias=True),
+    # k = 16 with a shared expert: the compact combine takes a token's slots in two groups
+    # of 8 and adds the shared row after the last group
+    "compact_k16_shared": W("ck16", T=128, d=128, E=32, k=16, F=64, kind="swiglu", act="bf16",
+                            has_shared=True),
     # k = 4: compact expert-output rows with the shared expert's overflow weight, a
     # residual and a width that is not a multiple of 512 (a ragged 512-column chunk)
     "ovf_shared_k4_res": W("os3", T=300, d=320, E=8, k=4, F=128, kind="swiglu", act="bf16",
@@ -241,6 +245,7 @@ def test_forward_is_deterministic():
 
 
 @pytest.mark.parametrize("name,compact", [("swiglu_k8_cap_shared", True), ("max_E_max_k", True),
+                                          ("compact_k16_shared", True),
                                           ("wide_k4_shared", True), ("reroute_k8_shared", True),
                                           ("ovf_shared_k4_res", True), ("gelu_bias_k2", False),
                                           ("ovf_shared_k2_res", False)])

@@ -175,8 +175,8 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const OT* __restrict__ 
 // ahead, so the bytes in flight do not depend on registers or occupancy. A step is one
 // 512-column chunk of a token and a group of up to 8 slots: each slot's row piece is
 // 1 KB contiguous (a lane copies 16 bytes at lane * 8 and at 256 + lane * 8 columns),
-// with the chunk's 16 exponent bytes per slot, and with the first group the shared-expert
-// row (fp32) and the residual row. Row pieces of 512 bytes (256 columns) ran no faster
+// with the chunk's 16 exponent bytes per slot, with the first group the residual row and
+// with the last group (where it is added) the shared-expert row (fp32). Row pieces of 512 bytes (256 columns) ran no faster
 // than the fp32 rows' 1 KB pieces: the scattered row reads are bound by their count.
 constexpr int CH16_STAGES = 3, CH16_WARPS = 6, CH16_COLS = 512;
 constexpr int CH16_DATA = kCombineGroup * 2 * 32 * 16;   // slot rows
@@ -260,14 +260,12 @@ __global__ void __launch_bounds__(CH16_WARPS * 32, 1) combine_h16_kernel(
                         if (rr[u] >= 0)
                             cp_async_cg16(sa + ((u * 2 + hf) * 32 + lane) * 16,
                                           y16 + (long long)rr[u] * d + ca);
-                    if (g == 0) {
-                        if (y_shared) {
-                            const float* ys = y_shared + t * d + ca;
-                            cp_async_cg16(sa + CH16_SH + (hf * 32 + lane) * 32, ys);
-                            cp_async_cg16(sa + CH16_SH + (hf * 32 + lane) * 32 + 16, ys + 4);
-                        }
-                        if (add_residual)
-                            cp_async_cg16(sa + CH16_RES + (hf * 32 + lane) * 16, x + t * d + ca);
+                    if (g == 0 && add_residual)
+                        cp_async_cg16(sa + CH16_RES + (hf * 32 + lane) * 16, x + t * d + ca);
+                    if (g == groups - 1 && y_shared) {   // added after the last group
+                        const float* ys = y_shared + t * d + ca;
+                        cp_async_cg16(sa + CH16_SH + (hf * 32 + lane) * 32, ys);
+                        cp_async_cg16(sa + CH16_SH + (hf * 32 + lane) * 32 + 16, ys + 4);
                     }
                 }
                 // the chunk's 16 exponent bytes (a row holds 16 * chunks of them)
