@@ -3,6 +3,7 @@
 //  the k kept logits); adv12 4.1 steps 1-3 and Q1 (renormalise the kept weights);
 //  "MoE 混合专家架构" 4.2 数值稳定性 (max-subtracted softmax).]
 #pragma once
+#include <type_traits>
 #include "common.cuh"
 
 namespace moe {
@@ -225,46 +226,54 @@ __global__ void __launch_bounds__(256, 3) topk_renorm_kernel(const float* __rest
     const int lane = threadIdx.x & 31;
     const long long t0 = (long long)blockIdx.x * kTopkTok;
     const int nt = (int)min((long long)kTopkTok, (long long)T - t0);
-    // Each thread forms kTopkSums logits at a time and issues all their part loads before
-    // the first add, so that one memory round trip serves several sums.
-    constexpr int kTopkSums = 4;
+    // Logits: every thread issues the part loads of several sums before their adds, so one
+    // memory round trip serves them. Few parts (the tensor-core router's three terms): 8
+    // sums per thread, all parts in one batch of 4 (DeepSeek-V3 shape: 53 -> 39 us); many
+    // parts (the split-K router's K slices, decode): 4 sums per thread, parts in batches
+    // of 8 (one sum per thread with batches of 32 was slower: T = 8, 21 -> 59 us). Adds
+    // run in part order.
     const int n = nt * E;
-    for (int i0 = threadIdx.x; i0 < n; i0 += kTopkSums * blockDim.x) {
-        const float* L[kTopkSums];
-        float s[kTopkSums];
+    auto form = [&](auto es_tag, auto pb_tag) {
+        constexpr int ES = decltype(es_tag)::value, PB = decltype(pb_tag)::value;
+        for (int i0 = threadIdx.x; i0 < n; i0 += ES * blockDim.x) {
+            const float* L[ES];
+            float s[ES];
 #pragma unroll
-        for (int u = 0; u < kTopkSums; ++u) {
-            const int i = i0 + u * blockDim.x;
-            const int tt = i / E, e = i - tt * E;
-            L[u] = parts + (t0 + tt) * row_stride + e;
-            s[u] = (i < n) ? L[u][0] : 0.0f;
+            for (int u = 0; u < ES; ++u) {
+                const int i = min(i0 + u * (int)blockDim.x, n - 1);
+                const int tt = i / E, e = i - tt * E;
+                L[u] = parts + (t0 + tt) * row_stride + e;
+                s[u] = 0.0f;
+            }
+            for (int p = 0; p < n_parts; p += PB) {
+                float v[ES][PB];
+#pragma unroll
+                for (int u = 0; u < ES; ++u)
+#pragma unroll
+                    for (int q = 0; q < PB; ++q)
+                        v[u][q] = (i0 + u * (int)blockDim.x < n && p + q < n_parts)
+                                      ? L[u][(long long)(p + q) * part_stride]
+                                      : 0.0f;
+#pragma unroll
+                for (int u = 0; u < ES; ++u)
+#pragma unroll
+                    for (int q = 0; q < PB; ++q)
+                        if (p + q < n_parts) s[u] = (p + q == 0) ? v[u][q] : s[u] + v[u][q];
+            }
+#pragma unroll
+            for (int u = 0; u < ES; ++u) {
+                const int i = i0 + u * blockDim.x;
+                if (i >= n) break;
+                const int tt = i / E, e = i - tt * E;
+                float sv = s[u];
+                if (bias) sv += bias[e];
+                sL[i] = sv;
+                if (logits) logits[(t0 + tt) * E + e] = sv;
+            }
         }
-        for (int p = 1; p < n_parts; p += 8) {
-            float v[kTopkSums][8];
-#pragma unroll
-            for (int u = 0; u < kTopkSums; ++u)
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    v[u][q] = (i0 + u * (int)blockDim.x < n && p + q < n_parts)
-                                  ? L[u][(p + q) * part_stride]
-                                  : 0.0f;
-#pragma unroll
-            for (int u = 0; u < kTopkSums; ++u)
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    if (p + q < n_parts) s[u] += v[u][q];
-        }
-#pragma unroll
-        for (int u = 0; u < kTopkSums; ++u) {
-            const int i = i0 + u * blockDim.x;
-            if (i >= n) break;
-            const int tt = i / E, e = i - tt * E;
-            float sv = s[u];
-            if (bias) sv += bias[e];
-            sL[i] = sv;
-            if (logits) logits[(t0 + tt) * E + e] = sv;
-        }
-    }
+    };
+    if (n_parts <= 4) form(std::integral_constant<int, 8>{}, std::integral_constant<int, 4>{});
+    else form(std::integral_constant<int, 4>{}, std::integral_constant<int, 8>{});
     __syncthreads();
     const int wt = threadIdx.x >> 5;
     if (wt >= nt) return;
