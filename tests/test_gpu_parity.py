@@ -109,6 +109,12 @@ SMALL = {
     # the same with k = 4 (compact rows) and a shared expert whose two tiles also pair up
     "pair_down_k4_shared": W("pd4", T=256, d=192, E=4, k=4, F=128, kind="gelu", act="bf16",
                              cf=1.0, has_shared=True, expert_bias=True),
+    # at most 32 assignments: the single-warp dispatch, with capacity drops (hot expert),
+    # and top-1 with the dropped tokens' rows written by the dispatch (fused combine)
+    "tiny_dispatch_cap": W("td1", T=12, d=64, E=4, k=2, F=64, kind="gelu", act="bf16",
+                           cf=0.5, gate_bias="hot"),
+    "tiny_dispatch_top1_res": W("td2", T=20, d=64, E=4, k=1, F=64, kind="gelu", act="bf16",
+                                cf=0.5, gate_bias="hot", add_residual=True),
     # k = 16 with a shared expert: the compact combine takes a token's slots in two groups
     # of 8 and adds the shared row after the last group
     "compact_k16_shared": W("ck16", T=128, d=128, E=32, k=16, F=64, kind="swiglu", act="bf16",
@@ -404,6 +410,34 @@ def test_out_of_range_expert_id_is_skipped_and_reported():
     sd = to_np(outs[5])
     assert sd[5, 0] == -1 and sd[17, 0] == -1
     assert to_np(outs[0]).sum() == T * k - 2
+
+
+def test_out_of_range_expert_id_tiny_dispatch():
+    # at most 32 assignments run the single-warp dispatch: bad ids are skipped and reported
+    T, k, E = 10, 2, 8
+    cfg = moe.make_config(T, 64, E, k, 64, 0.0, "gelu")
+    g = torch.Generator(device="cpu").manual_seed(5)
+    idx = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    idx[3, 1] = E
+    idx[7, 0] = -3
+    good = idx.clone().numpy()
+    good[3, 1] = good[7, 0] = -1
+    i32 = dict(dtype=torch.int32, device="cuda")
+    outs = [torch.empty(E, **i32), torch.empty(E, **i32), torch.empty(E + 1, **i32),
+            torch.empty(T * k, **i32), torch.empty(T * k, **i32), torch.empty(T, k, **i32)]
+    ws = torch.empty(moe.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    moe.dispatch(cfg, idx.cuda(), None, *outs, None, ws)
+    assert moe.last_device_status() == moe._capi.MOE_ERR_DEVICE_INDEX
+    ld, off, sd = to_np(outs[0]), to_np(outs[2]), to_np(outs[5])
+    assert sd[3, 1] == -1 and sd[7, 0] == -1
+    assert np.array_equal(ld, np.bincount(good[good >= 0], minlength=E))
+    assert np.array_equal(off, np.concatenate([[0], np.cumsum(ld)]))
+    pt, ps = to_np(outs[3]), to_np(outs[4])
+    for t in range(T):
+        for j in range(k):
+            if good[t, j] >= 0:
+                p = sd[t, j]
+                assert pt[p] == t and ps[p] == j and off[good[t, j]] <= p < off[good[t, j] + 1]
 
 
 def test_out_of_range_expert_id_single_cta_dispatch():

@@ -483,6 +483,91 @@ __global__ void __launch_bounds__(1024) dispatch_one_cta_kernel(
     }
 }
 
+// ---- the whole dispatch for n = T * k <= 32 assignments: one warp ---------------------
+// Lane i holds assignment i (token i / k, slot i % k). Its rank among the assignments of
+// its expert in token order is the number of lower lanes in its __match_any_sync group;
+// each group's lowest lane writes the group's size as the expert's load. Each lane then
+// scans a contiguous run of experts (counts min(load, cap), their offsets and 128-row
+// tile counts), a warp scan joins the runs, and the kept assignments are scattered.
+// Same outputs as dispatch_one_cta_kernel, without its block-wide phases.
+constexpr int kTinyAssign = 32;
+__global__ void __launch_bounds__(32) dispatch_tiny_kernel(
+    const int* __restrict__ idx, int T, int k, int E, int cap, int* __restrict__ load,
+    int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ perm_token,
+    int* __restrict__ perm_slot, int* __restrict__ slot_dest, int* __restrict__ mtile_offsets,
+    unsigned long long* __restrict__ counters, int n_counters, DroppedRows dr) {
+    pdl_entry();
+    extern __shared__ int tsm[];
+    int* s_load = tsm;       // [E]
+    int* s_off = tsm + E;    // [E]
+    const int lane = threadIdx.x;
+    if (counters && lane < n_counters) counters[lane] = 0ull;
+    const int n = T * k;
+    for (int e = lane; e < E; e += 32) s_load[e] = 0;
+    int ex = -1;
+    if (lane < n) {
+        ex = idx[lane];
+        if (ex < 0 || ex >= E) {
+            raise_error(DEVERR_INDEX);
+            ex = -1;
+        }
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, ex);
+    const unsigned lower = peers & ((1u << lane) - 1u);
+    const int rank = __popc(lower);
+    __syncwarp();
+    if (ex >= 0 && lower == 0) s_load[ex] = __popc(peers);
+    __syncwarp();
+    // lane l scans experts [l * per, (l + 1) * per)
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int kept_run = 0, tiles_run = 0;
+    for (int e = e0; e < e1; ++e) {
+        const int kept = min(s_load[e], cap);
+        kept_run += kept;
+        tiles_run += (kept + kMTile - 1) / kMTile;
+    }
+    int kept_incl = kept_run, tiles_incl = tiles_run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, kept_incl, off);
+        const int b = __shfl_up_sync(0xffffffffu, tiles_incl, off);
+        if (lane >= off) {
+            kept_incl += a;
+            tiles_incl += b;
+        }
+    }
+    int koff = kept_incl - kept_run, toff = tiles_incl - tiles_run;
+    for (int e = e0; e < e1; ++e) {
+        const int l = s_load[e], kept = min(l, cap);
+        load[e] = l;
+        counts[e] = kept;
+        offsets[e] = koff;
+        s_off[e] = koff;
+        if (mtile_offsets) mtile_offsets[e] = toff;
+        koff += kept;
+        toff += (kept + kMTile - 1) / kMTile;
+    }
+    if (lane == 31) {
+        offsets[E] = kept_incl;
+        if (mtile_offsets) mtile_offsets[E] = tiles_incl;
+    }
+    __syncwarp();
+    bool dropped = false;
+    if (lane < n) {
+        if (ex >= 0 && rank < cap) {
+            const int pos = s_off[ex] + rank;
+            perm_token[pos] = lane / k;
+            perm_slot[pos] = lane % k;
+            slot_dest[lane] = pos;
+        } else {
+            slot_dest[lane] = -1;
+            dropped = true;
+        }
+    }
+    if (dr.out) write_dropped_rows(dr, __ballot_sync(0xffffffffu, dropped), 0, lane);
+}
+
 // ---- the same copy organised by token (k >= 2): one warp per token reads its row of x once
 // and writes it to each of its kept slots' rows (slot_dest[t*k + j] >= 0), so x is read
 // once instead of k times. 16-byte vectors, four per lane in flight; row_bytes is a

@@ -569,6 +569,11 @@ moe_status dispatch_impl(const moe_config& c, const int32_t* idx, const void* x,
         MOE_LAUNCH("dispatch_rank_reroute", s,
                    launch_k(dispatch_rank_kernel<kRankReroute>, nb, 256, rsm, s, prop, T, k, E,
                             cap, blockoff, offsets, perm_token, perm_slot, slot_dest, idx, cnt0, dr));
+    } else if ((long long)T * k <= kTinyAssign) {
+        MOE_LAUNCH("dispatch_tiny", s,
+                   launch_k(dispatch_tiny_kernel, 1, 32, 2 * E * sizeof(int), s, idx, T, k, E, cap,
+                            load, counts, offsets, perm_token, perm_slot, slot_dest, mtile,
+                            counters, 2, dr));
     } else if (dispatch_one_cta(c)) {
         MOE_LAUNCH("dispatch_one_cta", s,
                    launch_k(dispatch_one_cta_kernel, 1, 1024, 33 * E * sizeof(int), s, idx, T, k,
