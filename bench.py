@@ -158,7 +158,8 @@ def _weight_bytes(wl):
 
 
 def _base_name(name):
-    return re.sub(r"_q[48]t?_", "_", name)   # INT8 / INT4-weight kernels: same algorithm
+    # INT8 / INT4-weight kernels and the bf16 weight-streaming kernel: same algorithm
+    return re.sub(r"_(q[48]t?|st)_", "_", name)
 
 
 def kernel_roofline_cost(wl, name, P, touched):
@@ -243,6 +244,8 @@ KERNEL_FILES = {
     "grouped_gemm_q4t": ["grouped_gemm_q8t.cuh", "grouped_gemm_q8.cuh", "grouped_gemm.cuh",
                          "common.cuh"],
     "grouped_gemm_q8": ["grouped_gemm_q8.cuh", "grouped_gemm.cuh", "common.cuh"],
+    "grouped_gemm_st": ["grouped_gemm_q8t.cuh", "grouped_gemm_q8.cuh", "grouped_gemm.cuh",
+                        "common.cuh"],
     "grouped_gemm": ["grouped_gemm.cuh", "common.cuh"],
     "router_gemm_tc": ["grouped_gemm.cuh", "common.cuh"],
     "router_gemm_topk": ["grouped_gemm.cuh", "common.cuh"],

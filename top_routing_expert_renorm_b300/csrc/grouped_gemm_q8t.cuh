@@ -19,6 +19,9 @@
 // INT4 codes (BITS = 4) are packed two per byte along K (even k in the low nibble), so a
 // 128-byte box row holds 256 codes: each code stage then feeds two TMEM stages of 128
 // codes, and K splits start on a code stage (an even number of 128-code blocks).
+// bf16 weights (BITS = 16, no row scales) stream the same way for decode-sized groups:
+// a 128-byte box row holds 64 weights, so two code stages feed one TMEM stage, and the
+// converters copy the rows into TMEM unchanged.
 //   warp 0       unit scheduler + TMA of the codes (two 128-row boxes of 128 bytes,
 //                128-byte swizzle) into a QT_NQ-deep ring;
 //   warps 1, 15  MMA issuers (A from TMEM, B from shared memory), warp 1 for the weight
@@ -115,8 +118,9 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
     static_assert(EPI == EPI_GELU_BF16 || EPI == EPI_SWIGLU_BF16 || EPI == EPI_SCALE_F32 ||
                       EPI == EPI_F32,
                   "epilogue not supported by the swapped INT8 kernel");
-    static_assert(BITS == 8 || BITS == 4, "codes are 8 or 4 bits wide");
-    constexpr int KPQ = 8 / BITS;   // 128-code K blocks per code stage
+    static_assert(BITS == 8 || BITS == 4 || BITS == 16, "codes are 8 or 4 bits wide, or bf16");
+    constexpr int KPQ = BITS == 16 ? 1 : 8 / BITS;   // 128-code K blocks per code stage
+    constexpr int QPK = BITS == 16 ? 2 : 1;          // code stages per 128-code K block
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -252,8 +256,9 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
                 const int n0 = (EPI == EPI_SWIGLU_BF16) ? nb * 128 : nb * GM_BN;
                 const int b0 = g * p.b_rows_per_group + n0;
                 const int b1 = b0 + p.up_offset;
-                // code stage kb holds 128-code blocks KPQ*kb .. KPQ*kb + KPQ-1 (x = kb * 128 bytes)
-                for (int kb = kb0 / KPQ; kb < (kb1 + KPQ - 1) / KPQ; ++kb) {
+                // code stage kb holds 128-code blocks KPQ*kb .. KPQ*kb + KPQ-1 (x = kb * 128
+                // bytes); bf16: stages 2 kb and 2 kb + 1 hold the halves of block kb
+                for (int kb = kb0 * QPK / KPQ; kb < (kb1 * QPK + KPQ - 1) / KPQ; ++kb) {
                     if (*s_abort || !mbar_wait(bar(QEMPTY + stage), ph ^ 1)) {
                         *s_abort = 1;
                         ok = false;
@@ -358,6 +363,58 @@ __global__ void __launch_bounds__(QT_THREADS, 1)
             const int kb0 = ks * p.kb_per_split;
             const int kb1 = min(kblocks, kb0 + p.kb_per_split);
             for (int kb = kb0; kb < kb1; ++kb) {
+                if constexpr (BITS == 16) {
+                    // bf16: codes 0..63 of the block from code stage qs, 64..127 from the next;
+                    // each stage is released once its half is copied
+                    const bool w_ok = !*s_abort && mbar_wait(bar(CEMPTY + cs), cph ^ 1);
+                    if (!__all_sync(0xffffffffu, w_ok)) {
+                        if (lane == 0) *s_abort = 1;
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint32_t v[2][32];
+                    bool got = true;
+#pragma unroll
+                    for (int hs = 0; hs < 2; ++hs) {
+                        const bool q_ok = !*s_abort && mbar_wait(bar(QFULL + qs), qph);
+                        if (!__all_sync(0xffffffffu, q_ok)) {
+                            got = false;
+                            break;
+                        }
+                        const uint8_t* row = q_tiles + qs * QT_Q_BYTES + r * QT_BK;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const uint4 w = *reinterpret_cast<const uint4*>(row + ((c ^ sw) << 4));
+                            v[hs][4 * c + 0] = w.x;
+                            v[hs][4 * c + 1] = w.y;
+                            v[hs][4 * c + 2] = w.z;
+                            v[hs][4 * c + 3] = w.w;
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(QEMPTY + qs));   // codes consumed
+                        if (++qs == QT_NQ) {
+                            qs = 0;
+                            qph ^= 1;
+                        }
+                    }
+                    if (!got) {
+                        if (lane == 0) *s_abort = 1;
+                        ok = false;
+                        break;
+                    }
+                    tmem_store_32cols(t_lane + cs * 128, v[0]);
+                    tmem_store_32cols(t_lane + cs * 128 + 32, v[1]);
+                    tmem_store_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(CFULL + cs));
+                    if (++cs == QT_NC) {
+                        cs = 0;
+                        cph ^= 1;
+                    }
+                    continue;
+                }
                 // sub: the 128-code block of the code stage. The stage's first block waits
                 // for the codes; its last block (or the unit's last) releases them.
                 const int sub = (kb - kb0) % KPQ;

@@ -377,14 +377,22 @@ RouterPlan router_plan(const moe_config& c) {
 
 // Weight-only quantised experts: codes plus one fp32 scale per weight row.
 bool quant_w(const moe_config& c) { return c.w_dtype == MOE_I8 || c.w_dtype == MOE_I4; }
-int code_bits(const moe_config& c) { return c.w_dtype == MOE_I4 ? 4 : 8; }
+// Bits per weight code of the expert GEMMs (16: bf16 weights).
+int code_bits(const moe_config& c) {
+    return c.w_dtype == MOE_I4 ? 4 : c.w_dtype == MOE_I8 ? 8 : 16;
+}
 
 // INT8 experts with few rows per group run the weight-streaming kernel
 // (grouped_gemm_q8t_kernel: operands swapped, 32-row activation tiles): the routed
 // experts when they average at most 32 rows, the shared expert up to 64 tokens.
-// INT4 experts always run it.
+// INT4 experts always run it. Routed bf16 experts run its bf16 mode when they average at
+// most kStreamBf16Rows rows (decode): the 128-row tiles of the bf16 kernel would carry
+// a zero-filled A tile for each token row.
+constexpr int kStreamBf16Rows = 4;
 bool q8t_routed(const moe_config& c) {
-    return c.w_dtype == MOE_I4 || (c.w_dtype == MOE_I8 && (long long)c.T * c.top_k <= 32ll * c.E);
+    if (c.w_dtype == MOE_I4) return true;
+    if (c.w_dtype == MOE_I8) return (long long)c.T * c.top_k <= 32ll * c.E;
+    return is_bf16_kind(c) && (long long)c.T * c.top_k <= (long long)kStreamBf16Rows * c.E;
 }
 bool q8t_shared(const moe_config& c) {
     return c.w_dtype == MOE_I4 || (c.w_dtype == MOE_I8 && c.T <= 64);
@@ -421,7 +429,7 @@ ExpertTiles expert_tiles(const moe_config& c) {
 // Split plan of a weight-streaming launch, in 128-code K blocks. An INT4 code stage holds
 // two of them and a split must start on one, so INT4 plans are made over 256-code blocks.
 SplitPlan qt_split_plan(long long max_mtiles, int n_tiles, int K, int sms, int bits) {
-    const int per = 8 / bits;
+    const int per = bits >= 8 ? 1 : 8 / bits;
     SplitPlan sp = split_plan(max_mtiles, n_tiles, K, sms, QT_BK * per);
     sp.kbs *= per;
     return sp;
@@ -647,12 +655,20 @@ const char* gemm_q8_name() {
 
 template <int EPI>
 const char* gemm_q8t_name(int bits) {
-    const bool q4 = bits == 4;
+    const int b = bits == 4 ? 0 : bits == 8 ? 1 : 2;
+    static const char* const f32[3] = {"grouped_gemm_q4t_f32", "grouped_gemm_q8t_f32",
+                                       "grouped_gemm_st_f32"};
+    static const char* const gelu[3] = {"grouped_gemm_q4t_gelu", "grouped_gemm_q8t_gelu",
+                                        "grouped_gemm_st_gelu"};
+    static const char* const swiglu[3] = {"grouped_gemm_q4t_swiglu", "grouped_gemm_q8t_swiglu",
+                                          "grouped_gemm_st_swiglu"};
+    static const char* const scale[3] = {"grouped_gemm_q4t_scale", "grouped_gemm_q8t_scale",
+                                         "grouped_gemm_st_scale"};
     switch (EPI) {
-        case EPI_F32: return q4 ? "grouped_gemm_q4t_f32" : "grouped_gemm_q8t_f32";
-        case EPI_GELU_BF16: return q4 ? "grouped_gemm_q4t_gelu" : "grouped_gemm_q8t_gelu";
-        case EPI_SWIGLU_BF16: return q4 ? "grouped_gemm_q4t_swiglu" : "grouped_gemm_q8t_swiglu";
-        default: return q4 ? "grouped_gemm_q4t_scale" : "grouped_gemm_q8t_scale";
+        case EPI_F32: return f32[b];
+        case EPI_GELU_BF16: return gelu[b];
+        case EPI_SWIGLU_BF16: return swiglu[b];
+        default: return scale[b];
     }
 }
 
@@ -739,14 +755,16 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     if (G > GM_MAX_GROUPS) return MOE_ERR_UNSUPPORTED;
     if (EPI == EPI_SCALE_H16 && (w_scale || (sp.S > 1 && partial) || !out_exp || ld_out % 32 != 0))
         return MOE_ERR_UNSUPPORTED;
-    swap_ab = swap_ab && w_scale != nullptr;
+    // (bf16 weights stream through the swapped kernel too: w_bits 16, no row scales)
+    swap_ab = swap_ab && (w_scale != nullptr || w_bits == 16);
     if (swap_ab && !q8t_supports(EPI)) return MOE_ERR_UNSUPPORTED;
     if (w_scale && w_bits != 8 && (w_bits != 4 || !swap_ab)) return MOE_ERR_UNSUPPORTED;
     if (w_bits == 4 && sp.S > 1 && sp.kbs % 2 != 0) return MOE_ERR_UNSUPPORTED;
     CUtensorMap ta, tb, ta2, tb2;
     const bool gathered = a_gather && !w_scale;
     if (xg >= 0 && (w_scale || sp.S > 1 || !B2)) return MOE_ERR_UNSUPPORTED;
-    const uint64_t b_cols = (w_scale && w_bits == 4) ? (uint64_t)K / 2 : (uint64_t)K;   // bytes
+    const uint64_t b_cols = (w_scale && w_bits == 4) ? (uint64_t)K / 2
+                            : (swap_ab && w_bits == 16) ? 2ull * K : (uint64_t)K;   // bytes
     if (swap_ab ? !make_tmap_i8(&tb, B, (uint64_t)b_rows_total, b_cols, GM_BN / 2, QT_BK,
                                 CU_TENSOR_MAP_SWIZZLE_128B)
         : w_scale ? !make_tmap_i8(&tb, B, (uint64_t)b_rows_total, (uint64_t)K, GM_BN / 2)
@@ -845,10 +863,11 @@ moe_status launch_gemm(const void* A, int64_t a_rows, int K, const void* B, int6
     const int grid = num_sms();
     if (swap_ab) {
         if constexpr (q8t_supports(EPI)) {
-            static std::once_flag qt_once[2][64];
-            static cudaError_t qt_err[2][64];
-            const int b4 = w_bits == 4 ? 1 : 0;
-            auto kern = b4 ? grouped_gemm_q8t_kernel<EPI, 4> : grouped_gemm_q8t_kernel<EPI, 8>;
+            static std::once_flag qt_once[3][64];
+            static cudaError_t qt_err[3][64];
+            const int b4 = w_bits == 4 ? 1 : w_bits == 16 ? 2 : 0;
+            auto kern = b4 == 1 ? grouped_gemm_q8t_kernel<EPI, 4>
+                        : b4 == 2 ? grouped_gemm_q8t_kernel<EPI, 16> : grouped_gemm_q8t_kernel<EPI, 8>;
             if (dev >= 0 && dev < 64) {
                 std::call_once(qt_once[b4][dev], [&] {
                     qt_err[b4][dev] = cudaFuncSetAttribute(kern,
@@ -1350,8 +1369,8 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate
     // itself (no x_perm copy, which is k times the size of x). With fewer slots per token
     // the copy is cheaper than the slower A loads of the gathering kernel (16-byte cp.async
     // instead of TMA), and 256-row tiles read a materialised x_perm (see expert_tiles).
-    const bool gather_a =
-        is_bf16_kind(c) && !quant_w(c) && c.top_k >= 4 && expert_tiles(c).up == 1;
+    const bool gather_a = is_bf16_kind(c) && !quant_w(c) && !q8t_routed(c) && c.top_k >= 4 &&
+                          expert_tiles(c).up == 1;
     float* y = at<float>(ws, L.y);
     int32_t* mtile = at<int32_t>(ws, L.mtile);
     // Top-1 layers without a shared expert write the output from the down projection.
@@ -1375,16 +1394,16 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate
                           hist_by_router));
     // The shared expert as group E of the routed up projection (one launch, one tail).
     const FfnPlan fpl = ffn_plan(c);
-    const bool merge_shared = c.has_shared && is_bf16_kind(c) && !quant_w(c) && fpl.up.S == 1 &&
-                              fpl.sh_up.S == 1 && fpl.sh_down.S == 1;
+    const bool merge_shared = c.has_shared && is_bf16_kind(c) && !quant_w(c) && !q8t_routed(c) &&
+                              fpl.up.S == 1 && fpl.sh_up.S == 1 && fpl.sh_down.S == 1;
     // Compact routed rows of y (fp16 + a power-of-two scale per 32 columns, inside the fp32
     // region: values in its first Pmax * d * 2 bytes, then Pmax rows of compact_exp_ld(d)
     // exponent bytes; the shared rows keep their fp32 place after the routed ones).
     // k >= 4 only: with fewer slots per token the compact combine's copy pipeline holds
     // too few rows per step to beat the fp32 combine (Mixtral-shaped top-2 layer: 0.061 ms
     // against 0.045 ms), and the bytes saved are small.
-    const bool compact_y = !c.y_fp32 && is_bf16_kind(c) && !quant_w(c) && !fuse1 &&
-                           fpl.down.S == 1 && c.top_k >= 4;
+    const bool compact_y = !c.y_fp32 && is_bf16_kind(c) && !quant_w(c) && !q8t_routed(c) &&
+                           !fuse1 && fpl.down.S == 1 && c.top_k >= 4;
     int8_t* y_exp = compact_y ? reinterpret_cast<int8_t*>(y) + (long long)c.T * c.top_k * c.d * 2
                               : nullptr;
     MOE_TRY(ffn_impl(c, x_perm, offsets, *routed, shared, x, w, perm_token, perm_slot, y, mtile,
