@@ -28,6 +28,11 @@
 // For SwiGLU a tile's 256 B rows are 128 gate rows (n0..) and 128 up rows
 // (F+n0..) of the same expert, loaded as two TMA boxes, so the epilogue can form
 // silu(gate) * up for 128 output columns without repacking the weights.
+// CTA pairs (GemmParams::pair): two-CTA clusters take pairs of consecutive 128-row tiles
+// of one group and N block; each CTA loads half of the B tile and multicasts it to both.
+// Outputs: bf16 rows (GELU / SwiGLU, top-1 combine), fp32 rows (32-byte stores, or with
+// 128-row tiles one bulk tensor store per warp and 32 x 32 box staged in shared memory),
+// or compact rows (EPI_SCALE_H16: fp16 with a power-of-two scale per 32 columns).
 #pragma once
 #include "common.cuh"
 
