@@ -112,8 +112,9 @@ typedef struct {
                                   (w1 [E][N1][d/2], w2 [E][d][F/2] bytes; see moe_quantize_i4). */
     int32_t overflow;          /* moe_overflow; 0 = MOE_OVERFLOW_DROP */
     int32_t y_fp32;            /* Expert-output rows inside moe_forward (routed experts with
-                                  bf16 weights, top_k >= 4 and an unsplit down projection;
-                                  other layers always keep fp32 rows): 0 = fp16 with one
+                                  bf16 weights, top_k >= 4, more than 4 rows per expert on
+                                  average and an unsplit down projection; other layers
+                                  always keep fp32 rows): 0 = fp16 with one
                                   power-of-two scale per 32 columns of a row (half the bytes
                                   of fp32; every element keeps fp16's 11-bit significand and
                                   no finite value overflows), 1 = fp32, as moe_expert_ffn
@@ -221,7 +222,9 @@ moe_status moe_combine(const moe_config* cfg, const void* x, const float* y,
 /* The whole layer: route -> dispatch -> expert FFNs -> combine, stream-ordered, no
  * host synchronisation. out [T, d] act_dtype. Optional outputs (nullable):
  * topk_idx [T, k], topk_w [T, k], load [E]. ws must hold moe_workspace_size(cfg)
- * bytes (checked against ws_bytes). */
+ * bytes (checked against ws_bytes). Results equal the staged entry points' up to the
+ * expert-output row format (moe_config.y_fp32) and floating-point summation order; with
+ * y_fp32 = 1 (or fp32 rows anyway) the operations are the same. */
 moe_status moe_forward(const moe_config* cfg, const void* x, const float* W_gate,
                        const float* gate_bias, const moe_expert_weights* routed,
                        const moe_expert_weights* shared, void* out, int32_t* topk_idx,
