@@ -119,6 +119,21 @@ def test_compact_expert_rows_cost_the_same_roofline_and_fewer_bytes():
         assert fa == fb and ba - bb == P * wl.d * 2 - P * wl.d // 32
 
 
+def test_weight_streaming_kernels_cost_like_their_algorithm():
+    # the bf16 weight-streaming kernel (decode) and the INT8 / INT4 ones are costed as the
+    # projection they compute; their source hash covers the weight-streaming kernel's files
+    wl = get("decode8")
+    P, touched = 64, 61
+    for name in ("grouped_gemm_st_swiglu", "grouped_gemm_st_scale"):
+        base = name.replace("_st_", "_")
+        assert bench._base_name(name) == base
+        assert bench.kernel_roofline_cost(wl, name, P, touched) == bench.kernel_roofline_cost(wl, base, P, touched)
+        assert bench.kernel_algorithmic_cost(wl, name, P, touched) == bench.kernel_algorithmic_cost(wl, base, P, touched)
+    assert "grouped_gemm_q8t.cuh" in next(v for k, v in bench.KERNEL_FILES.items()
+                                           if "grouped_gemm_st_swiglu".startswith(k))
+    assert bench.kernel_sources_hash("grouped_gemm_st_swiglu") != bench.kernel_sources_hash("grouped_gemm_swiglu")
+
+
 def test_l2_is_flushed_unless_a_forward_streams_several_times_the_l2():
     # the tiny layer and the small quantised decode layers fit (or nearly fit) in the
     # 126 MB L2: a buffer larger than L2 is written between their timed steps; layers
